@@ -1,0 +1,174 @@
+"""Seeded synthetic inputs for the GroupNorm(+SiLU) workloads.
+
+This module holds no GroupNorm arithmetic: it draws numbers and rounds them
+to bf16 bit patterns.  It is the one piece of code that both the CUDA path's
+callers and the fp64 oracle's callers share, so that both sides see the very
+same input bytes.
+
+The shapes are the FLUX.2 VAE decoder GroupNorm shapes of the kernel
+micro-benchmark on the sglang PR #33451 page ("FLUX.2 VAE decoder fast path
+behind quality=high", section "Speedup", first table), written as (N, C, H, W)
+of a channels_last tensor, plus the small 64x64 case.  The value
+distributions stand in for decoder activations (the pages print none):
+
+  x     ~ N(mean, std) fp32, rounded to bf16 (round to nearest even)
+  gamma ~ U(0.5, 1.5) fp32,   beta ~ N(0, 0.1) fp32
+  cfg3  adds a per-channel offset U(-1, 1) to x ~ N(4, 0.25): a
+        cancellation stress for the statistics.
+
+Seeds: x = 1000 + index, gamma = 2000 + index, beta = 3000 + index, channel
+offsets = 4000; numpy PCG64 (``numpy.random.default_rng``).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+# Values are drawn in fixed-size chunks so that the stream of numbers (and so
+# every byte of the tensor) does not depend on how much memory is at hand.
+_CHUNK = 1 << 24
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round binary32 values to bf16 (round to nearest, ties to even) and
+    return the 16-bit patterns.  Inputs must be finite."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to binary32."""
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32)
+            << np.uint32(16)).view(np.float32)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int          # seed index
+    N: int
+    C: int
+    H: int
+    W: int
+    G: int = 32
+    eps: float = 1e-6
+    x_mean: float = 0.0
+    x_std: float = 1.0
+    channel_offset: float = 0.0   # half-width a of per-channel offsets U(-a, a); 0 = none
+    silu_modes: tuple = (True,)
+    note: str = ""
+    pages_us_h200: float | None = None   # the pages' two-pass time for this shape (context)
+
+    @property
+    def L(self) -> int:
+        return self.H * self.W
+
+    @property
+    def elements(self) -> int:
+        return self.N * self.L * self.C
+
+    @property
+    def nchw(self) -> tuple:
+        return (self.N, self.C, self.H, self.W)
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "N": self.N, "C": self.C, "H": self.H, "W": self.W,
+                "G": self.G, "eps": self.eps, "layout": "NHWC (channels_last)",
+                "x": (f"N({self.x_mean},{self.x_std})"
+                      + (f"+U(-{self.channel_offset},{self.channel_offset})[c]"
+                         if self.channel_offset else "")),
+                "gamma": "U(0.5,1.5)", "beta": "N(0,0.1)"}
+
+
+WORKLOADS = [
+    Workload("gn_silu_c128_64x64", 0, 1, 128, 64, 64,
+             note="small case the oracle finishes in well under a second"),
+    Workload("gn_silu_c512_128x128", 1, 1, 512, 128, 128,
+             note="VAE mid-block shape", pages_us_h200=76.0),
+    Workload("gn_c512_256x256_offset_stress", 2, 1, 512, 256, 256, x_mean=4.0, x_std=0.25,
+             channel_offset=1.0, silu_modes=(True, False),
+             note="mean 4, sigma 0.25, per-channel offsets: cancellation stress",
+             pages_us_h200=121.0),
+    Workload("gn_silu_c512_512x512", 3, 1, 512, 512, 512,
+             note="256 MiB activation", pages_us_h200=311.1),
+    Workload("gn_silu_c256_1024x1024", 4, 1, 256, 1024, 1024, x_std=2.0,
+             note="512 MiB up-block shape", pages_us_h200=913.8),
+    Workload("gn_silu_c128_1024x1024", 5, 1, 128, 1024, 1024, x_std=2.0,
+             note="256 MiB up-block shape", pages_us_h200=307.9),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _normal_bits(rng: np.random.Generator, count: int, C: int, mean: float, std: float,
+                 offsets: np.ndarray | None) -> np.ndarray:
+    out = np.empty(count, np.uint16)
+    done = 0
+    while done < count:
+        k = min(_CHUNK, count - done)   # _CHUNK is a multiple of every C used here
+        v = rng.standard_normal(k, dtype=np.float32)
+        v *= np.float32(std)
+        v += np.float32(mean)
+        if offsets is not None:
+            v = v.reshape(-1, C)
+            v += offsets[None, :]
+            v = v.reshape(-1)
+        out[done:done + k] = f32_to_bf16_bits(v)
+        done += k
+    return out
+
+
+def affine_params(index: int, C: int) -> tuple[np.ndarray, np.ndarray]:
+    gamma = np.random.default_rng(2000 + index).uniform(0.5, 1.5, C).astype(np.float32)
+    beta = (np.random.default_rng(3000 + index).standard_normal(C, dtype=np.float32)
+            * np.float32(0.1))
+    return gamma, beta
+
+
+def make_inputs(w: Workload) -> dict:
+    """x_bits uint16 [N, L, C] (bf16 patterns, channels innermost), gamma and
+    beta float32 [C]."""
+    offsets = None
+    if w.channel_offset:
+        offsets = np.random.default_rng(4000).uniform(
+            -w.channel_offset, w.channel_offset, w.C).astype(np.float32)
+    if _CHUNK % w.C:
+        raise ValueError("C must divide the draw chunk")
+    rng = np.random.default_rng(1000 + w.index)
+    x = _normal_bits(rng, w.elements, w.C, w.x_mean, w.x_std, offsets)
+    gamma, beta = affine_params(w.index, w.C)
+    return {"x_bits": x.reshape(w.N, w.L, w.C), "gamma": gamma, "beta": beta}
+
+
+def make_case(N: int, L: int, C: int, seed: int, *, mean: float = 0.0, std: float = 1.0,
+              channel_offset: float = 0.0, kind: str = "normal") -> dict:
+    """A seeded test case of any shape.
+
+    kind: "normal"   x ~ N(mean, std) (+ per-channel offsets U(-a, a))
+          "constant" every x equals bf16(mean)
+          "grid"     x = k/8 for integers k in [-64, 64]: values whose
+                     affine images 2x+1 are also exact bf16 numbers
+    """
+    rng = np.random.default_rng(seed)
+    count = N * L * C
+    if kind == "normal":
+        offsets = None
+        if channel_offset:
+            offsets = rng.uniform(-channel_offset, channel_offset, C).astype(np.float32)
+        v = rng.standard_normal(count, dtype=np.float32) * np.float32(std) + np.float32(mean)
+        if offsets is not None:
+            v = (v.reshape(-1, C) + offsets[None, :]).reshape(-1)
+        x = f32_to_bf16_bits(v)
+    elif kind == "constant":
+        x = f32_to_bf16_bits(np.full(count, mean, np.float32))
+    elif kind == "grid":
+        k = rng.integers(-64, 65, count)
+        x = f32_to_bf16_bits((k / 8.0).astype(np.float32))
+    else:
+        raise ValueError(f"unknown kind {kind!r}")
+    gamma = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    beta = (rng.standard_normal(C, dtype=np.float32) * np.float32(0.1))
+    return {"x_bits": x.reshape(N, L, C), "gamma": gamma, "beta": beta}
+

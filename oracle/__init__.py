@@ -1,0 +1,164 @@
+"""fp64 CPU oracle for channels-last GroupNorm (+SiLU) -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference arm may import this package.  The CUDA library and its
+Python binding never import it; the two share no code.
+
+The arithmetic lives in ``gn_oracle.c`` (plain C, fp64, OpenMP over the
+(n, g) groups), which writes out the definition given by the sglang PR
+#33451 page ("FLUX.2 VAE decoder fast path behind quality=high", section
+"Modifications", item 1): per-(batch, group) mean and biased variance over
+(N, L, C) rows with C innermost, rstd = 1/sqrt(var + eps), the per-channel
+affine, then SiLU if requested.  This module only compiles that file with
+gcc and marshals numpy arrays through ctypes.
+
+Parity pins: the oracle is checked against brute force on tiny tensors, a
+library special case (``torch.nn.functional.group_norm`` in float64), closed
+forms and invariants in ``tests/test_oracle_pins.py``; every exported
+function is pinned there.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "gn_oracle.c")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "libgn_oracle.so")
+
+# -ffp-contract=off keeps gcc from fusing a*b+c into an FMA (it does so by
+# default on aarch64), so x86 and Arm hosts round identically.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+          "-fno-fast-math"]
+
+_lock = threading.Lock()
+_default = None
+
+
+def build(source: str = SOURCE, out: str = LIB_PATH, force: bool = False) -> str:
+    """Compile ``source`` into the shared library ``out`` (gcc + OpenMP)."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(source)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, source, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library (the real one, or a
+    deliberately broken copy built by the mutation tests)."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        lib.gn_oracle_stats.argtypes = [_p, _i64, _i64, _i64, _i64, ctypes.c_double,
+                                        _p, _p, _p, ctypes.c_int]
+        lib.gn_oracle_stats.restype = ctypes.c_int
+        lib.gn_oracle_forward.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, ctypes.c_double,
+                                          ctypes.c_int, _p, _p, _p, ctypes.c_int]
+        lib.gn_oracle_forward.restype = ctypes.c_int
+        lib.gn_oracle_apply_at.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _p, _p,
+                                           ctypes.c_int, _p, _i64, _p, ctypes.c_int]
+        lib.gn_oracle_apply_at.restype = ctypes.c_int
+        lib.gn_oracle_max_threads.argtypes = []
+        lib.gn_oracle_max_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = lib_path
+
+    # -- helpers -----------------------------------------------------------
+    @staticmethod
+    def _prep(x_bits, gamma=None, beta=None):
+        x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        if x_bits.ndim != 3:
+            raise ValueError("x_bits must be [N, L, C] bf16 bit patterns (uint16)")
+        out = [x_bits]
+        for v in (gamma, beta):
+            if v is not None:
+                out.append(np.ascontiguousarray(v, dtype=np.float32))
+        return out
+
+    def max_threads(self) -> int:
+        return int(self.lib.gn_oracle_max_threads())
+
+    # -- entry points ------------------------------------------------------
+    def stats(self, x_bits, G: int, eps: float, nthreads: int = 0):
+        """Return (mean, var, rstd), each float64 [N, G]."""
+        (x_bits,) = self._prep(x_bits)
+        N, L, C = x_bits.shape
+        mean = np.empty((N, G), np.float64)
+        var = np.empty((N, G), np.float64)
+        rstd = np.empty((N, G), np.float64)
+        rc = self.lib.gn_oracle_stats(x_bits.ctypes.data, N, L, C, G, float(eps),
+                                      mean.ctypes.data, var.ctypes.data, rstd.ctypes.data,
+                                      int(nthreads))
+        if rc != 0:
+            raise ValueError(f"gn_oracle_stats rejected its arguments (rc={rc})")
+        return mean, var, rstd
+
+    def forward(self, x_bits, gamma, beta, G: int, eps: float, apply_silu: bool,
+                nthreads: int = 0):
+        """Return (y float64 [N, L, C], mean float64 [N, G], rstd float64 [N, G])."""
+        x_bits, gamma, beta = self._prep(x_bits, gamma, beta)
+        N, L, C = x_bits.shape
+        if gamma.shape != (C,) or beta.shape != (C,):
+            raise ValueError("gamma and beta must have shape [C]")
+        y = np.empty((N, L, C), np.float64)
+        mean = np.empty((N, G), np.float64)
+        rstd = np.empty((N, G), np.float64)
+        rc = self.lib.gn_oracle_forward(x_bits.ctypes.data, gamma.ctypes.data,
+                                        beta.ctypes.data, N, L, C, G, float(eps),
+                                        int(bool(apply_silu)), y.ctypes.data,
+                                        mean.ctypes.data, rstd.ctypes.data, int(nthreads))
+        if rc != 0:
+            raise ValueError(f"gn_oracle_forward rejected its arguments (rc={rc})")
+        return y, mean, rstd
+
+    def apply_at(self, x_bits, gamma, beta, G: int, mean, rstd, apply_silu: bool,
+                 flat_index, nthreads: int = 0):
+        """y (float64) at the given flat indices of the [N, L, C] tensor."""
+        x_bits, gamma, beta = self._prep(x_bits, gamma, beta)
+        N, L, C = x_bits.shape
+        mean = np.ascontiguousarray(mean, np.float64)
+        rstd = np.ascontiguousarray(rstd, np.float64)
+        idx = np.ascontiguousarray(flat_index, np.int64)
+        y = np.empty(idx.shape, np.float64)
+        rc = self.lib.gn_oracle_apply_at(x_bits.ctypes.data, gamma.ctypes.data,
+                                         beta.ctypes.data, N, L, C, G, mean.ctypes.data,
+                                         rstd.ctypes.data, int(bool(apply_silu)),
+                                         idx.ctypes.data, idx.size, y.ctypes.data,
+                                         int(nthreads))
+        if rc != 0:
+            raise ValueError(f"gn_oracle_apply_at rejected its arguments (rc={rc})")
+        return y
+
+
+def get() -> Oracle:
+    """The oracle built from ``gn_oracle.c`` (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+def stats(*a, **k):
+    return get().stats(*a, **k)
+
+
+def forward(*a, **k):
+    return get().forward(*a, **k)
+
+
+def apply_at(*a, **k):
+    return get().apply_at(*a, **k)
