@@ -1,0 +1,494 @@
+"""Benchmark of channels-last GroupNorm+SiLU on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+                    [--workload NAME] [--variant auto|fused|two_pass] [--no-sweep]
+
+A step is one call of the whole path (pass 1, finalize, pass 2) on one
+synthetic bf16 activation of the workload (default: N=1 C=512 H=W=128, the
+FLUX.2 VAE mid-block GroupNorm shape).  Inputs are seeded (see
+``channels_last_groupnorm_gb300/workloads.py``) and already resident in HBM;
+consecutive steps rotate over enough buffer sets that no step finds its
+input in L2.  ``value`` is effective bandwidth: N*L*C*4 bytes (read x once,
+write y once) per step, summed over ranks, divided by the slowest rank's
+time.  ``e2e`` repeats the measurement through the C ABI from pinned host
+buffers with the host<->device copies inside the timed region.
+
+Under torchrun each rank runs its own replica on its own GPU (the
+operation has no cross-GPU exchange); rank 0 prints the line.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NHWC GroupNorm+SiLU µs/call and HBM GB/s (% of GB300 peak), bf16 G=32"
+DEFAULT_WORKLOAD = "gn_silu_c512_128x128"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh"]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; also exercised with gloo on CPU by the tests)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_timing(elapsed_s: float, units: float, device=None):
+    """(max elapsed over ranks, sum of units over ranks); identity when not
+    distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, traffic
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "of measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("", "[N/A]") else None,
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons),
+                "power_w_max": max((r["power"] for r in rows if r["power"] is not None),
+                                   default=None)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "channels_last_groupnorm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, variant: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    src = kernel_source_hash()
+    for line in lines:
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#"):
+            wname, var, sha, nbytes = parts
+            if wname == workload and var == variant and sha == src:
+                return float(nbytes)
+    return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def upload(case, device):
+    import numpy as np
+    import torch
+    x = torch.from_numpy(case["x_bits"].view(np.int16)).to(device).view(torch.bfloat16)
+    return (x.contiguous(), torch.from_numpy(case["gamma"]).to(device),
+            torch.from_numpy(case["beta"]).to(device))
+
+
+def buffer_sets_for(nbytes_per_set: int, l2_bytes: int, cap: int = 64) -> int:
+    """Enough rotating buffer sets that the sets together exceed twice L2."""
+    need = -(-2 * l2_bytes // max(1, nbytes_per_set))
+    return int(max(1, min(cap, need)))
+
+
+def time_calls(call, nsets, steps, stream):
+    """Per-step CUDA-event durations (ms) of `steps` calls rotating over the
+    buffer sets, plus the total elapsed time of the region (s)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        call(i % nsets)
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, t0.elapsed_time(t1) / 1e3
+
+
+def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, sampler=None,
+                     seeded=True):
+    """Device-resident timing of one workload.  Returns a dict."""
+    import torch
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    from channels_last_groupnorm_gb300 import workloads as wl
+
+    if seeded:
+        x0, gamma, beta = upload(wl.make_inputs(w), device)
+    else:   # same distributions drawn on the device (sweep of the larger shapes)
+        gen = torch.Generator(device=device).manual_seed(1000 + w.index)
+        x0 = (torch.randn(w.N, w.L, w.C, generator=gen, device=device) * w.x_std
+              + w.x_mean).to(torch.bfloat16)
+        gamma_np, beta_np = wl.affine_params(w.index, w.C)
+        gamma = torch.from_numpy(gamma_np).to(device)
+        beta = torch.from_numpy(beta_np).to(device)
+    elems = w.elements
+    set_bytes = 4 * elems
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    nsets = buffer_sets_for(set_bytes, l2)
+    free, _ = torch.cuda.mem_get_info(device)
+    nsets = max(1, min(nsets, int(0.5 * free // set_bytes)))
+    xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
+    ys = [torch.empty_like(x0) for _ in range(nsets)]
+    h = stream.cuda_stream
+
+    def call(i):
+        rc = gs.raw_gn_silu_rows_ex(xs[i].data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+                                    ys[i].data_ptr(), w.N, w.L, w.C, w.G, w.eps, 1,
+                                    variant=variant_id, stream=h)
+        if rc != 0:
+            raise RuntimeError(f"gn_silu_rows_ex failed: {gs.status_string(rc)}")
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, warmup)):
+            call(i % nsets)
+        torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.start()
+        if soak_s > 0:
+            t_end = time.time() + soak_s
+            i = 0
+            while time.time() < t_end:
+                for _ in range(50):
+                    call(i % nsets)
+                    i += 1
+                torch.cuda.synchronize()
+        before = gs.gn_kernel_launch_count()
+        per, elapsed = time_calls(call, nsets, steps, stream)
+        launches = gs.gn_kernel_launch_count() - before
+        clocks = sampler.stop() if sampler is not None else None
+    status = gs.gn_device_status(False)
+    if status != 0:
+        raise RuntimeError(f"device status after timing: {gs.status_string(status)}")
+    res = {"elapsed_s": elapsed, "per_step_ms": per, "nsets": nsets, "set_bytes": set_bytes,
+           "launches": launches, "clocks": clocks,
+           "variant": {1: "two_pass", 2: "fused"}.get(
+               gs.gn_silu_pick_variant(w.N, w.L, w.C, w.G) if variant_id == 0 else variant_id,
+               "?")}
+    del xs, ys
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_e2e(w, variant_id, steps, warmup, device, stream):
+    """Through the C ABI from pinned host buffers: H2D of x, gamma, beta, the
+    call, D2H of y, every step, all inside the timed region."""
+    import numpy as np
+    import torch
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    from channels_last_groupnorm_gb300 import workloads as wl
+
+    case = wl.make_inputs(w)
+    hx = torch.from_numpy(case["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hg = torch.from_numpy(case["gamma"]).pin_memory()
+    hb = torch.from_numpy(case["beta"]).pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    dx = torch.empty_like(hx, device=device)
+    dg = torch.empty_like(hg, device=device)
+    db = torch.empty_like(hb, device=device)
+    dy = torch.empty_like(hx, device=device)
+    h = stream.cuda_stream
+
+    def step(_):
+        dx.copy_(hx, non_blocking=True)
+        dg.copy_(hg, non_blocking=True)
+        db.copy_(hb, non_blocking=True)
+        rc = gs.raw_gn_silu_rows_ex(dx.data_ptr(), dg.data_ptr(), db.data_ptr(), dy.data_ptr(),
+                                    w.N, w.L, w.C, w.G, w.eps, 1, variant=variant_id, stream=h)
+        if rc != 0:
+            raise RuntimeError(gs.status_string(rc))
+        hy.copy_(dy, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, warmup)):
+            step(i)
+        torch.cuda.synchronize()
+        per, elapsed = time_calls(step, 1, steps, stream)
+    h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
+    d2h = hy.numel() * 2
+    return elapsed, h2d, d2h
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The fp64 oracle on this host's cores, on the full workload tensor,
+    repeated until about `budget_s` of CPU time has passed."""
+    import oracle
+    from channels_last_groupnorm_gb300 import workloads as wl
+    case = wl.make_inputs(w)
+    orc = oracle.get()
+    cores = orc.max_threads()
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        orc.forward(case["x_bits"], case["gamma"], case["beta"], w.G, w.eps, True)
+        calls += 1
+        if time.perf_counter() - t0 >= budget_s or calls >= 50:
+            break
+    dt = (time.perf_counter() - t0) / calls
+    return {"value": 4.0 * w.elements / dt / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "us_per_call": dt * 1e6,
+            "sample": f"{calls} full calls of the fp64 oracle on the {w.name} tensor "
+                      f"({w.elements} elements), {cores} OpenMP threads"}
+
+
+def sweep(variant_id, device, stream, peak):
+    """Every workload shape: us/call and effective bandwidth at 4 B/elem
+    (read once + write once) and 6 B/elem (two-pass byte count)."""
+    from channels_last_groupnorm_gb300 import workloads as wl
+    out = []
+    for w in wl.WORKLOADS:
+        r = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24))
+        us = statistics.median(r["per_step_ms"]) * 1e3
+        gbs4 = 4.0 * w.elements / (us * 1e-6) / 1e9
+        gbs6 = 6.0 * w.elements / (us * 1e-6) / 1e9
+        out.append({"workload": w.name, "variant": r["variant"], "us_per_call": round(us, 2),
+                    "gbs_4B": round(gbs4, 1), "gbs_6B": round(gbs6, 1),
+                    "frac_4B": round(gbs4 / peak, 3), "frac_6B": round(gbs6 / peak, 3),
+                    "pages_h200_us": w.pages_us_h200,
+                    "l2": f"{r['nsets']} rotating buffer sets of {r['set_bytes'] >> 20} MiB"})
+    return out
+
+
+def run_ours(args):
+    import torch
+    from channels_last_groupnorm_gb300 import build as gnbuild
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    from channels_last_groupnorm_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if rank == 0 or not os.path.exists(gnbuild.LIB_PATH):
+        gnbuild.build()
+    barrier()
+    gs.lib()
+    w = wl.BY_NAME[args.workload]
+    variant_id = {"auto": 0, "two_pass": 1, "fused": 2}[args.variant]
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = hbm_peak()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    r = measure_workload(w, variant_id, args.steps, args.warmup, device, stream,
+                         soak_s=args.soak, sampler=sampler)
+    ms_per_step = r["elapsed_s"] * 1e3 / args.steps
+    units = 4.0 * w.elements * args.steps
+    elapsed, total_units = reduce_timing(r["elapsed_s"], units,
+                                         device=device if world > 1 else None)
+    value = total_units / elapsed / 1e9
+
+    per = r["per_step_ms"]
+    launch_ms = statistics.mean(per)
+    alg_bytes = 4.0 * w.elements
+    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(w.name, r["variant"])
+
+    e2e_s, h2d, d2h = measure_e2e(w, variant_id, max(5, args.steps // 2), args.warmup, device,
+                                  stream)
+    e2e_steps = max(5, args.steps // 2)
+    e2e_elapsed, e2e_units = reduce_timing(e2e_s, 4.0 * w.elements * e2e_steps,
+                                           device=device if world > 1 else None)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_call": round(ms_per_step * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; x~N(0,1) bf16, gamma~U(0.5,1.5), beta~N(0,0.1))",
+        "config": {**w.describe(), "silu": True, "variant": r["variant"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {r['nsets']} rotating buffer sets of "
+                         f"{r['set_bytes'] >> 20} MiB (x+y)",
+                   "bytes_per_step": "N*L*C*4 (x read once, y written once)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic,
+                     "kernel": "gn_fused_kernel" if r["variant"] == "fused"
+                               else "pass1+finalize+pass2",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "launch_us_mean": round(launch_ms * 1e3, 3),
+                     "launch_us_median": round(statistics.median(per) * 1e3, 3)},
+        "e2e": {"value": round(e2e_units / e2e_elapsed / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_call": round(e2e_s * 1e6 / e2e_steps, 2)},
+        "gpu_launches": int(r["launches"]),
+        "clocks": r["clocks"],
+    }
+    if w.pages_us_h200:
+        pages_gbs = 4.0 * w.elements / (w.pages_us_h200 * 1e-6) / 1e9
+        line["vs_baseline"] = round(value / (pages_gbs * world), 3)
+        line["baseline_note"] = (f"pages' two-pass Triton kernel on H200: {w.pages_us_h200} us/call"
+                                 f" = {pages_gbs:.1f} GB/s at 4 B/elem (context, other hardware)")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0 and not args.no_sweep:
+        line["sweep"] = sweep(variant_id, device, stream, peak)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from channels_last_groupnorm_gb300 import workloads as wl
+    w = wl.BY_NAME[args.workload]
+    case = wl.make_inputs(w)
+    orc = oracle.get()
+    cores = orc.max_threads()
+    # size each step so that warm-up + steps take about two minutes at most
+    t0 = time.perf_counter()
+    orc.forward(case["x_bits"][:, : max(1, w.L // 16)], case["gamma"], case["beta"], w.G,
+                w.eps, True)
+    per_row = (time.perf_counter() - t0) / max(1, w.L // 16)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.L, budget / max(per_row, 1e-9))))
+    sample = case["x_bits"][:, :rows]
+    for _ in range(args.warmup):
+        orc.forward(sample, case["gamma"], case["beta"], w.G, w.eps, True)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.forward(sample, case["gamma"], case["beta"], w.G, w.eps, True)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 4.0 * w.N * rows * w.C / dt / 1e9
+    desc = (f"fp64 oracle on the first {rows} of {w.L} rows of the {w.name} tensor "
+            f"per step, {cores} OpenMP threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": w.describe(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--variant", choices=["auto", "fused", "two_pass"], default="auto")
+    ap.add_argument("--soak", type=float, default=1.5,
+                    help="seconds of untimed calls while the clock sampler runs")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,21 @@
-"""GB300-native channels-last GroupNorm(+SiLU)."""
+"""GB300-native channels-last GroupNorm(+SiLU).
+
+The computation runs in ``libgnsilu.so`` (hand-written sm_103a CUDA behind
+the C ABI of ``include/gnsilu.h``); ``gnsilu`` is its Python binding.
+Build the library with ``python -m channels_last_groupnorm_gb300.build``.
+"""
+from .gnsilu import (  # noqa: F401
+    GnError,
+    VARIANT_AUTO,
+    VARIANT_FUSED,
+    VARIANT_TWO_PASS,
+    gn_abi_version,
+    gn_device_status,
+    gn_kernel_launch_count,
+    gn_silu_nhwc,
+    gn_silu_pick_variant,
+    gn_silu_rows,
+    gn_silu_rows_ex,
+    gn_silu_workspace_bytes,
+    status_string,
+)

@@ -1,0 +1,425 @@
+// gn_capi.cu -- the extern "C" boundary of libgnsilu (declared in
+// include/gnsilu.h): argument validation, the per-shape launch plan, the
+// library-owned workspaces, and dispatch to the kernels in gn_kernels.cu.
+//
+// The rejection contract follows the sglang PR #33451 page ("FLUX.2 VAE
+// decoder fast path behind quality=high", section "Modifications", item 1):
+// unsupported inputs (non-power-of-two C, C > 2048, ...) are refused so the
+// caller can fall back; here they return a status code and nothing runs.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/gnsilu.h"
+#include "gn_internal.h"
+
+namespace {
+
+using gn::Args;
+using gn::Geom;
+
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;      // max dynamic shared memory per block
+    int smem_per_sm = 0;
+    int coop = 0;
+    int major = 0, minor = 0;
+};
+std::map<int, DeviceInfo> g_devices;
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+uint64_t env_u64(const char *name, uint64_t dflt)
+{
+    const char *v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    char *end = nullptr;
+    const unsigned long long r = std::strtoull(v, &end, 0);
+    return (end && *end == '\0') ? static_cast<uint64_t>(r) : dflt;
+}
+
+// Timeout of every bounded wait inside the kernels.
+uint64_t wait_timeout_ns()
+{
+    static const uint64_t t = env_u64("GN_WAIT_TIMEOUT_MS", 2000) * 1000000ull;
+    return t;
+}
+
+// L2 eviction hints of the bulk copies (bit meanings in gn_internal.h).
+uint32_t l2_hints()
+{
+    static const uint32_t h = static_cast<uint32_t>(env_u64("GN_L2_HINTS", 0));
+    return h;
+}
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Pure host checks (no CUDA call), in a fixed order.
+int validate(const void *x, const float *gamma, const float *beta, const void *y, int64_t N, int64_t L,
+             int64_t C, int64_t G, float eps, const float *mean_out, const float *rstd_out)
+{
+    if (!x || !gamma || !beta || !y) return GN_ERR_NULL;
+    if (N < 1 || L < 1) return GN_ERR_SHAPE;
+    if (C < 8 || C > 2048 || (C & (C - 1)) != 0) return GN_ERR_CHANNELS;
+    if (G < 1 || C % G != 0) return GN_ERR_CHANNELS;
+    if (N > INT64_MAX / L) return GN_ERR_SHAPE;
+    const int64_t rows = N * L;
+    if (rows > INT64_MAX / (2 * C)) return GN_ERR_SHAPE;
+    if (N > INT64_MAX / (4 * G)) return GN_ERR_SHAPE;
+    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(x) % 16 || addr(y) % 16) return GN_ERR_ALIGN;
+    if (addr(gamma) % 4 || addr(beta) % 4) return GN_ERR_ALIGN;
+    if (addr(mean_out) % 4 || addr(rstd_out) % 4) return GN_ERR_ALIGN;
+    if (!std::isfinite(eps) || eps < 0.f) return GN_ERR_EPS;
+    const size_t bytes = static_cast<size_t>(rows) * static_cast<size_t>(2 * C);
+    if (x != y && ranges_overlap(x, bytes, y, bytes)) return GN_ERR_ALIAS;
+    const size_t cb = static_cast<size_t>(4 * C);
+    if (ranges_overlap(y, bytes, gamma, cb) || ranges_overlap(y, bytes, beta, cb)) return GN_ERR_ALIAS;
+    const size_t sb = static_cast<size_t>(4 * N * G);
+    for (const float *s : {mean_out, rstd_out}) {
+        if (!s) continue;
+        if (ranges_overlap(s, sb, y, bytes) || ranges_overlap(s, sb, x, bytes) ||
+            ranges_overlap(s, sb, gamma, cb) || ranges_overlap(s, sb, beta, cb))
+            return GN_ERR_ALIAS;
+    }
+    if (mean_out && rstd_out && ranges_overlap(mean_out, sb, rstd_out, sb)) return GN_ERR_ALIAS;
+    return GN_OK;
+}
+
+// Current device, checked to be an sm_103 part; kernel attributes set once.
+int current_device(int *dev_out, DeviceInfo *info_out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ||
+            cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev)) {
+            cudaGetLastError();
+            return GN_ERR_DEVICE;
+        }
+        if (d.major != 10 || d.minor != 3) return GN_ERR_DEVICE;
+        if (gn::prepare_kernels(static_cast<uint32_t>(d.smem_optin)) != cudaSuccess) {
+            cudaGetLastError();
+            return GN_ERR_CUDA;
+        }
+        d.ready = true;
+    }
+    *dev_out = dev;
+    *info_out = d;
+    return GN_OK;
+}
+
+struct Plan {
+    Geom g{};
+    int kind = 0;            // GN_VARIANT_TWO_PASS or GN_VARIANT_FUSED
+    int grid = 0;
+    size_t off_partial = 0, off_chstat = 0, off_st = 0, off_mean = 0, off_rstd = 0;
+    size_t ws_bytes = 0;
+};
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Geometry of one schedule: piece size, segments per batch entry, grid and
+// ring depth; plus the workspace layout.
+Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const DeviceInfo &d)
+{
+    Plan p;
+    p.kind = kind;
+    Geom &g = p.g;
+    g.N = N;
+    g.L = L;
+    g.C = static_cast<int32_t>(C);
+    g.G = static_cast<int32_t>(G);
+    g.Cg = static_cast<int32_t>(C / G);
+    g.V = static_cast<int32_t>(C / 8);
+    const int64_t row_bytes = 2 * C;
+    const int per_sm = (kind == GN_VARIANT_FUSED) ? 1 : 2;
+    const int64_t grid_target = static_cast<int64_t>(d.sm_count) * per_sm;
+    const int64_t total_bytes = N * L * row_bytes;
+    // pieces as large as 16 KB, smaller when that leaves fewer than about
+    // four pieces per CTA; never below one row
+    int64_t pb = gn::kMaxPieceBytes;
+    while (pb > row_bytes && pb > gn::kMinPieceBytes && total_bytes / pb < 4 * grid_target) pb /= 2;
+    if (pb < row_bytes) pb = row_bytes;
+    g.piece_bytes = static_cast<int32_t>(pb);
+    g.rows_per_piece = static_cast<int32_t>(pb / row_bytes);
+    g.pieces_per_n = (L + g.rows_per_piece - 1) / g.rows_per_piece;
+    int64_t S = grid_target / N;
+    if (S < 1) S = 1;
+    if (S > g.pieces_per_n) S = g.pieces_per_n;
+    if (S > gn::kMaxSegments) S = gn::kMaxSegments;
+    g.S = static_cast<int32_t>(S);
+    g.items = N * S;
+    p.grid = static_cast<int>(g.items < grid_target ? g.items : grid_target);
+    // ring depth from the shared memory left next to the auxiliary arrays
+    const int kind_smem = (kind == GN_VARIANT_FUSED) ? gn::kFused : gn::kPass1;
+    const int64_t budget = (kind == GN_VARIANT_FUSED) ? d.smem_optin : (d.smem_per_sm / per_sm - 1024);
+    int64_t ring = (budget - static_cast<int64_t>(gn::aux_smem_bytes(g, kind_smem))) / pb;
+    if (ring > gn::kMaxRing) ring = gn::kMaxRing;
+    g.ring = static_cast<int32_t>(ring);
+    // workspace
+    size_t off = 256;   // barrier words
+    p.off_partial = off;
+    off = align256(off + static_cast<size_t>(N) * C * S * sizeof(float2));
+    p.off_chstat = off;
+    off = align256(off + static_cast<size_t>(N) * C * sizeof(float2));
+    p.off_st = off;
+    off = align256(off + static_cast<size_t>(N) * C * sizeof(float2));
+    p.off_mean = off;
+    off = align256(off + static_cast<size_t>(N) * G * sizeof(float));
+    p.off_rstd = off;
+    off = align256(off + static_cast<size_t>(N) * G * sizeof(float));
+    p.ws_bytes = off;
+    return p;
+}
+
+bool fused_launchable(const Plan &p, const DeviceInfo &d)
+{
+    if (!d.coop || p.g.ring < 2) return false;
+    int blocks = 0;
+    const uint32_t smem = gn::make_layout(p.g, gn::kFused).total;
+    if (smem > static_cast<uint32_t>(d.smem_optin)) return false;
+    if (gn::fused_blocks_per_sm(true, smem, &blocks) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return blocks >= 1 && p.grid <= blocks * d.sm_count;
+}
+
+int resolve_variant(int variant, int64_t N, int64_t L, int64_t C, int64_t G, const DeviceInfo &d, Plan *out)
+{
+    if (variant == GN_VARIANT_TWO_PASS) {
+        *out = make_plan(N, L, C, G, GN_VARIANT_TWO_PASS, d);
+        return out->g.ring >= 2 ? GN_OK : GN_ERR_VARIANT;
+    }
+    if (variant == GN_VARIANT_FUSED || variant == GN_VARIANT_AUTO) {
+        Plan f = make_plan(N, L, C, G, GN_VARIANT_FUSED, d);
+        if (fused_launchable(f, d)) {
+            *out = f;
+            return GN_OK;
+        }
+        if (variant == GN_VARIANT_FUSED) return GN_ERR_VARIANT;
+        *out = make_plan(N, L, C, G, GN_VARIANT_TWO_PASS, d);
+        return out->g.ring >= 2 ? GN_OK : GN_ERR_VARIANT;
+    }
+    return GN_ERR_VARIANT;
+}
+
+size_t workspace_bytes_any(int64_t N, int64_t L, int64_t C, int64_t G, const DeviceInfo &d)
+{
+    const Plan a = make_plan(N, L, C, G, GN_VARIANT_TWO_PASS, d);
+    const Plan b = make_plan(N, L, C, G, GN_VARIANT_FUSED, d);
+    return a.ws_bytes > b.ws_bytes ? a.ws_bytes : b.ws_bytes;
+}
+
+// Library-owned workspace of (device, stream), grown on demand.
+int library_workspace(int dev, cudaStream_t stream, size_t bytes, void **ptr)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace &w = g_workspaces[{dev, stream}];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            if (cudaFree(w.ptr) != cudaSuccess) {   // synchronises: no kernel still uses it
+                cudaGetLastError();
+                return GN_ERR_CUDA;
+            }
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        const size_t want = bytes + bytes / 4;   // headroom for nearby shapes
+        void *p = nullptr;
+        if (cudaMalloc(&p, want) != cudaSuccess || cudaMemset(p, 0, want) != cudaSuccess) {
+            cudaGetLastError();
+            if (p) cudaFree(p);
+            return GN_ERR_CUDA;
+        }
+        w.ptr = p;
+        w.bytes = want;
+    }
+    *ptr = w.ptr;
+    return GN_OK;
+}
+
+int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N, int64_t L, int64_t C,
+        int64_t G, float eps, int apply_silu, float *mean_out, float *rstd_out, void *workspace,
+        size_t workspace_bytes, int variant, void *stream)
+{
+    int rc = validate(x, gamma, beta, y, N, L, C, G, eps, mean_out, rstd_out);
+    if (rc != GN_OK) return rc;
+    if (variant < GN_VARIANT_AUTO || variant > GN_VARIANT_FUSED) return GN_ERR_VARIANT;
+    if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256) return GN_ERR_ALIGN;
+    int dev = -1;
+    DeviceInfo d;
+    if ((rc = current_device(&dev, &d)) != GN_OK) return rc;
+    Plan p;
+    if ((rc = resolve_variant(variant, N, L, C, G, d, &p)) != GN_OK) return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = workspace;
+    if (ws) {
+        if (workspace_bytes < workspace_bytes_any(N, L, C, G, d)) return GN_ERR_WORKSPACE;
+    } else if ((rc = library_workspace(dev, s, workspace_bytes_any(N, L, C, G, d), &ws)) != GN_OK) {
+        return rc;
+    }
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    Args a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.y = static_cast<uint16_t *>(y);
+    a.gamma = gamma;
+    a.beta = beta;
+    a.eps = eps;
+    a.l2_hints = l2_hints();
+    a.g = p.g;
+    a.partial = reinterpret_cast<float2 *>(base + p.off_partial);
+    a.chstat = reinterpret_cast<float2 *>(base + p.off_chstat);
+    a.st = reinterpret_cast<float2 *>(base + p.off_st);
+    a.mean = mean_out ? mean_out : reinterpret_cast<float *>(base + p.off_mean);
+    a.rstd = rstd_out ? rstd_out : reinterpret_cast<float *>(base + p.off_rstd);
+    a.sync = reinterpret_cast<unsigned int *>(base);
+    a.timeout_ns = wait_timeout_ns();
+    const bool silu = apply_silu != 0;
+    cudaError_t e;
+    if (p.kind == GN_VARIANT_FUSED) {
+        e = gn::launch_fused(a, p.grid, silu, s);
+        if (e == cudaSuccess) g_launches.fetch_add(1);
+    } else {
+        e = gn::launch_pass1(a, p.grid, s);
+        if (e == cudaSuccess) {
+            g_launches.fetch_add(1);
+            e = gn::launch_finalize(a, s);
+        }
+        if (e == cudaSuccess) {
+            g_launches.fetch_add(1);
+            e = gn::launch_pass2(a, p.grid, silu, s);
+        }
+        if (e == cudaSuccess) g_launches.fetch_add(1);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    return GN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gn_silu_rows_ex(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16, int64_t N,
+                    int64_t L, int64_t C, int64_t G, float eps, int apply_silu, float *mean_out,
+                    float *rstd_out, void *workspace, size_t workspace_bytes, int variant, void *stream)
+{
+    return run(x_bf16, gamma, beta, y_bf16, N, L, C, G, eps, apply_silu, mean_out, rstd_out, workspace,
+               workspace_bytes, variant, stream);
+}
+
+int gn_silu_rows(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16, int64_t N,
+                 int64_t L, int64_t C, int64_t G, float eps, int apply_silu, void *stream)
+{
+    return run(x_bf16, gamma, beta, y_bf16, N, L, C, G, eps, apply_silu, nullptr, nullptr, nullptr, 0,
+               GN_VARIANT_AUTO, stream);
+}
+
+int gn_silu_nhwc(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16, int64_t N,
+                 int64_t H, int64_t W, int64_t C, int64_t G, float eps, int apply_silu, void *stream)
+{
+    if (H < 1 || W < 1 || H > INT64_MAX / W) {
+        if (!x_bf16 || !gamma || !beta || !y_bf16) return GN_ERR_NULL;
+        return GN_ERR_SHAPE;
+    }
+    return gn_silu_rows(x_bf16, gamma, beta, y_bf16, N, H * W, C, G, eps, apply_silu, stream);
+}
+
+size_t gn_silu_workspace_bytes(int64_t N, int64_t L, int64_t C, int64_t G)
+{
+    if (N < 1 || L < 1 || N > INT64_MAX / L || N * L > INT64_MAX / (2 * 2048)) return 0;
+    if (C < 8 || C > 2048 || (C & (C - 1)) != 0 || G < 1 || C % G != 0) return 0;
+    int dev = -1;
+    DeviceInfo d;
+    if (current_device(&dev, &d) != GN_OK) return 0;
+    return workspace_bytes_any(N, L, C, G, d);
+}
+
+int gn_silu_pick_variant(int64_t N, int64_t L, int64_t C, int64_t G)
+{
+    if (N < 1 || L < 1 || N > INT64_MAX / L) return -GN_ERR_SHAPE;
+    if (C < 8 || C > 2048 || (C & (C - 1)) != 0 || G < 1 || C % G != 0) return -GN_ERR_CHANNELS;
+    int dev = -1;
+    DeviceInfo d;
+    const int rc = current_device(&dev, &d);
+    if (rc != GN_OK) return -rc;
+    Plan p;
+    const int r = resolve_variant(GN_VARIANT_AUTO, N, L, C, G, d, &p);
+    return r == GN_OK ? p.kind : -r;
+}
+
+uint64_t gn_kernel_launch_count(void) { return g_launches.load(); }
+
+int gn_device_status(int clear)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_DEVICE;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return GN_ERR_CUDA;
+    unsigned int st = 0;
+    if (gn::read_device_status(&st) != cudaSuccess) return GN_ERR_CUDA;
+    if (clear) {
+        if (gn::clear_device_status() != cudaSuccess) return GN_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (auto &kv : g_workspaces) {
+            if (kv.first.first == dev && kv.second.ptr && cudaMemset(kv.second.ptr, 0, 256) != cudaSuccess)
+                return GN_ERR_CUDA;
+        }
+    }
+    return st ? GN_ERR_KERNEL : GN_OK;
+}
+
+const char *gn_status_string(int status)
+{
+    switch (status) {
+    case GN_OK: return "GN_OK: success";
+    case GN_ERR_NULL: return "GN_ERR_NULL: a required pointer is NULL";
+    case GN_ERR_SHAPE: return "GN_ERR_SHAPE: N, L, H or W below 1, or the element count overflows";
+    case GN_ERR_CHANNELS: return "GN_ERR_CHANNELS: C must be a power of two in [8, 2048] and G must divide C";
+    case GN_ERR_ALIGN: return "GN_ERR_ALIGN: x/y need 16-byte, gamma/beta/statistics 4-byte, workspace 256-byte alignment";
+    case GN_ERR_EPS: return "GN_ERR_EPS: eps must be finite and non-negative";
+    case GN_ERR_ALIAS: return "GN_ERR_ALIAS: y overlaps x (other than in place) or another argument";
+    case GN_ERR_WORKSPACE: return "GN_ERR_WORKSPACE: workspace smaller than gn_silu_workspace_bytes()";
+    case GN_ERR_CUDA: return "GN_ERR_CUDA: a CUDA call or kernel launch failed";
+    case GN_ERR_DEVICE: return "GN_ERR_DEVICE: no CUDA device, or the device is not sm_103";
+    case GN_ERR_VARIANT: return "GN_ERR_VARIANT: unknown variant, or it cannot be launched for this shape";
+    case GN_ERR_KERNEL: return "GN_ERR_KERNEL: a kernel gave up a bounded wait";
+    default: return "unknown gn status";
+    }
+}
+
+int gn_abi_version(void) { return 1; }
+
+}  // extern "C"

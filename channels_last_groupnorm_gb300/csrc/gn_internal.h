@@ -1,0 +1,100 @@
+// gn_internal.h -- geometry and launch interface shared by the kernels
+// (gn_kernels.cu) and the C ABI layer (gn_capi.cu).  Not installed.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gn {
+
+constexpr int kConsumers = 256;                 // consumer threads per CTA (8 warps)
+constexpr int kConsumerWarps = kConsumers / 32;
+constexpr int kThreads = kConsumers + 32;       // + one producer warp
+constexpr int kMaxRing = 32;                    // ring slots (one bit each in a 32-bit mask)
+constexpr int kMaxPieceBytes = 16384;
+constexpr int kMinPieceBytes = 1024;
+constexpr int kPartialsPerLane = 16;
+constexpr int kMaxSegments = 32 * kPartialsPerLane;   // segments per batch entry
+constexpr int kScratchBytes = 16384;            // pass-1 CTA reduction scratch
+constexpr int kSyncWords = 64;                  // 256-byte workspace header
+
+// The (N, L, C) tensor is cut into pieces of whole rows (one bulk copy
+// each); the pieces of one batch entry are split into S contiguous
+// segments, and a work item is one (n, segment) pair.
+struct Geom {
+    int64_t N, L;
+    int32_t C, G, Cg, V;          // V = C / 8 sixteen-byte vectors per row
+    int32_t rows_per_piece;
+    int32_t piece_bytes;          // rows_per_piece * C * 2
+    int64_t pieces_per_n;
+    int32_t S;                    // segments per batch entry
+    int32_t ring;                 // ring slots in shared memory
+    int64_t items;                // N * S
+};
+
+struct Args {
+    const uint16_t *x;            // bf16 [N][L][C]
+    uint16_t *y;                  // bf16 [N][L][C]
+    const float *gamma, *beta;    // [C]
+    float eps;
+    uint32_t l2_hints;            // bit 0: pass-2 loads evict_first, bit 1: pass-2
+                                  // stores evict_first, bit 2: pass-1 loads evict_last
+    Geom g;
+    float2 *partial;              // [N][C][S] segment (mean, M2)
+    float2 *chstat;               // [N][C]    channel (mean, M2)   (fused)
+    float2 *st;                   // [N][C]    (scale, shift)       (two-pass)
+    float *mean, *rstd;           // [N][G]
+    unsigned int *sync;           // barrier words (fused)
+    uint64_t timeout_ns;          // bound on every wait
+};
+
+// Byte offsets inside a CTA's dynamic shared memory.
+struct Layout {
+    uint32_t ring, scratch, kvec, st, gstat, bars, flags, total;
+};
+
+enum Kind { kPass1 = 1, kPass2 = 2, kFused = 3 };
+
+__host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(const Geom &g, int kind)
+{
+    Layout s;
+    uint32_t off = static_cast<uint32_t>(g.ring) * static_cast<uint32_t>(g.piece_bytes);
+    s.ring = 0;
+    s.scratch = off;
+    if (kind != kPass2) off += kScratchBytes;
+    s.kvec = off;
+    if (kind != kPass2) off += align_up(4u * g.C, 16);
+    s.st = off;
+    if (kind == kFused) off += 8u * g.C;
+    s.gstat = off;
+    if (kind == kFused) off += align_up(8u * g.G, 16);
+    s.bars = align_up(off, 16);
+    off = s.bars + 16u * g.ring;
+    s.flags = off;
+    off += 16;
+    s.total = off;
+    return s;
+}
+
+// Dynamic shared memory besides the ring, for a given kind.
+inline uint32_t aux_smem_bytes(const Geom &g, int kind)
+{
+    Geom t = g;
+    t.ring = 0;
+    return make_layout(t, kind).total + 16u * kMaxRing;
+}
+
+// Host-side launchers (gn_kernels.cu).  They return the first CUDA error.
+cudaError_t launch_pass1(const Args &a, int grid, cudaStream_t s);
+cudaError_t launch_finalize(const Args &a, cudaStream_t s);
+cudaError_t launch_pass2(const Args &a, int grid, bool silu, cudaStream_t s);
+cudaError_t launch_fused(const Args &a, int grid, bool silu, cudaStream_t s);
+// Maximum co-resident CTAs per SM of the fused kernel with `smem` bytes.
+cudaError_t fused_blocks_per_sm(bool silu, uint32_t smem, int *blocks);
+cudaError_t prepare_kernels(uint32_t max_smem);
+cudaError_t read_device_status(unsigned int *status);
+cudaError_t clear_device_status();
+
+}  // namespace gn

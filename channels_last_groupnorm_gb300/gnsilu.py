@@ -1,0 +1,242 @@
+"""Python binding of libgnsilu (``include/gnsilu.h``): argument marshalling only.
+
+Every step of the computation runs in the CUDA kernels of ``libgnsilu.so``;
+this module checks tensor metadata, takes device pointers and the current
+stream from PyTorch, and calls the C entry point of the same name.  There is
+no CPU or PyTorch fallback: if the library is missing, every entry point
+raises.
+
+Unsupported inputs give ``None``, the contract of the sglang PR #33451 page
+("FLUX.2 VAE decoder fast path behind quality=high", section
+"Modifications", item 2: non-CUDA, grad enabled, non-power-of-two C,
+C > 2048, not channels_last), so callers can fall back to their own path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+import warnings
+
+LIB_NAME = "libgnsilu.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+
+GN_OK = 0
+GN_ERR_NULL = 1
+GN_ERR_SHAPE = 2
+GN_ERR_CHANNELS = 3
+GN_ERR_ALIGN = 4
+GN_ERR_EPS = 5
+GN_ERR_ALIAS = 6
+GN_ERR_WORKSPACE = 7
+GN_ERR_CUDA = 8
+GN_ERR_DEVICE = 9
+GN_ERR_VARIANT = 10
+GN_ERR_KERNEL = 11
+
+VARIANT_AUTO = 0
+VARIANT_TWO_PASS = 1
+VARIANT_FUSED = 2
+
+# statuses that mean "this input is not supported" (the caller falls back)
+UNSUPPORTED = {GN_ERR_SHAPE, GN_ERR_CHANNELS, GN_ERR_ALIGN, GN_ERR_EPS, GN_ERR_ALIAS}
+
+EXPORTS = {
+    # name: (restype, argtypes)
+    "gn_silu_nhwc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 5
+                     + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "gn_silu_rows": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4
+                     + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "gn_silu_rows_ex": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4
+                        + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
+    "gn_silu_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4),
+    "gn_silu_pick_variant": (ctypes.c_int, [ctypes.c_int64] * 4),
+    "gn_kernel_launch_count": (ctypes.c_uint64, []),
+    "gn_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "gn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gn_abi_version": (ctypes.c_int, []),
+}
+
+
+class GnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}" if what else status_string(status))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded ``libgnsilu.so`` (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m channels_last_groupnorm_gb300.build` (nvcc, sm_103a)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in EXPORTS.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gn_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------------------
+# raw C entry points (integer device pointers)
+# ---------------------------------------------------------------------------
+def raw_gn_silu_rows_ex(x, gamma, beta, y, N, L, C, G, eps, apply_silu, mean_out=0, rstd_out=0,
+                        workspace=0, workspace_bytes=0, variant=VARIANT_AUTO, stream=0) -> int:
+    return lib().gn_silu_rows_ex(x, gamma, beta, y, N, L, C, G, float(eps), int(apply_silu),
+                                 mean_out or None, rstd_out or None, workspace or None,
+                                 workspace_bytes, variant, stream or None)
+
+
+def raw_gn_silu_rows(x, gamma, beta, y, N, L, C, G, eps, apply_silu, stream=0) -> int:
+    return lib().gn_silu_rows(x, gamma, beta, y, N, L, C, G, float(eps), int(apply_silu),
+                              stream or None)
+
+
+def raw_gn_silu_nhwc(x, gamma, beta, y, N, H, W, C, G, eps, apply_silu, stream=0) -> int:
+    return lib().gn_silu_nhwc(x, gamma, beta, y, N, H, W, C, G, float(eps), int(apply_silu),
+                              stream or None)
+
+
+def gn_silu_workspace_bytes(N: int, L: int, C: int, G: int) -> int:
+    return int(lib().gn_silu_workspace_bytes(N, L, C, G))
+
+
+def gn_silu_pick_variant(N: int, L: int, C: int, G: int) -> int:
+    return int(lib().gn_silu_pick_variant(N, L, C, G))
+
+
+def gn_kernel_launch_count() -> int:
+    return int(lib().gn_kernel_launch_count())
+
+
+def gn_device_status(clear: bool = False) -> int:
+    return int(lib().gn_device_status(int(bool(clear))))
+
+
+def gn_abi_version() -> int:
+    return int(lib().gn_abi_version())
+
+
+# ---------------------------------------------------------------------------
+# tensor entry points
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _affine_ok(t, C, device) -> bool:
+    torch = _torch()
+    return (t is not None and t.is_cuda and t.device == device and t.dtype == torch.float32
+            and t.dim() == 1 and t.numel() == C and t.is_contiguous())
+
+
+def _grad_blocked(*ts) -> bool:
+    torch = _torch()
+    return torch.is_grad_enabled() and any(t is not None and t.requires_grad for t in ts)
+
+
+def _stream_handle(device, stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _finish(rc: int, what: str):
+    if rc == GN_OK:
+        return True
+    if rc in UNSUPPORTED:
+        warnings.warn(f"{what}: unsupported input ({status_string(rc)})", stacklevel=3)
+        return False
+    raise GnError(rc, what)
+
+
+def gn_silu_nhwc(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: bool = True,
+                 out=None, stream=None):
+    """GroupNorm(+SiLU) of a channels_last bf16 CUDA tensor (N, C, H, W).
+
+    Returns y with x's shape and memory format, or None when the input is
+    not supported (the caller then falls back)."""
+    lib()
+    torch = _torch()
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16
+            and x.dim() == 4):
+        return None
+    if not x.is_contiguous(memory_format=torch.channels_last) or _grad_blocked(x, gamma, beta):
+        return None
+    N, C, H, W = x.shape
+    if not (_affine_ok(gamma, C, x.device) and _affine_ok(beta, C, x.device)):
+        return None
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.channels_last)
+    elif not (out.shape == x.shape and out.dtype == x.dtype and out.device == x.device
+              and out.is_contiguous(memory_format=torch.channels_last)):
+        return None
+    with torch.cuda.device(x.device):
+        rc = raw_gn_silu_nhwc(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
+                              N, H, W, C, G, eps, apply_silu, _stream_handle(x.device, stream))
+    return out if _finish(rc, "gn_silu_nhwc") else None
+
+
+def gn_silu_rows(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: bool = True,
+                 out=None, stream=None):
+    """GroupNorm(+SiLU) of contiguous bf16 CUDA rows (N, L, C).  Returns y or
+    None when the input is not supported."""
+    lib()
+    torch = _torch()
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16
+            and x.dim() == 3 and x.is_contiguous()) or _grad_blocked(x, gamma, beta):
+        return None
+    N, L, C = x.shape
+    if not (_affine_ok(gamma, C, x.device) and _affine_ok(beta, C, x.device)):
+        return None
+    if out is None:
+        out = torch.empty_like(x)
+    elif not (out.shape == x.shape and out.dtype == x.dtype and out.device == x.device
+              and out.is_contiguous()):
+        return None
+    with torch.cuda.device(x.device):
+        rc = raw_gn_silu_rows(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
+                              N, L, C, G, eps, apply_silu, _stream_handle(x.device, stream))
+    return out if _finish(rc, "gn_silu_rows") else None
+
+
+def gn_silu_rows_ex(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: bool = True,
+                    out=None, variant: int = VARIANT_AUTO, workspace=None, stream=None):
+    """``gn_silu_rows`` that also returns the fp32 statistics:
+    (y, mean [N, G], rstd [N, G]), or None when unsupported.  ``workspace``
+    is an optional uint8 CUDA tensor (see ``gn_silu_workspace_bytes``)."""
+    lib()
+    torch = _torch()
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16
+            and x.dim() == 3 and x.is_contiguous()) or _grad_blocked(x, gamma, beta):
+        return None
+    N, L, C = x.shape
+    if not (_affine_ok(gamma, C, x.device) and _affine_ok(beta, C, x.device)):
+        return None
+    if out is None:
+        out = torch.empty_like(x)
+    mean = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    rstd = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    with torch.cuda.device(x.device):
+        rc = raw_gn_silu_rows_ex(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
+                                 N, L, C, G, eps, apply_silu, mean.data_ptr(), rstd.data_ptr(),
+                                 ws_ptr, ws_bytes, variant, _stream_handle(x.device, stream))
+    return (out, mean, rstd) if _finish(rc, "gn_silu_rows_ex") else None

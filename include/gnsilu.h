@@ -1,0 +1,148 @@
+/*
+ * gnsilu.h -- C ABI of libgnsilu: channels-last GroupNorm (+SiLU) on GB300.
+ *
+ * The operation (sglang PR #33451, "FLUX.2 VAE decoder fast path behind
+ * quality=high", section "Modifications", item 1): x is bf16 in (N, L, C)
+ * rows with C innermost -- a channels_last (N, C, H, W) tensor seen through a
+ * free permute view, L = H*W.  For each batch entry n and each of the G
+ * channel groups g (Cg = C/G consecutive channels), over the L*Cg elements:
+ *
+ *     mean[n,g] = average of x          var[n,g] = biased variance of x
+ *     rstd[n,g] = 1 / sqrt(var[n,g] + eps)
+ *     scale[n,c] = gamma[c] * rstd[n,g]          (affine folded per channel)
+ *     shift[n,c] = beta[c] - mean[n,g] * scale[n,c]
+ *     y = x * scale + shift, then y = y * sigmoid(y) when apply_silu != 0
+ *
+ * computed as a pass-1 partial reduction, a finalize step and a pass-2
+ * elementwise apply (the two-pass structure on that page), with fp32
+ * statistics and one round-to-nearest-even rounding of y to bf16.
+ *
+ * Supported inputs (the page's "unsupported inputs are rejected" contract,
+ * same section, item 2): C a power of two in [8, 2048], G >= 1 dividing C,
+ * N, L >= 1.  Unsupported inputs return a non-zero status and touch nothing.
+ *
+ * Memory and streams: every pointer argument is a DEVICE pointer owned by
+ * the caller; the library never frees caller memory.  x and y are bf16
+ * (uint16 bit patterns) [N][L][C] contiguous, 16-byte aligned; gamma and
+ * beta are fp32 [C], 4-byte aligned.  y may equal x exactly (in place) but
+ * must not overlap it otherwise, nor overlap gamma or beta.  Work is
+ * enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ * and the call returns without synchronising: a return of GN_OK means the
+ * arguments were valid and the kernels were launched.  Faults that happen
+ * later surface at the caller's next synchronisation, and the kernels'
+ * own bounded-wait failures are reported by gn_device_status().
+ *
+ * Thread safety: calls from several host threads are safe.  Calls on
+ * different streams of one device that use the library's own workspace are
+ * safe (the workspace is kept per device and stream); two calls that share
+ * one caller-provided workspace must not overlap on the GPU.
+ */
+#ifndef GNSILU_H
+#define GNSILU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum gn_status_code {
+    GN_OK = 0,
+    GN_ERR_NULL = 1,       /* a required pointer is NULL */
+    GN_ERR_SHAPE = 2,      /* N, L (or H, W) < 1, or the element count overflows */
+    GN_ERR_CHANNELS = 3,   /* C not a power of two in [8, 2048], G < 1 or C % G != 0 */
+    GN_ERR_ALIGN = 4,      /* x or y not 16-byte aligned; gamma, beta, mean/rstd outputs
+                              not 4-byte aligned; workspace not 256-byte aligned */
+    GN_ERR_EPS = 5,        /* eps not finite or negative */
+    GN_ERR_ALIAS = 6,      /* y overlaps x without being equal to it, or overlaps
+                              gamma, beta or a statistics output */
+    GN_ERR_WORKSPACE = 7,  /* caller workspace smaller than gn_silu_workspace_bytes() */
+    GN_ERR_CUDA = 8,       /* a CUDA runtime call or kernel launch failed */
+    GN_ERR_DEVICE = 9,     /* no CUDA device, or the current device is not sm_103 */
+    GN_ERR_VARIANT = 10,   /* unknown variant, or the fused variant cannot be
+                              launched cooperatively for this shape */
+    GN_ERR_KERNEL = 11     /* gn_device_status(): a kernel gave up a bounded wait */
+};
+
+/* Kernel schedules selectable through gn_silu_rows_ex(). */
+enum gn_variant {
+    GN_VARIANT_AUTO = 0,      /* the library picks (fused when it can launch) */
+    GN_VARIANT_TWO_PASS = 1,  /* three launches: pass 1, finalize, pass 2 */
+    GN_VARIANT_FUSED = 2      /* one cooperative launch: pass 1, grid barrier,
+                                 finalize, grid barrier, pass 2; x re-read from
+                                 shared memory / L2 where it still sits there */
+};
+
+/*
+ * GroupNorm(+SiLU) of a channels_last (N, C, H, W) bf16 tensor, whose memory
+ * is [N][H][W][C].  Identical to gn_silu_rows() with L = H * W (the page's
+ * 4D entry served "via a free permute view").
+ */
+int gn_silu_nhwc(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16,
+                 int64_t N, int64_t H, int64_t W, int64_t C, int64_t G,
+                 float eps, int apply_silu, void *stream);
+
+/*
+ * GroupNorm(+SiLU) of (N, L, C) bf16 rows, channels innermost (the page's
+ * rows entry, "as used by attention").  Uses a workspace the library
+ * allocates on first use for each (device, stream) and grows when a larger
+ * shape arrives; that first call allocates (cudaMalloc) and so should come
+ * before any CUDA graph capture on the stream.
+ */
+int gn_silu_rows(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16,
+                 int64_t N, int64_t L, int64_t C, int64_t G,
+                 float eps, int apply_silu, void *stream);
+
+/*
+ * gn_silu_rows() with the statistics exported and the schedule and the
+ * workspace chosen by the caller.
+ *   mean_out, rstd_out : device fp32 [N * G] (index n * G + g), or NULL.
+ *   workspace          : device memory of at least
+ *                        gn_silu_workspace_bytes(N, L, C, G) bytes, 256-byte
+ *                        aligned, whose first 256 bytes are zero before its
+ *                        first use (cudaMemset once; the kernels leave them
+ *                        zero again after every successful call).  NULL
+ *                        selects the library's own workspace.
+ *   variant            : enum gn_variant.
+ */
+int gn_silu_rows_ex(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16,
+                    int64_t N, int64_t L, int64_t C, int64_t G,
+                    float eps, int apply_silu,
+                    float *mean_out, float *rstd_out,
+                    void *workspace, size_t workspace_bytes, int variant, void *stream);
+
+/* Workspace bytes gn_silu_rows_ex() needs for this shape on the CURRENT
+ * device (any variant).  Returns 0 if the shape is unsupported or there is
+ * no usable device. */
+size_t gn_silu_workspace_bytes(int64_t N, int64_t L, int64_t C, int64_t G);
+
+/* The variant GN_VARIANT_AUTO resolves to for this shape on the current
+ * device, or a negative status code. */
+int gn_silu_pick_variant(int64_t N, int64_t L, int64_t C, int64_t G);
+
+/* Number of CUDA kernels this library launched since the process started
+ * (all devices, all streams). */
+uint64_t gn_kernel_launch_count(void);
+
+/* Synchronises the current device, then returns GN_OK or GN_ERR_KERNEL if
+ * one of this library's kernels gave up a bounded wait since the last clear
+ * (GN_ERR_CUDA / GN_ERR_DEVICE if the device itself reports an error).
+ * Kernels launched while that flag is set return at once without writing
+ * any output.  clear != 0 resets the flag and re-zeroes the library's own
+ * workspaces on this device; a caller-provided workspace must then be
+ * re-zeroed by the caller. */
+int gn_device_status(int clear);
+
+/* Human-readable name of a status code (static storage). */
+const char *gn_status_string(int status);
+
+/* ABI version of this header: 1. */
+int gn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GNSILU_H */

@@ -1,0 +1,146 @@
+"""The C-ABI library on the host, without a GPU: it loads, exports every
+symbol the header declares, and rejects each kind of unsupported input with
+its status code before any CUDA call."""
+import math
+import os
+import re
+
+import pytest
+import torch
+
+from channels_last_groupnorm_gb300 import build as gnbuild
+from channels_last_groupnorm_gb300 import gnsilu as gs
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "gnsilu.h")
+
+X = 0x10000000          # stand-in device addresses (never dereferenced: every call
+Y = 0x20000000          # below is rejected before the library touches the device)
+GAM = 0x30000000
+BET = 0x30001000
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="valid stand-in pointers must never reach a real GPU")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gnbuild.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(gn_[a-z_0-9]+)\s*\(", text, re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    assert {"gn_silu_nhwc", "gn_silu_rows", "gn_silu_rows_ex", "gn_silu_workspace_bytes",
+            "gn_status_string", "gn_device_status", "gn_kernel_launch_count"} <= names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = gs.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(gs.EXPORTS)
+
+
+def test_abi_version_and_status_strings():
+    assert gs.gn_abi_version() == 1
+    for code in range(12):
+        s = gs.status_string(code)
+        assert s.startswith("GN_"), (code, s)
+    assert "unknown" in gs.status_string(99)
+
+
+def rows(**kw):
+    a = dict(x=X, gamma=GAM, beta=BET, y=Y, N=1, L=4, C=32, G=32, eps=1e-6, apply_silu=1)
+    a.update(kw)
+    return gs.raw_gn_silu_rows(a["x"], a["gamma"], a["beta"], a["y"], a["N"], a["L"], a["C"],
+                               a["G"], a["eps"], a["apply_silu"])
+
+
+def rows_ex(**kw):
+    a = dict(x=X, gamma=GAM, beta=BET, y=Y, N=1, L=4, C=32, G=32, eps=1e-6, apply_silu=1,
+             mean_out=0, rstd_out=0, workspace=0, workspace_bytes=0, variant=0)
+    a.update(kw)
+    return gs.raw_gn_silu_rows_ex(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=0), gs.GN_ERR_NULL),
+    (dict(y=0), gs.GN_ERR_NULL),
+    (dict(gamma=0), gs.GN_ERR_NULL),
+    (dict(beta=0), gs.GN_ERR_NULL),
+    (dict(N=0), gs.GN_ERR_SHAPE),
+    (dict(L=0), gs.GN_ERR_SHAPE),
+    (dict(N=-3), gs.GN_ERR_SHAPE),
+    (dict(N=1 << 40, L=1 << 40), gs.GN_ERR_SHAPE),
+    (dict(C=7, G=7), gs.GN_ERR_CHANNELS),
+    (dict(C=12, G=4), gs.GN_ERR_CHANNELS),
+    (dict(C=4, G=4), gs.GN_ERR_CHANNELS),
+    (dict(C=4096, G=32), gs.GN_ERR_CHANNELS),
+    (dict(C=64, G=0), gs.GN_ERR_CHANNELS),
+    (dict(C=64, G=3), gs.GN_ERR_CHANNELS),
+    (dict(C=64, G=128), gs.GN_ERR_CHANNELS),
+    (dict(x=X + 8), gs.GN_ERR_ALIGN),
+    (dict(y=Y + 2), gs.GN_ERR_ALIGN),
+    (dict(gamma=GAM + 2), gs.GN_ERR_ALIGN),
+    (dict(beta=BET + 1), gs.GN_ERR_ALIGN),
+    (dict(eps=math.nan), gs.GN_ERR_EPS),
+    (dict(eps=math.inf), gs.GN_ERR_EPS),
+    (dict(eps=-1e-6), gs.GN_ERR_EPS),
+    (dict(y=X + 16), gs.GN_ERR_ALIAS),
+    (dict(y=X - 16), gs.GN_ERR_ALIAS),
+    (dict(gamma=Y + 64), gs.GN_ERR_ALIAS),
+    (dict(beta=Y), gs.GN_ERR_ALIAS),
+])
+def test_rows_rejects(kw, code):
+    assert rows(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(variant=3), gs.GN_ERR_VARIANT),
+    (dict(variant=-1), gs.GN_ERR_VARIANT),
+    (dict(workspace=0x40000010, workspace_bytes=1 << 20), gs.GN_ERR_ALIGN),
+    (dict(mean_out=0x50000002), gs.GN_ERR_ALIGN),
+    (dict(mean_out=Y + 32), gs.GN_ERR_ALIAS),
+    (dict(mean_out=0x50000000, rstd_out=0x50000000 + 64), gs.GN_ERR_ALIAS),
+])
+def test_rows_ex_rejects(kw, code):
+    assert rows_ex(**kw) == code
+
+
+@pytest.mark.parametrize("H,W,code", [(0, 4, gs.GN_ERR_SHAPE), (4, -1, gs.GN_ERR_SHAPE),
+                                      (1 << 40, 1 << 40, gs.GN_ERR_SHAPE)])
+def test_nhwc_rejects_bad_spatial_shape(H, W, code):
+    assert gs.raw_gn_silu_nhwc(X, GAM, BET, Y, 1, H, W, 32, 32, 1e-6, 1) == code
+
+
+def test_nhwc_null_before_shape():
+    assert gs.raw_gn_silu_nhwc(0, GAM, BET, Y, 1, 0, 4, 32, 32, 1e-6, 1) == gs.GN_ERR_NULL
+
+
+@no_gpu
+def test_valid_arguments_without_a_device_report_no_device():
+    assert rows() == gs.GN_ERR_DEVICE
+    assert rows(y=X) == gs.GN_ERR_DEVICE          # in place is allowed
+    assert gs.gn_silu_workspace_bytes(1, 4, 32, 32) == 0
+    assert gs.gn_silu_pick_variant(1, 4, 32, 32) == -gs.GN_ERR_DEVICE
+
+
+def test_workspace_query_rejects_bad_shapes():
+    assert gs.gn_silu_workspace_bytes(1, 4, 12, 4) == 0
+    assert gs.gn_silu_workspace_bytes(0, 4, 32, 32) == 0
+    assert gs.gn_silu_pick_variant(1, 4, 12, 4) == -gs.GN_ERR_CHANNELS
+
+
+def test_tensor_binding_returns_none_for_cpu_tensors():
+    x = torch.zeros(1, 32, 2, 2, dtype=torch.bfloat16).to(memory_format=torch.channels_last)
+    g = torch.ones(32)
+    assert gs.gn_silu_nhwc(x, g, g) is None
+    assert gs.gn_silu_rows(x.reshape(1, 4, 32), g, g) is None
+    assert gs.gn_silu_rows_ex(x.reshape(1, 4, 32), g, g) is None
+
+
+def test_launch_counter_starts_readable():
+    assert gs.gn_kernel_launch_count() >= 0
