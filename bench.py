@@ -380,11 +380,15 @@ def run_ours(args):
     achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
     traffic = recorded_traffic(w.name, r["variant"])
 
-    e2e_s, h2d, d2h = measure_e2e(w, variant_id, max(5, args.steps // 2), args.warmup, device,
-                                  stream)
-    e2e_steps = max(5, args.steps // 2)
-    e2e_elapsed, e2e_units = reduce_timing(e2e_s, 4.0 * w.elements * e2e_steps,
-                                           device=device if world > 1 else None)
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(5, args.steps // 2)
+        e2e_s, h2d, d2h = measure_e2e(w, variant_id, e2e_steps, args.warmup, device, stream)
+        e2e_elapsed, e2e_units = reduce_timing(e2e_s, 4.0 * w.elements * e2e_steps,
+                                               device=device if world > 1 else None)
+        e2e = {"value": round(e2e_units / e2e_elapsed / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "us_per_call": round(e2e_s * 1e6 / e2e_steps, 2)}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -405,9 +409,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "launch_us_mean": round(launch_ms * 1e3, 3),
                      "launch_us_median": round(statistics.median(per) * 1e3, 3)},
-        "e2e": {"value": round(e2e_units / e2e_elapsed / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "us_per_call": round(e2e_s * 1e6 / e2e_steps, 2)},
+        "e2e": e2e,
         "gpu_launches": int(r["launches"]),
         "clocks": r["clocks"],
     }
@@ -481,6 +483,8 @@ def main(argv=None):
                     help="seconds of untimed calls while the clock sampler runs")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end measurement (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
