@@ -135,6 +135,44 @@ uint64_t gn_kernel_launch_count(void);
  * re-zeroed by the caller. */
 int gn_device_status(int clear);
 
+/* Size of the fixed scratch array used by gn_silu_rows_static(): 8 MiB. */
+#define GN_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * gn_silu_rows_ex() for callers that cannot allocate device memory.  (This
+ * entry point has no counterpart on the sglang PR #33451 page; it is a
+ * deployment convenience of this library.)
+ *
+ * Who needs it: code running while a CUDA graph is captured in global
+ * capture mode, where allocation calls are not allowed; plug-ins whose host
+ * framework owns every byte of device memory; latency-critical paths that
+ * cannot afford an allocator's implicit synchronisation.  gn_silu_rows()
+ * allocates its workspace on first use, and gn_silu_rows_ex() needs one from
+ * the caller; this entry point needs neither.
+ *
+ * The scratch (partial statistics and grid-barrier words) comes from one
+ * fixed array of GN_STATIC_SCRATCH_BYTES compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  No call
+ * to cudaMalloc, cudaFree or any other allocating routine is made.
+ *   - Shapes whose scratch need (gn_silu_workspace_bytes) exceeds
+ *     GN_STATIC_SCRATCH_BYTES are refused with GN_ERR_WORKSPACE and nothing
+ *     runs.  With C = 2048 that still covers N up to about 8 on a GB300.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls on a device share the one array, which keeps the previous
+ *     call's contents; each call clears the words that must start at zero
+ *     (an asynchronous memset on `stream`).  Calls whose GPU work overlaps
+ *     -- on different streams, or from different host threads -- race on
+ *     the array and must be serialised by the caller.
+ * Arguments, outputs, statistics and status codes are those of
+ * gn_silu_rows_ex() with the automatic schedule.
+ */
+int gn_silu_rows_static(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16,
+                        int64_t N, int64_t L, int64_t C, int64_t G,
+                        float eps, int apply_silu,
+                        float *mean_out, float *rstd_out, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gn_status_string(int status);
 
