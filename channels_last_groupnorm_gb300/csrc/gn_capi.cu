@@ -159,10 +159,9 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     g.Cg = static_cast<int32_t>(C / G);
     g.V = static_cast<int32_t>(C / 8);
     const int64_t row_bytes = 2 * C;
-    const int per_sm = (kind == GN_VARIANT_FUSED) ? 1 : 2;
-    const int64_t grid_target = static_cast<int64_t>(d.sm_count) * per_sm;
+    const int64_t grid_target = d.sm_count;   // one CTA per SM (544 threads, most of shared memory)
     const int64_t total_bytes = N * L * row_bytes;
-    // pieces as large as 16 KB, smaller when that leaves fewer than about
+    // pieces as large as 32 KB, smaller when that leaves fewer than about
     // four pieces per CTA; never below one row
     int64_t pb = gn::kMaxPieceBytes;
     while (pb > row_bytes && pb > gn::kMinPieceBytes && total_bytes / pb < 4 * grid_target) pb /= 2;
@@ -173,13 +172,15 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     int64_t S = grid_target / N;
     if (S < 1) S = 1;
     if (S > g.pieces_per_n) S = g.pieces_per_n;
-    if (S > gn::kMaxSegments) S = gn::kMaxSegments;
+    const int64_t max_seg = (kind == GN_VARIANT_FUSED) ? gn::kFusedMaxSegments : gn::kMaxSegments;
+    if (S > max_seg) S = max_seg;
     g.S = static_cast<int32_t>(S);
+    g.seg32 = (g.pieces_per_n * S < (int64_t(1) << 32)) ? 1 : 0;
     g.items = N * S;
     p.grid = static_cast<int>(g.items < grid_target ? g.items : grid_target);
     // ring depth from the shared memory left next to the auxiliary arrays
     const int kind_smem = (kind == GN_VARIANT_FUSED) ? gn::kFused : gn::kPass1;
-    const int64_t budget = (kind == GN_VARIANT_FUSED) ? d.smem_optin : (d.smem_per_sm / per_sm - 1024);
+    const int64_t budget = d.smem_optin;
     int64_t ring = (budget - static_cast<int64_t>(gn::aux_smem_bytes(g, kind_smem))) / pb;
     if (ring > gn::kMaxRing) ring = gn::kMaxRing;
     g.ring = static_cast<int32_t>(ring);
@@ -399,6 +400,25 @@ int gn_device_status(int clear)
         }
     }
     return st ? GN_ERR_KERNEL : GN_OK;
+}
+
+int gn_selftest_bounded_wait(int mode, int timeout_ms, int *done, int blocks, void *stream)
+{
+    if (mode < 0 || mode > 1 || timeout_ms < 0 || timeout_ms > 10000 || blocks < 1 || blocks > 1024)
+        return GN_ERR_SHAPE;
+    if (!done) return GN_ERR_NULL;
+    int dev = -1;
+    DeviceInfo d;
+    const int rc = current_device(&dev, &d);
+    if (rc != GN_OK) return rc;
+    const cudaError_t e = gn::launch_selftest_wait(mode, static_cast<uint64_t>(timeout_ms) * 1000000ull, done,
+                                                   blocks, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    g_launches.fetch_add(1);
+    return GN_OK;
 }
 
 const char *gn_status_string(int status)

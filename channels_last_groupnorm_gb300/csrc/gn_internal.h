@@ -7,14 +7,15 @@
 
 namespace gn {
 
-constexpr int kConsumers = 256;                 // consumer threads per CTA (8 warps)
+constexpr int kConsumers = 512;                 // consumer threads per CTA (16 warps)
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kThreads = kConsumers + 32;       // + one producer warp
 constexpr int kMaxRing = 32;                    // ring slots (one bit each in a 32-bit mask)
-constexpr int kMaxPieceBytes = 16384;
+constexpr int kMaxPieceBytes = 32768;
+constexpr int kMaxVecPerThread = kMaxPieceBytes / 16 / kConsumers;   // 16-byte vectors per thread per piece
 constexpr int kMinPieceBytes = 1024;
-constexpr int kPartialsPerLane = 16;
-constexpr int kMaxSegments = 32 * kPartialsPerLane;   // segments per batch entry
+constexpr int kMaxSegments = 512;               // segments per batch entry
+constexpr int kFusedMaxSegments = 160;          // ... in the fused kernel (5 records per lane)
 constexpr int kScratchBytes = 16384;            // pass-1 CTA reduction scratch
 constexpr int kSyncWords = 64;                  // 256-byte workspace header
 
@@ -30,6 +31,7 @@ struct Geom {
     int32_t S;                    // segments per batch entry
     int32_t ring;                 // ring slots in shared memory
     int64_t items;                // N * S
+    int32_t seg32;                // pieces_per_n * S < 2^32: segment bounds in 32-bit math
 };
 
 struct Args {
@@ -48,9 +50,10 @@ struct Args {
     uint64_t timeout_ns;          // bound on every wait
 };
 
-// Byte offsets inside a CTA's dynamic shared memory.
+// Byte offsets inside a CTA's dynamic shared memory.  `gstat` (per-group
+// mean / rstd of the fused kernel) shares the pass-1 scratch.
 struct Layout {
-    uint32_t ring, scratch, kvec, st, gstat, bars, flags, total;
+    uint32_t ring, scratch, kvec, st, gb, gstat, bars, flags, total;
 };
 
 enum Kind { kPass1 = 1, kPass2 = 2, kFused = 3 };
@@ -63,13 +66,14 @@ __host__ __device__ inline Layout make_layout(const Geom &g, int kind)
     uint32_t off = static_cast<uint32_t>(g.ring) * static_cast<uint32_t>(g.piece_bytes);
     s.ring = 0;
     s.scratch = off;
+    s.gstat = off;
     if (kind != kPass2) off += kScratchBytes;
     s.kvec = off;
     if (kind != kPass2) off += align_up(4u * g.C, 16);
     s.st = off;
     if (kind == kFused) off += 8u * g.C;
-    s.gstat = off;
-    if (kind == kFused) off += align_up(8u * g.G, 16);
+    s.gb = off;
+    if (kind == kFused) off += 8u * g.C;
     s.bars = align_up(off, 16);
     off = s.bars + 16u * g.ring;
     s.flags = off;
@@ -94,6 +98,7 @@ cudaError_t launch_fused(const Args &a, int grid, bool silu, cudaStream_t s);
 // Maximum co-resident CTAs per SM of the fused kernel with `smem` bytes.
 cudaError_t fused_blocks_per_sm(bool silu, uint32_t smem, int *blocks);
 cudaError_t prepare_kernels(uint32_t max_smem);
+cudaError_t launch_selftest_wait(int mode, uint64_t timeout_ns, int *done, int blocks, cudaStream_t s);
 cudaError_t read_device_status(unsigned int *status);
 cudaError_t clear_device_status();
 

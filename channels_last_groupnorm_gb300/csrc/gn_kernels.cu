@@ -8,20 +8,22 @@
 // pass-2 elementwise apply with optional SiLU.
 //
 // GB300 design:
-//  * The tensor is cut into "pieces" of whole rows (up to 16 KB); each CTA
+//  * The tensor is cut into "pieces" of whole rows (up to 32 KB); each CTA
 //    streams its pieces through a ring of shared-memory slots filled by bulk
 //    TMA copies (cp.async.bulk) issued by one producer thread, completion
-//    tracked on mbarriers.  Eight consumer warps read 16-byte vectors from
+//    tracked on mbarriers.  Sixteen consumer warps read 16-byte vectors from
 //    shared memory; with C a power of two each consumer thread always sees
-//    the same eight channels.
+//    the same eight channels.  Arithmetic on channel pairs uses the packed
+//    fp32x2 instructions of sm_100+ (add/sub/mul/fma .f32x2).
 //  * Pass 1 keeps, per thread, fp32 sums of (x - K) and (x - K)^2 with K a
 //    per-(work item, channel) shift (the item's first row), then reduces
 //    them per CTA with warp shuffles and shared memory into a per-segment
 //    (mean, M2) record.  Segments are merged with Chan's parallel formula,
 //    first over segments per channel, then over the channels of a group.
-//  * Pass 2 rewrites each piece in place in shared memory and sends it back
-//    with a bulk TMA store; pieces are visited in the reverse of pass-1 order
-//    so the most recently read rows (still in L2) come first.
+//  * Pass 2 loads pieces the same way, in the reverse of pass-1 order so the
+//    most recently read rows (still in L2) come first; each consumer thread
+//    takes its vectors out of the slot, releases the slot at once, and
+//    writes y with coalesced 16-byte global stores.
 //  * The fused kernel does all three steps in one cooperative launch with two
 //    grid barriers; pieces still in the ring after pass 1 are not re-read.
 //  * Every wait (mbarrier phase, grid barrier) is bounded by a deadline on
@@ -39,6 +41,66 @@ namespace gn {
 __device__ unsigned int g_status;
 
 // ---------------------------------------------------------------------------
+// packed fp32 pairs (sm_100+ f32x2 arithmetic)
+// ---------------------------------------------------------------------------
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t pk(float lo, float hi)
+{
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void upk(f2_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f2_t sub2(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c)
+{
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// the two bf16 values packed in a 32-bit word, widened exactly to fp32
+__device__ __forceinline__ f2_t bf2_to_f2(uint32_t w)
+{
+    return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// round a pair to bf16 (nearest even) and pack it, low half first
+__device__ __forceinline__ uint32_t f2_to_bf2(f2_t v)
+{
+    float lo, hi;
+    upk(v, lo, hi);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// ---------------------------------------------------------------------------
 // work-item cursor
 // ---------------------------------------------------------------------------
 struct Cursor {
@@ -49,21 +111,28 @@ struct Cursor {
     int64_t k;         // current piece
 };
 
+// first piece of segment s (segments split the pieces of a batch entry as
+// evenly as integer division allows)
+__device__ __forceinline__ int64_t segment_first_piece(const Geom &g, int32_t s)
+{
+    if (g.seg32)
+        return static_cast<uint32_t>(s) * static_cast<uint32_t>(g.pieces_per_n) / static_cast<uint32_t>(g.S);
+    return static_cast<int64_t>(s) * g.pieces_per_n / g.S;
+}
+
 __device__ __forceinline__ void load_item(const Geom &g, Cursor &c, int64_t it)
 {
     c.it = it;
     c.n = it / g.S;
     c.s = static_cast<int32_t>(it - c.n * g.S);
-    c.p0 = static_cast<int64_t>(c.s) * g.pieces_per_n / g.S;
-    c.p1 = static_cast<int64_t>(c.s + 1) * g.pieces_per_n / g.S;
+    c.p0 = segment_first_piece(g, c.s);
+    c.p1 = segment_first_piece(g, c.s + 1);
 }
 
 __device__ __forceinline__ int64_t segment_rows(const Geom &g, int32_t s)
 {
-    const int64_t p0 = static_cast<int64_t>(s) * g.pieces_per_n / g.S;
-    const int64_t p1 = static_cast<int64_t>(s + 1) * g.pieces_per_n / g.S;
-    const int64_t r0 = p0 * g.rows_per_piece;
-    const int64_t r1 = min(p1 * g.rows_per_piece, g.L);
+    const int64_t r0 = segment_first_piece(g, s) * g.rows_per_piece;
+    const int64_t r1 = min(segment_first_piece(g, s + 1) * g.rows_per_piece, g.L);
     return r1 - r0;
 }
 
@@ -155,48 +224,49 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
     }
 }
 
-// Grid-wide barrier for the cooperative fused kernel: one arrival per CTA on
-// a gpu-scope counter, then a bounded spin until `target` arrivals.
+// Grid-wide barrier for the cooperative fused kernel: one release-arrival
+// per CTA on a gpu-scope counter, then a bounded acquire-spin until `target`
+// arrivals.  The CTA barrier before the arrival orders every thread's
+// earlier global writes before it.
 __device__ __forceinline__ bool grid_sync(unsigned int *counter, unsigned int target, const Ctl &ctl)
 {
     __syncthreads();
     if (threadIdx.x == 0 && !*ctl.abort) {
-        __threadfence();
         atom_add_release_gpu(counter, 1u);
-        const uint64_t deadline = global_ns() + ctl.timeout_ns;
+        uint64_t deadline = 0;
 #pragma unroll 1
         for (uint32_t it = 0;; ++it) {
             if (ld_acquire_gpu(counter) >= target) break;
-            if ((it & 15u) == 15u && global_ns() > deadline) {
-                record_timeout(ctl);
-                break;
+            if ((it & 63u) == 63u) {
+                const uint64_t now = global_ns();
+                if (deadline == 0) {
+                    deadline = now + ctl.timeout_ns;
+                } else if (now > deadline) {
+                    record_timeout(ctl);
+                    break;
+                }
             }
-            __nanosleep(40);
         }
-        __threadfence();
     }
     __syncthreads();
     return !*ctl.abort;
 }
 
 // ---------------------------------------------------------------------------
-// bf16 helpers
+// SiLU on a pair: z * sigmoid(z), sigmoid from one ex2 and one reciprocal
+// per element (MUFU approximations, a few ulp in fp32; the MUFU pipes of an
+// SM retire about 32 of these per clock, so two per element stay well
+// below the element rate the memory system can feed)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+__device__ __forceinline__ f2_t silu2(f2_t z)
 {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x (low half) = lo
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-// SiLU(z) = z * sigmoid(z), sigmoid from one ex2 and one reciprocal (both
-// hardware approximations, a few ulp in fp32).
-__device__ __forceinline__ float silu(float z)
-{
-    const float e = ex2_approx(z * -1.4426950408889634f);   // exp(-z)
-    return z * rcp_approx(1.0f + e);
+    const f2_t t = mul2(z, pk(-1.4426950408889634f, -1.4426950408889634f));   // -z*log2(e)
+    float t0, t1;
+    upk(t, t0, t1);
+    const f2_t d = add2(pk(ex2_approx(t0), ex2_approx(t1)), pk(1.0f, 1.0f));    // 1 + exp(-z)
+    float d0, d1;
+    upk(d, d0, d1);
+    return mul2(z, pk(rcp_approx(d0), rcp_approx(d1)));
 }
 
 // ---------------------------------------------------------------------------
@@ -206,8 +276,9 @@ struct Smem {
     uint8_t *base;
     Layout lay;
     uint32_t ring_s;                       // shared address of the ring
-    __device__ uint32_t full(int slot) const { return smem_addr(base + lay.bars) + 16u * slot; }
-    __device__ uint32_t empty(int slot) const { return full(slot) + 8u; }
+    uint32_t bars_s;                       // shared address of the mbarriers
+    __device__ uint32_t full(int slot) const { return bars_s + 16u * slot; }
+    __device__ uint32_t empty(int slot) const { return bars_s + 16u * slot + 8u; }
     __device__ uint32_t slot_addr(int slot, int piece_bytes) const
     {
         return ring_s + static_cast<uint32_t>(slot) * static_cast<uint32_t>(piece_bytes);
@@ -273,57 +344,33 @@ __device__ void produce_pass1(const Args &a, const Smem &sm, int64_t T, Producer
 }
 
 // ---------------------------------------------------------------------------
-// producer (one thread): pass-2 loads and stores, pieces in reverse order.
-// `resident` pieces (the last ones of pass 1, fused kernel only) are still
-// in their ring slots and are not loaded again.
+// producer (one thread): pass-2 loads, pieces in reverse order.  `resident`
+// pieces (the last ones of pass 1, fused kernel only) are still in their
+// ring slots and are not loaded again.  A slot is refilled as soon as the
+// consumers have read it (they write y straight to global memory).
 // ---------------------------------------------------------------------------
 __device__ void produce_pass2(const Args &a, const Smem &sm, int64_t T, int64_t resident,
                               ProducerState &ps, const Ctl &ctl)
 {
     const Geom &g = a.g;
     if (T == 0) return;
-    const bool hint_ld = (a.l2_hints & 1u) != 0;
-    const bool hint_st = (a.l2_hints & 2u) != 0;
-    const uint64_t pol = (hint_ld || hint_st) ? policy_evict_first() : 0;
-    Cursor ld, st;
+    const bool hint = (a.l2_hints & 1u) != 0;
+    const uint64_t pol = hint ? policy_evict_first() : 0;
+    Cursor ld;
     cursor_last(g, ld);
-    cursor_last(g, st);
-    int slot = slot_of(T - 1, g.ring);        // slot of the load cursor's piece
-    int st_slot = slot;                       // slot of the store cursor's piece
-    bool ok = !*ctl.abort;
-
-    auto store_next = [&]() {
-        if (ok) ok = wait_phase(sm.empty(st_slot), (ps.empty_par >> st_slot) & 1u, ctl);
-        if (ok) {
-            ps.empty_par ^= 1u << st_slot;
-            const uint32_t bytes =
-                static_cast<uint32_t>(piece_rows(g, st.k)) * static_cast<uint32_t>(g.C) * 2u;
-            uint16_t *dst = a.y + piece_elem_offset(g, st.n, st.k);
-            if (hint_st)
-                bulk_store_hint(dst, sm.slot_addr(st_slot, g.piece_bytes), bytes, pol);
-            else
-                bulk_store(dst, sm.slot_addr(st_slot, g.piece_bytes), bytes);
-            bulk_commit();
-        }
-        cursor_prev(g, st);
-        st_slot = (st_slot == 0) ? g.ring - 1 : st_slot - 1;
-    };
-
-    int64_t stored = 0;
+    int slot = slot_of(T - 1, g.ring);
     for (int64_t q = T - 1; q >= 0; --q) {
         if (q < T - resident) {
             if (q + g.ring < T) {
-                store_next();
-                ++stored;
-                bulk_wait_read_all();     // the slot's bytes have left shared memory
+                // the slot still holds piece q + ring, processed earlier
+                if (!wait_phase(sm.empty(slot), (ps.empty_par >> slot) & 1u, ctl)) return;
+                ps.empty_par ^= 1u << slot;
             }
-            if (ok) issue_load(a, sm, ld, slot, ps, pol, hint_ld);
+            issue_load(a, sm, ld, slot, ps, pol, hint);
         }
         cursor_prev(g, ld);
         slot = (slot == 0) ? g.ring - 1 : slot - 1;
     }
-    for (; stored < T; ++stored) store_next();
-    bulk_wait_all();
 }
 
 // After an abort, let every load this producer issued land before the CTA
@@ -347,10 +394,22 @@ __device__ void drain_loads(const Smem &sm, const ProducerState &ps, int ring)
 // ---------------------------------------------------------------------------
 // consumers: pass 1
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_entry(float *scr, int idx, const float (&v1)[8], const float (&v2)[8])
+{
+    float4 *dst = reinterpret_cast<float4 *>(scr + idx * 16);
+    dst[0] = make_float4(v1[0], v1[1], v1[2], v1[3]);
+    dst[1] = make_float4(v1[4], v1[5], v1[6], v1[7]);
+    dst[2] = make_float4(v2[0], v2[1], v2[2], v2[3]);
+    dst[3] = make_float4(v2[4], v2[5], v2[6], v2[7]);
+}
+
 // Reduce the per-thread shifted sums of one work item into the item's
-// per-channel (mean, M2) record.
-__device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, const float (&s1)[8],
-                            const float (&s2)[8])
+// per-channel (mean, M2) record.  Threads that share a vector slot first
+// combine by warp shuffles (when the slot repeats inside a warp), then
+// through shared memory; when the scratch cannot hold every entry at once,
+// the upper half of the entries is first added into the lower half.
+__device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, const f2_t (&s1p)[4],
+                            const f2_t (&s2p)[4])
 {
     const Geom &g = a.g;
     const int tid = threadIdx.x;
@@ -358,12 +417,12 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
     const int warp = tid >> 5;
     float v1[8], v2[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        v1[j] = s1[j];
-        v2[j] = s2[j];
+    for (int i = 0; i < 4; ++i) {
+        upk(s1p[i], v1[2 * i], v1[2 * i + 1]);
+        upk(s2p[i], v2[2 * i], v2[2 * i + 1]);
     }
     int entries, entry;
-    bool writer;
+    bool holder;   // this thread holds one entry of its slot
     if (g.V < 32) {
         for (int off = g.V; off < 32; off <<= 1) {
 #pragma unroll
@@ -374,20 +433,33 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
         }
         entries = kConsumerWarps;
         entry = warp;
-        writer = lane < g.V;
+        holder = lane < g.V;
     } else {
         entries = kConsumers / g.V;
         entry = tid / g.V;
-        writer = true;
+        holder = true;
     }
     float *scr = reinterpret_cast<float *>(sm.base + sm.lay.scratch);
-    if (writer) {
-        float4 *dst = reinterpret_cast<float4 *>(scr + (entry * g.V + (tid % g.V)) * 16);
-        dst[0] = make_float4(v1[0], v1[1], v1[2], v1[3]);
-        dst[1] = make_float4(v1[4], v1[5], v1[6], v1[7]);
-        dst[2] = make_float4(v2[0], v2[1], v2[2], v2[3]);
-        dst[3] = make_float4(v2[4], v2[5], v2[6], v2[7]);
+    const int cap = kScratchBytes / (64 * g.V);   // entries per slot the scratch holds
+    const int vs_own = tid % g.V;
+    int live = entries;
+    while (live > cap) {
+        const int half = live >> 1;
+        if (holder && entry >= half) store_entry(scr, (entry - half) * g.V + vs_own, v1, v2);
+        named_sync(1, kConsumers);
+        if (holder && entry < half) {
+            const float *src = scr + (entry * g.V + vs_own) * 16;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v1[j] += src[j];
+                v2[j] += src[8 + j];
+            }
+        }
+        if (entry >= half) holder = false;
+        named_sync(1, kConsumers);
+        live = half;
     }
+    if (holder) store_entry(scr, entry * g.V + vs_own, v1, v2);
     named_sync(1, kConsumers);
     const float *kvec = reinterpret_cast<const float *>(sm.base + sm.lay.kvec);
     const int64_t r0 = c.p0 * g.rows_per_piece;
@@ -396,7 +468,7 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
     for (int ch = tid; ch < g.C; ch += kConsumers) {
         const int vs = ch >> 3, j = ch & 7;
         float S1 = 0.f, S2 = 0.f;
-        for (int e = 0; e < entries; ++e) {
+        for (int e = 0; e < live; ++e) {
             S1 += scr[(e * g.V + vs) * 16 + j];
             S2 += scr[(e * g.V + vs) * 16 + 8 + j];
         }
@@ -417,13 +489,13 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
     Cursor c;
     cursor_first(g, c);
     int slot = 0;
-    float K[8], s1[8], s2[8];
+    f2_t K[4], s1[4], s2[4];
     bool ok = !*ctl.abort;
     for (int64_t q = 0; q < T; ++q) {
         const bool first = (c.k == c.p0);
         if (first) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s1[j] = s2[j] = 0.f;
+            for (int i = 0; i < 4; ++i) s1[i] = s2[i] = 0ull;
         }
         if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
         full_par ^= 1u << slot;
@@ -431,15 +503,19 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
         if (ok) {
             if (first) {
                 const uint4 w = lds128(base + 16u * vslot);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    K[2 * i] = bf_lo(ws[i]);
-                    K[2 * i + 1] = bf_hi(ws[i]);
-                }
+                K[0] = bf2_to_f2(w.x);
+                K[1] = bf2_to_f2(w.y);
+                K[2] = bf2_to_f2(w.z);
+                K[3] = bf2_to_f2(w.w);
                 if (tid < g.V) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) kvec[8 * vslot + j] = K[j];
+                    float4 *kv = reinterpret_cast<float4 *>(kvec + 8 * vslot);
+                    float k0, k1, k2, k3, k4, k5, k6, k7;
+                    upk(K[0], k0, k1);
+                    upk(K[1], k2, k3);
+                    upk(K[2], k4, k5);
+                    upk(K[3], k6, k7);
+                    kv[0] = make_float4(k0, k1, k2, k3);
+                    kv[1] = make_float4(k4, k5, k6, k7);
                 }
             }
             const int nvec = piece_rows(g, c.k) * g.V;
@@ -449,12 +525,9 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float d0 = bf_lo(ws[i]) - K[2 * i];
-                    const float d1 = bf_hi(ws[i]) - K[2 * i + 1];
-                    s1[2 * i] += d0;
-                    s2[2 * i] = fmaf(d0, d0, s2[2 * i]);
-                    s1[2 * i + 1] += d1;
-                    s2[2 * i + 1] = fmaf(d1, d1, s2[2 * i + 1]);
+                    const f2_t d = sub2(bf2_to_f2(ws[i]), K[i]);
+                    s1[i] = add2(s1[i], d);
+                    s2[i] = fma2(d, d, s2[i]);
                 }
             }
         }
@@ -469,33 +542,39 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
 // ---------------------------------------------------------------------------
 // finalize pieces
 // ---------------------------------------------------------------------------
-// Chan merge of the S segment records of channel (n, c), by one warp.
+// Chan merge of the S segment records of channel (n, c), by one warp;
+// S <= 32 * PER_LANE.
+template <int PER_LANE>
 __device__ __forceinline__ float2 combine_channel(const Args &a, int64_t n, int c)
 {
     const Geom &g = a.g;
     const int lane = threadIdx.x & 31;
     const float2 *src = a.partial + (n * g.C + c) * g.S;
-    float mu[kPartialsPerLane], m2[kPartialsPerLane], cnt[kPartialsPerLane];
+    float mu[PER_LANE], m2[PER_LANE], cnt[PER_LANE];
     float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < kPartialsPerLane; ++i) {
+    for (int i = 0; i < PER_LANE; ++i) {
         const int s = lane + 32 * i;
         if (s < g.S) {
             const float2 v = __ldcg(src + s);
             mu[i] = v.x;
             m2[i] = v.y;
-            cnt[i] = static_cast<float>(segment_rows(g, s));
-            acc = fmaf(cnt[i], v.x, acc);
         } else {
-            mu[i] = m2[i] = cnt[i] = 0.f;
+            mu[i] = m2[i] = 0.f;
         }
+    }
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+        const int s = lane + 32 * i;
+        cnt[i] = (s < g.S) ? static_cast<float>(segment_rows(g, s)) : 0.f;
+        acc = fmaf(cnt[i], mu[i], acc);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     const float mean = acc / static_cast<float>(g.L);
     float acc2 = 0.f;
 #pragma unroll
-    for (int i = 0; i < kPartialsPerLane; ++i) {
+    for (int i = 0; i < PER_LANE; ++i) {
         const float d = mu[i] - mean;
         acc2 += fmaf(cnt[i] * d, d, m2[i]);
     }
@@ -524,42 +603,55 @@ __device__ __forceinline__ float2 combine_group(const Args &a, const float2 *ch,
 // consumers: pass 2 (reverse order, in place in shared memory)
 // ---------------------------------------------------------------------------
 template <bool SILU>
-__device__ __forceinline__ uint32_t apply_pair(uint32_t w, float s0, float t0, float s1, float t1)
+__device__ __forceinline__ uint32_t apply_pair(uint32_t w, f2_t sc, f2_t sh)
 {
-    float z0 = fmaf(bf_lo(w), s0, t0);
-    float z1 = fmaf(bf_hi(w), s1, t1);
-    if (SILU) {
-        z0 = silu(z0);
-        z1 = silu(z1);
-    }
-    return pack_bf16x2(z0, z1);
+    f2_t z = fma2(bf2_to_f2(w), sc, sh);
+    if (SILU) z = silu2(z);
+    return f2_to_bf2(z);
 }
 
-// Scale / shift of group statistics for batch entry n into shared memory
-// (fused kernel).  Written to the statistics outputs by the one CTA that
-// owns segment 0 of n.
+// Scale / shift of batch entry n into shared memory (fused kernel), from
+// the channel records of the whole grid and the gamma / beta table loaded at
+// kernel start.  All channel records come in with one batch of loads; then
+// one warp per group merges them (Chan: mean of the channel means, then the
+// within- plus between-channel squares) and writes the group's scale and
+// shift.  The statistics outputs are written by the one CTA that owns
+// segment 0 of n.
 __device__ void fused_group_finalize(const Args &a, const Smem &sm, int64_t n, bool write_stats)
 {
     const Geom &g = a.g;
     float2 *st = reinterpret_cast<float2 *>(sm.base + sm.lay.st);
-    float2 *gs = reinterpret_cast<float2 *>(sm.base + sm.lay.gstat);
-    const int tid = threadIdx.x;
-    // channel records -> shared memory (st doubles as staging)
-    for (int c = tid; c < g.C; c += kConsumers) st[c] = __ldcg(a.chstat + n * g.C + c);
+    const float2 *gb = reinterpret_cast<const float2 *>(sm.base + sm.lay.gb);
+    const int lane = threadIdx.x & 31;
+    const float Lf = static_cast<float>(g.L);
+    for (int c = threadIdx.x; c < g.C; c += kConsumers) st[c] = __ldcg(a.chstat + n * g.C + c);
     named_sync(1, kConsumers);
-    for (int grp = tid; grp < g.G; grp += kConsumers) {
-        const float2 r = combine_group(a, st + grp * g.Cg, g.Cg);
-        gs[grp] = r;
-        if (write_stats) {
-            a.mean[n * g.G + grp] = r.x;
-            a.rstd[n * g.G + grp] = r.y;
+    for (int grp = threadIdx.x >> 5; grp < g.G; grp += kConsumerWarps) {
+        const float2 *rec = st + grp * g.Cg;
+        float mu = 0.f;
+        for (int j = lane; j < g.Cg; j += 32) mu += rec[j].x;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mu += __shfl_xor_sync(0xffffffffu, mu, off);
+        mu /= static_cast<float>(g.Cg);
+        float M2 = 0.f;
+        for (int j = lane; j < g.Cg; j += 32) {
+            const float d = rec[j].x - mu;
+            M2 += fmaf(Lf * d, d, rec[j].y);
         }
-    }
-    named_sync(1, kConsumers);
-    for (int c = tid; c < g.C; c += kConsumers) {
-        const float2 r = gs[c / g.Cg];
-        const float sc = a.gamma[c] * r.y;
-        st[c] = make_float2(sc, a.beta[c] - r.x * sc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M2 += __shfl_xor_sync(0xffffffffu, M2, off);
+        const float var = fmaxf(M2 / (Lf * static_cast<float>(g.Cg)), 0.f);
+        const float rstd = 1.0f / sqrtf(var + a.eps);
+        if (write_stats && lane == 0) {
+            a.mean[n * g.G + grp] = mu;
+            a.rstd[n * g.G + grp] = rstd;
+        }
+        __syncwarp();   // every lane has read the group's records before they are overwritten
+        for (int j = lane; j < g.Cg; j += 32) {
+            const float2 ab = gb[grp * g.Cg + j];
+            const float sc = ab.x * rstd;
+            st[grp * g.Cg + j] = make_float2(sc, ab.y - mu * sc);
+        }
     }
     named_sync(1, kConsumers);
 }
@@ -576,28 +668,26 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
     cursor_last(g, c);
     int slot = slot_of(T - 1, g.ring);
     int64_t cur_item = -1, cur_n = -1;
-    float sc[8], sh[8];
+    f2_t sc[4], sh[4];
     bool ok = !*ctl.abort;
     for (int64_t q = T - 1; q >= 0; --q) {
         if (c.it != cur_item) {
             if (FUSED) {
                 if (c.n != cur_n) fused_group_finalize(a, sm, c.n, c.s == 0);
-                const float2 *st = reinterpret_cast<const float2 *>(sm.base + sm.lay.st);
+                const float4 *st = reinterpret_cast<const float4 *>(sm.base + sm.lay.st) + 4 * vslot;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float2 v = st[8 * vslot + j];
-                    sc[j] = v.x;
-                    sh[j] = v.y;
+                for (int j = 0; j < 4; ++j) {
+                    const float4 v = st[j];            // (s, t) of channels 2j, 2j+1
+                    sc[j] = pk(v.x, v.z);
+                    sh[j] = pk(v.y, v.w);
                 }
             } else {
                 const float4 *src = reinterpret_cast<const float4 *>(a.st + c.n * g.C + 8 * vslot);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float4 v = __ldcg(src + j);
-                    sc[2 * j] = v.x;
-                    sh[2 * j] = v.y;
-                    sc[2 * j + 1] = v.z;
-                    sh[2 * j + 1] = v.w;
+                    sc[j] = pk(v.x, v.z);
+                    sh[j] = pk(v.y, v.w);
                 }
             }
             cur_item = c.it;
@@ -607,24 +697,37 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
             if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
             full_par ^= 1u << slot;
         }
+        // Read this thread's vectors and compute their outputs before the
+        // slot is released: using every loaded value guarantees that no
+        // shared-memory load of any lane is still in flight when the warp
+        // signals the producer, which may then overwrite the slot.
+        uint4 o[kMaxVecPerThread];
+        int nvec = 0;
         if (ok) {
             const uint32_t base = sm.slot_addr(slot, g.piece_bytes);
-            const int nvec = piece_rows(g, c.k) * g.V;
-#pragma unroll 4
-            for (int v = tid; v < nvec; v += kConsumers) {
-                const uint32_t addr = base + 16u * v;
-                const uint4 w = lds128(addr);
-                uint4 o;
-                o.x = apply_pair<SILU>(w.x, sc[0], sh[0], sc[1], sh[1]);
-                o.y = apply_pair<SILU>(w.y, sc[2], sh[2], sc[3], sh[3]);
-                o.z = apply_pair<SILU>(w.z, sc[4], sh[4], sc[5], sh[5]);
-                o.w = apply_pair<SILU>(w.w, sc[6], sh[6], sc[7], sh[7]);
-                sts128(addr, o);
+            nvec = piece_rows(g, c.k) * g.V;
+#pragma unroll
+            for (int i = 0; i < kMaxVecPerThread; ++i) {
+                const int v = tid + i * kConsumers;
+                if (v < nvec) {
+                    const uint4 w = lds128(base + 16u * v);
+                    o[i].x = apply_pair<SILU>(w.x, sc[0], sh[0]);
+                    o[i].y = apply_pair<SILU>(w.y, sc[1], sh[1]);
+                    o[i].z = apply_pair<SILU>(w.z, sc[2], sh[2]);
+                    o[i].w = apply_pair<SILU>(w.w, sc[3], sh[3]);
+                }
             }
-            fence_proxy_async_smem();
         }
         __syncwarp();
-        if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));
+        if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));   // the slot may be refilled now
+        if (ok) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, c.n, c.k));
+#pragma unroll
+            for (int i = 0; i < kMaxVecPerThread; ++i) {
+                const int v = tid + i * kConsumers;
+                if (v < nvec) dst[v] = o[i];
+            }
+        }
         cursor_prev(g, c);
         slot = (slot == 0) ? g.ring - 1 : slot - 1;
     }
@@ -635,20 +738,23 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
 // ---------------------------------------------------------------------------
 extern __shared__ __align__(1024) uint8_t g_smem[];
 
-__device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl &ctl)
+__device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl &ctl, int64_t &T)
 {
     sm.base = g_smem;
     sm.lay = make_layout(a.g, kind);
     sm.ring_s = smem_addr(g_smem);
+    sm.bars_s = sm.ring_s + sm.lay.bars;
     volatile int *flags = reinterpret_cast<volatile int *>(g_smem + sm.lay.flags);
     if (threadIdx.x == 0) {
-        flags[0] = (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) ? 1 : 0;
+        const unsigned int st = *reinterpret_cast<volatile unsigned int *>(&g_status);
         for (int s = 0; s < a.g.ring; ++s) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), kConsumerWarps);
         }
         mbar_init_fence();
+        flags[0] = (st != 0u) ? 1 : 0;
     }
+    T = cta_piece_count(a.g);
     __syncthreads();
     ctl.abort = flags;
     ctl.timeout_ns = a.timeout_ns;
@@ -658,12 +764,12 @@ __device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl 
 // ---------------------------------------------------------------------------
 // kernels
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) gn_pass1_kernel(const __grid_constant__ Args a)
+__global__ void __launch_bounds__(kThreads, 1) gn_pass1_kernel(const __grid_constant__ Args a)
 {
     Smem sm;
     Ctl ctl;
-    if (!prologue(a, kPass1, sm, ctl)) return;
-    const int64_t T = cta_piece_count(a.g);
+    int64_t T;
+    if (!prologue(a, kPass1, sm, ctl, T)) return;
     if (threadIdx.x >= kConsumers) {
         if (threadIdx.x == kConsumers) {
             ProducerState ps{0u, 0u, 0u};
@@ -685,7 +791,7 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant_
     const int grp = static_cast<int>(blockIdx.x % g.G);
     const int warp = threadIdx.x >> 5;
     for (int j = warp; j < g.Cg; j += 8) {
-        const float2 r = combine_channel(a, n, grp * g.Cg + j);
+        const float2 r = combine_channel<kMaxSegments / 32>(a, n, grp * g.Cg + j);
         if ((threadIdx.x & 31) == 0) fin_smem[j] = r;
     }
     __syncthreads();
@@ -705,12 +811,12 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant_
 }
 
 template <bool SILU>
-__global__ void __launch_bounds__(kThreads) gn_pass2_kernel(const __grid_constant__ Args a)
+__global__ void __launch_bounds__(kThreads, 1) gn_pass2_kernel(const __grid_constant__ Args a)
 {
     Smem sm;
     Ctl ctl;
-    if (!prologue(a, kPass2, sm, ctl)) return;
-    const int64_t T = cta_piece_count(a.g);
+    int64_t T;
+    if (!prologue(a, kPass2, sm, ctl, T)) return;
     if (threadIdx.x >= kConsumers) {
         if (threadIdx.x == kConsumers) {
             ProducerState ps{0u, 0u, 0u};
@@ -728,13 +834,19 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
 {
     Smem sm;
     Ctl ctl;
-    if (!prologue(a, kFused, sm, ctl)) return;
+    int64_t T;
+    if (!prologue(a, kFused, sm, ctl, T)) return;
     const Geom &g = a.g;
-    const int64_t T = cta_piece_count(g);
     const int64_t resident = min(T, static_cast<int64_t>(g.ring));
     const bool producer = threadIdx.x == kConsumers;
     ProducerState ps{0u, 0u, 0u};
     uint32_t full_par = 0;
+
+    // gamma / beta into shared memory while the first pieces are in flight
+    if (threadIdx.x < kConsumers) {
+        float2 *gb = reinterpret_cast<float2 *>(g_smem + sm.lay.gb);
+        for (int c = threadIdx.x; c < g.C; c += kConsumers) gb[c] = make_float2(a.gamma[c], a.beta[c]);
+    }
 
     // pass 1
     if (producer) {
@@ -745,22 +857,22 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
     // every segment record of the grid is written
     grid_sync(a.sync, gridDim.x, ctl);
 
-    // finalize, step 1: channel records, (n, c) pairs spread over the grid
+    // finalize, step 1: channel records, (n, c) pairs spread over the grid,
+    // one warp each
     if (!*ctl.abort && threadIdx.x < kConsumers) {
         const int64_t tasks = g.N * g.C;
-        const int64_t per = (tasks + gridDim.x - 1) / gridDim.x;
-        const int64_t t0 = blockIdx.x * per;
-        const int64_t t1 = min(t0 + per, tasks);
-        for (int64_t t = t0 + (threadIdx.x >> 5); t < t1; t += kConsumerWarps) {
+        for (int64_t t = blockIdx.x + static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x; t < tasks;
+             t += static_cast<int64_t>(kConsumerWarps) * gridDim.x) {
             const int64_t n = t / g.C;
             const int c = static_cast<int>(t - n * g.C);
-            const float2 r = combine_channel(a, n, c);
+            const float2 r = combine_channel<kFusedMaxSegments / 32>(a, n, c);
             if ((threadIdx.x & 31) == 0) a.chstat[t] = r;
         }
     }
     grid_sync(a.sync, 2u * gridDim.x, ctl);
-    if (threadIdx.x == 0 && !*ctl.abort) {
-        // the last CTA past the second barrier re-arms the counters
+    if (threadIdx.x == kConsumers + 1 && !*ctl.abort) {
+        // the last CTA past the second barrier re-arms the counters (done by
+        // an otherwise idle producer-warp lane, off the consumers' path)
         if (atomicAdd(a.sync + 1, 1u) == gridDim.x - 1) {
             atomicExch(a.sync, 0u);
             atomicExch(a.sync + 1, 0u);
@@ -773,6 +885,42 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
         if (*ctl.abort) drain_loads(sm, ps, g.ring);
     } else if (threadIdx.x < kConsumers) {
         consume_pass2<SILU, true>(a, sm, T, resident, full_par, ctl);
+    }
+}
+
+// Diagnostic: waits that nothing will ever satisfy, so the bounded-wait
+// machinery must expire, record the sticky status and return.  mode 0: an
+// mbarrier phase no thread arrives on; mode 1: a grid-barrier count no CTA
+// reaches (the counter lives in this CTA's shared memory, so no global
+// state is involved).  Writes 1 to done[blockIdx.x] when the CTA returns.
+__global__ void __launch_bounds__(32) gn_selftest_wait_kernel(int mode, uint64_t timeout_ns, int *done)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ unsigned int counter;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        counter = 0;
+        mbar_init(smem_addr(&bar), 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    Ctl ctl;
+    ctl.abort = &abort_flag;
+    ctl.timeout_ns = timeout_ns;
+    if (threadIdx.x == 0) {
+        if (mode == 0) {
+            wait_phase(smem_addr(&bar), 0, ctl);
+        } else {
+            const uint64_t deadline = global_ns() + timeout_ns;
+            while (*reinterpret_cast<volatile unsigned int *>(&counter) < 1u) {
+                if (global_ns() > deadline) {
+                    record_timeout(ctl);
+                    break;
+                }
+            }
+        }
+        done[blockIdx.x] = abort_flag ? 1 : 2;
     }
 }
 
@@ -833,6 +981,12 @@ cudaError_t launch_fused(const Args &a, int grid, bool silu, cudaStream_t s)
     const void *fn = silu ? reinterpret_cast<const void *>(gn_fused_kernel<true>)
                           : reinterpret_cast<const void *>(gn_fused_kernel<false>);
     return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), params, smem_for(a, kFused), s);
+}
+
+cudaError_t launch_selftest_wait(int mode, uint64_t timeout_ns, int *done, int blocks, cudaStream_t s)
+{
+    gn_selftest_wait_kernel<<<blocks, 32, 0, s>>>(mode, timeout_ns, done);
+    return cudaGetLastError();
 }
 
 cudaError_t read_device_status(unsigned int *status)

@@ -53,6 +53,8 @@ EXPORTS = {
     "gn_silu_rows_static": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4
                             + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                ctypes.c_void_p]),
+    "gn_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                ctypes.c_int, ctypes.c_void_p]),
     "gn_silu_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4),
     "gn_silu_pick_variant": (ctypes.c_int, [ctypes.c_int64] * 4),
     "gn_kernel_launch_count": (ctypes.c_uint64, []),

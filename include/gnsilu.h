@@ -135,6 +135,15 @@ uint64_t gn_kernel_launch_count(void);
  * re-zeroed by the caller. */
 int gn_device_status(int clear);
 
+/* Diagnostic of the kernels' failure handling: launches `blocks` CTAs that
+ * each wait for something nothing will ever do -- mode 0: an mbarrier phase
+ * no thread arrives on; mode 1: a barrier count no CTA reaches -- bounded by
+ * timeout_ms (0..10000).  Each CTA must give up, record the sticky status
+ * that gn_device_status() reports as GN_ERR_KERNEL, write 1 to
+ * done[blockIdx] (device int array) and return.  The caller clears the
+ * status afterwards with gn_device_status(1).  Asynchronous on `stream`. */
+int gn_selftest_bounded_wait(int mode, int timeout_ms, int *done, int blocks, void *stream);
+
 /* Size of the fixed scratch array used by gn_silu_rows_static(): 8 MiB. */
 #define GN_STATIC_SCRATCH_BYTES (8u << 20)
 
