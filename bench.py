@@ -8,7 +8,9 @@ synthetic bf16 activation of the workload (default: N=1 C=512 H=W=128, the
 FLUX.2 VAE mid-block GroupNorm shape).  Inputs are seeded (see
 ``channels_last_groupnorm_gb300/workloads.py``) and already resident in HBM;
 consecutive steps rotate over enough buffer sets that no step finds its
-input in L2.  ``value`` is effective bandwidth: N*L*C*4 bytes (read x once,
+input in L2.  The timed steps are captured once into a CUDA graph and
+replayed (``--launch stream`` launches them one by one instead).  ``value``
+is effective bandwidth: N*L*C*4 bytes (read x once,
 write y once) per step, summed over ranks, divided by the slowest rank's
 time.  ``e2e`` repeats the measurement through the C ABI from pinned host
 buffers with the host<->device copies inside the timed region.
@@ -201,8 +203,39 @@ def time_calls(call, nsets, steps, stream):
     return per, t0.elapsed_time(t1) / 1e3
 
 
+def capture_steps(call, nsets, steps, stream):
+    """A CUDA graph holding `steps` consecutive calls (rotating over the
+    buffer sets), or None if the calls cannot be captured."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(steps):
+                call(i % nsets)
+    except Exception:   # noqa: BLE001 -- any capture failure falls back to stream launches
+        torch.cuda.synchronize()
+        return None
+    return graph
+
+
+def time_graph(graph, stream):
+    """Elapsed time (s) of one replay of a captured sequence of steps."""
+    import torch
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return t0.elapsed_time(t1) / 1e3
+
+
 def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, sampler=None,
-                     seeded=True):
+                     seeded=True, launch="graph"):
     """Device-resident timing of one workload.  Returns a dict."""
     import torch
     from channels_last_groupnorm_gb300 import gnsilu as gs
@@ -249,14 +282,25 @@ def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, s
                     i += 1
                 torch.cuda.synchronize()
         before = gs.gn_kernel_launch_count()
-        per, elapsed = time_calls(call, nsets, steps, stream)
-        launches = gs.gn_kernel_launch_count() - before
+        call(0)
+        per_call = gs.gn_kernel_launch_count() - before   # kernels one call launches
+        graph = capture_steps(call, nsets, steps, stream) if launch == "graph" else None
+        if graph is not None:
+            graph.replay()                      # upload + warm the graph
+            elapsed = time_graph(graph, stream)
+            per = [elapsed * 1e3 / steps] * steps
+            mode = "cuda-graph"
+        else:
+            per, elapsed = time_calls(call, nsets, steps, stream)
+            mode = "stream"
+        launches = per_call * steps
         clocks = sampler.stop() if sampler is not None else None
+        del graph
     status = gs.gn_device_status(False)
     if status != 0:
         raise RuntimeError(f"device status after timing: {gs.status_string(status)}")
     res = {"elapsed_s": elapsed, "per_step_ms": per, "nsets": nsets, "set_bytes": set_bytes,
-           "launches": launches, "clocks": clocks,
+           "launches": launches, "clocks": clocks, "launch": mode,
            "variant": {1: "two_pass", 2: "fused"}.get(
                gs.gn_silu_pick_variant(w.N, w.L, w.C, w.G) if variant_id == 0 else variant_id,
                "?")}
@@ -326,13 +370,14 @@ def cpu_baseline(w, budget_s=12.0):
                       f"({w.elements} elements), {cores} OpenMP threads"}
 
 
-def sweep(variant_id, device, stream, peak):
+def sweep(variant_id, device, stream, peak, launch="graph"):
     """Every workload shape: us/call and effective bandwidth at 4 B/elem
     (read once + write once) and 6 B/elem (two-pass byte count)."""
     from channels_last_groupnorm_gb300 import workloads as wl
     out = []
     for w in wl.WORKLOADS:
-        r = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24))
+        r = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24),
+                             launch=launch)
         us = statistics.median(r["per_step_ms"]) * 1e3
         gbs4 = 4.0 * w.elements / (us * 1e-6) / 1e9
         gbs6 = 6.0 * w.elements / (us * 1e-6) / 1e9
@@ -340,7 +385,8 @@ def sweep(variant_id, device, stream, peak):
                     "gbs_4B": round(gbs4, 1), "gbs_6B": round(gbs6, 1),
                     "frac_4B": round(gbs4 / peak, 3), "frac_6B": round(gbs6 / peak, 3),
                     "pages_h200_us": w.pages_us_h200,
-                    "l2": f"{r['nsets']} rotating buffer sets of {r['set_bytes'] >> 20} MiB"})
+                    "l2": f"{r['nsets']} rotating buffer sets of {r['set_bytes'] >> 20} MiB",
+                    "launch": r["launch"]})
     return out
 
 
@@ -367,7 +413,7 @@ def run_ours(args):
 
     sampler = ClockSampler(local) if rank == 0 else None
     r = measure_workload(w, variant_id, args.steps, args.warmup, device, stream,
-                         soak_s=args.soak, sampler=sampler)
+                         soak_s=args.soak, sampler=sampler, launch=args.launch)
     ms_per_step = r["elapsed_s"] * 1e3 / args.steps
     units = 4.0 * w.elements * args.steps
     elapsed, total_units = reduce_timing(r["elapsed_s"], units,
@@ -400,7 +446,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {r['nsets']} rotating buffer sets of "
                          f"{r['set_bytes'] >> 20} MiB (x+y)",
-                   "bytes_per_step": "N*L*C*4 (x read once, y written once)"},
+                   "bytes_per_step": "N*L*C*4 (x read once, y written once)",
+                   "launch": r["launch"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic,
@@ -421,7 +468,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0 and not args.no_sweep:
-        line["sweep"] = sweep(variant_id, device, stream, peak)
+        line["sweep"] = sweep(variant_id, device, stream, peak, launch=args.launch)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -479,6 +526,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", choices=["auto", "fused", "two_pass"], default="auto")
+    ap.add_argument("--launch", choices=["graph", "stream"], default="graph",
+                    help="submit the timed steps as one captured CUDA graph, or one stream "
+                         "launch per step")
     ap.add_argument("--soak", type=float, default=1.5,
                     help="seconds of untimed calls while the clock sampler runs")
     ap.add_argument("--no-sweep", action="store_true")

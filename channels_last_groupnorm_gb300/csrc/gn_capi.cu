@@ -139,7 +139,7 @@ struct Plan {
     Geom g{};
     int kind = 0;            // GN_VARIANT_TWO_PASS or GN_VARIANT_FUSED
     int grid = 0;
-    size_t off_partial = 0, off_chstat = 0, off_st = 0, off_mean = 0, off_rstd = 0;
+    size_t off_partial = 0, off_gstat = 0, off_st = 0, off_mean = 0, off_rstd = 0;
     size_t ws_bytes = 0;
 };
 
@@ -175,7 +175,7 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     const int64_t max_seg = (kind == GN_VARIANT_FUSED) ? gn::kFusedMaxSegments : gn::kMaxSegments;
     if (S > max_seg) S = max_seg;
     g.S = static_cast<int32_t>(S);
-    g.seg32 = (g.pieces_per_n * S < (int64_t(1) << 32)) ? 1 : 0;
+    g.seg32 = (g.pieces_per_n < (int64_t(1) << 32)) ? 1 : 0;
     g.items = N * S;
     p.grid = static_cast<int>(g.items < grid_target ? g.items : grid_target);
     // ring depth from the shared memory left next to the auxiliary arrays
@@ -187,9 +187,9 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     // workspace
     size_t off = 256;   // barrier words
     p.off_partial = off;
-    off = align256(off + static_cast<size_t>(N) * C * S * sizeof(float2));
-    p.off_chstat = off;
-    off = align256(off + static_cast<size_t>(N) * C * sizeof(float2));
+    off = align256(off + static_cast<size_t>(N) * C * S * sizeof(float4));
+    p.off_gstat = off;
+    off = align256(off + static_cast<size_t>(N) * G * sizeof(float2));
     p.off_st = off;
     off = align256(off + static_cast<size_t>(N) * C * sizeof(float2));
     p.off_mean = off;
@@ -296,8 +296,8 @@ int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N
     a.eps = eps;
     a.l2_hints = l2_hints();
     a.g = p.g;
-    a.partial = reinterpret_cast<float2 *>(base + p.off_partial);
-    a.chstat = reinterpret_cast<float2 *>(base + p.off_chstat);
+    a.partial = reinterpret_cast<float4 *>(base + p.off_partial);
+    a.gstat = reinterpret_cast<float2 *>(base + p.off_gstat);
     a.st = reinterpret_cast<float2 *>(base + p.off_st);
     a.mean = mean_out ? mean_out : reinterpret_cast<float *>(base + p.off_mean);
     a.rstd = rstd_out ? rstd_out : reinterpret_cast<float *>(base + p.off_rstd);

@@ -20,8 +20,8 @@ constexpr int kScratchBytes = 16384;            // pass-1 CTA reduction scratch
 constexpr int kSyncWords = 64;                  // 256-byte workspace header
 
 // The (N, L, C) tensor is cut into pieces of whole rows (one bulk copy
-// each); the pieces of one batch entry are split into S contiguous
-// segments, and a work item is one (n, segment) pair.
+// each); the pieces of one batch entry are dealt out round-robin to S work
+// items, a work item being one (n, s) pair: item s owns pieces s, s + S, ...
 struct Geom {
     int64_t N, L;
     int32_t C, G, Cg, V;          // V = C / 8 sixteen-byte vectors per row
@@ -31,7 +31,7 @@ struct Geom {
     int32_t S;                    // segments per batch entry
     int32_t ring;                 // ring slots in shared memory
     int64_t items;                // N * S
-    int32_t seg32;                // pieces_per_n * S < 2^32: segment bounds in 32-bit math
+    int32_t seg32;                // pieces_per_n < 2^32: piece counts in 32-bit math
 };
 
 struct Args {
@@ -42,8 +42,8 @@ struct Args {
     uint32_t l2_hints;            // bit 0: pass-2 loads evict_first, bit 1: pass-2
                                   // stores evict_first, bit 2: pass-1 loads evict_last
     Geom g;
-    float2 *partial;              // [N][C][S] segment (mean, M2)
-    float2 *chstat;               // [N][C]    channel (mean, M2)   (fused)
+    float4 *partial;              // [N][C][S] item (mean, M2, count, unused)
+    float2 *gstat;                // [N][G]    group (mean, rstd)   (fused)
     float2 *st;                   // [N][C]    (scale, shift)       (two-pass)
     float *mean, *rstd;           // [N][G]
     unsigned int *sync;           // barrier words (fused)

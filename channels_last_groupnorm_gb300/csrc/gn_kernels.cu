@@ -13,13 +13,14 @@
 //    TMA copies (cp.async.bulk) issued by one producer thread, completion
 //    tracked on mbarriers.  Sixteen consumer warps read 16-byte vectors from
 //    shared memory; with C a power of two each consumer thread always sees
-//    the same eight channels.  Arithmetic on channel pairs uses the packed
-//    fp32x2 instructions of sm_100+ (add/sub/mul/fma .f32x2).
+//    the same eight channels.  Pass-1 arithmetic on channel pairs uses the
+//    packed fp32x2 instructions of sm_100+ (add/sub/fma .f32x2).
 //  * Pass 1 keeps, per thread, fp32 sums of (x - K) and (x - K)^2 with K a
 //    per-(work item, channel) shift (the item's first row), then reduces
-//    them per CTA with warp shuffles and shared memory into a per-segment
-//    (mean, M2) record.  Segments are merged with Chan's parallel formula,
-//    first over segments per channel, then over the channels of a group.
+//    them per CTA with warp shuffles and shared memory into a per-item
+//    (mean, M2, count) record.  Items are merged with Chan's parallel
+//    formula, first over items per channel, then over the channels of a
+//    group.
 //  * Pass 2 loads pieces the same way, in the reverse of pass-1 order so the
 //    most recently read rows (still in L2) come first; each consumer thread
 //    takes its vectors out of the slot, releases the slot at once, and
@@ -71,13 +72,6 @@ __device__ __forceinline__ f2_t sub2(f2_t a, f2_t b)
     return d;
 }
 
-__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b)
-{
-    f2_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 __device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c)
 {
     f2_t d;
@@ -91,33 +85,25 @@ __device__ __forceinline__ f2_t bf2_to_f2(uint32_t w)
     return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// round a pair to bf16 (nearest even) and pack it, low half first
-__device__ __forceinline__ uint32_t f2_to_bf2(f2_t v)
-{
-    float lo, hi;
-    upk(v, lo, hi);
-    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
 // ---------------------------------------------------------------------------
-// work-item cursor
+// work-item cursor.  Work item (n, s) owns the pieces k = s, s + S, s + 2S, ...
+// of batch entry n: interleaving spreads every CTA's reads over the whole
+// address range, so no CTA is stuck with a slower stretch of memory.
 // ---------------------------------------------------------------------------
 struct Cursor {
     int64_t it;        // work item id (n * S + s)
     int64_t n;
     int32_t s;
-    int64_t p0, p1;    // piece range of the item inside batch entry n
+    int64_t k_last;    // last piece of the item
     int64_t k;         // current piece
 };
 
-// first piece of segment s (segments split the pieces of a batch entry as
-// evenly as integer division allows)
-__device__ __forceinline__ int64_t segment_first_piece(const Geom &g, int32_t s)
+// pieces of item s in one batch entry (S <= pieces_per_n, so at least one)
+__device__ __forceinline__ int64_t item_pieces(const Geom &g, int32_t s)
 {
     if (g.seg32)
-        return static_cast<uint32_t>(s) * static_cast<uint32_t>(g.pieces_per_n) / static_cast<uint32_t>(g.S);
-    return static_cast<int64_t>(s) * g.pieces_per_n / g.S;
+        return static_cast<uint32_t>(g.pieces_per_n - 1 - s) / static_cast<uint32_t>(g.S) + 1;
+    return (g.pieces_per_n - 1 - s) / g.S + 1;
 }
 
 __device__ __forceinline__ void load_item(const Geom &g, Cursor &c, int64_t it)
@@ -125,15 +111,15 @@ __device__ __forceinline__ void load_item(const Geom &g, Cursor &c, int64_t it)
     c.it = it;
     c.n = it / g.S;
     c.s = static_cast<int32_t>(it - c.n * g.S);
-    c.p0 = segment_first_piece(g, c.s);
-    c.p1 = segment_first_piece(g, c.s + 1);
+    c.k_last = c.s + (item_pieces(g, c.s) - 1) * g.S;
 }
 
-__device__ __forceinline__ int64_t segment_rows(const Geom &g, int32_t s)
+// rows covered by item s: whole pieces, less the short tail of the last
+// piece of the batch entry if the item owns it
+__device__ __forceinline__ int64_t item_rows(const Geom &g, const Cursor &c)
 {
-    const int64_t r0 = segment_first_piece(g, s) * g.rows_per_piece;
-    const int64_t r1 = min(segment_first_piece(g, s + 1) * g.rows_per_piece, g.L);
-    return r1 - r0;
+    const int64_t rows = item_pieces(g, c.s) * g.rows_per_piece;
+    return (c.k_last == g.pieces_per_n - 1) ? rows - (g.pieces_per_n * g.rows_per_piece - g.L) : rows;
 }
 
 __device__ __forceinline__ int32_t piece_rows(const Geom &g, int64_t k)
@@ -150,28 +136,28 @@ __device__ __forceinline__ int64_t piece_elem_offset(const Geom &g, int64_t n, i
 __device__ __forceinline__ int64_t cta_piece_count(const Geom &g)
 {
     int64_t t = 0;
-    for (int64_t it = blockIdx.x; it < g.items; it += gridDim.x) {
-        Cursor c;
-        load_item(g, c, it);
-        t += c.p1 - c.p0;
-    }
+    for (int64_t it = blockIdx.x; it < g.items; it += gridDim.x)
+        t += item_pieces(g, static_cast<int32_t>(it % g.S));
     return t;
 }
 
 __device__ __forceinline__ void cursor_first(const Geom &g, Cursor &c)
 {
     load_item(g, c, blockIdx.x);
-    c.k = c.p0;
+    c.k = c.s;
 }
 
 // returns false when the CTA has no further piece
 __device__ __forceinline__ bool cursor_next(const Geom &g, Cursor &c)
 {
-    if (++c.k < c.p1) return true;
+    if (c.k < c.k_last) {
+        c.k += g.S;
+        return true;
+    }
     const int64_t it = c.it + gridDim.x;
     if (it >= g.items) return false;
     load_item(g, c, it);
-    c.k = c.p0;
+    c.k = c.s;
     return true;
 }
 
@@ -179,16 +165,19 @@ __device__ __forceinline__ void cursor_last(const Geom &g, Cursor &c)
 {
     const int64_t last = blockIdx.x + ((g.items - 1 - blockIdx.x) / gridDim.x) * gridDim.x;
     load_item(g, c, last);
-    c.k = c.p1 - 1;
+    c.k = c.k_last;
 }
 
 __device__ __forceinline__ bool cursor_prev(const Geom &g, Cursor &c)
 {
-    if (--c.k >= c.p0) return true;
+    if (c.k > c.s) {
+        c.k -= g.S;
+        return true;
+    }
     const int64_t it = c.it - gridDim.x;
     if (it < 0) return false;
     load_item(g, c, it);
-    c.k = c.p1 - 1;
+    c.k = c.k_last;
     return true;
 }
 
@@ -250,23 +239,6 @@ __device__ __forceinline__ bool grid_sync(unsigned int *counter, unsigned int ta
     }
     __syncthreads();
     return !*ctl.abort;
-}
-
-// ---------------------------------------------------------------------------
-// SiLU on a pair: z * sigmoid(z), sigmoid from one ex2 and one reciprocal
-// per element (MUFU approximations, a few ulp in fp32; the MUFU pipes of an
-// SM retire about 32 of these per clock, so two per element stay well
-// below the element rate the memory system can feed)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ f2_t silu2(f2_t z)
-{
-    const f2_t t = mul2(z, pk(-1.4426950408889634f, -1.4426950408889634f));   // -z*log2(e)
-    float t0, t1;
-    upk(t, t0, t1);
-    const f2_t d = add2(pk(ex2_approx(t0), ex2_approx(t1)), pk(1.0f, 1.0f));    // 1 + exp(-z)
-    float d0, d1;
-    upk(d, d0, d1);
-    return mul2(z, pk(rcp_approx(d0), rcp_approx(d1)));
 }
 
 // ---------------------------------------------------------------------------
@@ -394,18 +366,23 @@ __device__ void drain_loads(const Smem &sm, const ProducerState &ps, int ring)
 // ---------------------------------------------------------------------------
 // consumers: pass 1
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void store_entry(float *scr, int idx, const float (&v1)[8], const float (&v2)[8])
+// Scratch layout of the CTA reduction: [quantity j = 0..15][entry][slot]
+// floats (j < 8: sum of x - K for channel 8*slot + j; j >= 8: sum of
+// squares), so that consecutive threads (consecutive slots) touch
+// consecutive words and the stores are free of bank conflicts.
+__device__ __forceinline__ void store_entry(float *scr, int cap, int V, int entry, int vs, const float (&v1)[8],
+                                            const float (&v2)[8])
 {
-    float4 *dst = reinterpret_cast<float4 *>(scr + idx * 16);
-    dst[0] = make_float4(v1[0], v1[1], v1[2], v1[3]);
-    dst[1] = make_float4(v1[4], v1[5], v1[6], v1[7]);
-    dst[2] = make_float4(v2[0], v2[1], v2[2], v2[3]);
-    dst[3] = make_float4(v2[4], v2[5], v2[6], v2[7]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        scr[(j * cap + entry) * V + vs] = v1[j];
+        scr[((8 + j) * cap + entry) * V + vs] = v2[j];
+    }
 }
 
 // Reduce the per-thread shifted sums of one work item into the item's
-// per-channel (mean, M2) record.  Threads that share a vector slot first
-// combine by warp shuffles (when the slot repeats inside a warp), then
+// per-channel (mean, M2, count) record.  Threads that share a vector slot
+// first combine by warp shuffles (when the slot repeats inside a warp), then
 // through shared memory; when the scratch cannot hold every entry at once,
 // the upper half of the entries is first added into the lower half.
 __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, const f2_t (&s1p)[4],
@@ -445,36 +422,36 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
     int live = entries;
     while (live > cap) {
         const int half = live >> 1;
-        if (holder && entry >= half) store_entry(scr, (entry - half) * g.V + vs_own, v1, v2);
+        if (holder && entry >= half) store_entry(scr, cap, g.V, entry - half, vs_own, v1, v2);
         named_sync(1, kConsumers);
         if (holder && entry < half) {
-            const float *src = scr + (entry * g.V + vs_own) * 16;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                v1[j] += src[j];
-                v2[j] += src[8 + j];
+                v1[j] += scr[(j * cap + entry) * g.V + vs_own];
+                v2[j] += scr[((8 + j) * cap + entry) * g.V + vs_own];
             }
         }
         if (entry >= half) holder = false;
         named_sync(1, kConsumers);
         live = half;
     }
-    if (holder) store_entry(scr, entry * g.V + vs_own, v1, v2);
+    if (holder) store_entry(scr, cap, g.V, entry, vs_own, v1, v2);
     named_sync(1, kConsumers);
     const float *kvec = reinterpret_cast<const float *>(sm.base + sm.lay.kvec);
-    const int64_t r0 = c.p0 * g.rows_per_piece;
-    const int64_t r1 = min(c.p1 * g.rows_per_piece, g.L);
-    const float count = static_cast<float>(r1 - r0);
-    for (int ch = tid; ch < g.C; ch += kConsumers) {
-        const int vs = ch >> 3, j = ch & 7;
+    const float count = static_cast<float>(item_rows(g, c));
+    // thread t finishes channel 8 * (t % V) + t / V: consecutive threads
+    // read consecutive slots of one quantity row
+    for (int idx = tid; idx < g.C; idx += kConsumers) {
+        const int vs = idx % g.V, j = idx / g.V;
+        const int ch = 8 * vs + j;
         float S1 = 0.f, S2 = 0.f;
         for (int e = 0; e < live; ++e) {
-            S1 += scr[(e * g.V + vs) * 16 + j];
-            S2 += scr[(e * g.V + vs) * 16 + 8 + j];
+            S1 += scr[(j * cap + e) * g.V + vs];
+            S2 += scr[((8 + j) * cap + e) * g.V + vs];
         }
         const float m = S1 / count;
         const float M2 = fmaxf(S2 - S1 * m, 0.f);
-        a.partial[(c.n * g.C + ch) * g.S + c.s] = make_float2(kvec[ch] + m, M2);
+        a.partial[(c.n * g.C + ch) * g.S + c.s] = make_float4(kvec[ch] + m, M2, count, 0.f);
     }
     named_sync(1, kConsumers);
 }
@@ -492,7 +469,7 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
     f2_t K[4], s1[4], s2[4];
     bool ok = !*ctl.abort;
     for (int64_t q = 0; q < T; ++q) {
-        const bool first = (c.k == c.p0);
+        const bool first = (c.k == c.s);
         if (first) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) s1[i] = s2[i] = 0ull;
@@ -533,7 +510,7 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
         }
         __syncwarp();
         if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));
-        if (c.k + 1 == c.p1) reduce_item(a, sm, c, s1, s2);
+        if (c.k == c.k_last) reduce_item(a, sm, c, s1, s2);
         cursor_next(g, c);
         slot = (slot + 1 == g.ring) ? 0 : slot + 1;
     }
@@ -549,109 +526,95 @@ __device__ __forceinline__ float2 combine_channel(const Args &a, int64_t n, int 
 {
     const Geom &g = a.g;
     const int lane = threadIdx.x & 31;
-    const float2 *src = a.partial + (n * g.C + c) * g.S;
-    float mu[PER_LANE], m2[PER_LANE], cnt[PER_LANE];
+    const float4 *src = a.partial + (n * g.C + c) * g.S;
+    float4 r[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+        const int s = lane + 32 * i;
+        r[i] = (s < g.S) ? __ldcg(src + s) : make_float4(0.f, 0.f, 0.f, 0.f);   // (mean, M2, count, -)
+    }
     float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-        const int s = lane + 32 * i;
-        if (s < g.S) {
-            const float2 v = __ldcg(src + s);
-            mu[i] = v.x;
-            m2[i] = v.y;
-        } else {
-            mu[i] = m2[i] = 0.f;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-        const int s = lane + 32 * i;
-        cnt[i] = (s < g.S) ? static_cast<float>(segment_rows(g, s)) : 0.f;
-        acc = fmaf(cnt[i], mu[i], acc);
-    }
+    for (int i = 0; i < PER_LANE; ++i) acc = fmaf(r[i].z, r[i].x, acc);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     const float mean = acc / static_cast<float>(g.L);
     float acc2 = 0.f;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
-        const float d = mu[i] - mean;
-        acc2 += fmaf(cnt[i] * d, d, m2[i]);
+        const float d = r[i].x - mean;
+        acc2 += fmaf(r[i].z * d, d, r[i].y);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc2 += __shfl_xor_sync(0xffffffffu, acc2, off);
     return make_float2(mean, acc2);
 }
 
-// Chan merge of the Cg channel records of group (n, g): (mean, rstd).
-__device__ __forceinline__ float2 combine_group(const Args &a, const float2 *ch, int Cg)
+// Chan merge of the Cg channel records of one group, by one warp: the mean
+// of the channel means, then the within- plus between-channel squares.
+// Returns (mean, rstd) in every lane.
+__device__ __forceinline__ float2 merge_group_warp(const float2 *rec, int Cg, float Lf, float eps)
 {
+    const int lane = threadIdx.x & 31;
     float mu = 0.f;
-    for (int j = 0; j < Cg; ++j) mu += ch[j].x;
+    for (int j = lane; j < Cg; j += 32) mu += rec[j].x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mu += __shfl_xor_sync(0xffffffffu, mu, off);
     mu /= static_cast<float>(Cg);
-    const float Lf = static_cast<float>(a.g.L);
     float M2 = 0.f;
-    for (int j = 0; j < Cg; ++j) {
-        const float d = ch[j].x - mu;
-        M2 += fmaf(Lf * d, d, ch[j].y);
+    for (int j = lane; j < Cg; j += 32) {
+        const float d = rec[j].x - mu;
+        M2 += fmaf(Lf * d, d, rec[j].y);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M2 += __shfl_xor_sync(0xffffffffu, M2, off);
     const float var = fmaxf(M2 / (Lf * static_cast<float>(Cg)), 0.f);
-    return make_float2(mu, 1.0f / sqrtf(var + a.eps));
+    return make_float2(mu, 1.0f / sqrtf(var + eps));
 }
 
 // ---------------------------------------------------------------------------
 // consumers: pass 2 (reverse order, in place in shared memory)
 // ---------------------------------------------------------------------------
-template <bool SILU>
-__device__ __forceinline__ uint32_t apply_pair(uint32_t w, f2_t sc, f2_t sh)
+// SiLU(z) = z * sigmoid(z): sigmoid from one ex2 and one reciprocal (MUFU
+// approximations, a few ulp in fp32; the MUFU pipes of an SM retire about 32
+// of these per clock, far above the element rate memory can feed).
+__device__ __forceinline__ float silu1(float z)
 {
-    f2_t z = fma2(bf2_to_f2(w), sc, sh);
-    if (SILU) z = silu2(z);
-    return f2_to_bf2(z);
+    const float e = ex2_approx(z * -1.4426950408889634f);   // exp(-z)
+    return z * rcp_approx(1.0f + e);
 }
 
-// Scale / shift of batch entry n into shared memory (fused kernel), from
-// the channel records of the whole grid and the gamma / beta table loaded at
-// kernel start.  All channel records come in with one batch of loads; then
-// one warp per group merges them (Chan: mean of the channel means, then the
-// within- plus between-channel squares) and writes the group's scale and
-// shift.  The statistics outputs are written by the one CTA that owns
-// segment 0 of n.
-__device__ void fused_group_finalize(const Args &a, const Smem &sm, int64_t n, bool write_stats)
+// y = x * scale + shift (+ SiLU) for the two bf16 values of one word.
+template <bool SILU>
+__device__ __forceinline__ uint32_t apply_pair(uint32_t w, float s0, float t0, float s1, float t1)
+{
+    float z0 = fmaf(__uint_as_float(w << 16), s0, t0);
+    float z1 = fmaf(__uint_as_float(w & 0xffff0000u), s1, t1);
+    if (SILU) {
+        z0 = silu1(z0);
+        z1 = silu1(z1);
+    }
+    const __nv_bfloat162 h = __floats2bfloat162_rn(z0, z1);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Scale / shift of batch entry n into shared memory (fused kernel): the
+// G group records (mean, rstd) written by the finalize step of the whole
+// grid come in with one small batch of loads, then every channel folds its
+// gamma / beta (loaded at kernel start) with its group's statistics.
+__device__ void fused_scale_shift(const Args &a, const Smem &sm, int64_t n)
 {
     const Geom &g = a.g;
     float2 *st = reinterpret_cast<float2 *>(sm.base + sm.lay.st);
     const float2 *gb = reinterpret_cast<const float2 *>(sm.base + sm.lay.gb);
-    const int lane = threadIdx.x & 31;
-    const float Lf = static_cast<float>(g.L);
-    for (int c = threadIdx.x; c < g.C; c += kConsumers) st[c] = __ldcg(a.chstat + n * g.C + c);
+    float2 *gs = reinterpret_cast<float2 *>(sm.base + sm.lay.gstat);
+    for (int grp = threadIdx.x; grp < g.G; grp += kConsumers) gs[grp] = __ldcg(a.gstat + n * g.G + grp);
     named_sync(1, kConsumers);
-    for (int grp = threadIdx.x >> 5; grp < g.G; grp += kConsumerWarps) {
-        const float2 *rec = st + grp * g.Cg;
-        float mu = 0.f;
-        for (int j = lane; j < g.Cg; j += 32) mu += rec[j].x;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mu += __shfl_xor_sync(0xffffffffu, mu, off);
-        mu /= static_cast<float>(g.Cg);
-        float M2 = 0.f;
-        for (int j = lane; j < g.Cg; j += 32) {
-            const float d = rec[j].x - mu;
-            M2 += fmaf(Lf * d, d, rec[j].y);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M2 += __shfl_xor_sync(0xffffffffu, M2, off);
-        const float var = fmaxf(M2 / (Lf * static_cast<float>(g.Cg)), 0.f);
-        const float rstd = 1.0f / sqrtf(var + a.eps);
-        if (write_stats && lane == 0) {
-            a.mean[n * g.G + grp] = mu;
-            a.rstd[n * g.G + grp] = rstd;
-        }
-        __syncwarp();   // every lane has read the group's records before they are overwritten
-        for (int j = lane; j < g.Cg; j += 32) {
-            const float2 ab = gb[grp * g.Cg + j];
-            const float sc = ab.x * rstd;
-            st[grp * g.Cg + j] = make_float2(sc, ab.y - mu * sc);
-        }
+    for (int c = threadIdx.x; c < g.C; c += kConsumers) {
+        const float2 r = gs[c / g.Cg];
+        const float2 ab = gb[c];
+        const float sc = ab.x * r.y;
+        st[c] = make_float2(sc, ab.y - r.x * sc);
     }
     named_sync(1, kConsumers);
 }
@@ -668,27 +631,24 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
     cursor_last(g, c);
     int slot = slot_of(T - 1, g.ring);
     int64_t cur_item = -1, cur_n = -1;
-    f2_t sc[4], sh[4];
+    float sc[8], sh[8];
     bool ok = !*ctl.abort;
     for (int64_t q = T - 1; q >= 0; --q) {
         if (c.it != cur_item) {
+            const float4 *src;
             if (FUSED) {
-                if (c.n != cur_n) fused_group_finalize(a, sm, c.n, c.s == 0);
-                const float4 *st = reinterpret_cast<const float4 *>(sm.base + sm.lay.st) + 4 * vslot;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 v = st[j];            // (s, t) of channels 2j, 2j+1
-                    sc[j] = pk(v.x, v.z);
-                    sh[j] = pk(v.y, v.w);
-                }
+                if (c.n != cur_n) fused_scale_shift(a, sm, c.n);
+                src = reinterpret_cast<const float4 *>(sm.base + sm.lay.st) + 4 * vslot;
             } else {
-                const float4 *src = reinterpret_cast<const float4 *>(a.st + c.n * g.C + 8 * vslot);
+                src = reinterpret_cast<const float4 *>(a.st + c.n * g.C + 8 * vslot);
+            }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 v = __ldcg(src + j);
-                    sc[j] = pk(v.x, v.z);
-                    sh[j] = pk(v.y, v.w);
-                }
+            for (int j = 0; j < 4; ++j) {
+                const float4 v = FUSED ? src[j] : __ldcg(src + j);   // (s, t) of channels 2j, 2j+1
+                sc[2 * j] = v.x;
+                sh[2 * j] = v.y;
+                sc[2 * j + 1] = v.z;
+                sh[2 * j + 1] = v.w;
             }
             cur_item = c.it;
             cur_n = c.n;
@@ -711,10 +671,10 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
                 const int v = tid + i * kConsumers;
                 if (v < nvec) {
                     const uint4 w = lds128(base + 16u * v);
-                    o[i].x = apply_pair<SILU>(w.x, sc[0], sh[0]);
-                    o[i].y = apply_pair<SILU>(w.y, sc[1], sh[1]);
-                    o[i].z = apply_pair<SILU>(w.z, sc[2], sh[2]);
-                    o[i].w = apply_pair<SILU>(w.w, sc[3], sh[3]);
+                    o[i].x = apply_pair<SILU>(w.x, sc[0], sh[0], sc[1], sh[1]);
+                    o[i].y = apply_pair<SILU>(w.y, sc[2], sh[2], sc[3], sh[3]);
+                    o[i].z = apply_pair<SILU>(w.z, sc[4], sh[4], sc[5], sh[5]);
+                    o[i].w = apply_pair<SILU>(w.w, sc[6], sh[6], sc[7], sh[7]);
                 }
             }
         }
@@ -795,11 +755,13 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant_
         if ((threadIdx.x & 31) == 0) fin_smem[j] = r;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const float2 r = combine_group(a, fin_smem, g.Cg);
-        fin_smem[g.Cg] = r;
-        a.mean[n * g.G + grp] = r.x;
-        a.rstd[n * g.G + grp] = r.y;
+    if (warp == 0) {
+        const float2 r = merge_group_warp(fin_smem, g.Cg, static_cast<float>(g.L), a.eps);
+        if (threadIdx.x == 0) {
+            fin_smem[g.Cg] = r;
+            a.mean[n * g.G + grp] = r.x;
+            a.rstd[n * g.G + grp] = r.y;
+        }
     }
     __syncthreads();
     const float2 r = fin_smem[g.Cg];
@@ -857,16 +819,30 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
     // every segment record of the grid is written
     grid_sync(a.sync, gridDim.x, ctl);
 
-    // finalize, step 1: channel records, (n, c) pairs spread over the grid,
-    // one warp each
+    // finalize, step 1: one (n, g) group per CTA at a time, spread over the
+    // grid: a warp per channel merges that channel's segment records, then
+    // warp 0 merges the group and publishes (mean, rstd)
     if (!*ctl.abort && threadIdx.x < kConsumers) {
-        const int64_t tasks = g.N * g.C;
-        for (int64_t t = blockIdx.x + static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x; t < tasks;
-             t += static_cast<int64_t>(kConsumerWarps) * gridDim.x) {
-            const int64_t n = t / g.C;
-            const int c = static_cast<int>(t - n * g.C);
-            const float2 r = combine_channel<kFusedMaxSegments / 32>(a, n, c);
-            if ((threadIdx.x & 31) == 0) a.chstat[t] = r;
+        float2 *rec = reinterpret_cast<float2 *>(g_smem + sm.lay.scratch);   // [Cg]
+        const int warp = threadIdx.x >> 5;
+        const int64_t tasks = g.N * g.G;
+        for (int64_t t = blockIdx.x; t < tasks; t += gridDim.x) {
+            const int64_t n = t / g.G;
+            const int grp = static_cast<int>(t - n * g.G);
+            for (int j = warp; j < g.Cg; j += kConsumerWarps) {
+                const float2 r = combine_channel<kFusedMaxSegments / 32>(a, n, grp * g.Cg + j);
+                if ((threadIdx.x & 31) == 0) rec[j] = r;
+            }
+            named_sync(1, kConsumers);
+            if (warp == 0) {
+                const float2 r = merge_group_warp(rec, g.Cg, static_cast<float>(g.L), a.eps);
+                if (threadIdx.x == 0) {
+                    a.gstat[t] = r;
+                    a.mean[t] = r.x;
+                    a.rstd[t] = r.y;
+                }
+            }
+            named_sync(1, kConsumers);
         }
     }
     grid_sync(a.sync, 2u * gridDim.x, ctl);
@@ -879,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
         }
     }
 
-    // finalize step 2 (per CTA, in consume_pass2) and pass 2
+    // finalize step 2 (scale / shift per CTA, in consume_pass2) and pass 2
     if (producer) {
         produce_pass2(a, sm, T, resident, ps, ctl);
         if (*ctl.abort) drain_loads(sm, ps, g.ring);
