@@ -158,6 +158,10 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     g.G = static_cast<int32_t>(G);
     g.Cg = static_cast<int32_t>(C / G);
     g.V = static_cast<int32_t>(C / 8);
+    g.log2V = 0;
+    while ((1 << g.log2V) < g.V) ++g.log2V;
+    g.log2Cg = 0;
+    while ((1 << g.log2Cg) < g.Cg) ++g.log2Cg;
     const int64_t row_bytes = 2 * C;
     const int64_t grid_target = d.sm_count;   // one CTA per SM (544 threads, most of shared memory)
     const int64_t total_bytes = N * L * row_bytes;
@@ -187,7 +191,7 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     // workspace
     size_t off = 256;   // barrier words
     p.off_partial = off;
-    off = align256(off + static_cast<size_t>(N) * C * S * sizeof(float4));
+    off = align256(off + static_cast<size_t>(N) * G * S * sizeof(float4));
     p.off_gstat = off;
     off = align256(off + static_cast<size_t>(N) * G * sizeof(float2));
     p.off_st = off;

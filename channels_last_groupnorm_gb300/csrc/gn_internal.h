@@ -17,6 +17,8 @@ constexpr int kMinPieceBytes = 1024;
 constexpr int kMaxSegments = 512;               // segments per batch entry
 constexpr int kFusedMaxSegments = 160;          // ... in the fused kernel (5 records per lane)
 constexpr int kScratchBytes = 16384;            // pass-1 CTA reduction scratch
+constexpr int kOneBarrierRecords = 8192;        // fused kernel: every CTA merges all G*S item records
+                                                // of its batch entry itself when there are at most this many
 constexpr int kSyncWords = 64;                  // 256-byte workspace header
 
 // The (N, L, C) tensor is cut into pieces of whole rows (one bulk copy
@@ -25,6 +27,7 @@ constexpr int kSyncWords = 64;                  // 256-byte workspace header
 struct Geom {
     int64_t N, L;
     int32_t C, G, Cg, V;          // V = C / 8 sixteen-byte vectors per row
+    int32_t log2V, log2Cg;        // C and Cg are powers of two
     int32_t rows_per_piece;
     int32_t piece_bytes;          // rows_per_piece * C * 2
     int64_t pieces_per_n;
@@ -42,7 +45,7 @@ struct Args {
     uint32_t l2_hints;            // bit 0: pass-2 loads evict_first, bit 1: pass-2
                                   // stores evict_first, bit 2: pass-1 loads evict_last
     Geom g;
-    float4 *partial;              // [N][C][S] item (mean, M2, count, unused)
+    float4 *partial;              // [N][G][S] group record per item (mean, M2, rows, unused)
     float2 *gstat;                // [N][G]    group (mean, rstd)   (fused)
     float2 *st;                   // [N][C]    (scale, shift)       (two-pass)
     float *mean, *rstd;           // [N][G]
@@ -51,9 +54,10 @@ struct Args {
 };
 
 // Byte offsets inside a CTA's dynamic shared memory.  `gstat` (per-group
-// mean / rstd of the fused kernel) shares the pass-1 scratch.
+// mean / rstd of the fused kernel) shares the pass-1 scratch; `chs` (the
+// per-channel (mean, M2) of one work item) shares `st` in the fused kernel.
 struct Layout {
-    uint32_t ring, scratch, kvec, st, gb, gstat, bars, flags, total;
+    uint32_t ring, scratch, kvec, chs, st, gb, gstat, bars, flags, total;
 };
 
 enum Kind { kPass1 = 1, kPass2 = 2, kFused = 3 };
@@ -70,8 +74,13 @@ __host__ __device__ inline Layout make_layout(const Geom &g, int kind)
     if (kind != kPass2) off += kScratchBytes;
     s.kvec = off;
     if (kind != kPass2) off += align_up(4u * g.C, 16);
+    s.chs = off;
+    if (kind == kPass1) off += 8u * g.C;
     s.st = off;
-    if (kind == kFused) off += 8u * g.C;
+    if (kind == kFused) {
+        s.chs = off;
+        off += 8u * g.C;
+    }
     s.gb = off;
     if (kind == kFused) off += 8u * g.C;
     s.bars = align_up(off, 16);

@@ -17,16 +17,18 @@
 //    packed fp32x2 instructions of sm_100+ (add/sub/fma .f32x2).
 //  * Pass 1 keeps, per thread, fp32 sums of (x - K) and (x - K)^2 with K a
 //    per-(work item, channel) shift (the item's first row), then reduces
-//    them per CTA with warp shuffles and shared memory into a per-item
-//    (mean, M2, count) record.  Items are merged with Chan's parallel
-//    formula, first over items per channel, then over the channels of a
-//    group.
+//    them per CTA with warp shuffles and shared memory into per-channel
+//    (mean, M2) and merges those (Chan's parallel formula) into one
+//    (mean, M2, rows) record per (batch entry, group, item).  The finalize
+//    merges the items' records of each group the same way.
 //  * Pass 2 loads pieces the same way, in the reverse of pass-1 order so the
 //    most recently read rows (still in L2) come first; each consumer thread
 //    takes its vectors out of the slot, releases the slot at once, and
 //    writes y with coalesced 16-byte global stores.
-//  * The fused kernel does all three steps in one cooperative launch with two
-//    grid barriers; pieces still in the ring after pass 1 are not re-read.
+//  * The fused kernel does all three steps in one cooperative launch: after
+//    one grid barrier every CTA merges the G*S records of its batch entry
+//    itself (a second barrier is used only when there are very many
+//    groups); pieces still in the ring after pass 1 are not re-read.
 //  * Every wait (mbarrier phase, grid barrier) is bounded by a deadline on
 //    the global timer, counted from the start of that wait; on expiry the
 //    kernel records a sticky status, stops issuing work, drains its own
@@ -366,25 +368,42 @@ __device__ void drain_loads(const Smem &sm, const ProducerState &ps, int ring)
 // ---------------------------------------------------------------------------
 // consumers: pass 1
 // ---------------------------------------------------------------------------
-// Scratch layout of the CTA reduction: [quantity j = 0..15][entry][slot]
-// floats (j < 8: sum of x - K for channel 8*slot + j; j >= 8: sum of
-// squares), so that consecutive threads (consecutive slots) touch
-// consecutive words and the stores are free of bank conflicts.
-__device__ __forceinline__ void store_entry(float *scr, int cap, int V, int entry, int vs, const float (&v1)[8],
-                                            const float (&v2)[8])
+__device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        scr[(j * cap + entry) * V + vs] = v1[j];
-        scr[((8 + j) * cap + entry) * V + vs] = v2[j];
-    }
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Scratch layout of the CTA reduction: float4 [quad q = 0..3][entry][slot]
+// (q = 0, 1: sums of x - K of channels 8*slot + 0..3, + 4..7; q = 2, 3: the
+// sums of squares), so that consecutive threads (consecutive slots) touch
+// consecutive 16-byte words: no bank conflicts, four stores per thread.
+__device__ __forceinline__ float4 *scr_at(float4 *scr, int cap, const Geom &g, int q, int entry, int vs)
+{
+    return scr + (((q * cap + entry) << g.log2V) + vs);
+}
+
+__device__ __forceinline__ void store_entry(float4 *scr, int cap, const Geom &g, int entry, int vs,
+                                            const float (&v1)[8], const float (&v2)[8])
+{
+    *scr_at(scr, cap, g, 0, entry, vs) = make_float4(v1[0], v1[1], v1[2], v1[3]);
+    *scr_at(scr, cap, g, 1, entry, vs) = make_float4(v1[4], v1[5], v1[6], v1[7]);
+    *scr_at(scr, cap, g, 2, entry, vs) = make_float4(v2[0], v2[1], v2[2], v2[3]);
+    *scr_at(scr, cap, g, 3, entry, vs) = make_float4(v2[4], v2[5], v2[6], v2[7]);
+}
+
+__device__ __forceinline__ float comp(const float4 &v, int j)
+{
+    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
 // Reduce the per-thread shifted sums of one work item into the item's
-// per-channel (mean, M2, count) record.  Threads that share a vector slot
+// per-group (mean, M2, rows) records.  Threads that share a vector slot
 // first combine by warp shuffles (when the slot repeats inside a warp), then
 // through shared memory; when the scratch cannot hold every entry at once,
-// the upper half of the entries is first added into the lower half.
+// the upper half of the entries is first added into the lower half.  The
+// per-channel results are then merged into one record per group.
 __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, const f2_t (&s1p)[4],
                             const f2_t (&s2p)[4])
 {
@@ -398,6 +417,7 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
         upk(s1p[i], v1[2 * i], v1[2 * i + 1]);
         upk(s2p[i], v2[2 * i], v2[2 * i + 1]);
     }
+    const int vs_own = tid & (g.V - 1);
     int entries, entry;
     bool holder;   // this thread holds one entry of its slot
     if (g.V < 32) {
@@ -412,46 +432,76 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
         entry = warp;
         holder = lane < g.V;
     } else {
-        entries = kConsumers / g.V;
-        entry = tid / g.V;
+        entries = kConsumers >> g.log2V;
+        entry = tid >> g.log2V;
         holder = true;
     }
-    float *scr = reinterpret_cast<float *>(sm.base + sm.lay.scratch);
-    const int cap = kScratchBytes / (64 * g.V);   // entries per slot the scratch holds
-    const int vs_own = tid % g.V;
+    float4 *scr = reinterpret_cast<float4 *>(sm.base + sm.lay.scratch);
+    const int cap = (kScratchBytes / 64) >> g.log2V;   // entries per slot the scratch holds
     int live = entries;
     while (live > cap) {
         const int half = live >> 1;
-        if (holder && entry >= half) store_entry(scr, cap, g.V, entry - half, vs_own, v1, v2);
+        if (holder && entry >= half) store_entry(scr, cap, g, entry - half, vs_own, v1, v2);
         named_sync(1, kConsumers);
         if (holder && entry < half) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                v1[j] += scr[(j * cap + entry) * g.V + vs_own];
-                v2[j] += scr[((8 + j) * cap + entry) * g.V + vs_own];
-            }
+            const float4 a0 = *scr_at(scr, cap, g, 0, entry, vs_own);
+            const float4 a1 = *scr_at(scr, cap, g, 1, entry, vs_own);
+            const float4 b0 = *scr_at(scr, cap, g, 2, entry, vs_own);
+            const float4 b1 = *scr_at(scr, cap, g, 3, entry, vs_own);
+            v1[0] += a0.x; v1[1] += a0.y; v1[2] += a0.z; v1[3] += a0.w;
+            v1[4] += a1.x; v1[5] += a1.y; v1[6] += a1.z; v1[7] += a1.w;
+            v2[0] += b0.x; v2[1] += b0.y; v2[2] += b0.z; v2[3] += b0.w;
+            v2[4] += b1.x; v2[5] += b1.y; v2[6] += b1.z; v2[7] += b1.w;
         }
         if (entry >= half) holder = false;
         named_sync(1, kConsumers);
         live = half;
     }
-    if (holder) store_entry(scr, cap, g.V, entry, vs_own, v1, v2);
+    if (holder) store_entry(scr, cap, g, entry, vs_own, v1, v2);
     named_sync(1, kConsumers);
     const float *kvec = reinterpret_cast<const float *>(sm.base + sm.lay.kvec);
+    float2 *chs = reinterpret_cast<float2 *>(sm.base + sm.lay.chs);
     const float count = static_cast<float>(item_rows(g, c));
-    // thread t finishes channel 8 * (t % V) + t / V: consecutive threads
-    // read consecutive slots of one quantity row
+    const float inv_count = 1.0f / count;
+    // per channel (mean, M2) of the item; thread t finishes channel
+    // 8 * (t % V) + t / V: consecutive threads read consecutive slots
     for (int idx = tid; idx < g.C; idx += kConsumers) {
-        const int vs = idx % g.V, j = idx / g.V;
+        const int vs = idx & (g.V - 1), j = idx >> g.log2V;
         const int ch = 8 * vs + j;
         float S1 = 0.f, S2 = 0.f;
         for (int e = 0; e < live; ++e) {
-            S1 += scr[(j * cap + e) * g.V + vs];
-            S2 += scr[((8 + j) * cap + e) * g.V + vs];
+            S1 += comp(*scr_at(scr, cap, g, j >> 2, e, vs), j & 3);
+            S2 += comp(*scr_at(scr, cap, g, 2 + (j >> 2), e, vs), j & 3);
         }
-        const float m = S1 / count;
-        const float M2 = fmaxf(S2 - S1 * m, 0.f);
-        a.partial[(c.n * g.C + ch) * g.S + c.s] = make_float4(kvec[ch] + m, M2, count, 0.f);
+        const float m = S1 * inv_count;
+        chs[ch] = make_float2(kvec[ch] + m, fmaxf(S2 - S1 * m, 0.f));
+    }
+    named_sync(1, kConsumers);
+    // channels -> one record per group (Chan with equal counts: the mean of
+    // the channel means, then the within- plus between-channel squares).
+    // With Cg <= 16 a warp takes two groups, one per half-warp.
+    const float inv_cg = 1.0f / static_cast<float>(g.Cg);   // exact: Cg is a power of two
+    const int span = g.Cg <= 16 ? 16 : 32;                  // lanes per group
+    const int sub = lane / span;                            // which group of the warp
+    const int sl = lane & (span - 1);
+    const int per_warp = 32 / span;
+    for (int base = warp * per_warp; base < g.G; base += kConsumerWarps * per_warp) {
+        const int grp = base + sub;
+        const bool active = grp < g.G;
+        const float2 *cr = chs + (active ? grp : 0) * g.Cg;
+        float mu = 0.f;
+        if (active)
+            for (int j = sl; j < g.Cg; j += span) mu += cr[j].x;
+        for (int off = span >> 1; off > 0; off >>= 1) mu += __shfl_xor_sync(0xffffffffu, mu, off);
+        mu *= inv_cg;
+        float M2 = 0.f;
+        if (active)
+            for (int j = sl; j < g.Cg; j += span) {
+                const float d = cr[j].x - mu;
+                M2 += fmaf(count * d, d, cr[j].y);
+            }
+        for (int off = span >> 1; off > 0; off >>= 1) M2 += __shfl_xor_sync(0xffffffffu, M2, off);
+        if (active && sl == 0) a.partial[(c.n * g.G + grp) * g.S + c.s] = make_float4(mu, M2, count, 0.f);
     }
     named_sync(1, kConsumers);
 }
@@ -461,7 +511,7 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
     const Geom &g = a.g;
     if (T == 0) return;
     const int tid = threadIdx.x;
-    const int vslot = tid % g.V;
+    const int vslot = tid & (g.V - 1);
     float *kvec = reinterpret_cast<float *>(sm.base + sm.lay.kvec);
     Cursor c;
     cursor_first(g, c);
@@ -519,57 +569,36 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
 // ---------------------------------------------------------------------------
 // finalize pieces
 // ---------------------------------------------------------------------------
-// Chan merge of the S segment records of channel (n, c), by one warp;
-// S <= 32 * PER_LANE.
+// Chan merge, by one warp, of the S item records of group (n, grp): each
+// record holds the mean and M2 of rows * Cg elements.  Returns (mean, rstd)
+// in every lane.  Lane l holds records l, l + 32, ... (S <= 32 * PER_LANE);
+// records past S are zero, which leaves every sum unchanged.
 template <int PER_LANE>
-__device__ __forceinline__ float2 combine_channel(const Args &a, int64_t n, int c)
+__device__ __forceinline__ float2 merge_items_warp(const Args &a, int64_t n, int grp)
 {
     const Geom &g = a.g;
     const int lane = threadIdx.x & 31;
-    const float4 *src = a.partial + (n * g.C + c) * g.S;
+    const float4 *src = a.partial + (n * g.G + grp) * g.S;
     float4 r[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
         const int s = lane + 32 * i;
-        r[i] = (s < g.S) ? __ldcg(src + s) : make_float4(0.f, 0.f, 0.f, 0.f);   // (mean, M2, count, -)
+        r[i] = (s < g.S) ? __ldcg(src + s) : make_float4(0.f, 0.f, 0.f, 0.f);   // (mean, M2, rows, -)
     }
     float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) acc = fmaf(r[i].z, r[i].x, acc);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    const float mean = acc / static_cast<float>(g.L);
+    const float Lf = static_cast<float>(g.L);
+    const float mean = warp_sum(acc) / Lf;
+    const float cgf = static_cast<float>(g.Cg);
     float acc2 = 0.f;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
         const float d = r[i].x - mean;
-        acc2 += fmaf(r[i].z * d, d, r[i].y);
+        acc2 += fmaf(cgf * r[i].z * d, d, r[i].y);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc2 += __shfl_xor_sync(0xffffffffu, acc2, off);
-    return make_float2(mean, acc2);
-}
-
-// Chan merge of the Cg channel records of one group, by one warp: the mean
-// of the channel means, then the within- plus between-channel squares.
-// Returns (mean, rstd) in every lane.
-__device__ __forceinline__ float2 merge_group_warp(const float2 *rec, int Cg, float Lf, float eps)
-{
-    const int lane = threadIdx.x & 31;
-    float mu = 0.f;
-    for (int j = lane; j < Cg; j += 32) mu += rec[j].x;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mu += __shfl_xor_sync(0xffffffffu, mu, off);
-    mu /= static_cast<float>(Cg);
-    float M2 = 0.f;
-    for (int j = lane; j < Cg; j += 32) {
-        const float d = rec[j].x - mu;
-        M2 += fmaf(Lf * d, d, rec[j].y);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M2 += __shfl_xor_sync(0xffffffffu, M2, off);
-    const float var = fmaxf(M2 / (Lf * static_cast<float>(Cg)), 0.f);
-    return make_float2(mu, 1.0f / sqrtf(var + eps));
+    const float var = fmaxf(warp_sum(acc2) / (Lf * cgf), 0.f);
+    return make_float2(mean, 1.0f / sqrtf(var + a.eps));
 }
 
 // ---------------------------------------------------------------------------
@@ -619,6 +648,36 @@ __device__ void fused_scale_shift(const Args &a, const Smem &sm, int64_t n)
     named_sync(1, kConsumers);
 }
 
+// Scale / shift of batch entry n when every CTA merges the group records
+// itself (one-barrier fused schedule): one warp per group merges the S item
+// records, then every channel folds its gamma / beta with its group's
+// statistics.  The CTA that owns item 0 of n writes the statistics outputs.
+__device__ void fused_local_stats(const Args &a, const Smem &sm, int64_t n, bool write_stats)
+{
+    const Geom &g = a.g;
+    float2 *st = reinterpret_cast<float2 *>(sm.base + sm.lay.st);
+    const float2 *gb = reinterpret_cast<const float2 *>(sm.base + sm.lay.gb);
+    float2 *gs = reinterpret_cast<float2 *>(sm.base + sm.lay.gstat);
+    for (int grp = threadIdx.x >> 5; grp < g.G; grp += kConsumerWarps) {
+        const float2 r = merge_items_warp<kFusedMaxSegments / 32>(a, n, grp);
+        if ((threadIdx.x & 31) == 0) {
+            gs[grp] = r;
+            if (write_stats) {
+                a.mean[n * g.G + grp] = r.x;
+                a.rstd[n * g.G + grp] = r.y;
+            }
+        }
+    }
+    named_sync(1, kConsumers);
+    for (int c = threadIdx.x; c < g.C; c += kConsumers) {
+        const float2 r = gs[c / g.Cg];
+        const float2 ab = gb[c];
+        const float sc = ab.x * r.y;
+        st[c] = make_float2(sc, ab.y - r.x * sc);
+    }
+    named_sync(1, kConsumers);
+}
+
 template <bool SILU, bool FUSED>
 __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t resident, uint32_t &full_par,
                               const Ctl &ctl)
@@ -626,7 +685,7 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
     const Geom &g = a.g;
     if (T == 0) return;
     const int tid = threadIdx.x;
-    const int vslot = tid % g.V;
+    const int vslot = tid & (g.V - 1);
     Cursor c;
     cursor_last(g, c);
     int slot = slot_of(T - 1, g.ring);
@@ -637,7 +696,12 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
         if (c.it != cur_item) {
             const float4 *src;
             if (FUSED) {
-                if (c.n != cur_n) fused_scale_shift(a, sm, c.n);
+                if (c.n != cur_n) {
+                    if (g.G * g.S <= kOneBarrierRecords)
+                        fused_local_stats(a, sm, c.n, c.s == 0);
+                    else
+                        fused_scale_shift(a, sm, c.n);
+                }
                 src = reinterpret_cast<const float4 *>(sm.base + sm.lay.st) + 4 * vslot;
             } else {
                 src = reinterpret_cast<const float4 *>(a.st + c.n * g.C + 8 * vslot);
@@ -742,30 +806,23 @@ __global__ void __launch_bounds__(kThreads, 1) gn_pass1_kernel(const __grid_cons
     consume_pass1(a, sm, T, full_par, ctl);
 }
 
+// Two-pass schedule, step 2: one warp per (n, g) merges the group's item
+// records, writes mean / rstd and the scale / shift of its Cg channels.
 __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant__ Args a)
 {
-    extern __shared__ __align__(16) float2 fin_smem[];   // [Cg] channel records + 1
     if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return;
     const Geom &g = a.g;
-    const int64_t n = blockIdx.x / g.G;
-    const int grp = static_cast<int>(blockIdx.x % g.G);
-    const int warp = threadIdx.x >> 5;
-    for (int j = warp; j < g.Cg; j += 8) {
-        const float2 r = combine_channel<kMaxSegments / 32>(a, n, grp * g.Cg + j);
-        if ((threadIdx.x & 31) == 0) fin_smem[j] = r;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (t >= g.N * g.G) return;
+    const int64_t n = t / g.G;
+    const int grp = static_cast<int>(t - n * g.G);
+    const int lane = threadIdx.x & 31;
+    const float2 r = merge_items_warp<kMaxSegments / 32>(a, n, grp);
+    if (lane == 0) {
+        a.mean[t] = r.x;
+        a.rstd[t] = r.y;
     }
-    __syncthreads();
-    if (warp == 0) {
-        const float2 r = merge_group_warp(fin_smem, g.Cg, static_cast<float>(g.L), a.eps);
-        if (threadIdx.x == 0) {
-            fin_smem[g.Cg] = r;
-            a.mean[n * g.G + grp] = r.x;
-            a.rstd[n * g.G + grp] = r.y;
-        }
-    }
-    __syncthreads();
-    const float2 r = fin_smem[g.Cg];
-    for (int j = threadIdx.x; j < g.Cg; j += 256) {
+    for (int j = lane; j < g.Cg; j += 32) {
         const int c = grp * g.Cg + j;
         const float sc = a.gamma[c] * r.y;
         a.st[n * g.C + c] = make_float2(sc, a.beta[c] - r.x * sc);
@@ -816,38 +873,30 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
     } else if (threadIdx.x < kConsumers) {
         consume_pass1(a, sm, T, full_par, ctl);
     }
-    // every segment record of the grid is written
+    // every item record of the grid is written
     grid_sync(a.sync, gridDim.x, ctl);
-
-    // finalize, step 1: one (n, g) group per CTA at a time, spread over the
-    // grid: a warp per channel merges that channel's segment records, then
-    // warp 0 merges the group and publishes (mean, rstd)
-    if (!*ctl.abort && threadIdx.x < kConsumers) {
-        float2 *rec = reinterpret_cast<float2 *>(g_smem + sm.lay.scratch);   // [Cg]
-        const int warp = threadIdx.x >> 5;
-        const int64_t tasks = g.N * g.G;
-        for (int64_t t = blockIdx.x; t < tasks; t += gridDim.x) {
-            const int64_t n = t / g.G;
-            const int grp = static_cast<int>(t - n * g.G);
-            for (int j = warp; j < g.Cg; j += kConsumerWarps) {
-                const float2 r = combine_channel<kFusedMaxSegments / 32>(a, n, grp * g.Cg + j);
-                if ((threadIdx.x & 31) == 0) rec[j] = r;
-            }
-            named_sync(1, kConsumers);
-            if (warp == 0) {
-                const float2 r = merge_group_warp(rec, g.Cg, static_cast<float>(g.L), a.eps);
-                if (threadIdx.x == 0) {
+    const bool one_barrier = g.G * g.S <= kOneBarrierRecords;
+    if (!one_barrier) {
+        // finalize, step 1 (many groups): one warp per (n, g) task, spread
+        // over the grid, merges the group's item records and publishes
+        // (mean, rstd); a second barrier makes them visible to every CTA
+        if (!*ctl.abort && threadIdx.x < kConsumers) {
+            const int64_t tasks = g.N * g.G;
+            for (int64_t t = static_cast<int64_t>(blockIdx.x) * kConsumerWarps + (threadIdx.x >> 5); t < tasks;
+                 t += static_cast<int64_t>(gridDim.x) * kConsumerWarps) {
+                const int64_t n = t / g.G;
+                const float2 r = merge_items_warp<kFusedMaxSegments / 32>(a, n, static_cast<int>(t - n * g.G));
+                if ((threadIdx.x & 31) == 0) {
                     a.gstat[t] = r;
                     a.mean[t] = r.x;
                     a.rstd[t] = r.y;
                 }
             }
-            named_sync(1, kConsumers);
         }
+        grid_sync(a.sync, 2u * gridDim.x, ctl);
     }
-    grid_sync(a.sync, 2u * gridDim.x, ctl);
     if (threadIdx.x == kConsumers + 1 && !*ctl.abort) {
-        // the last CTA past the second barrier re-arms the counters (done by
+        // the last CTA past the last barrier re-arms the counters (done by
         // an otherwise idle producer-warp lane, off the consumers' path)
         if (atomicAdd(a.sync + 1, 1u) == gridDim.x - 1) {
             atomicExch(a.sync, 0u);
@@ -855,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
         }
     }
 
-    // finalize step 2 (scale / shift per CTA, in consume_pass2) and pass 2
+    // group statistics / scale and shift (per CTA, in consume_pass2), pass 2
     if (producer) {
         produce_pass2(a, sm, T, resident, ps, ctl);
         if (*ctl.abort) drain_loads(sm, ps, g.ring);
@@ -918,7 +967,7 @@ cudaError_t prepare_kernels(uint32_t max_smem)
         return e;
     if ((e = cudaFuncSetAttribute(gn_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sz)))
         return e;
-    return cudaFuncSetAttribute(gn_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 2049 + 16);
+    return cudaSuccess;
 }
 
 cudaError_t launch_pass1(const Args &a, int grid, cudaStream_t s)
@@ -929,8 +978,7 @@ cudaError_t launch_pass1(const Args &a, int grid, cudaStream_t s)
 
 cudaError_t launch_finalize(const Args &a, cudaStream_t s)
 {
-    const uint32_t smem = 8u * (a.g.Cg + 1);
-    gn_finalize_kernel<<<static_cast<unsigned>(a.g.N * a.g.G), 256, smem, s>>>(a);
+    gn_finalize_kernel<<<static_cast<unsigned>((a.g.N * a.g.G + 7) / 8), 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

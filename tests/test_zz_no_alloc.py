@@ -68,7 +68,7 @@ def test_static_matches_ordinary_entry_point_twice(shape, silu):
 
 
 def test_static_refuses_shapes_beyond_its_scratch():
-    N, L, C, G = 256, 16, 2048, 32
+    N, L, C, G = 1024, 16, 2048, 32       # 64 MiB of x; scale/shift alone need 16 MiB
     assert gs.gn_silu_workspace_bytes(N, L, C, G) > STATIC_SCRATCH_BYTES
     x = torch.zeros((N, L, C), dtype=torch.bfloat16, device="cuda")
     g = torch.ones(C, device="cuda")
