@@ -234,6 +234,13 @@ def time_graph(graph, stream):
     return t0.elapsed_time(t1) / 1e3
 
 
+def raw_entry(w):
+    """The C entry point a workload goes through: gn_silu_rows_any for a C
+    that is not a power of two (and for 5D input), else gn_silu_rows_ex."""
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    return gs.raw_gn_silu_rows_any if (w.general or w.D > 1) else gs.raw_gn_silu_rows_ex
+
+
 def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, sampler=None,
                      seeded=True, launch="graph"):
     """Device-resident timing of one workload.  Returns a dict."""
@@ -259,13 +266,13 @@ def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, s
     xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
     ys = [torch.empty_like(x0) for _ in range(nsets)]
     h = stream.cuda_stream
+    entry = raw_entry(w)
 
     def call(i):
-        rc = gs.raw_gn_silu_rows_ex(xs[i].data_ptr(), gamma.data_ptr(), beta.data_ptr(),
-                                    ys[i].data_ptr(), w.N, w.L, w.C, w.G, w.eps, 1,
-                                    variant=variant_id, stream=h)
+        rc = entry(xs[i].data_ptr(), gamma.data_ptr(), beta.data_ptr(), ys[i].data_ptr(), w.N, w.L,
+                   w.C, w.G, w.eps, 1, variant=variant_id, stream=h)
         if rc != 0:
-            raise RuntimeError(f"gn_silu_rows_ex failed: {gs.status_string(rc)}")
+            raise RuntimeError(f"{entry.__name__} failed: {gs.status_string(rc)}")
 
     with torch.cuda.stream(stream):
         for i in range(max(3, warmup)):
@@ -327,13 +334,14 @@ def measure_e2e(w, variant_id, steps, warmup, device, stream):
     db = torch.empty_like(hb, device=device)
     dy = torch.empty_like(hx, device=device)
     h = stream.cuda_stream
+    entry = raw_entry(w)
 
     def step(_):
         dx.copy_(hx, non_blocking=True)
         dg.copy_(hg, non_blocking=True)
         db.copy_(hb, non_blocking=True)
-        rc = gs.raw_gn_silu_rows_ex(dx.data_ptr(), dg.data_ptr(), db.data_ptr(), dy.data_ptr(),
-                                    w.N, w.L, w.C, w.G, w.eps, 1, variant=variant_id, stream=h)
+        rc = entry(dx.data_ptr(), dg.data_ptr(), db.data_ptr(), dy.data_ptr(),
+                   w.N, w.L, w.C, w.G, w.eps, 1, variant=variant_id, stream=h)
         if rc != 0:
             raise RuntimeError(gs.status_string(rc))
         hy.copy_(dy, non_blocking=True)
@@ -371,17 +379,19 @@ def cpu_baseline(w, budget_s=12.0):
 
 
 def sweep(variant_id, device, stream, peak, launch="graph"):
-    """Every workload shape: us/call and effective bandwidth at 4 B/elem
-    (read once + write once) and 6 B/elem (two-pass byte count)."""
+    """Every workload shape, the general-channel ones included: us/call and
+    effective bandwidth at 4 B/elem (read once + write once) and 6 B/elem
+    (two-pass byte count)."""
     from channels_last_groupnorm_gb300 import workloads as wl
     out = []
-    for w in wl.WORKLOADS:
+    for w in wl.WORKLOADS + wl.GENERAL_WORKLOADS:
         r = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24),
                              launch=launch)
         us = statistics.median(r["per_step_ms"]) * 1e3
         gbs4 = 4.0 * w.elements / (us * 1e-6) / 1e9
         gbs6 = 6.0 * w.elements / (us * 1e-6) / 1e9
-        out.append({"workload": w.name, "variant": r["variant"], "us_per_call": round(us, 2),
+        out.append({"workload": w.name, "C": w.C, "variant": r["variant"],
+                    "us_per_call": round(us, 2),
                     "gbs_4B": round(gbs4, 1), "gbs_6B": round(gbs6, 1),
                     "frac_4B": round(gbs4 / peak, 3), "frac_6B": round(gbs6 / peak, 3),
                     "pages_h200_us": w.pages_us_h200,

@@ -12,9 +12,11 @@ from .gnsilu import (  # noqa: F401
     gn_abi_version,
     gn_device_status,
     gn_kernel_launch_count,
+    gn_silu_ndhwc,
     gn_silu_nhwc,
     gn_silu_pick_variant,
     gn_silu_rows,
+    gn_silu_rows_any,
     gn_silu_rows_ex,
     gn_silu_workspace_bytes,
     status_string,

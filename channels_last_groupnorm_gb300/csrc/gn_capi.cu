@@ -6,6 +6,7 @@
 // decoder fast path behind quality=high", section "Modifications", item 1):
 // unsupported inputs (non-power-of-two C, C > 2048, ...) are refused so the
 // caller can fall back; here they return a status code and nothing runs.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -71,14 +72,24 @@ bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
     return a0 < b0 + nb && b0 < a0 + na;
 }
 
+// Channel counts an entry point serves: the power-of-two entries take the
+// page's contract (C a power of two in [8, 2048]); the general entries take
+// any C that is a multiple of 8 (one 16-byte vector) up to 2048.  Either way
+// G divides C.
+bool channels_ok(int64_t C, int64_t G, bool general)
+{
+    if (C < 8 || C > 2048) return false;
+    if (general ? (C % 8 != 0) : ((C & (C - 1)) != 0)) return false;
+    return G >= 1 && C % G == 0;
+}
+
 // Pure host checks (no CUDA call), in a fixed order.
 int validate(const void *x, const float *gamma, const float *beta, const void *y, int64_t N, int64_t L,
-             int64_t C, int64_t G, float eps, const float *mean_out, const float *rstd_out)
+             int64_t C, int64_t G, float eps, const float *mean_out, const float *rstd_out, bool general)
 {
     if (!x || !gamma || !beta || !y) return GN_ERR_NULL;
     if (N < 1 || L < 1) return GN_ERR_SHAPE;
-    if (C < 8 || C > 2048 || (C & (C - 1)) != 0) return GN_ERR_CHANNELS;
-    if (G < 1 || C % G != 0) return GN_ERR_CHANNELS;
+    if (!channels_ok(C, G, general)) return GN_ERR_CHANNELS;
     if (N > INT64_MAX / L) return GN_ERR_SHAPE;
     const int64_t rows = N * L;
     if (rows > INT64_MAX / (2 * C)) return GN_ERR_SHAPE;
@@ -158,18 +169,17 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     g.G = static_cast<int32_t>(G);
     g.Cg = static_cast<int32_t>(C / G);
     g.V = static_cast<int32_t>(C / 8);
-    g.log2V = 0;
-    while ((1 << g.log2V) < g.V) ++g.log2V;
-    g.log2Cg = 0;
-    while ((1 << g.log2Cg) < g.Cg) ++g.log2Cg;
+    g.A = (gn::kConsumers / g.V) * g.V;
     const int64_t row_bytes = 2 * C;
     const int64_t grid_target = d.sm_count;   // one CTA per SM (544 threads, most of shared memory)
     const int64_t total_bytes = N * L * row_bytes;
-    // pieces as large as 32 KB, smaller when that leaves fewer than about
-    // four pieces per CTA; never below one row
-    int64_t pb = gn::kMaxPieceBytes;
-    while (pb > row_bytes && pb > gn::kMinPieceBytes && total_bytes / pb < 4 * grid_target) pb /= 2;
-    if (pb < row_bytes) pb = row_bytes;
+    // pieces of whole rows, as large as 32 KB and at most kMaxVecPerThread
+    // vectors per data-carrying consumer thread; smaller when that leaves
+    // fewer than about four pieces per CTA; never below one row
+    const int64_t pb_cap = std::min<int64_t>(gn::kMaxPieceBytes, int64_t(g.A) * gn::kMaxVecPerThread * 16);
+    int64_t pb = pb_cap / row_bytes * row_bytes;
+    while (pb > row_bytes && pb > gn::kMinPieceBytes && total_bytes / pb < 4 * grid_target)
+        pb = std::max<int64_t>(row_bytes, (pb / 2) / row_bytes * row_bytes);
     g.piece_bytes = static_cast<int32_t>(pb);
     g.rows_per_piece = static_cast<int32_t>(pb / row_bytes);
     g.pieces_per_n = (L + g.rows_per_piece - 1) / g.rows_per_piece;
@@ -273,9 +283,9 @@ int library_workspace(int dev, cudaStream_t stream, size_t bytes, void **ptr)
 
 int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N, int64_t L, int64_t C,
         int64_t G, float eps, int apply_silu, float *mean_out, float *rstd_out, void *workspace,
-        size_t workspace_bytes, int variant, void *stream)
+        size_t workspace_bytes, int variant, void *stream, bool general = false)
 {
-    int rc = validate(x, gamma, beta, y, N, L, C, G, eps, mean_out, rstd_out);
+    int rc = validate(x, gamma, beta, y, N, L, C, G, eps, mean_out, rstd_out, general);
     if (rc != GN_OK) return rc;
     if (variant < GN_VARIANT_AUTO || variant > GN_VARIANT_FUSED) return GN_ERR_VARIANT;
     if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256) return GN_ERR_ALIGN;
@@ -343,6 +353,26 @@ int gn_silu_rows_ex(const void *x_bf16, const float *gamma, const float *beta, v
                workspace_bytes, variant, stream);
 }
 
+int gn_silu_rows_any(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16, int64_t N,
+                     int64_t L, int64_t C, int64_t G, float eps, int apply_silu, float *mean_out,
+                     float *rstd_out, void *workspace, size_t workspace_bytes, int variant, void *stream)
+{
+    return run(x_bf16, gamma, beta, y_bf16, N, L, C, G, eps, apply_silu, mean_out, rstd_out, workspace,
+               workspace_bytes, variant, stream, true);
+}
+
+int gn_silu_ndhwc(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16, int64_t N,
+                  int64_t D, int64_t H, int64_t W, int64_t C, int64_t G, float eps, int apply_silu,
+                  void *stream)
+{
+    if (D < 1 || H < 1 || W < 1 || H > INT64_MAX / W || D > INT64_MAX / (H * W)) {
+        if (!x_bf16 || !gamma || !beta || !y_bf16) return GN_ERR_NULL;
+        return GN_ERR_SHAPE;
+    }
+    return run(x_bf16, gamma, beta, y_bf16, N, D * H * W, C, G, eps, apply_silu, nullptr, nullptr, nullptr, 0,
+               GN_VARIANT_AUTO, stream, true);
+}
+
 int gn_silu_rows(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16, int64_t N,
                  int64_t L, int64_t C, int64_t G, float eps, int apply_silu, void *stream)
 {
@@ -363,7 +393,7 @@ int gn_silu_nhwc(const void *x_bf16, const float *gamma, const float *beta, void
 size_t gn_silu_workspace_bytes(int64_t N, int64_t L, int64_t C, int64_t G)
 {
     if (N < 1 || L < 1 || N > INT64_MAX / L || N * L > INT64_MAX / (2 * 2048)) return 0;
-    if (C < 8 || C > 2048 || (C & (C - 1)) != 0 || G < 1 || C % G != 0) return 0;
+    if (!channels_ok(C, G, true)) return 0;
     int dev = -1;
     DeviceInfo d;
     if (current_device(&dev, &d) != GN_OK) return 0;
@@ -373,7 +403,7 @@ size_t gn_silu_workspace_bytes(int64_t N, int64_t L, int64_t C, int64_t G)
 int gn_silu_pick_variant(int64_t N, int64_t L, int64_t C, int64_t G)
 {
     if (N < 1 || L < 1 || N > INT64_MAX / L) return -GN_ERR_SHAPE;
-    if (C < 8 || C > 2048 || (C & (C - 1)) != 0 || G < 1 || C % G != 0) return -GN_ERR_CHANNELS;
+    if (!channels_ok(C, G, true)) return -GN_ERR_CHANNELS;
     int dev = -1;
     DeviceInfo d;
     const int rc = current_device(&dev, &d);
@@ -431,7 +461,9 @@ const char *gn_status_string(int status)
     case GN_OK: return "GN_OK: success";
     case GN_ERR_NULL: return "GN_ERR_NULL: a required pointer is NULL";
     case GN_ERR_SHAPE: return "GN_ERR_SHAPE: N, L, H or W below 1, or the element count overflows";
-    case GN_ERR_CHANNELS: return "GN_ERR_CHANNELS: C must be a power of two in [8, 2048] and G must divide C";
+    case GN_ERR_CHANNELS:
+        return "GN_ERR_CHANNELS: C must be a power of two in [8, 2048] (a multiple of 8 up to 2048 for "
+               "gn_silu_rows_any / gn_silu_ndhwc) and G must divide C";
     case GN_ERR_ALIGN: return "GN_ERR_ALIGN: x/y need 16-byte, gamma/beta/statistics 4-byte, workspace 256-byte alignment";
     case GN_ERR_EPS: return "GN_ERR_EPS: eps must be finite and non-negative";
     case GN_ERR_ALIAS: return "GN_ERR_ALIAS: y overlaps x (other than in place) or another argument";
@@ -444,6 +476,6 @@ const char *gn_status_string(int status)
     }
 }
 
-int gn_abi_version(void) { return 1; }
+int gn_abi_version(void) { return 2; }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ constexpr int kSyncWords = 64;                  // 256-byte workspace header
 struct Geom {
     int64_t N, L;
     int32_t C, G, Cg, V;          // V = C / 8 sixteen-byte vectors per row
-    int32_t log2V, log2Cg;        // C and Cg are powers of two
+    int32_t A;                    // consumer threads that carry data: (512 / V) * V
     int32_t rows_per_piece;
     int32_t piece_bytes;          // rows_per_piece * C * 2
     int64_t pieces_per_n;

@@ -375,13 +375,27 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// Vector-slot bookkeeping.  A thread's 16-byte vector v of a piece holds
+// channels 8 * (v % V) .. + 7.  POW2: C is a power of two, so V divides the
+// 512 consumer threads and every one carries data (A = 512) and the slot
+// arithmetic is a mask and a shift.  Otherwise A = (512 / V) * V threads
+// carry data and the slot arithmetic divides.
+template <bool POW2>
+__device__ __forceinline__ int carriers(const Geom &g) { return POW2 ? kConsumers : g.A; }
+
+template <bool POW2>
+__device__ __forceinline__ int vec_slot(const Geom &g, int t) { return POW2 ? (t & (g.V - 1)) : (t % g.V); }
+
+template <bool POW2>
+__device__ __forceinline__ int vec_rank(const Geom &g, int t) { return POW2 ? (t >> (__ffs(g.V) - 1)) : (t / g.V); }
+
 // Scratch layout of the CTA reduction: float4 [quad q = 0..3][entry][slot]
 // (q = 0, 1: sums of x - K of channels 8*slot + 0..3, + 4..7; q = 2, 3: the
 // sums of squares), so that consecutive threads (consecutive slots) touch
 // consecutive 16-byte words: no bank conflicts, four stores per thread.
 __device__ __forceinline__ float4 *scr_at(float4 *scr, int cap, const Geom &g, int q, int entry, int vs)
 {
-    return scr + (((q * cap + entry) << g.log2V) + vs);
+    return scr + ((q * cap + entry) * g.V + vs);
 }
 
 __device__ __forceinline__ void store_entry(float4 *scr, int cap, const Geom &g, int entry, int vs,
@@ -404,6 +418,7 @@ __device__ __forceinline__ float comp(const float4 &v, int j)
 // through shared memory; when the scratch cannot hold every entry at once,
 // the upper half of the entries is first added into the lower half.  The
 // per-channel results are then merged into one record per group.
+template <bool POW2>
 __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, const f2_t (&s1p)[4],
                             const f2_t (&s2p)[4])
 {
@@ -417,10 +432,10 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
         upk(s1p[i], v1[2 * i], v1[2 * i + 1]);
         upk(s2p[i], v2[2 * i], v2[2 * i + 1]);
     }
-    const int vs_own = tid & (g.V - 1);
+    const int vs_own = vec_slot<POW2>(g, tid);
     int entries, entry;
     bool holder;   // this thread holds one entry of its slot
-    if (g.V < 32) {
+    if (g.V < 32 && (32 % g.V) == 0) {
         for (int off = g.V; off < 32; off <<= 1) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -432,18 +447,20 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
         entry = warp;
         holder = lane < g.V;
     } else {
-        entries = kConsumers >> g.log2V;
-        entry = tid >> g.log2V;
-        holder = true;
+        // slots repeat across warps (or irregularly inside them): one entry
+        // per data-carrying thread
+        entries = vec_rank<POW2>(g, carriers<POW2>(g));
+        entry = vec_rank<POW2>(g, tid);
+        holder = tid < carriers<POW2>(g);
     }
     float4 *scr = reinterpret_cast<float4 *>(sm.base + sm.lay.scratch);
-    const int cap = (kScratchBytes / 64) >> g.log2V;   // entries per slot the scratch holds
+    const int cap = (kScratchBytes / 64) / g.V;   // entries per slot the scratch holds (>= 1)
     int live = entries;
     while (live > cap) {
-        const int half = live >> 1;
+        const int half = (live + 1) >> 1;        // entries [half, live) fold into [0, live - half)
         if (holder && entry >= half) store_entry(scr, cap, g, entry - half, vs_own, v1, v2);
         named_sync(1, kConsumers);
-        if (holder && entry < half) {
+        if (holder && entry + half < live) {
             const float4 a0 = *scr_at(scr, cap, g, 0, entry, vs_own);
             const float4 a1 = *scr_at(scr, cap, g, 1, entry, vs_own);
             const float4 b0 = *scr_at(scr, cap, g, 2, entry, vs_own);
@@ -466,7 +483,7 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
     // per channel (mean, M2) of the item; thread t finishes channel
     // 8 * (t % V) + t / V: consecutive threads read consecutive slots
     for (int idx = tid; idx < g.C; idx += kConsumers) {
-        const int vs = idx & (g.V - 1), j = idx >> g.log2V;
+        const int vs = vec_slot<POW2>(g, idx), j = vec_rank<POW2>(g, idx);
         const int ch = 8 * vs + j;
         float S1 = 0.f, S2 = 0.f;
         for (int e = 0; e < live; ++e) {
@@ -480,7 +497,7 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
     // channels -> one record per group (Chan with equal counts: the mean of
     // the channel means, then the within- plus between-channel squares).
     // With Cg <= 16 a warp takes two groups, one per half-warp.
-    const float inv_cg = 1.0f / static_cast<float>(g.Cg);   // exact: Cg is a power of two
+    const float cgf = static_cast<float>(g.Cg);
     const int span = g.Cg <= 16 ? 16 : 32;                  // lanes per group
     const int sub = lane / span;                            // which group of the warp
     const int sl = lane & (span - 1);
@@ -493,7 +510,7 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
         if (active)
             for (int j = sl; j < g.Cg; j += span) mu += cr[j].x;
         for (int off = span >> 1; off > 0; off >>= 1) mu += __shfl_xor_sync(0xffffffffu, mu, off);
-        mu *= inv_cg;
+        mu /= cgf;
         float M2 = 0.f;
         if (active)
             for (int j = sl; j < g.Cg; j += span) {
@@ -506,12 +523,15 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
     named_sync(1, kConsumers);
 }
 
+template <bool POW2>
 __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t &full_par, const Ctl &ctl)
 {
     const Geom &g = a.g;
     if (T == 0) return;
     const int tid = threadIdx.x;
-    const int vslot = tid & (g.V - 1);
+    const int vslot = vec_slot<POW2>(g, tid);
+    const int A = carriers<POW2>(g);
+    const bool carrier = tid < A;
     float *kvec = reinterpret_cast<float *>(sm.base + sm.lay.kvec);
     Cursor c;
     cursor_first(g, c);
@@ -547,7 +567,7 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
             }
             const int nvec = piece_rows(g, c.k) * g.V;
 #pragma unroll 4
-            for (int v = tid; v < nvec; v += kConsumers) {
+            for (int v = carrier ? tid : nvec; v < nvec; v += A) {
                 const uint4 w = lds128(base + 16u * v);
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -560,7 +580,7 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
         }
         __syncwarp();
         if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));
-        if (c.k == c.k_last) reduce_item(a, sm, c, s1, s2);
+        if (c.k == c.k_last) reduce_item<POW2>(a, sm, c, s1, s2);
         cursor_next(g, c);
         slot = (slot + 1 == g.ring) ? 0 : slot + 1;
     }
@@ -678,14 +698,16 @@ __device__ void fused_local_stats(const Args &a, const Smem &sm, int64_t n, bool
     named_sync(1, kConsumers);
 }
 
-template <bool SILU, bool FUSED>
+template <bool SILU, bool FUSED, bool POW2>
 __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t resident, uint32_t &full_par,
                               const Ctl &ctl)
 {
     const Geom &g = a.g;
     if (T == 0) return;
     const int tid = threadIdx.x;
-    const int vslot = tid & (g.V - 1);
+    const int vslot = vec_slot<POW2>(g, tid);
+    const int A = carriers<POW2>(g);
+    const int v0 = (tid < A) ? tid : (1 << 30);   // threads past A carry no data
     Cursor c;
     cursor_last(g, c);
     int slot = slot_of(T - 1, g.ring);
@@ -732,7 +754,7 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
             nvec = piece_rows(g, c.k) * g.V;
 #pragma unroll
             for (int i = 0; i < kMaxVecPerThread; ++i) {
-                const int v = tid + i * kConsumers;
+                const int v = v0 + i * A;
                 if (v < nvec) {
                     const uint4 w = lds128(base + 16u * v);
                     o[i].x = apply_pair<SILU>(w.x, sc[0], sh[0], sc[1], sh[1]);
@@ -748,7 +770,7 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
             uint4 *dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, c.n, c.k));
 #pragma unroll
             for (int i = 0; i < kMaxVecPerThread; ++i) {
-                const int v = tid + i * kConsumers;
+                const int v = v0 + i * A;
                 if (v < nvec) dst[v] = o[i];
             }
         }
@@ -788,6 +810,7 @@ __device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl 
 // ---------------------------------------------------------------------------
 // kernels
 // ---------------------------------------------------------------------------
+template <bool POW2>
 __global__ void __launch_bounds__(kThreads, 1) gn_pass1_kernel(const __grid_constant__ Args a)
 {
     Smem sm;
@@ -803,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) gn_pass1_kernel(const __grid_cons
         return;
     }
     uint32_t full_par = 0;
-    consume_pass1(a, sm, T, full_par, ctl);
+    consume_pass1<POW2>(a, sm, T, full_par, ctl);
 }
 
 // Two-pass schedule, step 2: one warp per (n, g) merges the group's item
@@ -829,7 +852,7 @@ __global__ void __launch_bounds__(256) gn_finalize_kernel(const __grid_constant_
     }
 }
 
-template <bool SILU>
+template <bool SILU, bool POW2>
 __global__ void __launch_bounds__(kThreads, 1) gn_pass2_kernel(const __grid_constant__ Args a)
 {
     Smem sm;
@@ -845,10 +868,10 @@ __global__ void __launch_bounds__(kThreads, 1) gn_pass2_kernel(const __grid_cons
         return;
     }
     uint32_t full_par = 0;
-    consume_pass2<SILU, false>(a, sm, T, 0, full_par, ctl);
+    consume_pass2<SILU, false, POW2>(a, sm, T, 0, full_par, ctl);
 }
 
-template <bool SILU>
+template <bool SILU, bool POW2>
 __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_constant__ Args a)
 {
     Smem sm;
@@ -871,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
     if (producer) {
         produce_pass1(a, sm, T, ps, ctl, true);
     } else if (threadIdx.x < kConsumers) {
-        consume_pass1(a, sm, T, full_par, ctl);
+        consume_pass1<POW2>(a, sm, T, full_par, ctl);
     }
     // every item record of the grid is written
     grid_sync(a.sync, gridDim.x, ctl);
@@ -909,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
         produce_pass2(a, sm, T, resident, ps, ctl);
         if (*ctl.abort) drain_loads(sm, ps, g.ring);
     } else if (threadIdx.x < kConsumers) {
-        consume_pass2<SILU, true>(a, sm, T, resident, full_par, ctl);
+        consume_pass2<SILU, true, POW2>(a, sm, T, resident, full_par, ctl);
     }
 }
 
@@ -954,26 +977,58 @@ __global__ void __launch_bounds__(32) gn_selftest_wait_kernel(int mode, uint64_t
 // ---------------------------------------------------------------------------
 static uint32_t smem_for(const Args &a, int kind) { return make_layout(a.g, kind).total; }
 
+// The POW2 instantiations serve every C whose vector slots divide the 512
+// consumer threads (C a power of two); the others serve the rest.
+static bool pow2_slots(const Geom &g) { return kConsumers % g.V == 0; }
+
+static const void *pass1_fn(bool pow2)
+{
+    return pow2 ? reinterpret_cast<const void *>(gn_pass1_kernel<true>)
+                : reinterpret_cast<const void *>(gn_pass1_kernel<false>);
+}
+
+static const void *pass2_fn(bool silu, bool pow2)
+{
+    if (silu)
+        return pow2 ? reinterpret_cast<const void *>(gn_pass2_kernel<true, true>)
+                    : reinterpret_cast<const void *>(gn_pass2_kernel<true, false>);
+    return pow2 ? reinterpret_cast<const void *>(gn_pass2_kernel<false, true>)
+                : reinterpret_cast<const void *>(gn_pass2_kernel<false, false>);
+}
+
+static const void *fused_fn(bool silu, bool pow2)
+{
+    if (silu)
+        return pow2 ? reinterpret_cast<const void *>(gn_fused_kernel<true, true>)
+                    : reinterpret_cast<const void *>(gn_fused_kernel<true, false>);
+    return pow2 ? reinterpret_cast<const void *>(gn_fused_kernel<false, true>)
+                : reinterpret_cast<const void *>(gn_fused_kernel<false, false>);
+}
+
 cudaError_t prepare_kernels(uint32_t max_smem)
 {
-    cudaError_t e;
     const int sz = static_cast<int>(max_smem);
-    if ((e = cudaFuncSetAttribute(gn_pass1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sz))) return e;
-    if ((e = cudaFuncSetAttribute(gn_pass2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sz)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gn_pass2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sz)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gn_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sz)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gn_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sz)))
-        return e;
+    for (int pow2 = 0; pow2 < 2; ++pow2) {
+        const void *fns[] = {pass1_fn(pow2), pass2_fn(true, pow2), pass2_fn(false, pow2), fused_fn(true, pow2),
+                             fused_fn(false, pow2)};
+        for (const void *fn : fns) {
+            const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, sz);
+            if (e != cudaSuccess) return e;
+        }
+    }
     return cudaSuccess;
+}
+
+static cudaError_t launch_plain(const void *fn, const Args &a, int grid, uint32_t smem, cudaStream_t s)
+{
+    Args copy = a;
+    void *params[] = {&copy};
+    return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), params, smem, s);
 }
 
 cudaError_t launch_pass1(const Args &a, int grid, cudaStream_t s)
 {
-    gn_pass1_kernel<<<grid, kThreads, smem_for(a, kPass1), s>>>(a);
-    return cudaGetLastError();
+    return launch_plain(pass1_fn(pow2_slots(a.g)), a, grid, smem_for(a, kPass1), s);
 }
 
 cudaError_t launch_finalize(const Args &a, cudaStream_t s)
@@ -984,27 +1039,28 @@ cudaError_t launch_finalize(const Args &a, cudaStream_t s)
 
 cudaError_t launch_pass2(const Args &a, int grid, bool silu, cudaStream_t s)
 {
-    if (silu)
-        gn_pass2_kernel<true><<<grid, kThreads, smem_for(a, kPass2), s>>>(a);
-    else
-        gn_pass2_kernel<false><<<grid, kThreads, smem_for(a, kPass2), s>>>(a);
-    return cudaGetLastError();
+    return launch_plain(pass2_fn(silu, pow2_slots(a.g)), a, grid, smem_for(a, kPass2), s);
 }
 
 cudaError_t fused_blocks_per_sm(bool silu, uint32_t smem, int *blocks)
 {
-    if (silu)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gn_fused_kernel<true>, kThreads, smem);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gn_fused_kernel<false>, kThreads, smem);
+    // the smaller of the two instantiations' figures, so that the answer
+    // holds whichever one a launch picks
+    int b0 = 0, b1 = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, fused_fn(silu, false), kThreads, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, fused_fn(silu, true), kThreads, smem);
+    if (e != cudaSuccess) return e;
+    *blocks = b0 < b1 ? b0 : b1;
+    return cudaSuccess;
 }
 
 cudaError_t launch_fused(const Args &a, int grid, bool silu, cudaStream_t s)
 {
     Args copy = a;
     void *params[] = {&copy};
-    const void *fn = silu ? reinterpret_cast<const void *>(gn_fused_kernel<true>)
-                          : reinterpret_cast<const void *>(gn_fused_kernel<false>);
-    return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), params, smem_for(a, kFused), s);
+    return cudaLaunchCooperativeKernel(fused_fn(silu, pow2_slots(a.g)), dim3(grid), dim3(kThreads), params,
+                                       smem_for(a, kFused), s);
 }
 
 cudaError_t launch_selftest_wait(int mode, uint64_t timeout_ns, int *done, int blocks, cudaStream_t s)

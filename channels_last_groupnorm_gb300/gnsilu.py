@@ -10,6 +10,9 @@ Unsupported inputs give ``None``, the contract of the sglang PR #33451 page
 ("FLUX.2 VAE decoder fast path behind quality=high", section
 "Modifications", item 2: non-CUDA, grad enabled, non-power-of-two C,
 C > 2048, not channels_last), so callers can fall back to their own path.
+``gn_silu_rows_any`` and ``gn_silu_ndhwc`` take any C that is a multiple of 8
+up to 2048 (any channels per group) and 5D channels-last input, the range of
+the page's existing general kernel (same section, item 1, third bullet).
 """
 from __future__ import annotations
 
@@ -50,6 +53,11 @@ EXPORTS = {
     "gn_silu_rows_ex": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4
                         + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
+    "gn_silu_rows_any": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4
+                         + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
+    "gn_silu_ndhwc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 6
+                      + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "gn_silu_rows_static": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4
                             + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                ctypes.c_void_p]),
@@ -104,6 +112,18 @@ def raw_gn_silu_rows_ex(x, gamma, beta, y, N, L, C, G, eps, apply_silu, mean_out
     return lib().gn_silu_rows_ex(x, gamma, beta, y, N, L, C, G, float(eps), int(apply_silu),
                                  mean_out or None, rstd_out or None, workspace or None,
                                  workspace_bytes, variant, stream or None)
+
+
+def raw_gn_silu_rows_any(x, gamma, beta, y, N, L, C, G, eps, apply_silu, mean_out=0, rstd_out=0,
+                         workspace=0, workspace_bytes=0, variant=VARIANT_AUTO, stream=0) -> int:
+    return lib().gn_silu_rows_any(x, gamma, beta, y, N, L, C, G, float(eps), int(apply_silu),
+                                  mean_out or None, rstd_out or None, workspace or None,
+                                  workspace_bytes, variant, stream or None)
+
+
+def raw_gn_silu_ndhwc(x, gamma, beta, y, N, D, H, W, C, G, eps, apply_silu, stream=0) -> int:
+    return lib().gn_silu_ndhwc(x, gamma, beta, y, N, D, H, W, C, G, float(eps), int(apply_silu),
+                               stream or None)
 
 
 def raw_gn_silu_rows(x, gamma, beta, y, N, L, C, G, eps, apply_silu, stream=0) -> int:
@@ -225,6 +245,47 @@ def gn_silu_rows_ex(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: 
     """``gn_silu_rows`` that also returns the fp32 statistics:
     (y, mean [N, G], rstd [N, G]), or None when unsupported.  ``workspace``
     is an optional uint8 CUDA tensor (see ``gn_silu_workspace_bytes``)."""
+    return _rows_with_stats(raw_gn_silu_rows_ex, "gn_silu_rows_ex", x, gamma, beta, G, eps,
+                            apply_silu, out, variant, workspace, stream)
+
+
+def gn_silu_rows_any(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: bool = True,
+                     out=None, variant: int = VARIANT_AUTO, workspace=None, stream=None):
+    """``gn_silu_rows_ex`` for any C that is a multiple of 8 up to 2048 and
+    any G dividing C: (y, mean [N, G], rstd [N, G]), or None when
+    unsupported."""
+    return _rows_with_stats(raw_gn_silu_rows_any, "gn_silu_rows_any", x, gamma, beta, G, eps,
+                            apply_silu, out, variant, workspace, stream)
+
+
+def gn_silu_ndhwc(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: bool = True,
+                  out=None, stream=None):
+    """GroupNorm(+SiLU) of a channels_last_3d bf16 CUDA tensor (N, C, D, H, W),
+    any C that is a multiple of 8 up to 2048.  Returns y with x's shape and
+    memory format, or None when the input is not supported."""
+    lib()
+    torch = _torch()
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16
+            and x.dim() == 5):
+        return None
+    if not x.is_contiguous(memory_format=torch.channels_last_3d) or _grad_blocked(x, gamma, beta):
+        return None
+    N, C, D, H, W = x.shape
+    if not (_affine_ok(gamma, C, x.device) and _affine_ok(beta, C, x.device)):
+        return None
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.channels_last_3d)
+    elif not (out.shape == x.shape and out.dtype == x.dtype and out.device == x.device
+              and out.is_contiguous(memory_format=torch.channels_last_3d)):
+        return None
+    with torch.cuda.device(x.device):
+        rc = raw_gn_silu_ndhwc(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
+                               N, D, H, W, C, G, eps, apply_silu, _stream_handle(x.device, stream))
+    return out if _finish(rc, "gn_silu_ndhwc") else None
+
+
+def _rows_with_stats(raw, what, x, gamma, beta, G, eps, apply_silu, out, variant, workspace,
+                     stream):
     lib()
     torch = _torch()
     if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16
@@ -241,7 +302,7 @@ def gn_silu_rows_ex(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: 
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     with torch.cuda.device(x.device):
-        rc = raw_gn_silu_rows_ex(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
-                                 N, L, C, G, eps, apply_silu, mean.data_ptr(), rstd.data_ptr(),
-                                 ws_ptr, ws_bytes, variant, _stream_handle(x.device, stream))
-    return (out, mean, rstd) if _finish(rc, "gn_silu_rows_ex") else None
+        rc = raw(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
+                 N, L, C, G, eps, apply_silu, mean.data_ptr(), rstd.data_ptr(),
+                 ws_ptr, ws_bytes, variant, _stream_handle(x.device, stream))
+    return (out, mean, rstd) if _finish(rc, what) else None

@@ -8,7 +8,10 @@ same input bytes.
 The shapes are the FLUX.2 VAE decoder GroupNorm shapes of the kernel
 micro-benchmark on the sglang PR #33451 page ("FLUX.2 VAE decoder fast path
 behind quality=high", section "Speedup", first table), written as (N, C, H, W)
-of a channels_last tensor, plus the small 64x64 case.  The value
+of a channels_last tensor, plus the small 64x64 case.  GENERAL_WORKLOADS
+are shapes for the generalised entry points (non-power-of-two C, 5D
+channels-last input with D frames), which the pages name but do not
+measure; they use the same distributions.  The value
 distributions stand in for decoder activations (the pages print none):
 
   x     ~ N(mean, std) fp32, rounded to bf16 (round to nearest even)
@@ -53,6 +56,7 @@ class Workload:
     H: int
     W: int
     G: int = 32
+    D: int = 1                    # frames of a 5D (N, C, D, H, W) input; 1 = 4D
     eps: float = 1e-6
     x_mean: float = 0.0
     x_std: float = 1.0
@@ -63,7 +67,12 @@ class Workload:
 
     @property
     def L(self) -> int:
-        return self.H * self.W
+        return self.D * self.H * self.W
+
+    @property
+    def general(self) -> bool:
+        """C is not a power of two: only the general entry points take it."""
+        return self.C & (self.C - 1) != 0
 
     @property
     def elements(self) -> int:
@@ -74,8 +83,10 @@ class Workload:
         return (self.N, self.C, self.H, self.W)
 
     def describe(self) -> dict:
-        return {"workload": self.name, "N": self.N, "C": self.C, "H": self.H, "W": self.W,
-                "G": self.G, "eps": self.eps, "layout": "NHWC (channels_last)",
+        spatial = {"D": self.D} if self.D > 1 else {}
+        return {"workload": self.name, "N": self.N, "C": self.C, **spatial, "H": self.H,
+                "W": self.W, "G": self.G, "eps": self.eps,
+                "layout": "NDHWC (channels_last_3d)" if self.D > 1 else "NHWC (channels_last)",
                 "x": (f"N({self.x_mean},{self.x_std})"
                       + (f"+U(-{self.channel_offset},{self.channel_offset})[c]"
                          if self.channel_offset else "")),
@@ -99,7 +110,14 @@ WORKLOADS = [
              note="256 MiB up-block shape", pages_us_h200=307.9),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+GENERAL_WORKLOADS = [
+    Workload("gn_silu_c960_128x128", 10, 1, 960, 128, 128, note="C = 960, Cg = 30"),
+    Workload("gn_silu_c320_256x256", 11, 1, 320, 256, 256, note="C = 320, Cg = 10"),
+    Workload("gn_silu_c384_d8_128x128", 12, 1, 384, 128, 128, D=8,
+             note="5D channels-last video latent, C = 384, Cg = 12"),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + GENERAL_WORKLOADS}
 
 
 def _normal_bits(rng: np.random.Generator, count: int, C: int, mean: float, std: float,
@@ -107,7 +125,7 @@ def _normal_bits(rng: np.random.Generator, count: int, C: int, mean: float, std:
     out = np.empty(count, np.uint16)
     done = 0
     while done < count:
-        k = min(_CHUNK, count - done)   # _CHUNK is a multiple of every C used here
+        k = min(_CHUNK // C * C, count - done)   # whole rows; _CHUNK itself for a power-of-two C
         v = rng.standard_normal(k, dtype=np.float32)
         v *= np.float32(std)
         v += np.float32(mean)
@@ -134,8 +152,6 @@ def make_inputs(w: Workload) -> dict:
     if w.channel_offset:
         offsets = np.random.default_rng(4000).uniform(
             -w.channel_offset, w.channel_offset, w.C).astype(np.float32)
-    if _CHUNK % w.C:
-        raise ValueError("C must divide the draw chunk")
     rng = np.random.default_rng(1000 + w.index)
     x = _normal_bits(rng, w.elements, w.C, w.x_mean, w.x_std, offsets)
     gamma, beta = affine_params(w.index, w.C)

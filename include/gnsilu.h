@@ -20,6 +20,10 @@
  * Supported inputs (the page's "unsupported inputs are rejected" contract,
  * same section, item 2): C a power of two in [8, 2048], G >= 1 dividing C,
  * N, L >= 1.  Unsupported inputs return a non-zero status and touch nothing.
+ * Two further entry points, gn_silu_rows_any() and gn_silu_ndhwc(), widen C
+ * to any multiple of 8 up to 2048 (any channels per group, e.g. C = 320 or
+ * 960) and add 5D channels-last input: the range the page's existing
+ * general kernel serves (same section, item 1, third bullet).
  *
  * Memory and streams: every pointer argument is a DEVICE pointer owned by
  * the caller; the library never frees caller memory.  x and y are bf16
@@ -52,7 +56,9 @@ enum gn_status_code {
     GN_OK = 0,
     GN_ERR_NULL = 1,       /* a required pointer is NULL */
     GN_ERR_SHAPE = 2,      /* N, L (or H, W) < 1, or the element count overflows */
-    GN_ERR_CHANNELS = 3,   /* C not a power of two in [8, 2048], G < 1 or C % G != 0 */
+    GN_ERR_CHANNELS = 3,   /* C not a power of two in [8, 2048] (for gn_silu_rows_any and
+                              gn_silu_ndhwc: not a multiple of 8 in [8, 2048]),
+                              G < 1 or C % G != 0 */
     GN_ERR_ALIGN = 4,      /* x or y not 16-byte aligned; gamma, beta, mean/rstd outputs
                               not 4-byte aligned; workspace not 256-byte aligned */
     GN_ERR_EPS = 5,        /* eps not finite or negative */
@@ -113,9 +119,41 @@ int gn_silu_rows_ex(const void *x_bf16, const float *gamma, const float *beta, v
                     float *mean_out, float *rstd_out,
                     void *workspace, size_t workspace_bytes, int variant, void *stream);
 
-/* Workspace bytes gn_silu_rows_ex() needs for this shape on the CURRENT
- * device (any variant).  Returns 0 if the shape is unsupported or there is
- * no usable device. */
+/*
+ * gn_silu_rows_ex() for any channel count C that is a multiple of 8 in
+ * [8, 2048] and any G dividing C -- every channels-per-group Cg = C / G,
+ * including the non-power-of-two C of the page's existing general kernel
+ * ("any channels-per-group", sglang PR #33451, section "Modifications",
+ * item 1, third bullet).  The operation, arguments, alignment, aliasing,
+ * workspace and status codes are those of gn_silu_rows_ex(); the kernels are
+ * the same, with the per-vector channel bookkeeping done by division instead
+ * of shifts.  For a power-of-two C the results equal gn_silu_rows_ex()'s
+ * bit for bit.  C not a multiple of 8 (a row that is not whole 16-byte
+ * vectors) gives GN_ERR_CHANNELS.
+ */
+int gn_silu_rows_any(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16,
+                     int64_t N, int64_t L, int64_t C, int64_t G,
+                     float eps, int apply_silu,
+                     float *mean_out, float *rstd_out,
+                     void *workspace, size_t workspace_bytes, int variant, void *stream);
+
+/*
+ * GroupNorm(+SiLU) of a 5D channels-last bf16 tensor (N, C, D, H, W) whose
+ * memory is [N][D][H][W][C] (torch.channels_last_3d), such as the
+ * HunyuanVAE-style video latents the page's general kernel serves (same
+ * section, item 1, third bullet; "Speedup", note under the kernel table).
+ * Statistics run over all D*H*W positions and the Cg channels of a group;
+ * identical to gn_silu_rows_any() with L = D * H * W, the library's own
+ * workspace and the automatic schedule.  C: a multiple of 8 in [8, 2048].
+ */
+int gn_silu_ndhwc(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16,
+                  int64_t N, int64_t D, int64_t H, int64_t W, int64_t C, int64_t G,
+                  float eps, int apply_silu, void *stream);
+
+/* Workspace bytes gn_silu_rows_ex() / gn_silu_rows_any() need for this shape
+ * on the CURRENT device (any variant).  Accepts any C that is a multiple of
+ * 8 in [8, 2048].  Returns 0 if the shape is unsupported or there is no
+ * usable device. */
 size_t gn_silu_workspace_bytes(int64_t N, int64_t L, int64_t C, int64_t G);
 
 /* The variant GN_VARIANT_AUTO resolves to for this shape on the current
@@ -185,7 +223,8 @@ int gn_silu_rows_static(const void *x_bf16, const float *gamma, const float *bet
 /* Human-readable name of a status code (static storage). */
 const char *gn_status_string(int status);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2 (1 lacked gn_silu_rows_any and
+ * gn_silu_ndhwc). */
 int gn_abi_version(void);
 
 #ifdef __cplusplus

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert gs.gn_abi_version() == 1
+    assert gs.gn_abi_version() == 2
     for code in range(12):
         s = gs.status_string(code)
         assert s.startswith("GN_"), (code, s)
@@ -144,3 +144,61 @@ def test_tensor_binding_returns_none_for_cpu_tensors():
 
 def test_launch_counter_starts_readable():
     assert gs.gn_kernel_launch_count() >= 0
+
+
+def rows_any(**kw):
+    a = dict(x=X, gamma=GAM, beta=BET, y=Y, N=1, L=4, C=320, G=32, eps=1e-6, apply_silu=1,
+             mean_out=0, rstd_out=0, workspace=0, workspace_bytes=0, variant=0)
+    a.update(kw)
+    return gs.raw_gn_silu_rows_any(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=0), gs.GN_ERR_NULL),
+    (dict(L=0), gs.GN_ERR_SHAPE),
+    (dict(C=12, G=4), gs.GN_ERR_CHANNELS),        # a row is not whole 16-byte vectors
+    (dict(C=4, G=4), gs.GN_ERR_CHANNELS),
+    (dict(C=2056, G=8), gs.GN_ERR_CHANNELS),      # above 2048
+    (dict(C=320, G=3), gs.GN_ERR_CHANNELS),       # G does not divide C
+    (dict(C=320, G=0), gs.GN_ERR_CHANNELS),
+    (dict(x=X + 8), gs.GN_ERR_ALIGN),
+    (dict(y=X + 16), gs.GN_ERR_ALIAS),
+    (dict(eps=-1.0), gs.GN_ERR_EPS),
+    (dict(variant=5), gs.GN_ERR_VARIANT),
+])
+def test_rows_any_rejects(kw, code):
+    assert rows_any(**kw) == code
+
+
+@pytest.mark.parametrize("C,G", [(320, 32), (24, 8), (960, 32), (2040, 8)])
+def test_power_of_two_entries_still_reject_general_channel_counts(C, G):
+    assert rows(C=C, G=G) == gs.GN_ERR_CHANNELS
+    assert rows_ex(C=C, G=G) == gs.GN_ERR_CHANNELS
+    assert gs.raw_gn_silu_nhwc(X, GAM, BET, Y, 1, 2, 2, C, G, 1e-6, 1) == gs.GN_ERR_CHANNELS
+
+
+@no_gpu
+@pytest.mark.parametrize("C,G", [(320, 32), (24, 8), (960, 32), (2040, 8), (256, 32), (8, 1)])
+def test_rows_any_accepts_general_channel_counts(C, G):
+    # accepted by validation; without a GPU the next check reports no device
+    assert rows_any(C=C, G=G) == gs.GN_ERR_DEVICE
+    assert gs.raw_gn_silu_ndhwc(X, GAM, BET, Y, 1, 2, 2, 2, C, G, 1e-6, 1) == gs.GN_ERR_DEVICE
+
+
+@pytest.mark.parametrize("D,H,W,code", [(0, 2, 2, gs.GN_ERR_SHAPE), (2, 0, 2, gs.GN_ERR_SHAPE),
+                                        (2, 2, -1, gs.GN_ERR_SHAPE),
+                                        (1 << 30, 1 << 20, 1 << 20, gs.GN_ERR_SHAPE)])
+def test_ndhwc_rejects_bad_spatial_shape(D, H, W, code):
+    assert gs.raw_gn_silu_ndhwc(X, GAM, BET, Y, 1, D, H, W, 320, 32, 1e-6, 1) == code
+    assert gs.raw_gn_silu_ndhwc(0, GAM, BET, Y, 1, D, H, W, 320, 32, 1e-6, 1) == gs.GN_ERR_NULL
+
+
+def test_ndhwc_rejects_channels_like_rows_any():
+    assert gs.raw_gn_silu_ndhwc(X, GAM, BET, Y, 1, 2, 2, 2, 12, 4, 1e-6, 1) == gs.GN_ERR_CHANNELS
+
+
+def test_general_tensor_bindings_return_none_for_cpu_tensors():
+    x = torch.zeros(1, 320, 2, 2, 2, dtype=torch.bfloat16).to(memory_format=torch.channels_last_3d)
+    g = torch.ones(320)
+    assert gs.gn_silu_ndhwc(x, g, g) is None
+    assert gs.gn_silu_rows_any(torch.zeros(1, 8, 320, dtype=torch.bfloat16), g, g) is None

@@ -67,3 +67,14 @@ def test_shapes_and_timings_match_the_pages_table():
     for w in quoted:
         assert w.nchw in table, w.name
         assert table[w.nchw] == w.pages_us_h200
+
+
+def test_general_workloads_draw_whole_rows_deterministically():
+    w = wl.Workload("probe_c960", 10, 1, 960, 8, 8, D=3)
+    assert w.general and w.L == 3 * 8 * 8
+    a = wl.make_inputs(w)
+    b = wl.make_inputs(w)
+    assert a["x_bits"].shape == (1, 192, 960)
+    assert np.array_equal(a["x_bits"], b["x_bits"])
+    assert {x.name for x in wl.GENERAL_WORKLOADS} <= set(wl.BY_NAME)
+    assert all(x.general or x.D > 1 for x in wl.GENERAL_WORKLOADS)
