@@ -190,6 +190,9 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     if (S > max_seg) S = max_seg;
     g.S = static_cast<int32_t>(S);
     g.seg32 = (g.pieces_per_n < (int64_t(1) << 32)) ? 1 : 0;
+    g.base_pieces = (g.pieces_per_n - 1) / g.S;
+    g.last_item = static_cast<int32_t>((g.pieces_per_n - 1) % g.S);
+    g.tail_rows = static_cast<int32_t>(L - (g.pieces_per_n - 1) * g.rows_per_piece);
     g.items = N * S;
     p.grid = static_cast<int>(g.items < grid_target ? g.items : grid_target);
     // ring depth from the shared memory left next to the auxiliary arrays
@@ -201,7 +204,7 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     // workspace
     size_t off = 256;   // barrier words
     p.off_partial = off;
-    off = align256(off + static_cast<size_t>(N) * G * S * sizeof(float4));
+    off = align256(off + static_cast<size_t>(N) * G * S * sizeof(float2));
     p.off_gstat = off;
     off = align256(off + static_cast<size_t>(N) * G * sizeof(float2));
     p.off_st = off;
@@ -310,7 +313,7 @@ int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N
     a.eps = eps;
     a.l2_hints = l2_hints();
     a.g = p.g;
-    a.partial = reinterpret_cast<float4 *>(base + p.off_partial);
+    a.partial = reinterpret_cast<float2 *>(base + p.off_partial);
     a.gstat = reinterpret_cast<float2 *>(base + p.off_gstat);
     a.st = reinterpret_cast<float2 *>(base + p.off_st);
     a.mean = mean_out ? mean_out : reinterpret_cast<float *>(base + p.off_mean);

@@ -7,7 +7,7 @@
 
 namespace gn {
 
-constexpr int kConsumers = 512;                 // consumer threads per CTA (16 warps)
+constexpr int kConsumers = 256;                 // consumer threads per CTA (8 warps)
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kThreads = kConsumers + 32;       // + one producer warp
 constexpr int kMaxRing = 32;                    // ring slots (one bit each in a 32-bit mask)
@@ -27,7 +27,7 @@ constexpr int kSyncWords = 64;                  // 256-byte workspace header
 struct Geom {
     int64_t N, L;
     int32_t C, G, Cg, V;          // V = C / 8 sixteen-byte vectors per row
-    int32_t A;                    // consumer threads that carry data: (512 / V) * V
+    int32_t A;                    // consumer threads that carry data: (kConsumers / V) * V
     int32_t rows_per_piece;
     int32_t piece_bytes;          // rows_per_piece * C * 2
     int64_t pieces_per_n;
@@ -35,6 +35,11 @@ struct Geom {
     int32_t ring;                 // ring slots in shared memory
     int64_t items;                // N * S
     int32_t seg32;                // pieces_per_n < 2^32: piece counts in 32-bit math
+    // pieces of item s: base_pieces + (s <= last_item); item last_item owns
+    // the batch entry's last piece, which holds tail_rows rows
+    int64_t base_pieces;          // (pieces_per_n - 1) / S
+    int32_t last_item;            // (pieces_per_n - 1) % S
+    int32_t tail_rows;            // L - (pieces_per_n - 1) * rows_per_piece
 };
 
 struct Args {
@@ -45,7 +50,8 @@ struct Args {
     uint32_t l2_hints;            // bit 0: pass-2 loads evict_first, bit 1: pass-2
                                   // stores evict_first, bit 2: pass-1 loads evict_last
     Geom g;
-    float4 *partial;              // [N][G][S] group record per item (mean, M2, rows, unused)
+    float2 *partial;              // [N][G][S] group record per item (mean, M2); its rows
+                                  // follow from the geometry (item_rows_f)
     float2 *gstat;                // [N][G]    group (mean, rstd)   (fused)
     float2 *st;                   // [N][C]    (scale, shift)       (two-pass)
     float *mean, *rstd;           // [N][G]

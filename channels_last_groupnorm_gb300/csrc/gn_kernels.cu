@@ -74,6 +74,13 @@ __device__ __forceinline__ f2_t sub2(f2_t a, f2_t b)
     return d;
 }
 
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c)
 {
     f2_t d;
@@ -103,9 +110,14 @@ struct Cursor {
 // pieces of item s in one batch entry (S <= pieces_per_n, so at least one)
 __device__ __forceinline__ int64_t item_pieces(const Geom &g, int32_t s)
 {
-    if (g.seg32)
-        return static_cast<uint32_t>(g.pieces_per_n - 1 - s) / static_cast<uint32_t>(g.S) + 1;
-    return (g.pieces_per_n - 1 - s) / g.S + 1;
+    return g.base_pieces + (s <= g.last_item ? 1 : 0);
+}
+
+// rows of item s (as a float, for the statistics)
+__device__ __forceinline__ float item_rows_f(const Geom &g, int32_t s)
+{
+    const int64_t rows = item_pieces(g, s) * g.rows_per_piece;
+    return static_cast<float>(s == g.last_item ? rows - (g.rows_per_piece - g.tail_rows) : rows);
 }
 
 __device__ __forceinline__ void load_item(const Geom &g, Cursor &c, int64_t it)
@@ -116,13 +128,6 @@ __device__ __forceinline__ void load_item(const Geom &g, Cursor &c, int64_t it)
     c.k_last = c.s + (item_pieces(g, c.s) - 1) * g.S;
 }
 
-// rows covered by item s: whole pieces, less the short tail of the last
-// piece of the batch entry if the item owns it
-__device__ __forceinline__ int64_t item_rows(const Geom &g, const Cursor &c)
-{
-    const int64_t rows = item_pieces(g, c.s) * g.rows_per_piece;
-    return (c.k_last == g.pieces_per_n - 1) ? rows - (g.pieces_per_n * g.rows_per_piece - g.L) : rows;
-}
 
 __device__ __forceinline__ int32_t piece_rows(const Geom &g, int64_t k)
 {
@@ -134,9 +139,38 @@ __device__ __forceinline__ int64_t piece_elem_offset(const Geom &g, int64_t n, i
     return (n * g.L + k * g.rows_per_piece) * g.C;
 }
 
+// One work item as the consumers see it: batch entry n, segment s, its
+// piece count, and whether it owns the batch entry's short last piece.
+struct Item {
+    int64_t n;
+    int32_t s;
+    int64_t np;
+    bool tail;
+};
+
+__device__ __forceinline__ Item make_item(const Geom &g, int64_t it)
+{
+    Item m;
+    m.n = it / g.S;
+    m.s = static_cast<int32_t>(it - m.n * g.S);
+    m.np = item_pieces(g, m.s);
+    m.tail = (m.s + (m.np - 1) * g.S) == g.pieces_per_n - 1;
+    return m;
+}
+
+// rows covered by an item: whole pieces, less the short tail of the last
+// piece of the batch entry if the item owns it
+__device__ __forceinline__ int64_t rows_of(const Geom &g, const Item &m)
+{
+    const int64_t rows = m.np * g.rows_per_piece;
+    return m.tail ? rows - (g.pieces_per_n * g.rows_per_piece - g.L) : rows;
+}
+
 // pieces this CTA processes, over all its items
 __device__ __forceinline__ int64_t cta_piece_count(const Geom &g)
 {
+    if (g.items <= gridDim.x)   // one item per CTA (grids are never wider than the items)
+        return item_pieces(g, static_cast<int32_t>(blockIdx.x % static_cast<uint32_t>(g.S)));
     int64_t t = 0;
     for (int64_t it = blockIdx.x; it < g.items; it += gridDim.x)
         t += item_pieces(g, static_cast<int32_t>(it % g.S));
@@ -197,20 +231,25 @@ __device__ __forceinline__ void record_timeout(const Ctl &ctl)
     atomicOr(&g_status, 1u);
 }
 
+// Waiting threads sleep in the try_wait (up to kWaitSleepNs per round)
+// rather than spin, so that warps still busy with the previous piece keep
+// the issue slots.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &ctl)
 {
-    if (*ctl.abort) return false;
+    // a completed phase is safe to consume even after an abort elsewhere in
+    // the CTA; the abort is noticed on the first wait that does not complete
     if (mbar_try_wait(bar, parity)) return true;
+    if (*ctl.abort) return false;
     const uint64_t deadline = global_ns() + ctl.timeout_ns;
 #pragma unroll 1
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 31u) {
-            if (*ctl.abort) return false;
-            if (global_ns() > deadline) {
-                record_timeout(ctl);
-                return false;
-            }
+    for (;;) {
+        if (mbar_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (*ctl.abort) return false;
+        if (global_ns() > deadline) {
+            record_timeout(ctl);
+            return false;
         }
     }
 }
@@ -377,8 +416,8 @@ __device__ __forceinline__ float warp_sum(float v)
 
 // Vector-slot bookkeeping.  A thread's 16-byte vector v of a piece holds
 // channels 8 * (v % V) .. + 7.  POW2: C is a power of two, so V divides the
-// 512 consumer threads and every one carries data (A = 512) and the slot
-// arithmetic is a mask and a shift.  Otherwise A = (512 / V) * V threads
+// kConsumers threads and every one carries data (A = kConsumers) and the
+// slot arithmetic is a mask and a shift.  Otherwise A = (kConsumers / V) * V threads
 // carry data and the slot arithmetic divides.
 template <bool POW2>
 __device__ __forceinline__ int carriers(const Geom &g) { return POW2 ? kConsumers : g.A; }
@@ -419,8 +458,8 @@ __device__ __forceinline__ float comp(const float4 &v, int j)
 // the upper half of the entries is first added into the lower half.  The
 // per-channel results are then merged into one record per group.
 template <bool POW2>
-__device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, const f2_t (&s1p)[4],
-                            const f2_t (&s2p)[4])
+__device__ void reduce_item_general(const Args &a, const Smem &sm, const Item &m, const f2_t (&s1p)[4],
+                                    const f2_t (&s2p)[4])
 {
     const Geom &g = a.g;
     const int tid = threadIdx.x;
@@ -478,7 +517,7 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
     named_sync(1, kConsumers);
     const float *kvec = reinterpret_cast<const float *>(sm.base + sm.lay.kvec);
     float2 *chs = reinterpret_cast<float2 *>(sm.base + sm.lay.chs);
-    const float count = static_cast<float>(item_rows(g, c));
+    const float count = static_cast<float>(rows_of(g, m));
     const float inv_count = 1.0f / count;
     // per channel (mean, M2) of the item; thread t finishes channel
     // 8 * (t % V) + t / V: consecutive threads read consecutive slots
@@ -518,9 +557,155 @@ __device__ void reduce_item(const Args &a, const Smem &sm, const Cursor &c, cons
                 M2 += fmaf(count * d, d, cr[j].y);
             }
         for (int off = span >> 1; off > 0; off >>= 1) M2 += __shfl_xor_sync(0xffffffffu, M2, off);
-        if (active && sl == 0) a.partial[(c.n * g.G + grp) * g.S + c.s] = make_float4(mu, M2, count, 0.f);
+        if (active && sl == 0) a.partial[(m.n * g.G + grp) * g.S + m.s] = make_float2(mu, M2);
     }
     named_sync(1, kConsumers);
+}
+
+// Vectors per carrier thread of a full piece, when that is a power of two up
+// to kMaxVecPerThread (the bodies below are compiled for those counts);
+// 0 otherwise.
+__device__ __forceinline__ int vec_kind(int nvec, int A)
+{
+#pragma unroll
+    for (int k = kMaxVecPerThread; k >= 1; k >>= 1)
+        if (nvec == k * A) return k;
+    return 0;
+}
+
+// Shifted sums of the vectors tid, tid + A, ... of one piece.  VPT > 0: a
+// full piece of exactly VPT vectors per carrier thread (no bounds checks);
+// VPT == 0: a piece of any size (the short last piece of a batch entry).
+template <int VPT>
+__device__ __forceinline__ void p1_piece(uint32_t base, int tid, int A, int nvec, const f2_t (&K)[4], f2_t (&s1)[4],
+                                         f2_t (&s2)[4])
+{
+    if (VPT > 0) {
+        uint4 w[VPT > 0 ? VPT : 1];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) w[i] = lds128(base + 16u * static_cast<uint32_t>(tid + i * A));
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const f2_t d = sub2(bf2_to_f2(ws[j]), K[j]);
+                s1[j] = add2(s1[j], d);
+                s2[j] = fma2(d, d, s2[j]);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int v = tid; v < nvec; v += A) {
+            const uint4 w = lds128(base + 16u * v);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const f2_t d = sub2(bf2_to_f2(ws[j]), K[j]);
+                s1[j] = add2(s1[j], d);
+                s2[j] = fma2(d, d, s2[j]);
+            }
+        }
+    }
+}
+
+// Power-of-two C: the item's per-group (mean, M2, rows) records straight
+// from the per-thread sums, without per-channel statistics.  Every channel
+// of a group shares the group's shift K_g, so sums of different channels
+// of one group add directly.  U = max(1, 8 / Cg) groups per thread; a group
+// covers spg = max(1, Cg / 8) vector slots.
+//  1. each thread folds its eight channel sums into its U group sums;
+//  2. a butterfly over the lane offsets that stay inside a group (offsets
+//     below spg: neighbouring slots of the group; offsets of V and more:
+//     the same slot in another row of the warp) gives every lane its
+//     group's warp total;
+//  3. one lane per (warp or row, group) writes that total to shared memory;
+//  4. thread t adds the R partials of group t in a fixed order, so the
+//     result is deterministic.
+template <int U>
+__device__ void reduce_item_pow2(const Args &a, const Smem &sm, const Item &m, const f2_t (&s1p)[4],
+                                 const f2_t (&s2p)[4])
+{
+    const Geom &g = a.g;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int V = g.V, Cg = g.Cg;
+    const int vslot = tid & (V - 1);
+    const int spg = Cg >= 8 ? Cg >> 3 : 1;
+    float c1[8], c2[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        upk(s1p[i], c1[2 * i], c1[2 * i + 1]);
+        upk(s2p[i], c2[2 * i], c2[2 * i + 1]);
+    }
+    float u1[U], u2[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        constexpr int W = 8 / U;   // channels per group sum
+        float x1 = 0.f, x2 = 0.f;
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            x1 += c1[u * W + j];
+            x2 += c2[u * W + j];
+        }
+        u1[u] = x1;
+        u2[u] = x2;
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        if (off < spg || off >= V) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                u1[u] += __shfl_xor_sync(0xffffffffu, u1[u], off);
+                u2[u] += __shfl_xor_sync(0xffffffffu, u2[u], off);
+            }
+        }
+    }
+    float2 *scr = reinterpret_cast<float2 *>(sm.base + sm.lay.scratch);
+    const int sub = spg > 32 ? spg >> 5 : 1;          // warps per group and row
+    const int R = V <= 32 ? kConsumerWarps : (kConsumers / V) * sub;
+    const bool rep = (V >= 32 || lane < V) && (spg > 32 ? lane == 0 : (vslot & (spg - 1)) == 0);
+    if (rep) {
+        const int p = V <= 32 ? warp : (tid / V) * sub + ((vslot & (spg - 1)) >> 5);
+        const int t0 = (8 * vslot) / Cg;
+#pragma unroll
+        for (int u = 0; u < U; ++u) scr[p * g.G + t0 + u] = make_float2(u1[u], u2[u]);
+    }
+    named_sync(1, kConsumers);
+    const float *kvec = reinterpret_cast<const float *>(sm.base + sm.lay.kvec);
+    const float rows = static_cast<float>(rows_of(g, m));
+    const float inv_n = 1.0f / (rows * static_cast<float>(Cg));
+    for (int t = tid; t < g.G; t += kConsumers) {
+        float S1 = 0.f, S2 = 0.f;
+        for (int p = 0; p < R; ++p) {
+            const float2 v = scr[p * g.G + t];
+            S1 += v.x;
+            S2 += v.y;
+        }
+        const float mo = S1 * inv_n;   // mean - K_g
+        a.partial[(m.n * g.G + t) * g.S + m.s] = make_float2(kvec[t * Cg] + mo, fmaxf(S2 - S1 * mo, 0.f));
+    }
+    named_sync(1, kConsumers);
+}
+
+template <bool POW2>
+__device__ __forceinline__ void reduce_item(const Args &a, const Smem &sm, const Item &m, const f2_t (&s1p)[4],
+                                            const f2_t (&s2p)[4])
+{
+    if (POW2) {
+        const int Cg = a.g.Cg;
+        if (Cg >= 8)
+            reduce_item_pow2<1>(a, sm, m, s1p, s2p);
+        else if (Cg == 4)
+            reduce_item_pow2<2>(a, sm, m, s1p, s2p);
+        else if (Cg == 2)
+            reduce_item_pow2<4>(a, sm, m, s1p, s2p);
+        else
+            reduce_item_pow2<8>(a, sm, m, s1p, s2p);
+    } else {
+        reduce_item_general<POW2>(a, sm, m, s1p, s2p);
+    }
 }
 
 template <bool POW2>
@@ -531,120 +716,211 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
     const int tid = threadIdx.x;
     const int vslot = vec_slot<POW2>(g, tid);
     const int A = carriers<POW2>(g);
-    const bool carrier = tid < A;
+    const bool carrier = POW2 || tid < A;
+    const int full_nvec = g.rows_per_piece * g.V;
+    const int tail_nvec = static_cast<int>(g.L - (g.pieces_per_n - 1) * g.rows_per_piece) * g.V;
+    const int kind_full = vec_kind(full_nvec, A);
     float *kvec = reinterpret_cast<float *>(sm.base + sm.lay.kvec);
-    Cursor c;
-    cursor_first(g, c);
     int slot = 0;
-    f2_t K[4], s1[4], s2[4];
+    uint32_t base = sm.ring_s;
     bool ok = !*ctl.abort;
-    for (int64_t q = 0; q < T; ++q) {
-        const bool first = (c.k == c.s);
-        if (first) {
+    for (int64_t it = blockIdx.x; it < g.items; it += gridDim.x) {
+        const Item m = make_item(g, it);
+        f2_t K[4], s1[4], s2[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) s1[i] = s2[i] = 0ull;
-        }
-        if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
-        full_par ^= 1u << slot;
-        const uint32_t base = sm.slot_addr(slot, g.piece_bytes);
-        if (ok) {
-            if (first) {
-                const uint4 w = lds128(base + 16u * vslot);
-                K[0] = bf2_to_f2(w.x);
-                K[1] = bf2_to_f2(w.y);
-                K[2] = bf2_to_f2(w.z);
-                K[3] = bf2_to_f2(w.w);
-                if (tid < g.V) {
-                    float4 *kv = reinterpret_cast<float4 *>(kvec + 8 * vslot);
-                    float k0, k1, k2, k3, k4, k5, k6, k7;
-                    upk(K[0], k0, k1);
-                    upk(K[1], k2, k3);
-                    upk(K[2], k4, k5);
-                    upk(K[3], k6, k7);
-                    kv[0] = make_float4(k0, k1, k2, k3);
-                    kv[1] = make_float4(k4, k5, k6, k7);
+        for (int i = 0; i < 4; ++i) s1[i] = s2[i] = 0ull;
+        for (int64_t j = 0; j < m.np; ++j) {
+            if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
+            full_par ^= 1u << slot;
+            if (ok) {
+                if (j == 0) {
+                    // the shift K of a channel: its group's first channel in
+                    // the item's first row (shared by the whole group)
+                    float kc[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = 8 * vslot + i;
+                        const int c0 = POW2 ? (c & ~(g.Cg - 1)) : (c / g.Cg) * g.Cg;
+                        kc[i] = __uint_as_float(lds_u16(base + 2u * c0) << 16);
+                    }
+                    K[0] = pk(kc[0], kc[1]);
+                    K[1] = pk(kc[2], kc[3]);
+                    K[2] = pk(kc[4], kc[5]);
+                    K[3] = pk(kc[6], kc[7]);
+                    if (tid < g.V) {
+                        float4 *kv = reinterpret_cast<float4 *>(kvec + 8 * vslot);
+                        float k0, k1, k2, k3, k4, k5, k6, k7;
+                        upk(K[0], k0, k1);
+                        upk(K[1], k2, k3);
+                        upk(K[2], k4, k5);
+                        upk(K[3], k6, k7);
+                        kv[0] = make_float4(k0, k1, k2, k3);
+                        kv[1] = make_float4(k4, k5, k6, k7);
+                    }
+                }
+                const bool short_piece = m.tail && j == m.np - 1;
+                const int kind = short_piece ? 0 : kind_full;
+                const int nvec = short_piece ? tail_nvec : full_nvec;
+                if (carrier) {
+                    if (kind == 8)
+                        p1_piece<8>(base, tid, A, nvec, K, s1, s2);
+                    else if (kind == 4)
+                        p1_piece<4>(base, tid, A, nvec, K, s1, s2);
+                    else if (kind == 2)
+                        p1_piece<2>(base, tid, A, nvec, K, s1, s2);
+                    else if (kind == 1)
+                        p1_piece<1>(base, tid, A, nvec, K, s1, s2);
+                    else
+                        p1_piece<0>(base, tid, A, nvec, K, s1, s2);
                 }
             }
-            const int nvec = piece_rows(g, c.k) * g.V;
-#pragma unroll 4
-            for (int v = carrier ? tid : nvec; v < nvec; v += A) {
-                const uint4 w = lds128(base + 16u * v);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const f2_t d = sub2(bf2_to_f2(ws[i]), K[i]);
-                    s1[i] = add2(s1[i], d);
-                    s2[i] = fma2(d, d, s2[i]);
-                }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));
+            if (++slot == g.ring) {
+                slot = 0;
+                base = sm.ring_s;
+            } else {
+                base += static_cast<uint32_t>(g.piece_bytes);
             }
         }
-        __syncwarp();
-        if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));
-        if (c.k == c.k_last) reduce_item<POW2>(a, sm, c, s1, s2);
-        cursor_next(g, c);
-        slot = (slot + 1 == g.ring) ? 0 : slot + 1;
+        reduce_item<POW2>(a, sm, m, s1, s2);
     }
 }
 
 // ---------------------------------------------------------------------------
 // finalize pieces
 // ---------------------------------------------------------------------------
-// Chan merge, by one warp, of the S item records of group (n, grp): each
-// record holds the mean and M2 of rows * Cg elements.  Returns (mean, rstd)
-// in every lane.  Lane l holds records l, l + 32, ... (S <= 32 * PER_LANE);
-// records past S are zero, which leaves every sum unchanged.
-template <int PER_LANE>
-__device__ __forceinline__ float2 merge_items_warp(const Args &a, int64_t n, int grp)
+// Chan merge, by one warp, of the S item records (mean, M2) of each of GB
+// groups (grp0, grp0 + gstride, ...; groups at or past G give nothing).
+// Record s covers item_rows_f(s) * Cg elements.  Lane l holds records
+// l, l + 32, ... (S <= 32 * PER_LANE); records past S count zero rows,
+// which leaves every sum unchanged.  All GB * PER_LANE loads are issued
+// before the first is used, so a batch costs one L2 round trip.  Returns
+// (mean, rstd) of every group in every lane.
+template <int PER_LANE, int GB>
+__device__ __forceinline__ void merge_groups_warp(const Args &a, int64_t n, int grp0, int gstride, float2 (&out)[GB])
 {
     const Geom &g = a.g;
     const int lane = threadIdx.x & 31;
-    const float4 *src = a.partial + (n * g.G + grp) * g.S;
-    float4 r[PER_LANE];
+    float2 r[GB][PER_LANE];
+#pragma unroll
+    for (int b = 0; b < GB; ++b) {
+        const int grp = grp0 + b * gstride;
+        const float2 *src = a.partial + (n * g.G + (grp < g.G ? grp : 0)) * g.S;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+            const int s = lane + 32 * i;
+            r[b][i] = (grp < g.G && s < g.S) ? __ldcg(src + s) : make_float2(0.f, 0.f);
+        }
+    }
+    float rows[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
         const int s = lane + 32 * i;
-        r[i] = (s < g.S) ? __ldcg(src + s) : make_float4(0.f, 0.f, 0.f, 0.f);   // (mean, M2, rows, -)
+        rows[i] = s < g.S ? item_rows_f(g, s) : 0.f;
     }
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) acc = fmaf(r[i].z, r[i].x, acc);
     const float Lf = static_cast<float>(g.L);
-    const float mean = warp_sum(acc) / Lf;
     const float cgf = static_cast<float>(g.Cg);
-    float acc2 = 0.f;
+    float acc[GB];
 #pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-        const float d = r[i].x - mean;
-        acc2 += fmaf(cgf * r[i].z * d, d, r[i].y);
+    for (int b = 0; b < GB; ++b) {
+        acc[b] = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) acc[b] = fmaf(rows[i], r[b][i].x, acc[b]);
     }
-    const float var = fmaxf(warp_sum(acc2) / (Lf * cgf), 0.f);
-    return make_float2(mean, 1.0f / sqrtf(var + a.eps));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int b = 0; b < GB; ++b) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+    float mean[GB], acc2[GB];
+#pragma unroll
+    for (int b = 0; b < GB; ++b) {
+        mean[b] = acc[b] / Lf;
+        acc2[b] = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+            const float d = r[b][i].x - mean[b];
+            acc2[b] += fmaf(cgf * rows[i] * d, d, r[b][i].y);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int b = 0; b < GB; ++b) acc2[b] += __shfl_xor_sync(0xffffffffu, acc2[b], off);
+#pragma unroll
+    for (int b = 0; b < GB; ++b) {
+        const float var = fmaxf(acc2[b] / (Lf * cgf), 0.f);
+        out[b] = make_float2(mean[b], 1.0f / sqrtf(var + a.eps));
+    }
+}
+
+template <int PER_LANE>
+__device__ __forceinline__ float2 merge_items_warp(const Args &a, int64_t n, int grp)
+{
+    float2 r[1];
+    merge_groups_warp<PER_LANE, 1>(a, n, grp, 0, r);
+    return r[0];
 }
 
 // ---------------------------------------------------------------------------
 // consumers: pass 2 (reverse order, in place in shared memory)
 // ---------------------------------------------------------------------------
-// SiLU(z) = z * sigmoid(z): sigmoid from one ex2 and one reciprocal (MUFU
-// approximations, a few ulp in fp32; the MUFU pipes of an SM retire about 32
-// of these per clock, far above the element rate memory can feed).
-__device__ __forceinline__ float silu1(float z)
-{
-    const float e = ex2_approx(z * -1.4426950408889634f);   // exp(-z)
-    return z * rcp_approx(1.0f + e);
-}
-
-// y = x * scale + shift (+ SiLU) for the two bf16 values of one word.
+// y = x * scale + shift (+ SiLU) for the two bf16 values of one word, on
+// a packed pair: z = fma(x, s, t), then SiLU(z) = z * sigmoid(z) with
+// sigmoid(z) = 1 / d, d = 1 + 2^(-z log2 e), from MUFU approximations (ex2,
+// rcp; a few ulp of fp32).  A GB300 SM retires 32 ex2 but only 16
+// reciprocals per clock, so the pair shares one reciprocal:
+// 1/d0 = d1 / (d0 d1), 1/d1 = d0 / (d0 d1).  The exponent is capped at 63 so
+// that d0 d1 stays finite (the cap moves sigmoid only where it is below
+// 2^-63, i.e. z < -43, where the output rounds to zero anyway).
 template <bool SILU>
-__device__ __forceinline__ uint32_t apply_pair(uint32_t w, float s0, float t0, float s1, float t1)
+__device__ __forceinline__ uint32_t apply_pair(uint32_t w, f2_t st_s, f2_t st_t)
 {
-    float z0 = fmaf(__uint_as_float(w << 16), s0, t0);
-    float z1 = fmaf(__uint_as_float(w & 0xffff0000u), s1, t1);
+    f2_t z = fma2(bf2_to_f2(w), st_s, st_t);
     if (SILU) {
-        z0 = silu1(z0);
-        z1 = silu1(z1);
+        const f2_t arg = mul2(z, pk(-1.4426950408889634f, -1.4426950408889634f));
+        float a0, a1;
+        upk(arg, a0, a1);
+        const f2_t den = add2(pk(ex2_approx(fminf(a0, 63.f)), ex2_approx(fminf(a1, 63.f))), pk(1.0f, 1.0f));
+        float d0, d1;
+        upk(den, d0, d1);
+        const float r = rcp_approx(d0 * d1);
+        z = mul2(mul2(z, pk(d1, d0)), pk(r, r));
     }
+    float z0, z1;
+    upk(z, z0, z1);
     const __nv_bfloat162 h = __floats2bfloat162_rn(z0, z1);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Outputs of vectors tid, tid + A, ... of one piece into o[]; VPT > 0: a
+// full piece of exactly VPT vectors per carrier thread, VPT == 0: any size
+// up to kMaxVecPerThread vectors per thread (the short last piece).
+template <bool SILU, int VPT>
+__device__ __forceinline__ void p2_compute(uint32_t base, int tid, int A, int nvec, const f2_t (&S)[4],
+                                           const f2_t (&Tt)[4], uint4 (&o)[kMaxVecPerThread])
+{
+#pragma unroll
+    for (int i = 0; i < (VPT > 0 ? VPT : kMaxVecPerThread); ++i) {
+        const int v = tid + i * A;
+        if (VPT > 0 || v < nvec) {
+            const uint4 w = lds128(base + 16u * static_cast<uint32_t>(v));
+            o[i].x = apply_pair<SILU>(w.x, S[0], Tt[0]);
+            o[i].y = apply_pair<SILU>(w.y, S[1], Tt[1]);
+            o[i].z = apply_pair<SILU>(w.z, S[2], Tt[2]);
+            o[i].w = apply_pair<SILU>(w.w, S[3], Tt[3]);
+        }
+    }
+}
+
+// dst points at this thread's first vector (piece start + tid)
+template <int VPT>
+__device__ __forceinline__ void p2_store(uint4 *dst, int tid, int A, int nvec, const uint4 (&o)[kMaxVecPerThread])
+{
+#pragma unroll
+    for (int i = 0; i < (VPT > 0 ? VPT : kMaxVecPerThread); ++i) {
+        if (VPT > 0 || tid + i * A < nvec) dst[i * A] = o[i];
+    }
 }
 
 // Scale / shift of batch entry n into shared memory (fused kernel): the
@@ -678,13 +954,21 @@ __device__ void fused_local_stats(const Args &a, const Smem &sm, int64_t n, bool
     float2 *st = reinterpret_cast<float2 *>(sm.base + sm.lay.st);
     const float2 *gb = reinterpret_cast<const float2 *>(sm.base + sm.lay.gb);
     float2 *gs = reinterpret_cast<float2 *>(sm.base + sm.lay.gstat);
-    for (int grp = threadIdx.x >> 5; grp < g.G; grp += kConsumerWarps) {
-        const float2 r = merge_items_warp<kFusedMaxSegments / 32>(a, n, grp);
+    constexpr int GB = 4;   // groups per warp per batch
+    for (int grp0 = threadIdx.x >> 5; grp0 < g.G; grp0 += kConsumerWarps * GB) {
+        float2 r[GB];
+        merge_groups_warp<kFusedMaxSegments / 32, GB>(a, n, grp0, kConsumerWarps, r);
         if ((threadIdx.x & 31) == 0) {
-            gs[grp] = r;
-            if (write_stats) {
-                a.mean[n * g.G + grp] = r.x;
-                a.rstd[n * g.G + grp] = r.y;
+#pragma unroll
+            for (int b = 0; b < GB; ++b) {
+                const int grp = grp0 + b * kConsumerWarps;
+                if (grp < g.G) {
+                    gs[grp] = r[b];
+                    if (write_stats) {
+                        a.mean[n * g.G + grp] = r[b].x;
+                        a.rstd[n * g.G + grp] = r[b].y;
+                    }
+                }
             }
         }
     }
@@ -707,75 +991,96 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
     const int tid = threadIdx.x;
     const int vslot = vec_slot<POW2>(g, tid);
     const int A = carriers<POW2>(g);
-    const int v0 = (tid < A) ? tid : (1 << 30);   // threads past A carry no data
-    Cursor c;
-    cursor_last(g, c);
+    const bool carrier = POW2 || tid < A;   // threads past A carry no data
+    const int full_nvec = g.rows_per_piece * g.V;
+    const int tail_nvec = static_cast<int>(g.L - (g.pieces_per_n - 1) * g.rows_per_piece) * g.V;
+    const int kind_full = vec_kind(full_nvec, A);
+    // y vectors between consecutive pieces of an item (S pieces apart; at
+    // most 512 * 2048)
+    const int item_stride = g.S * (g.piece_bytes / 16);
     int slot = slot_of(T - 1, g.ring);
-    int64_t cur_item = -1, cur_n = -1;
-    float sc[8], sh[8];
+    uint32_t base = sm.slot_addr(slot, g.piece_bytes);
+    int64_t cur_n = -1;
     bool ok = !*ctl.abort;
-    for (int64_t q = T - 1; q >= 0; --q) {
-        if (c.it != cur_item) {
+    const int64_t last_it = blockIdx.x + ((g.items - 1 - blockIdx.x) / gridDim.x) * gridDim.x;
+    for (int64_t it = last_it; it >= 0; it -= gridDim.x) {
+        const Item m = make_item(g, it);
+        // (scale, shift) of the thread's eight channels, as pairs
+        f2_t S[4], Tt[4];
+        {
             const float4 *src;
             if (FUSED) {
-                if (c.n != cur_n) {
+                if (m.n != cur_n) {
                     if (g.G * g.S <= kOneBarrierRecords)
-                        fused_local_stats(a, sm, c.n, c.s == 0);
+                        fused_local_stats(a, sm, m.n, m.s == 0);
                     else
-                        fused_scale_shift(a, sm, c.n);
+                        fused_scale_shift(a, sm, m.n);
                 }
                 src = reinterpret_cast<const float4 *>(sm.base + sm.lay.st) + 4 * vslot;
             } else {
-                src = reinterpret_cast<const float4 *>(a.st + c.n * g.C + 8 * vslot);
+                src = reinterpret_cast<const float4 *>(a.st + m.n * g.C + 8 * vslot);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float4 v = FUSED ? src[j] : __ldcg(src + j);   // (s, t) of channels 2j, 2j+1
-                sc[2 * j] = v.x;
-                sh[2 * j] = v.y;
-                sc[2 * j + 1] = v.z;
-                sh[2 * j + 1] = v.w;
+                S[j] = pk(v.x, v.z);
+                Tt[j] = pk(v.y, v.w);
             }
-            cur_item = c.it;
-            cur_n = c.n;
+            cur_n = m.n;
         }
-        if (q < T - resident) {
-            if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
-            full_par ^= 1u << slot;
-        }
-        // Read this thread's vectors and compute their outputs before the
-        // slot is released: using every loaded value guarantees that no
-        // shared-memory load of any lane is still in flight when the warp
-        // signals the producer, which may then overwrite the slot.
-        uint4 o[kMaxVecPerThread];
-        int nvec = 0;
-        if (ok) {
-            const uint32_t base = sm.slot_addr(slot, g.piece_bytes);
-            nvec = piece_rows(g, c.k) * g.V;
-#pragma unroll
-            for (int i = 0; i < kMaxVecPerThread; ++i) {
-                const int v = v0 + i * A;
-                if (v < nvec) {
-                    const uint4 w = lds128(base + 16u * v);
-                    o[i].x = apply_pair<SILU>(w.x, sc[0], sh[0], sc[1], sh[1]);
-                    o[i].y = apply_pair<SILU>(w.y, sc[2], sh[2], sc[3], sh[3]);
-                    o[i].z = apply_pair<SILU>(w.z, sc[4], sh[4], sc[5], sh[5]);
-                    o[i].w = apply_pair<SILU>(w.w, sc[6], sh[6], sc[7], sh[7]);
-                }
+        // y of the item's last piece; earlier pieces sit item_stride vectors lower
+        uint4 *dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, m.n, m.s + (m.np - 1) * g.S)) + tid;
+        for (int64_t j = m.np - 1; j >= 0; --j) {
+            if (resident > 0) {
+                --resident;   // still in its ring slot from pass 1
+            } else {
+                if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
+                full_par ^= 1u << slot;
+            }
+            const bool short_piece = m.tail && j == m.np - 1;
+            const int kind = short_piece ? 0 : kind_full;
+            const int nvec = short_piece ? tail_nvec : full_nvec;
+            const bool work = ok && carrier;
+            // Read this thread's vectors and compute their outputs before the
+            // slot is released: using every loaded value guarantees that no
+            // shared-memory load of any lane is still in flight when the warp
+            // signals the producer, which may then overwrite the slot.
+            uint4 o[kMaxVecPerThread];
+            if (work) {
+                if (kind == 8)
+                    p2_compute<SILU, 8>(base, tid, A, nvec, S, Tt, o);
+                else if (kind == 4)
+                    p2_compute<SILU, 4>(base, tid, A, nvec, S, Tt, o);
+                else if (kind == 2)
+                    p2_compute<SILU, 2>(base, tid, A, nvec, S, Tt, o);
+                else if (kind == 1)
+                    p2_compute<SILU, 1>(base, tid, A, nvec, S, Tt, o);
+                else
+                    p2_compute<SILU, 0>(base, tid, A, nvec, S, Tt, o);
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));   // the slot may be refilled now
+            if (work) {
+                if (kind == 8)
+                    p2_store<8>(dst, tid, A, nvec, o);
+                else if (kind == 4)
+                    p2_store<4>(dst, tid, A, nvec, o);
+                else if (kind == 2)
+                    p2_store<2>(dst, tid, A, nvec, o);
+                else if (kind == 1)
+                    p2_store<1>(dst, tid, A, nvec, o);
+                else
+                    p2_store<0>(dst, tid, A, nvec, o);
+            }
+            dst -= item_stride;
+            if (slot == 0) {
+                slot = g.ring - 1;
+                base = sm.slot_addr(slot, g.piece_bytes);
+            } else {
+                --slot;
+                base -= static_cast<uint32_t>(g.piece_bytes);
             }
         }
-        __syncwarp();
-        if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));   // the slot may be refilled now
-        if (ok) {
-            uint4 *dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, c.n, c.k));
-#pragma unroll
-            for (int i = 0; i < kMaxVecPerThread; ++i) {
-                const int v = v0 + i * A;
-                if (v < nvec) dst[v] = o[i];
-            }
-        }
-        cursor_prev(g, c);
-        slot = (slot == 0) ? g.ring - 1 : slot - 1;
     }
 }
 
@@ -791,13 +1096,14 @@ __device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl 
     sm.ring_s = smem_addr(g_smem);
     sm.bars_s = sm.ring_s + sm.lay.bars;
     volatile int *flags = reinterpret_cast<volatile int *>(g_smem + sm.lay.flags);
-    if (threadIdx.x == 0) {
-        const unsigned int st = *reinterpret_cast<volatile unsigned int *>(&g_status);
-        for (int s = 0; s < a.g.ring; ++s) {
+    if (threadIdx.x < 32) {
+        for (int s = threadIdx.x; s < a.g.ring; s += 32) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), kConsumerWarps);
         }
         mbar_init_fence();
+    } else if (threadIdx.x == 32) {
+        const unsigned int st = *reinterpret_cast<volatile unsigned int *>(&g_status);
         flags[0] = (st != 0u) ? 1 : 0;
     }
     T = cta_piece_count(a.g);
@@ -977,7 +1283,7 @@ __global__ void __launch_bounds__(32) gn_selftest_wait_kernel(int mode, uint64_t
 // ---------------------------------------------------------------------------
 static uint32_t smem_for(const Args &a, int kind) { return make_layout(a.g, kind).total; }
 
-// The POW2 instantiations serve every C whose vector slots divide the 512
+// The POW2 instantiations serve every C whose vector slots divide the
 // consumer threads (C a power of two); the others serve the rest.
 static bool pow2_slots(const Geom &g) { return kConsumers % g.V == 0; }
 

@@ -55,6 +55,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet sleeps in
+// hardware until it completes or `sleep_ns` pass, instead of returning at
+// once: a waiting warp then takes no issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint32_t sleep_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(sleep_ns)
+        : "memory");
+    return done != 0;
+}
+
 // ---- bulk copies (TMA, non-tensor) ----------------------------------------------
 // global -> shared, completion counted in bytes on an mbarrier
 __device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void *src, uint32_t bytes,
@@ -132,6 +148,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)
                  : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
+{
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
     return v;
 }
 
