@@ -193,6 +193,26 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     g.base_pieces = (g.pieces_per_n - 1) / g.S;
     g.last_item = static_cast<int32_t>((g.pieces_per_n - 1) % g.S);
     g.tail_rows = static_cast<int32_t>(L - (g.pieces_per_n - 1) * g.rows_per_piece);
+    g.inv_L = static_cast<float>(1.0 / static_cast<double>(L));
+    g.inv_LCg = static_cast<float>(1.0 / (static_cast<double>(L) * static_cast<double>(g.Cg)));
+    g.Cg_pow2 = (g.Cg & (g.Cg - 1)) == 0 ? 1 : 0;
+    g.log2_Cg = 0;
+    while ((1 << g.log2_Cg) < g.Cg) ++g.log2_Cg;
+    // per-CTA merge of the fused kernel: enough lanes per group that each
+    // holds at most kStatRecords records, and as many as the 256 consumer
+    // threads allow for few groups
+    int lanes = 1;
+    while (lanes < 32 && (S + lanes - 1) / lanes > gn::kStatRecords) lanes *= 2;
+    int spread = 1;
+    while (spread < 32 && spread * 2 * G <= gn::kConsumers) spread *= 2;
+    g.stat_lanes = std::max(lanes, spread);
+    g.stat_log2 = 0;
+    while ((1 << g.stat_log2) < g.stat_lanes) ++g.stat_log2;
+    const int per_pass = gn::kConsumers / g.stat_lanes;
+    g.stat_passes = static_cast<int32_t>((G + per_pass - 1) / per_pass);
+    g.rows_lo = static_cast<float>(g.base_pieces * g.rows_per_piece);
+    g.rows_hi = static_cast<float>((g.base_pieces + 1) * g.rows_per_piece);
+    g.rows_short = static_cast<float>(g.rows_per_piece - g.tail_rows);
     g.items = N * S;
     p.grid = static_cast<int>(g.items < grid_target ? g.items : grid_target);
     // ring depth from the shared memory left next to the auxiliary arrays

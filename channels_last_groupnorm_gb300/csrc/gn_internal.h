@@ -17,6 +17,7 @@ constexpr int kMinPieceBytes = 1024;
 constexpr int kMaxSegments = 512;               // segments per batch entry
 constexpr int kFusedMaxSegments = 160;          // ... in the fused kernel (5 records per lane)
 constexpr int kScratchBytes = 16384;            // pass-1 CTA reduction scratch
+constexpr int kStatRecords = 20;               // fused kernel: item records per lane in the per-CTA merge
 constexpr int kOneBarrierRecords = 8192;        // fused kernel: every CTA merges all G*S item records
                                                 // of its batch entry itself when there are at most this many
 constexpr int kSyncWords = 64;                  // 256-byte workspace header
@@ -40,6 +41,12 @@ struct Geom {
     int64_t base_pieces;          // (pieces_per_n - 1) / S
     int32_t last_item;            // (pieces_per_n - 1) % S
     int32_t tail_rows;            // L - (pieces_per_n - 1) * rows_per_piece
+    float inv_L, inv_LCg;         // 1 / L and 1 / (L * Cg), rounded to fp32
+    int32_t Cg_pow2, log2_Cg;     // Cg is a power of two: Cg = 1 << log2_Cg
+    int32_t stat_lanes;           // fused kernel: lanes per group in the per-CTA merge (power of two <= 32)
+    int32_t stat_log2, stat_passes;   // log2(stat_lanes); passes over the groups
+    float rows_lo, rows_hi, rows_short;   // item rows (base_pieces, base_pieces + 1 pieces) and the
+                                          // short last piece's missing rows, as floats
 };
 
 struct Args {

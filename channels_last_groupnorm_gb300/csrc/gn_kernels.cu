@@ -116,8 +116,8 @@ __device__ __forceinline__ int64_t item_pieces(const Geom &g, int32_t s)
 // rows of item s (as a float, for the statistics)
 __device__ __forceinline__ float item_rows_f(const Geom &g, int32_t s)
 {
-    const int64_t rows = item_pieces(g, s) * g.rows_per_piece;
-    return static_cast<float>(s == g.last_item ? rows - (g.rows_per_piece - g.tail_rows) : rows);
+    const float rows = s <= g.last_item ? g.rows_hi : g.rows_lo;
+    return s == g.last_item ? rows - g.rows_short : rows;
 }
 
 __device__ __forceinline__ void load_item(const Geom &g, Cursor &c, int64_t it)
@@ -151,7 +151,8 @@ struct Item {
 __device__ __forceinline__ Item make_item(const Geom &g, int64_t it)
 {
     Item m;
-    m.n = it / g.S;
+    m.n = (g.items < (int64_t(1) << 31)) ? static_cast<int64_t>(static_cast<uint32_t>(it) / static_cast<uint32_t>(g.S))
+                                          : it / g.S;
     m.s = static_cast<int32_t>(it - m.n * g.S);
     m.np = item_pieces(g, m.s);
     m.tail = (m.s + (m.np - 1) * g.S) == g.pieces_per_n - 1;
@@ -298,7 +299,11 @@ struct Smem {
     }
 };
 
-__device__ __forceinline__ int slot_of(int64_t q, int ring) { return static_cast<int>(q % ring); }
+__device__ __forceinline__ int slot_of(int64_t q, int ring)
+{
+    return (q < (int64_t(1) << 31)) ? static_cast<int>(static_cast<uint32_t>(q) % static_cast<uint32_t>(ring))
+                                    : static_cast<int>(q % ring);
+}
 
 // ---------------------------------------------------------------------------
 // producer (one thread): pass-1 loads
@@ -803,10 +808,11 @@ __device__ __forceinline__ void merge_groups_warp(const Args &a, int64_t n, int 
     const Geom &g = a.g;
     const int lane = threadIdx.x & 31;
     float2 r[GB][PER_LANE];
+    const float2 *src_n = a.partial + n * g.G * g.S;   // then grp * S fits 32 bits
 #pragma unroll
     for (int b = 0; b < GB; ++b) {
         const int grp = grp0 + b * gstride;
-        const float2 *src = a.partial + (n * g.G + (grp < g.G ? grp : 0)) * g.S;
+        const float2 *src = src_n + (grp < g.G ? grp : 0) * g.S;
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
             const int s = lane + 32 * i;
@@ -819,7 +825,6 @@ __device__ __forceinline__ void merge_groups_warp(const Args &a, int64_t n, int 
         const int s = lane + 32 * i;
         rows[i] = s < g.S ? item_rows_f(g, s) : 0.f;
     }
-    const float Lf = static_cast<float>(g.L);
     const float cgf = static_cast<float>(g.Cg);
     float acc[GB];
 #pragma unroll
@@ -835,7 +840,7 @@ __device__ __forceinline__ void merge_groups_warp(const Args &a, int64_t n, int 
     float mean[GB], acc2[GB];
 #pragma unroll
     for (int b = 0; b < GB; ++b) {
-        mean[b] = acc[b] / Lf;
+        mean[b] = acc[b] * g.inv_L;
         acc2[b] = 0.f;
 #pragma unroll
         for (int i = 0; i < PER_LANE; ++i) {
@@ -849,8 +854,8 @@ __device__ __forceinline__ void merge_groups_warp(const Args &a, int64_t n, int 
         for (int b = 0; b < GB; ++b) acc2[b] += __shfl_xor_sync(0xffffffffu, acc2[b], off);
 #pragma unroll
     for (int b = 0; b < GB; ++b) {
-        const float var = fmaxf(acc2[b] / (Lf * cgf), 0.f);
-        out[b] = make_float2(mean[b], 1.0f / sqrtf(var + a.eps));
+        const float var = fmaxf(acc2[b] * g.inv_LCg, 0.f);
+        out[b] = make_float2(mean[b], rsqrtf(var + a.eps));
     }
 }
 
@@ -936,7 +941,7 @@ __device__ void fused_scale_shift(const Args &a, const Smem &sm, int64_t n)
     for (int grp = threadIdx.x; grp < g.G; grp += kConsumers) gs[grp] = __ldcg(a.gstat + n * g.G + grp);
     named_sync(1, kConsumers);
     for (int c = threadIdx.x; c < g.C; c += kConsumers) {
-        const float2 r = gs[c / g.Cg];
+        const float2 r = gs[g.Cg_pow2 ? (c >> g.log2_Cg) : (c / g.Cg)];
         const float2 ab = gb[c];
         const float sc = ab.x * r.y;
         st[c] = make_float2(sc, ab.y - r.x * sc);
@@ -945,46 +950,98 @@ __device__ void fused_scale_shift(const Args &a, const Smem &sm, int64_t n)
 }
 
 // Scale / shift of batch entry n when every CTA merges the group records
-// itself (one-barrier fused schedule): one warp per group merges the S item
-// records, then every channel folds its gamma / beta with its group's
-// statistics.  The CTA that owns item 0 of n writes the statistics outputs.
+// itself (one-barrier fused schedule).  P = stat_lanes lanes (a power of
+// two, at most a warp) take one group: lane `sub` loads records sub,
+// sub + P, ... (at most kStatRecords of them, all loads in flight at
+// once).  The records are merged around a shift K (record 0's mean, which
+// is within a few standard errors of the group mean):
+//   A1 = sum rows_s (m_s - K),  A2 = sum [M2_s + rows_s Cg (m_s - K)^2]
+//   mean = K + A1 / L,          M2 = A2 - Cg A1^2 / L
+// with one butterfly over the P lanes; those lanes then fold gamma / beta
+// of the group's channels.  The CTA that owns item 0 of n writes the
+// statistics outputs.
 __device__ void fused_local_stats(const Args &a, const Smem &sm, int64_t n, bool write_stats)
 {
     const Geom &g = a.g;
+    const int tid = threadIdx.x;
+    const int P = g.stat_lanes;
+    const int sub = tid & (P - 1);
+    const int src_lane = (tid & 31) & ~(P - 1);   // lane of sub 0 in this lane's P-group
+    const int per_pass = kConsumers >> g.stat_log2;
+    const int passes = g.stat_passes;
     float2 *st = reinterpret_cast<float2 *>(sm.base + sm.lay.st);
     const float2 *gb = reinterpret_cast<const float2 *>(sm.base + sm.lay.gb);
-    float2 *gs = reinterpret_cast<float2 *>(sm.base + sm.lay.gstat);
-    constexpr int GB = 4;   // groups per warp per batch
-    for (int grp0 = threadIdx.x >> 5; grp0 < g.G; grp0 += kConsumerWarps * GB) {
-        float2 r[GB];
-        merge_groups_warp<kFusedMaxSegments / 32, GB>(a, n, grp0, kConsumerWarps, r);
-        if ((threadIdx.x & 31) == 0) {
+    const float2 *src_n = a.partial + n * g.G * g.S;   // then grp * S fits 32 bits
+    const float cgf = static_cast<float>(g.Cg);
+    for (int pass = 0; pass < passes; ++pass) {
+        const int grp = (tid >> g.stat_log2) + pass * per_pass;
+        const bool valid = grp < g.G;
+        const float2 *src = src_n + (valid ? grp : 0) * g.S;
+        float2 r[kStatRecords];
 #pragma unroll
-            for (int b = 0; b < GB; ++b) {
-                const int grp = grp0 + b * kConsumerWarps;
-                if (grp < g.G) {
-                    gs[grp] = r[b];
-                    if (write_stats) {
-                        a.mean[n * g.G + grp] = r[b].x;
-                        a.rstd[n * g.G + grp] = r[b].y;
-                    }
-                }
+        for (int i = 0; i < kStatRecords; ++i) {
+            const int s_ = sub + P * i;
+            r[i] = (valid && s_ < g.S) ? __ldcg(src + s_) : make_float2(0.f, 0.f);
+        }
+        const float K = __shfl_sync(0xffffffffu, r[0].x, src_lane);
+        float A1 = 0.f, A2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < kStatRecords; ++i) {
+            const int s_ = sub + P * i;
+            const float rows = s_ < g.S ? item_rows_f(g, s_) : 0.f;
+            const float d = r[i].x - K;
+            A1 = fmaf(rows, d, A1);
+            A2 += fmaf(rows * cgf * d, d, r[i].y);
+        }
+        for (int off = 1; off < P; off <<= 1) {
+            A1 += __shfl_xor_sync(0xffffffffu, A1, off);
+            A2 += __shfl_xor_sync(0xffffffffu, A2, off);
+        }
+        const float mo = A1 * g.inv_L;
+        const float mean = K + mo;
+        const float var = fmaxf((A2 - cgf * A1 * mo) * g.inv_LCg, 0.f);
+        const float rstd = rsqrtf(var + a.eps);
+        if (valid) {
+            if (write_stats && sub == 0) {
+                a.mean[n * g.G + grp] = mean;
+                a.rstd[n * g.G + grp] = rstd;
+            }
+            for (int c = grp * g.Cg + sub; c < (grp + 1) * g.Cg; c += P) {
+                const float2 ab = gb[c];
+                const float sc = ab.x * rstd;
+                st[c] = make_float2(sc, ab.y - mean * sc);
             }
         }
     }
     named_sync(1, kConsumers);
-    for (int c = threadIdx.x; c < g.C; c += kConsumers) {
-        const float2 r = gs[c / g.Cg];
-        const float2 ab = gb[c];
-        const float sc = ab.x * r.y;
-        st[c] = make_float2(sc, ab.y - r.x * sc);
-    }
-    named_sync(1, kConsumers);
+}
+
+// Where a consumer thread starts pass 2: the CTA's last item, the ring slot
+// of its last piece and that piece's y address.  Integer divisions only;
+// the fused kernel works this out before pass 1, while the first bulk
+// copies are in flight, so that none of it sits between the grid barrier
+// and the first output.
+struct P2Start {
+    int64_t it;
+    Item m;
+    int slot;
+    uint4 *dst;
+};
+
+__device__ __forceinline__ P2Start pass2_start(const Args &a, int64_t T)
+{
+    const Geom &g = a.g;
+    P2Start p;
+    p.it = (g.items <= gridDim.x) ? blockIdx.x : blockIdx.x + ((g.items - 1 - blockIdx.x) / gridDim.x) * gridDim.x;
+    p.m = make_item(g, p.it);
+    p.slot = T > 0 ? slot_of(T - 1, g.ring) : 0;
+    p.dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, p.m.n, p.m.s + (p.m.np - 1) * g.S)) + threadIdx.x;
+    return p;
 }
 
 template <bool SILU, bool FUSED, bool POW2>
 __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t resident, uint32_t &full_par,
-                              const Ctl &ctl)
+                              const Ctl &ctl, const P2Start &start)
 {
     const Geom &g = a.g;
     if (T == 0) return;
@@ -998,13 +1055,14 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
     // y vectors between consecutive pieces of an item (S pieces apart; at
     // most 512 * 2048)
     const int item_stride = g.S * (g.piece_bytes / 16);
-    int slot = slot_of(T - 1, g.ring);
+    int slot = start.slot;
     uint32_t base = sm.slot_addr(slot, g.piece_bytes);
     int64_t cur_n = -1;
     bool ok = !*ctl.abort;
-    const int64_t last_it = blockIdx.x + ((g.items - 1 - blockIdx.x) / gridDim.x) * gridDim.x;
-    for (int64_t it = last_it; it >= 0; it -= gridDim.x) {
-        const Item m = make_item(g, it);
+    int64_t it = start.it;
+    Item m = start.m;
+    uint4 *dst = start.dst;   // y of the item's last piece, this thread's first vector
+    for (;;) {
         // (scale, shift) of the thread's eight channels, as pairs
         f2_t S[4], Tt[4];
         {
@@ -1028,8 +1086,7 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
             }
             cur_n = m.n;
         }
-        // y of the item's last piece; earlier pieces sit item_stride vectors lower
-        uint4 *dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, m.n, m.s + (m.np - 1) * g.S)) + tid;
+        // earlier pieces of the item sit item_stride vectors lower
         for (int64_t j = m.np - 1; j >= 0; --j) {
             if (resident > 0) {
                 --resident;   // still in its ring slot from pass 1
@@ -1081,6 +1138,10 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
                 base -= static_cast<uint32_t>(g.piece_bytes);
             }
         }
+        it -= gridDim.x;
+        if (it < 0) break;
+        m = make_item(g, it);
+        dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, m.n, m.s + (m.np - 1) * g.S)) + tid;
     }
 }
 
@@ -1174,7 +1235,7 @@ __global__ void __launch_bounds__(kThreads, 1) gn_pass2_kernel(const __grid_cons
         return;
     }
     uint32_t full_par = 0;
-    consume_pass2<SILU, false, POW2>(a, sm, T, 0, full_par, ctl);
+    consume_pass2<SILU, false, POW2>(a, sm, T, 0, full_par, ctl, pass2_start(a, T));
 }
 
 template <bool SILU, bool POW2>
@@ -1196,10 +1257,12 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
         for (int c = threadIdx.x; c < g.C; c += kConsumers) gb[c] = make_float2(a.gamma[c], a.beta[c]);
     }
 
-    // pass 1
+    // pass 1 (the consumers first work out where pass 2 will start)
+    P2Start start{};
     if (producer) {
         produce_pass1(a, sm, T, ps, ctl, true);
     } else if (threadIdx.x < kConsumers) {
+        start = pass2_start(a, T);
         consume_pass1<POW2>(a, sm, T, full_par, ctl);
     }
     // every item record of the grid is written
@@ -1238,7 +1301,7 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
         produce_pass2(a, sm, T, resident, ps, ctl);
         if (*ctl.abort) drain_loads(sm, ps, g.ring);
     } else if (threadIdx.x < kConsumers) {
-        consume_pass2<SILU, true, POW2>(a, sm, T, resident, full_par, ctl);
+        consume_pass2<SILU, true, POW2>(a, sm, T, resident, full_par, ctl, start);
     }
 }
 
