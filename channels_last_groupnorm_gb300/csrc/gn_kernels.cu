@@ -713,6 +713,63 @@ __device__ __forceinline__ void reduce_item(const Args &a, const Smem &sm, const
     }
 }
 
+// Consumer-side ring position and wait state, carried from piece to piece.
+struct RingPos {
+    int slot;
+    uint32_t base;        // shared address of the slot
+    uint32_t full_par;    // parity of the next full-barrier phase, per slot
+    bool ok;              // no wait has expired
+};
+
+// The shift K of the thread's eight channels: each channel's group's first
+// channel in the item's first row (shared by the whole group), read from
+// the item's first piece; threads tid < V also publish them per channel.
+template <bool POW2>
+__device__ __forceinline__ void item_shift(const Geom &g, const Smem &sm, uint32_t base, int vslot, f2_t (&K)[4])
+{
+    float kc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = 8 * vslot + i;
+        const int c0 = POW2 ? (c & ~(g.Cg - 1)) : (c / g.Cg) * g.Cg;
+        kc[i] = __uint_as_float(lds_u16(base + 2u * c0) << 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) K[i] = pk(kc[2 * i], kc[2 * i + 1]);
+    if (static_cast<int>(threadIdx.x) < g.V) {
+        float4 *kv = reinterpret_cast<float4 *>(sm.base + sm.lay.kvec) + 2 * vslot;
+        kv[0] = make_float4(kc[0], kc[1], kc[2], kc[3]);
+        kv[1] = make_float4(kc[4], kc[5], kc[6], kc[7]);
+    }
+}
+
+// `count` consecutive pieces of an item in pass 1, each of nvec vectors
+// (VPT per carrier thread when VPT > 0).  The first one sets the shift K
+// when need_k.
+template <bool POW2, int VPT>
+__device__ __forceinline__ void p1_run(const Geom &g, const Smem &sm, const Ctl &ctl, int64_t count, int nvec, int A,
+                                    bool carrier, int vslot, bool need_k, f2_t (&K)[4], f2_t (&s1)[4], f2_t (&s2)[4],
+                                    RingPos &rp)
+{
+    const int tid = threadIdx.x;
+    for (int64_t j = 0; j < count; ++j) {
+        if (rp.ok) rp.ok = wait_phase(sm.full(rp.slot), (rp.full_par >> rp.slot) & 1u, ctl);
+        rp.full_par ^= 1u << rp.slot;
+        if (rp.ok) {
+            if (need_k && j == 0) item_shift<POW2>(g, sm, rp.base, vslot, K);
+            if (carrier) p1_piece<VPT>(rp.base, tid, A, nvec, K, s1, s2);
+        }
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(sm.empty(rp.slot));
+        if (++rp.slot == g.ring) {
+            rp.slot = 0;
+            rp.base = sm.ring_s;
+        } else {
+            rp.base += static_cast<uint32_t>(g.piece_bytes);
+        }
+    }
+}
+
 template <bool POW2>
 __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t &full_par, const Ctl &ctl)
 {
@@ -723,73 +780,29 @@ __device__ void consume_pass1(const Args &a, const Smem &sm, int64_t T, uint32_t
     const int A = carriers<POW2>(g);
     const bool carrier = POW2 || tid < A;
     const int full_nvec = g.rows_per_piece * g.V;
-    const int tail_nvec = static_cast<int>(g.L - (g.pieces_per_n - 1) * g.rows_per_piece) * g.V;
+    const int tail_nvec = g.tail_rows * g.V;
     const int kind_full = vec_kind(full_nvec, A);
-    float *kvec = reinterpret_cast<float *>(sm.base + sm.lay.kvec);
-    int slot = 0;
-    uint32_t base = sm.ring_s;
-    bool ok = !*ctl.abort;
+    RingPos rp{0, sm.ring_s, full_par, !*ctl.abort};
     for (int64_t it = blockIdx.x; it < g.items; it += gridDim.x) {
         const Item m = make_item(g, it);
         f2_t K[4], s1[4], s2[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s1[i] = s2[i] = 0ull;
-        for (int64_t j = 0; j < m.np; ++j) {
-            if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
-            full_par ^= 1u << slot;
-            if (ok) {
-                if (j == 0) {
-                    // the shift K of a channel: its group's first channel in
-                    // the item's first row (shared by the whole group)
-                    float kc[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int c = 8 * vslot + i;
-                        const int c0 = POW2 ? (c & ~(g.Cg - 1)) : (c / g.Cg) * g.Cg;
-                        kc[i] = __uint_as_float(lds_u16(base + 2u * c0) << 16);
-                    }
-                    K[0] = pk(kc[0], kc[1]);
-                    K[1] = pk(kc[2], kc[3]);
-                    K[2] = pk(kc[4], kc[5]);
-                    K[3] = pk(kc[6], kc[7]);
-                    if (tid < g.V) {
-                        float4 *kv = reinterpret_cast<float4 *>(kvec + 8 * vslot);
-                        float k0, k1, k2, k3, k4, k5, k6, k7;
-                        upk(K[0], k0, k1);
-                        upk(K[1], k2, k3);
-                        upk(K[2], k4, k5);
-                        upk(K[3], k6, k7);
-                        kv[0] = make_float4(k0, k1, k2, k3);
-                        kv[1] = make_float4(k4, k5, k6, k7);
-                    }
-                }
-                const bool short_piece = m.tail && j == m.np - 1;
-                const int kind = short_piece ? 0 : kind_full;
-                const int nvec = short_piece ? tail_nvec : full_nvec;
-                if (carrier) {
-                    if (kind == 8)
-                        p1_piece<8>(base, tid, A, nvec, K, s1, s2);
-                    else if (kind == 4)
-                        p1_piece<4>(base, tid, A, nvec, K, s1, s2);
-                    else if (kind == 2)
-                        p1_piece<2>(base, tid, A, nvec, K, s1, s2);
-                    else if (kind == 1)
-                        p1_piece<1>(base, tid, A, nvec, K, s1, s2);
-                    else
-                        p1_piece<0>(base, tid, A, nvec, K, s1, s2);
-                }
-            }
-            __syncwarp();
-            if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));
-            if (++slot == g.ring) {
-                slot = 0;
-                base = sm.ring_s;
-            } else {
-                base += static_cast<uint32_t>(g.piece_bytes);
+        for (int i = 0; i < 4; ++i) K[i] = s1[i] = s2[i] = 0ull;
+        // the item's full pieces, then the batch entry's short last piece
+        const int64_t full = m.np - (m.tail ? 1 : 0);
+        if (full > 0) {
+            switch (kind_full) {
+            case 8: p1_run<POW2, 8>(g, sm, ctl, full, full_nvec, A, carrier, vslot, true, K, s1, s2, rp); break;
+            case 4: p1_run<POW2, 4>(g, sm, ctl, full, full_nvec, A, carrier, vslot, true, K, s1, s2, rp); break;
+            case 2: p1_run<POW2, 2>(g, sm, ctl, full, full_nvec, A, carrier, vslot, true, K, s1, s2, rp); break;
+            case 1: p1_run<POW2, 1>(g, sm, ctl, full, full_nvec, A, carrier, vslot, true, K, s1, s2, rp); break;
+            default: p1_run<POW2, 0>(g, sm, ctl, full, full_nvec, A, carrier, vslot, true, K, s1, s2, rp); break;
             }
         }
+        if (m.tail) p1_run<POW2, 0>(g, sm, ctl, 1, tail_nvec, A, carrier, vslot, full == 0, K, s1, s2, rp);
         reduce_item<POW2>(a, sm, m, s1, s2);
     }
+    full_par = rp.full_par;
 }
 
 // ---------------------------------------------------------------------------
@@ -898,33 +911,28 @@ __device__ __forceinline__ uint32_t apply_pair(uint32_t w, f2_t st_s, f2_t st_t)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Outputs of vectors tid, tid + A, ... of one piece into o[]; VPT > 0: a
-// full piece of exactly VPT vectors per carrier thread, VPT == 0: any size
-// up to kMaxVecPerThread vectors per thread (the short last piece).
+// Outputs of vectors tid, tid + A, ... of one piece, each stored as soon as
+// it is computed; dst points at this thread's first vector (piece start +
+// tid).  VPT > 0: a full piece of exactly VPT vectors per carrier thread,
+// VPT == 0: any size up to kMaxVecPerThread vectors per thread (the short
+// last piece).  When this returns, every shared-memory load of the thread
+// has been consumed by a store that is already issued.
 template <bool SILU, int VPT>
-__device__ __forceinline__ void p2_compute(uint32_t base, int tid, int A, int nvec, const f2_t (&S)[4],
-                                           const f2_t (&Tt)[4], uint4 (&o)[kMaxVecPerThread])
+__device__ __forceinline__ void p2_piece(uint32_t base, uint4 *dst, int tid, int A, int nvec, const f2_t (&S)[4],
+                                         const f2_t (&Tt)[4])
 {
 #pragma unroll
     for (int i = 0; i < (VPT > 0 ? VPT : kMaxVecPerThread); ++i) {
         const int v = tid + i * A;
         if (VPT > 0 || v < nvec) {
             const uint4 w = lds128(base + 16u * static_cast<uint32_t>(v));
-            o[i].x = apply_pair<SILU>(w.x, S[0], Tt[0]);
-            o[i].y = apply_pair<SILU>(w.y, S[1], Tt[1]);
-            o[i].z = apply_pair<SILU>(w.z, S[2], Tt[2]);
-            o[i].w = apply_pair<SILU>(w.w, S[3], Tt[3]);
+            uint4 o;
+            o.x = apply_pair<SILU>(w.x, S[0], Tt[0]);
+            o.y = apply_pair<SILU>(w.y, S[1], Tt[1]);
+            o.z = apply_pair<SILU>(w.z, S[2], Tt[2]);
+            o.w = apply_pair<SILU>(w.w, S[3], Tt[3]);
+            dst[i * A] = o;
         }
-    }
-}
-
-// dst points at this thread's first vector (piece start + tid)
-template <int VPT>
-__device__ __forceinline__ void p2_store(uint4 *dst, int tid, int A, int nvec, const uint4 (&o)[kMaxVecPerThread])
-{
-#pragma unroll
-    for (int i = 0; i < (VPT > 0 ? VPT : kMaxVecPerThread); ++i) {
-        if (VPT > 0 || tid + i * A < nvec) dst[i * A] = o[i];
     }
 }
 
@@ -1039,6 +1047,39 @@ __device__ __forceinline__ P2Start pass2_start(const Args &a, int64_t T)
     return p;
 }
 
+// `count` consecutive pieces of an item in pass 2, walked backwards, each of
+// nvec vectors (VPT per carrier thread when VPT > 0).  The first
+// `resident` pieces are still in their ring slots from pass 1.
+template <bool SILU, int VPT>
+__device__ __forceinline__ void p2_run(const Geom &g, const Smem &sm, const Ctl &ctl, int64_t count, int nvec, int A,
+                                    bool carrier, int item_stride, const f2_t (&S)[4], const f2_t (&Tt)[4],
+                                    int64_t &resident, uint4 *&dst, RingPos &rp)
+{
+    const int tid = threadIdx.x;
+    for (int64_t j = 0; j < count; ++j) {
+        if (resident > 0) {
+            --resident;
+        } else {
+            if (rp.ok) rp.ok = wait_phase(sm.full(rp.slot), (rp.full_par >> rp.slot) & 1u, ctl);
+            rp.full_par ^= 1u << rp.slot;
+        }
+        // Every loaded value is used by an issued store before the slot is
+        // released, so no shared-memory load of any lane is still in flight
+        // when the warp signals the producer, which may then overwrite it.
+        if (rp.ok && carrier) p2_piece<SILU, VPT>(rp.base, dst, tid, A, nvec, S, Tt);
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(sm.empty(rp.slot));   // the slot may be refilled now
+        dst -= item_stride;
+        if (rp.slot == 0) {
+            rp.slot = g.ring - 1;
+            rp.base = sm.slot_addr(rp.slot, g.piece_bytes);
+        } else {
+            --rp.slot;
+            rp.base -= static_cast<uint32_t>(g.piece_bytes);
+        }
+    }
+}
+
 template <bool SILU, bool FUSED, bool POW2>
 __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t resident, uint32_t &full_par,
                               const Ctl &ctl, const P2Start &start)
@@ -1050,15 +1091,13 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
     const int A = carriers<POW2>(g);
     const bool carrier = POW2 || tid < A;   // threads past A carry no data
     const int full_nvec = g.rows_per_piece * g.V;
-    const int tail_nvec = static_cast<int>(g.L - (g.pieces_per_n - 1) * g.rows_per_piece) * g.V;
+    const int tail_nvec = g.tail_rows * g.V;
     const int kind_full = vec_kind(full_nvec, A);
     // y vectors between consecutive pieces of an item (S pieces apart; at
     // most 512 * 2048)
     const int item_stride = g.S * (g.piece_bytes / 16);
-    int slot = start.slot;
-    uint32_t base = sm.slot_addr(slot, g.piece_bytes);
+    RingPos rp{start.slot, sm.slot_addr(start.slot, g.piece_bytes), full_par, !*ctl.abort};
     int64_t cur_n = -1;
-    bool ok = !*ctl.abort;
     int64_t it = start.it;
     Item m = start.m;
     uint4 *dst = start.dst;   // y of the item's last piece, this thread's first vector
@@ -1086,63 +1125,22 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
             }
             cur_n = m.n;
         }
-        // earlier pieces of the item sit item_stride vectors lower
-        for (int64_t j = m.np - 1; j >= 0; --j) {
-            if (resident > 0) {
-                --resident;   // still in its ring slot from pass 1
-            } else {
-                if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
-                full_par ^= 1u << slot;
-            }
-            const bool short_piece = m.tail && j == m.np - 1;
-            const int kind = short_piece ? 0 : kind_full;
-            const int nvec = short_piece ? tail_nvec : full_nvec;
-            const bool work = ok && carrier;
-            // Read this thread's vectors and compute their outputs before the
-            // slot is released: using every loaded value guarantees that no
-            // shared-memory load of any lane is still in flight when the warp
-            // signals the producer, which may then overwrite the slot.
-            uint4 o[kMaxVecPerThread];
-            if (work) {
-                if (kind == 8)
-                    p2_compute<SILU, 8>(base, tid, A, nvec, S, Tt, o);
-                else if (kind == 4)
-                    p2_compute<SILU, 4>(base, tid, A, nvec, S, Tt, o);
-                else if (kind == 2)
-                    p2_compute<SILU, 2>(base, tid, A, nvec, S, Tt, o);
-                else if (kind == 1)
-                    p2_compute<SILU, 1>(base, tid, A, nvec, S, Tt, o);
-                else
-                    p2_compute<SILU, 0>(base, tid, A, nvec, S, Tt, o);
-            }
-            __syncwarp();
-            if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));   // the slot may be refilled now
-            if (work) {
-                if (kind == 8)
-                    p2_store<8>(dst, tid, A, nvec, o);
-                else if (kind == 4)
-                    p2_store<4>(dst, tid, A, nvec, o);
-                else if (kind == 2)
-                    p2_store<2>(dst, tid, A, nvec, o);
-                else if (kind == 1)
-                    p2_store<1>(dst, tid, A, nvec, o);
-                else
-                    p2_store<0>(dst, tid, A, nvec, o);
-            }
-            dst -= item_stride;
-            if (slot == 0) {
-                slot = g.ring - 1;
-                base = sm.slot_addr(slot, g.piece_bytes);
-            } else {
-                --slot;
-                base -= static_cast<uint32_t>(g.piece_bytes);
-            }
+        // backwards: the batch entry's short last piece (if the item owns it), then the full ones
+        if (m.tail) p2_run<SILU, 0>(g, sm, ctl, 1, tail_nvec, A, carrier, item_stride, S, Tt, resident, dst, rp);
+        const int64_t full = m.np - (m.tail ? 1 : 0);
+        switch (kind_full) {
+        case 8: p2_run<SILU, 8>(g, sm, ctl, full, full_nvec, A, carrier, item_stride, S, Tt, resident, dst, rp); break;
+        case 4: p2_run<SILU, 4>(g, sm, ctl, full, full_nvec, A, carrier, item_stride, S, Tt, resident, dst, rp); break;
+        case 2: p2_run<SILU, 2>(g, sm, ctl, full, full_nvec, A, carrier, item_stride, S, Tt, resident, dst, rp); break;
+        case 1: p2_run<SILU, 1>(g, sm, ctl, full, full_nvec, A, carrier, item_stride, S, Tt, resident, dst, rp); break;
+        default: p2_run<SILU, 0>(g, sm, ctl, full, full_nvec, A, carrier, item_stride, S, Tt, resident, dst, rp); break;
         }
         it -= gridDim.x;
         if (it < 0) break;
         m = make_item(g, it);
         dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, m.n, m.s + (m.np - 1) * g.S)) + tid;
     }
+    full_par = rp.full_par;
 }
 
 // ---------------------------------------------------------------------------
