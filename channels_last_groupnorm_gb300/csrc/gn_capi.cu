@@ -171,7 +171,7 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     g.V = static_cast<int32_t>(C / 8);
     g.A = (gn::kConsumers / g.V) * g.V;
     const int64_t row_bytes = 2 * C;
-    const int64_t grid_target = d.sm_count;   // one CTA per SM (544 threads, most of shared memory)
+    const int64_t grid_target = d.sm_count;   // one CTA per SM (288 threads, most of shared memory)
     const int64_t total_bytes = N * L * row_bytes;
     // pieces of whole rows, as large as 32 KB and at most kMaxVecPerThread
     // vectors per data-carrying consumer thread; smaller when that leaves

@@ -11,20 +11,21 @@
 //  * The tensor is cut into "pieces" of whole rows (up to 32 KB); each CTA
 //    streams its pieces through a ring of shared-memory slots filled by bulk
 //    TMA copies (cp.async.bulk) issued by one producer thread, completion
-//    tracked on mbarriers.  Sixteen consumer warps read 16-byte vectors from
-//    shared memory; with C a power of two each consumer thread always sees
-//    the same eight channels.  Pass-1 arithmetic on channel pairs uses the
-//    packed fp32x2 instructions of sm_100+ (add/sub/fma .f32x2).
-//  * Pass 1 keeps, per thread, fp32 sums of (x - K) and (x - K)^2 with K a
-//    per-(work item, channel) shift (the item's first row), then reduces
-//    them per CTA with warp shuffles and shared memory into per-channel
-//    (mean, M2) and merges those (Chan's parallel formula) into one
-//    (mean, M2, rows) record per (batch entry, group, item).  The finalize
-//    merges the items' records of each group the same way.
+//    tracked on mbarriers.  Eight consumer warps read 16-byte vectors from
+//    shared memory; each consumer thread always sees the same eight
+//    channels, and a full piece is a fixed number of vectors per thread, so
+//    the piece loops are compiled per vector count.  Channel pairs use the
+//    packed fp32x2 instructions of sm_100+ (add/sub/mul/fma .f32x2).
+//  * Pass 1 keeps, per thread, fp32 sums of (x - K) and (x - K)^2, K being
+//    the channel's group's first value in the work item's first row (one
+//    shift per group, so sums of a group's channels add directly), then
+//    reduces them per CTA (warp butterflies and shared memory) into one
+//    (mean, M2) record per (batch entry, group, item).  The finalize merges
+//    the records of each group (Chan's parallel formula, around a shift).
 //  * Pass 2 loads pieces the same way, in the reverse of pass-1 order so the
 //    most recently read rows (still in L2) come first; each consumer thread
-//    takes its vectors out of the slot, releases the slot at once, and
-//    writes y with coalesced 16-byte global stores.
+//    computes and stores its outputs (coalesced 16-byte global stores) and
+//    then releases the slot.
 //  * The fused kernel does all three steps in one cooperative launch: after
 //    one grid barrier every CTA merges the G*S records of its batch entry
 //    itself (a second barrier is used only when there are very many
@@ -456,8 +457,9 @@ __device__ __forceinline__ float comp(const float4 &v, int j)
     return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-// Reduce the per-thread shifted sums of one work item into the item's
-// per-group (mean, M2, rows) records.  Threads that share a vector slot
+// Any C (the path of C that are not powers of two): reduce the per-thread
+// shifted sums of one work item into the item's per-group (mean, M2)
+// records.  Threads that share a vector slot
 // first combine by warp shuffles (when the slot repeats inside a warp), then
 // through shared memory; when the scratch cannot hold every entry at once,
 // the upper half of the entries is first added into the lower half.  The
@@ -614,7 +616,7 @@ __device__ __forceinline__ void p1_piece(uint32_t base, int tid, int A, int nvec
     }
 }
 
-// Power-of-two C: the item's per-group (mean, M2, rows) records straight
+// Power-of-two C: the item's per-group (mean, M2) records straight
 // from the per-thread sums, without per-channel statistics.  Every channel
 // of a group shares the group's shift K_g, so sums of different channels
 // of one group add directly.  U = max(1, 8 / Cg) groups per thread; a group
