@@ -242,7 +242,7 @@ def raw_entry(w):
 
 
 def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, sampler=None,
-                     seeded=True, launch="graph"):
+                     seeded=True, launch="graph", hot_l2=False):
     """Device-resident timing of one workload.  Returns a dict."""
     import torch
     from channels_last_groupnorm_gb300 import gnsilu as gs
@@ -260,7 +260,7 @@ def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, s
     elems = w.elements
     set_bytes = 4 * elems
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    nsets = buffer_sets_for(set_bytes, l2)
+    nsets = 1 if hot_l2 else buffer_sets_for(set_bytes, l2)
     free, _ = torch.cuda.mem_get_info(device)
     nsets = max(1, min(nsets, int(0.5 * free // set_bytes)))
     xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
@@ -356,9 +356,28 @@ def measure_e2e(w, variant_id, steps, warmup, device, stream):
     return elapsed, h2d, d2h
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or ''."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return ""
+
+
 def cpu_baseline(w, budget_s=12.0):
     """The fp64 oracle on this host's cores, on the full workload tensor,
-    repeated until about `budget_s` of CPU time has passed."""
+    repeated until about `budget_s` of CPU time has passed; plus a short
+    single-thread run."""
     import oracle
     from channels_last_groupnorm_gb300 import workloads as wl
     case = wl.make_inputs(w)
@@ -372,8 +391,18 @@ def cpu_baseline(w, budget_s=12.0):
         if time.perf_counter() - t0 >= budget_s or calls >= 50:
             break
     dt = (time.perf_counter() - t0) / calls
+    t1 = time.perf_counter()
+    calls1 = 0
+    while True:
+        orc.forward(case["x_bits"], case["gamma"], case["beta"], w.G, w.eps, True, nthreads=1)
+        calls1 += 1
+        if time.perf_counter() - t1 >= budget_s / 4 or calls1 >= 20:
+            break
+    dt1 = (time.perf_counter() - t1) / calls1
     return {"value": 4.0 * w.elements / dt / 1e9, "unit": "GB/s", "cores": cores,
-            "kind": "oracle", "us_per_call": dt * 1e6,
+            "kind": "oracle", "us_per_call": dt * 1e6, "cpu_model": cpu_model(),
+            "one_thread": {"value": round(4.0 * w.elements / dt1 / 1e9, 4), "unit": "GB/s",
+                           "us_per_call": round(dt1 * 1e6, 1), "calls": calls1},
             "sample": f"{calls} full calls of the fp64 oracle on the {w.name} tensor "
                       f"({w.elements} elements), {cores} OpenMP threads"}
 
@@ -390,8 +419,14 @@ def sweep(variant_id, device, stream, peak, launch="graph"):
         us = statistics.median(r["per_step_ms"]) * 1e3
         gbs4 = 4.0 * w.elements / (us * 1e-6) / 1e9
         gbs6 = 6.0 * w.elements / (us * 1e-6) / 1e9
+        hot = None
+        if w.elements <= 1 << 25:
+            # the small shapes also with one buffer set: x and y stay in L2
+            rh = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24),
+                                  launch=launch, hot_l2=True)
+            hot = round(statistics.median(rh["per_step_ms"]) * 1e3, 2)
         out.append({"workload": w.name, "C": w.C, "variant": r["variant"],
-                    "us_per_call": round(us, 2),
+                    "us_per_call": round(us, 2), "us_per_call_hot_l2": hot,
                     "gbs_4B": round(gbs4, 1), "gbs_6B": round(gbs6, 1),
                     "frac_4B": round(gbs4 / peak, 3), "frac_6B": round(gbs6 / peak, 3),
                     "pages_h200_us": w.pages_us_h200,
