@@ -12,6 +12,12 @@ The arithmetic lives in ``gn_oracle.c`` (plain C, fp64, OpenMP over the
 affine, then SiLU if requested.  This module only compiles that file with
 gcc and marshals numpy arrays through ctypes.
 
+The package also holds the oracle of the residual-gate update
+``y = residual + gate * update`` in half precision (``rga_oracle.c``; the
+prhub digest of sglang PR #33823, FLUX.2 bit-exact residual-gate fusion),
+which writes out the two roundings of the eager evaluation; ``rga()``
+returns it.
+
 Parity pins: the oracle is checked against brute force on tiny tensors, a
 library special case (``torch.nn.functional.group_norm`` in float64), closed
 forms and invariants in ``tests/test_oracle_pins.py``; every exported
@@ -162,3 +168,73 @@ def forward(*a, **k):
 
 def apply_at(*a, **k):
     return get().apply_at(*a, **k)
+
+
+# ---------------------------------------------------------------------------
+# residual-gate update oracle (rga_oracle.c): y = residual + gate * update in
+# half precision with the two roundings of the eager evaluation
+# ---------------------------------------------------------------------------
+RGA_SOURCE = os.path.join(_HERE, "rga_oracle.c")
+RGA_LIB_PATH = os.path.join(BUILD_DIR, "librga_oracle.so")
+FMT = {"bf16": 0, "fp16": 1}
+_rga_default = None
+
+
+class RgaOracle:
+    """ctypes view of one compiled residual-gate oracle library."""
+
+    def __init__(self, lib_path: str):
+        self.lib = ctypes.CDLL(lib_path)
+        f = self.lib.rga_oracle_forward
+        f.restype = ctypes.c_int
+        f.argtypes = [_p, _p, _p, _p, _i64, _i64, ctypes.c_int]
+        f = self.lib.rga_oracle_at
+        f.restype = ctypes.c_int
+        f.argtypes = [_p, _p, _p, _i64, _i64, ctypes.c_int, _p, _i64, _p]
+
+    @staticmethod
+    def _bits(a):
+        return np.ascontiguousarray(a).view(np.uint16)
+
+    def forward(self, residual_bits, update_bits, gate_bits, fmt: str):
+        """uint16 [rows, D] output bits for uint16 [rows, D] residual / update
+        bits and a uint16 [D] gate row."""
+        r = self._bits(residual_bits)
+        u = self._bits(update_bits)
+        g = self._bits(gate_bits).reshape(-1)
+        rows, D = r.shape
+        if u.shape != (rows, D) or g.shape != (D,):
+            raise ValueError("residual/update must be [rows, D] and gate [D]")
+        out = np.empty((rows, D), np.uint16)
+        rc = self.lib.rga_oracle_forward(r.ctypes.data, u.ctypes.data, g.ctypes.data, out.ctypes.data,
+                                         rows, D, FMT[fmt])
+        if rc != 0:
+            raise ValueError(f"rga_oracle_forward rejected its arguments (rc={rc})")
+        return out
+
+    def at(self, residual_bits, update_bits, gate_bits, fmt: str, flat_index):
+        """Output bits at the given flat indices of the [rows, D] tensors."""
+        r = self._bits(residual_bits)
+        u = self._bits(update_bits)
+        g = self._bits(gate_bits).reshape(-1)
+        rows, D = r.shape
+        idx = np.ascontiguousarray(flat_index, np.int64)
+        out = np.empty(idx.shape, np.uint16)
+        rc = self.lib.rga_oracle_at(r.ctypes.data, u.ctypes.data, g.ctypes.data, rows, D, FMT[fmt],
+                                    idx.ctypes.data, idx.size, out.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"rga_oracle_at rejected its arguments (rc={rc})")
+        return out
+
+
+def build_rga(source: str = RGA_SOURCE, out: str = RGA_LIB_PATH, force: bool = False) -> str:
+    return build(source=source, out=out, force=force)
+
+
+def rga() -> RgaOracle:
+    """The residual-gate oracle built from ``rga_oracle.c``."""
+    global _rga_default
+    with _lock:
+        if _rga_default is None:
+            _rga_default = RgaOracle(build_rga())
+        return _rga_default
