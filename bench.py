@@ -435,6 +435,48 @@ def sweep(variant_id, device, stream, peak, launch="graph"):
     return out
 
 
+def measure_rga(w, fmt, steps, device, stream, peak):
+    """gn_residual_gate_add on one residual-gate workload: CUDA-graph
+    replay of `steps` calls over rotating buffer sets (together more than
+    twice L2), µs per call and GB/s at 6 B per element (residual and update
+    read, y written; the gate row is negligible)."""
+    import torch
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    from channels_last_groupnorm_gb300 import workloads as wl
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[fmt]
+    r0, u0, g0 = (t.to(dt).to(device) for t in wl.make_rga_inputs(w))
+    set_bytes = 6 * w.elements
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    nsets = buffer_sets_for(set_bytes, l2)
+    sets = [(r0.clone(), u0.clone(), torch.empty_like(r0)) for _ in range(nsets)]
+    h = stream.cuda_stream
+    code = {"bf16": 0, "fp16": 1}[fmt]
+
+    def call(i):
+        r, u, y = sets[i]
+        rc = gs.raw_gn_residual_gate_add(r.data_ptr(), u.data_ptr(), g0.data_ptr(), y.data_ptr(), w.rows, w.D,
+                                         code, stream=h)
+        if rc != 0:
+            raise RuntimeError(gs.status_string(rc))
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            call(i % nsets)
+        torch.cuda.synchronize()
+        graph = capture_steps(call, nsets, steps, stream)
+        graph.replay()
+        elapsed = time_graph(graph, stream)
+        del graph
+    us = elapsed * 1e6 / steps
+    gbs = 6.0 * w.elements / (us * 1e-6) / 1e9
+    del sets
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "format": fmt, "us_per_call": round(us, 2), "gbs_6B": round(gbs, 1),
+            "frac_6B": round(gbs / peak, 3), "pages_fused_us_h200": w.pages_us_h200,
+            "pages_eager_us_h200": w.pages_eager_us_h200,
+            "l2": f"{nsets} rotating buffer sets of {set_bytes >> 20} MiB", "launch": "cuda-graph"}
+
+
 def run_ours(args):
     import torch
     from channels_last_groupnorm_gb300 import build as gnbuild
@@ -514,6 +556,8 @@ def run_ours(args):
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0 and not args.no_sweep:
         line["sweep"] = sweep(variant_id, device, stream, peak, launch=args.launch)
+        line["residual_gate"] = [measure_rga(rw, fmt, 50, device, stream, peak)
+                                 for rw in wl.RGA_WORKLOADS for fmt in ("bf16", "fp16")]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

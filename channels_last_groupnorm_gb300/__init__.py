@@ -19,5 +19,6 @@ from .gnsilu import (  # noqa: F401
     gn_silu_rows_any,
     gn_silu_rows_ex,
     gn_silu_workspace_bytes,
+    residual_gate_add,
     status_string,
 )

@@ -1,6 +1,6 @@
 """Build ``libgnsilu.so`` in-tree with nvcc for sm_103a.
 
-Two translation units are compiled in parallel and linked into a shared
+The translation units are compiled in parallel and linked into a shared
 library next to this file (the CUDA runtime is linked statically).
 """
 from __future__ import annotations
@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libgnsilu.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_static.cu"]
+SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_static.cu", "rga_kernels.cu"]
 HEADERS = ["gn_internal.h", "gn_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -495,10 +495,45 @@ const char *gn_status_string(int status)
     case GN_ERR_DEVICE: return "GN_ERR_DEVICE: no CUDA device, or the device is not sm_103";
     case GN_ERR_VARIANT: return "GN_ERR_VARIANT: unknown variant, or it cannot be launched for this shape";
     case GN_ERR_KERNEL: return "GN_ERR_KERNEL: a kernel gave up a bounded wait";
+    case GN_ERR_FORMAT: return "GN_ERR_FORMAT: the half format is neither bf16 (0) nor fp16 (1)";
     default: return "unknown gn status";
     }
 }
 
-int gn_abi_version(void) { return 2; }
+int gn_residual_gate_add(const void *residual, const void *update, const void *gate, void *out, int64_t rows,
+                         int64_t D, int format, void *stream)
+{
+    if (!residual || !update || !gate || !out) return GN_ERR_NULL;
+    if (rows < 0) return GN_ERR_SHAPE;
+    if (D < 8 || D % 8 != 0) return GN_ERR_CHANNELS;
+    if (rows > 0 && rows > INT64_MAX / (2 * D)) return GN_ERR_SHAPE;
+    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(residual) % 16 || addr(update) % 16 || addr(gate) % 16 || addr(out) % 16) return GN_ERR_ALIGN;
+    if (format != GN_FORMAT_BF16 && format != GN_FORMAT_FP16) return GN_ERR_FORMAT;
+    const size_t bytes = static_cast<size_t>(rows) * static_cast<size_t>(2 * D);
+    const size_t gbytes = static_cast<size_t>(2 * D);
+    if (out != residual && ranges_overlap(out, bytes, residual, bytes)) return GN_ERR_ALIAS;
+    if (out != update && ranges_overlap(out, bytes, update, bytes)) return GN_ERR_ALIAS;
+    if (ranges_overlap(out, bytes, gate, gbytes)) return GN_ERR_ALIAS;
+    int dev = -1;
+    DeviceInfo d;
+    const int rc = current_device(&dev, &d);
+    if (rc != GN_OK) return rc;
+    if (rows == 0) return GN_OK;
+    // enough resident threads to keep HBM busy, but no more blocks than vectors need
+    const int64_t nvec = rows * (D / 8);
+    const int64_t want = (nvec + 4 * gn::kRgaThreads - 1) / (4 * gn::kRgaThreads);
+    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 8LL * d.sm_count)));
+    const cudaError_t e = gn::launch_residual_gate(residual, update, gate, out, rows, D, format == GN_FORMAT_BF16,
+                                                   blocks, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    g_launches.fetch_add(1);
+    return GN_OK;
+}
+
+int gn_abi_version(void) { return 3; }
 
 }  // extern "C"

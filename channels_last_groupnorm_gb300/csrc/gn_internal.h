@@ -112,6 +112,13 @@ inline uint32_t aux_smem_bytes(const Geom &g, int kind)
     return make_layout(t, kind).total + 16u * kMaxRing;
 }
 
+constexpr int kRgaThreads = 256;   // threads per block of the residual-gate kernel
+
+// Residual-gate update y = residual + gate * update (rga_kernels.cu):
+// rows x D half-precision elements (D a multiple of 8), bf16 or fp16.
+cudaError_t launch_residual_gate(const void *residual, const void *update, const void *gate, void *out,
+                                 int64_t rows, int64_t D, bool bf16, int blocks, cudaStream_t s);
+
 // Host-side launchers (gn_kernels.cu).  They return the first CUDA error.
 cudaError_t launch_pass1(const Args &a, int grid, cudaStream_t s);
 cudaError_t launch_finalize(const Args &a, cudaStream_t s);

@@ -36,13 +36,14 @@ GN_ERR_CUDA = 8
 GN_ERR_DEVICE = 9
 GN_ERR_VARIANT = 10
 GN_ERR_KERNEL = 11
+GN_ERR_FORMAT = 12
 
 VARIANT_AUTO = 0
 VARIANT_TWO_PASS = 1
 VARIANT_FUSED = 2
 
 # statuses that mean "this input is not supported" (the caller falls back)
-UNSUPPORTED = {GN_ERR_SHAPE, GN_ERR_CHANNELS, GN_ERR_ALIGN, GN_ERR_EPS, GN_ERR_ALIAS}
+UNSUPPORTED = {GN_ERR_SHAPE, GN_ERR_CHANNELS, GN_ERR_ALIGN, GN_ERR_EPS, GN_ERR_ALIAS, GN_ERR_FORMAT}
 
 EXPORTS = {
     # name: (restype, argtypes)
@@ -61,6 +62,8 @@ EXPORTS = {
     "gn_silu_rows_static": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4
                             + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                ctypes.c_void_p]),
+    "gn_residual_gate_add": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 2
+                             + [ctypes.c_int, ctypes.c_void_p]),
     "gn_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                 ctypes.c_int, ctypes.c_void_p]),
     "gn_silu_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4),
@@ -306,3 +309,54 @@ def _rows_with_stats(raw, what, x, gamma, beta, G, eps, apply_silu, out, variant
                  N, L, C, G, eps, apply_silu, mean.data_ptr(), rstd.data_ptr(),
                  ws_ptr, ws_bytes, variant, _stream_handle(x.device, stream))
     return (out, mean, rstd) if _finish(rc, what) else None
+
+
+# ---------------------------------------------------------------------------
+# residual-gate update (the prhub digest of sglang PR #33823, FLUX.2
+# bit-exact residual-gate fusion): residual + gate * update in half
+# precision, bit for bit equal to the eager two-kernel evaluation
+# ---------------------------------------------------------------------------
+FORMAT = {"bfloat16": 0, "float16": 1}
+
+
+def raw_gn_residual_gate_add(residual, update, gate, out, rows, D, fmt, stream=0) -> int:
+    return lib().gn_residual_gate_add(residual, update, gate, out, rows, D, int(fmt), stream or None)
+
+
+def residual_gate_add(residual, update, gate, out=None, stream=None):
+    """``residual + gate * update`` for contiguous bf16 / fp16 CUDA tensors
+    of the same shape [..., D] and a gate broadcast along every dimension
+    but the last (shape [D] or [1, ..., 1, D]).  Returns the result (``out``
+    if given; ``out`` may be ``residual`` or ``update``) or None when the
+    input is not supported (not CUDA, fp32 or another dtype -- whose eager
+    evaluation rounds differently --, a gate that varies along another
+    dimension, D not a multiple of 8, non-contiguous), so the caller can
+    fall back to the eager expression."""
+    lib()
+    torch = _torch()
+    ts = (residual, update, gate)
+    if not all(isinstance(t, torch.Tensor) and t.is_cuda for t in ts):
+        return None
+    dt = residual.dtype
+    if str(dt).replace("torch.", "") not in FORMAT or update.dtype != dt or gate.dtype != dt:
+        return None
+    if residual.shape != update.shape or residual.dim() < 1 or _grad_blocked(*ts):
+        return None
+    D = residual.shape[-1]
+    if gate.shape[-1] != D or gate.numel() != D:
+        return None
+    if not (residual.is_contiguous() and update.is_contiguous() and gate.is_contiguous()):
+        return None
+    if not (residual.device == update.device == gate.device):
+        return None
+    if out is None:
+        out = torch.empty_like(residual)
+    elif not (out.shape == residual.shape and out.dtype == dt and out.device == residual.device
+              and out.is_contiguous()):
+        return None
+    rows = residual.numel() // D if D else 0
+    with torch.cuda.device(residual.device):
+        rc = raw_gn_residual_gate_add(residual.data_ptr(), update.data_ptr(), gate.data_ptr(), out.data_ptr(),
+                                      rows, D, FORMAT[str(dt).replace("torch.", "")],
+                                      _stream_handle(residual.device, stream))
+    return out if _finish(rc, "gn_residual_gate_add") else None

@@ -188,3 +188,56 @@ def make_case(N: int, L: int, C: int, seed: int, *, mean: float = 0.0, std: floa
     beta = (rng.standard_normal(C, dtype=np.float32) * np.float32(0.1))
     return {"x_bits": x.reshape(N, L, C), "gamma": gamma, "beta": beta}
 
+
+
+# ---------------------------------------------------------------------------
+# residual-gate update y = residual + gate * update: the shapes the prhub
+# digest of sglang PR #33823 (FLUX.2 bit-exact residual-gate fusion) names,
+# (1, 512, 3072) with its H200 micro-benchmark times and the FLUX.2-dev
+# 1024^2 shape (1, 4608, 6144), plus the FLUX.2-klein (D = 3072) stream at
+# the same token count.  Values: residual ~ N(0, 2), update ~ N(0, 1), gate
+# ~ U(-0.5, 0.5), drawn in fp32 (the caller rounds them to bf16 / fp16).
+# Seeds: 5000 + index (residual), 6000 + index (update), 7000 + index (gate).
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class RgaWorkload:
+    name: str
+    index: int
+    B: int
+    S: int
+    D: int
+    pages_us_h200: float | None = None        # fused kernel on H200 (context)
+    pages_eager_us_h200: float | None = None  # the eager pair on H200 (context)
+    note: str = ""
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.S
+
+    @property
+    def elements(self) -> int:
+        return self.rows * self.D
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "shape": [self.B, self.S, self.D], "gate": [1, 1, self.D],
+                "residual": "N(0,2)", "update": "N(0,1)", "gate_values": "U(-0.5,0.5)"}
+
+
+RGA_WORKLOADS = [
+    RgaWorkload("rga_flux2_klein_512x3072", 0, 1, 512, 3072, pages_us_h200=13.0, pages_eager_us_h200=12.1,
+                note="the page's micro-benchmark shape"),
+    RgaWorkload("rga_flux2_dev_4608x6144", 1, 1, 4608, 6144, note="FLUX.2-dev 1024^2 (the page's test case)"),
+    RgaWorkload("rga_flux2_klein_4608x3072", 2, 1, 4608, 3072, note="FLUX.2-klein stream at 1024^2"),
+]
+
+RGA_BY_NAME = {w.name: w for w in RGA_WORKLOADS}
+
+
+def make_rga_inputs(w: RgaWorkload):
+    """(residual, update, gate) as float32 torch tensors, shapes [B, S, D],
+    [B, S, D] and [D]."""
+    import torch
+    res = np.random.default_rng(5000 + w.index).standard_normal((w.B, w.S, w.D), dtype=np.float32) * np.float32(2.0)
+    upd = np.random.default_rng(6000 + w.index).standard_normal((w.B, w.S, w.D), dtype=np.float32)
+    gate = np.random.default_rng(7000 + w.index).uniform(-0.5, 0.5, w.D).astype(np.float32)
+    return torch.from_numpy(res), torch.from_numpy(upd), torch.from_numpy(gate)

@@ -69,7 +69,14 @@ enum gn_status_code {
     GN_ERR_DEVICE = 9,     /* no CUDA device, or the current device is not sm_103 */
     GN_ERR_VARIANT = 10,   /* unknown variant, or the fused variant cannot be
                               launched cooperatively for this shape */
-    GN_ERR_KERNEL = 11     /* gn_device_status(): a kernel gave up a bounded wait */
+    GN_ERR_KERNEL = 11,    /* gn_device_status(): a kernel gave up a bounded wait */
+    GN_ERR_FORMAT = 12     /* gn_residual_gate_add(): unknown half format */
+};
+
+/* Element formats of gn_residual_gate_add(). */
+enum gn_half_format {
+    GN_FORMAT_BF16 = 0,
+    GN_FORMAT_FP16 = 1
 };
 
 /* Kernel schedules selectable through gn_silu_rows_ex(). */
@@ -220,11 +227,40 @@ int gn_silu_rows_static(const void *x_bf16, const float *gamma, const float *bet
                         float eps, int apply_silu,
                         float *mean_out, float *rstd_out, void *stream);
 
+/*
+ * Residual-gate update of a transformer's residual stream (the prhub digest
+ * of sglang PR #33823, FLUX.2 bit-exact residual-gate fusion, sections
+ * "Functions and motivation" and "Implementation breakdown", items 1-3):
+ *
+ *     out[r, d] = residual[r, d] + gate[d] * update[r, d]
+ *
+ * in half precision, bit for bit equal to the eager two-kernel evaluation
+ * (the product rounded to the half format, then the sum rounded to it;
+ * round to nearest even, no fused multiply-add).  NaN results may carry any
+ * NaN payload.
+ *   residual, update, out : DEVICE [rows][D] bf16 or fp16 bit patterns
+ *                           (format: enum gn_half_format), contiguous,
+ *                           16-byte aligned.
+ *   gate                  : DEVICE [D] of the same format, 16-byte aligned:
+ *                           one row broadcast over all rows (a [1, ..., 1, D]
+ *                           modulation vector; per-batch gates are not
+ *                           taken, as on the page).
+ *   rows >= 0 (0: nothing to do), D a multiple of 8 (whole 16-byte vectors).
+ * out may equal residual or update exactly (in place) but must not overlap
+ * them otherwise, nor overlap gate.  Asynchronous on `stream`, like the
+ * other entry points; the caller owns every buffer.  Errors: GN_ERR_NULL,
+ * GN_ERR_SHAPE (rows < 0 or the element count overflows), GN_ERR_CHANNELS
+ * (D < 8 or not a multiple of 8), GN_ERR_ALIGN, GN_ERR_ALIAS, GN_ERR_FORMAT,
+ * GN_ERR_DEVICE, GN_ERR_CUDA.
+ */
+int gn_residual_gate_add(const void *residual, const void *update, const void *gate, void *out,
+                         int64_t rows, int64_t D, int format, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gn_status_string(int status);
 
-/* ABI version of this header: 2 (1 lacked gn_silu_rows_any and
- * gn_silu_ndhwc). */
+/* ABI version of this header: 3 (2 lacked gn_residual_gate_add; 1 also
+ * gn_silu_rows_any and gn_silu_ndhwc). */
 int gn_abi_version(void);
 
 #ifdef __cplusplus

@@ -45,8 +45,8 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert gs.gn_abi_version() == 2
-    for code in range(12):
+    assert gs.gn_abi_version() == 3
+    for code in range(13):
         s = gs.status_string(code)
         assert s.startswith("GN_"), (code, s)
     assert "unknown" in gs.status_string(99)
@@ -202,3 +202,46 @@ def test_general_tensor_bindings_return_none_for_cpu_tensors():
     g = torch.ones(320)
     assert gs.gn_silu_ndhwc(x, g, g) is None
     assert gs.gn_silu_rows_any(torch.zeros(1, 8, 320, dtype=torch.bfloat16), g, g) is None
+
+
+def rga(**kw):
+    a = dict(residual=X, update=Y, gate=GAM, out=0x40000000, rows=4, D=64, fmt=0)
+    a.update(kw)
+    return gs.raw_gn_residual_gate_add(a["residual"], a["update"], a["gate"], a["out"], a["rows"], a["D"],
+                                       a["fmt"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(residual=0), gs.GN_ERR_NULL),
+    (dict(update=0), gs.GN_ERR_NULL),
+    (dict(gate=0), gs.GN_ERR_NULL),
+    (dict(out=0), gs.GN_ERR_NULL),
+    (dict(rows=-1), gs.GN_ERR_SHAPE),
+    (dict(rows=1 << 60, D=1 << 20), gs.GN_ERR_SHAPE),
+    (dict(D=0), gs.GN_ERR_CHANNELS),
+    (dict(D=4), gs.GN_ERR_CHANNELS),
+    (dict(D=12), gs.GN_ERR_CHANNELS),
+    (dict(residual=X + 2), gs.GN_ERR_ALIGN),
+    (dict(gate=GAM + 8), gs.GN_ERR_ALIGN),
+    (dict(out=0x40000008), gs.GN_ERR_ALIGN),
+    (dict(fmt=2), gs.GN_ERR_FORMAT),
+    (dict(fmt=-1), gs.GN_ERR_FORMAT),
+    (dict(out=X + 16), gs.GN_ERR_ALIAS),
+    (dict(out=Y - 16), gs.GN_ERR_ALIAS),
+    (dict(out=GAM - 64), gs.GN_ERR_ALIAS),
+])
+def test_residual_gate_rejects(kw, code):
+    assert rga(**kw) == code
+
+
+@no_gpu
+def test_residual_gate_valid_arguments_without_a_device():
+    assert rga() == gs.GN_ERR_DEVICE
+    assert rga(out=X) == gs.GN_ERR_DEVICE          # in place on the residual
+    assert rga(out=Y, fmt=1) == gs.GN_ERR_DEVICE   # in place on the update, fp16
+    assert rga(rows=0) == gs.GN_ERR_DEVICE
+
+
+def test_residual_gate_binding_returns_none_for_cpu_tensors():
+    r = torch.zeros(2, 16, dtype=torch.bfloat16)
+    assert gs.residual_gate_add(r, r.clone(), torch.ones(16, dtype=torch.bfloat16)) is None
