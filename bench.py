@@ -493,6 +493,9 @@ def run_ours(args):
         gnbuild.build()
     barrier()
     gs.lib()
+    if args.workload in wl.RGA_BY_NAME:
+        run_rga(args, wl.RGA_BY_NAME[args.workload], device, rank, world)
+        return
     w = wl.BY_NAME[args.workload]
     variant_id = {"auto": 0, "two_pass": 1, "fused": 2}[args.variant]
     stream = torch.cuda.Stream(device)
@@ -563,6 +566,25 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_rga(args, w, device, rank, world):
+    """One residual-gate workload (bf16) on its own: the line reports its
+    bandwidth at 6 B/element; used for its profiles."""
+    import torch
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = hbm_peak()
+    r = measure_rga(w, "bf16", args.steps, device, stream, peak)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "residual + gate*update bf16 us/call and HBM GB/s (6 B/elem)", "value": r["gbs_6B"],
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "us_per_call": r["us_per_call"], "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": w.describe(),
+            "roofline": {"bound": "hbm", "achieved": r["gbs_6B"], "peak": peak, "unit": "GB/s",
+                         "frac": r["frac_6B"], "peak_kind": peak_kind, "traffic": None,
+                         "kernel": "rga_kernel", "algorithmic_bytes_per_launch": 6.0 * w.elements},
+        }), flush=True)
 
 
 # ---------------------------------------------------------------------------
