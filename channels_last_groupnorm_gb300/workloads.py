@@ -241,3 +241,73 @@ def make_rga_inputs(w: RgaWorkload):
     upd = np.random.default_rng(6000 + w.index).standard_normal((w.B, w.S, w.D), dtype=np.float32)
     gate = np.random.default_rng(7000 + w.index).uniform(-0.5, 0.5, w.D).astype(np.float32)
     return torch.from_numpy(res), torch.from_numpy(upd), torch.from_numpy(gate)
+
+
+# ---------------------------------------------------------------------------
+# Fused nearest-2x upsample + 3x3 conv (the decoder's up-sampler).  The pages
+# name the fusion (sglang PR #33451, "FLUX.2 VAE decoder fast path behind
+# quality=high", section "Modifications", item 2) but print no shapes; these
+# are the up-samplers of the FLUX.2 VAE decoder (block widths 512, 512, 256)
+# for a 1024^2 decode from a 128^2 latent, plus small shapes for exhaustive
+# checks.  Values: x ~ N(0, 1) (a resnet-block output), weight and bias ~
+# U(-b, b) with b = 1/sqrt(9 Cin) (PyTorch's default Conv2d initialisation),
+# drawn in fp32 and rounded to bf16.
+# Seeds: 8000 + index (x), 9000 + index (weight), 9500 + index (bias).
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class UpconvWorkload:
+    name: str
+    index: int
+    N: int
+    H: int          # input height (the output is 2H x 2W)
+    W: int
+    Cin: int
+    Cout: int
+    bias: bool = True
+    note: str = ""
+
+    @property
+    def out_pixels(self) -> int:
+        return self.N * 4 * self.H * self.W
+
+    @property
+    def flops(self) -> int:
+        """Multiply-adds x 2 of the folded evaluation: 4 taps per output."""
+        return 2 * self.out_pixels * self.Cout * 4 * self.Cin
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "x": [self.N, self.H, self.W, self.Cin],
+                "y": [self.N, 2 * self.H, 2 * self.W, self.Cout], "bias": self.bias,
+                "x_values": "N(0,1)", "weight_values": "U(-1/sqrt(9Cin), 1/sqrt(9Cin))"}
+
+
+UPCONV_WORKLOADS = [
+    UpconvWorkload("upconv_c64_co128_16x16", 0, 1, 16, 16, 64, 128, note="small, full oracle"),
+    UpconvWorkload("upconv_c512_128x128", 1, 1, 128, 128, 512, 512,
+                   note="FLUX.2 decoder up-block 0 at 1024^2 (128^2 -> 256^2)"),
+    UpconvWorkload("upconv_c512_256x256", 2, 1, 256, 256, 512, 512,
+                   note="FLUX.2 decoder up-block 1 at 1024^2 (256^2 -> 512^2)"),
+    UpconvWorkload("upconv_c256_512x512", 3, 1, 512, 512, 256, 256,
+                   note="FLUX.2 decoder up-block 2 at 1024^2 (512^2 -> 1024^2)"),
+]
+
+UPCONV_BY_NAME = {w.name: w for w in UPCONV_WORKLOADS}
+
+
+def make_upconv_case(N: int, H: int, W: int, Cin: int, Cout: int, index: int,
+                     bias: bool = True) -> dict:
+    """bf16 bit patterns: x [N, H, W, Cin], weight [Cout, Cin, 3, 3] and
+    bias [Cout] (None without bias)."""
+    b = 1.0 / np.sqrt(9.0 * Cin)
+    x = np.random.default_rng(8000 + index).standard_normal((N, H, W, Cin), dtype=np.float32)
+    w = np.random.default_rng(9000 + index).uniform(-b, b, (Cout, Cin, 3, 3)).astype(np.float32)
+    out = {"x_bits": f32_to_bf16_bits(x).reshape(N, H, W, Cin),
+           "w_bits": f32_to_bf16_bits(w).reshape(Cout, Cin, 3, 3), "bias_bits": None}
+    if bias:
+        bb = np.random.default_rng(9500 + index).uniform(-b, b, Cout).astype(np.float32)
+        out["bias_bits"] = f32_to_bf16_bits(bb)
+    return out
+
+
+def make_upconv_inputs(w: UpconvWorkload) -> dict:
+    return make_upconv_case(w.N, w.H, w.W, w.Cin, w.Cout, w.index, w.bias)

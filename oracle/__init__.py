@@ -16,7 +16,10 @@ The package also holds the oracle of the residual-gate update
 ``y = residual + gate * update`` in half precision (``rga_oracle.c``; the
 prhub digest of sglang PR #33823, FLUX.2 bit-exact residual-gate fusion),
 which writes out the two roundings of the eager evaluation; ``rga()``
-returns it.
+returns it.  ``upconv()`` returns the oracle of the decoder's fused
+nearest-2x upsample + 3x3 convolution (``upconv_oracle.c``; the sglang PR
+#33451 page, section "Modifications", item 2), which evaluates the upsample
+and the convolution as defined, in fp64.
 
 Parity pins: the oracle is checked against brute force on tiny tensors, a
 library special case (``torch.nn.functional.group_norm`` in float64), closed
@@ -238,3 +241,83 @@ def rga() -> RgaOracle:
         if _rga_default is None:
             _rga_default = RgaOracle(build_rga())
         return _rga_default
+
+
+# ---------------------------------------------------------------------------
+# fused nearest-2x upsample + 3x3 conv oracle (upconv_oracle.c): the two
+# steps written out as defined, fp64, unrounded output
+# ---------------------------------------------------------------------------
+UPCONV_SOURCE = os.path.join(_HERE, "upconv_oracle.c")
+UPCONV_LIB_PATH = os.path.join(BUILD_DIR, "libupconv_oracle.so")
+_upconv_default = None
+
+
+class UpconvOracle:
+    """ctypes view of one compiled upsample+conv oracle library."""
+
+    def __init__(self, lib_path: str):
+        self.lib = ctypes.CDLL(lib_path)
+        f = self.lib.upconv_oracle_forward
+        f.restype = ctypes.c_int
+        f.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _p, _p]
+        f = self.lib.upconv_oracle_at
+        f.restype = ctypes.c_int
+        f.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _p, _i64, _p, _p]
+
+    @staticmethod
+    def _args(x_bits, w_bits, bias_bits):
+        x = np.ascontiguousarray(x_bits).view(np.uint16)
+        w = np.ascontiguousarray(w_bits).view(np.uint16)
+        if x.ndim != 4 or w.ndim != 4 or w.shape[2:] != (3, 3) or w.shape[1] != x.shape[3]:
+            raise ValueError("x must be [N, H, W, Cin] and w [Cout, Cin, 3, 3] bf16 bits")
+        b = None
+        if bias_bits is not None:
+            b = np.ascontiguousarray(bias_bits).view(np.uint16).reshape(-1)
+            if b.shape != (w.shape[0],):
+                raise ValueError("bias must be [Cout] bf16 bits")
+        return x, w, b
+
+    def forward(self, x_bits, w_bits, bias_bits=None, with_abs: bool = False):
+        """y float64 [N, 2H, 2W, Cout] (and the absolute-term sums if asked)."""
+        x, w, b = self._args(x_bits, w_bits, bias_bits)
+        N, H, W, Cin = x.shape
+        Cout = w.shape[0]
+        y = np.empty((N, 2 * H, 2 * W, Cout), np.float64)
+        a = np.empty_like(y) if with_abs else None
+        rc = self.lib.upconv_oracle_forward(x.ctypes.data, w.ctypes.data,
+                                            None if b is None else b.ctypes.data,
+                                            N, H, W, Cin, Cout, y.ctypes.data,
+                                            None if a is None else a.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"upconv_oracle_forward rejected its arguments (rc={rc})")
+        return (y, a) if with_abs else y
+
+    def at(self, x_bits, w_bits, bias_bits, flat_index, with_abs: bool = False):
+        """y (and the absolute-term sums) at flat indices of [N, 2H, 2W, Cout]."""
+        x, w, b = self._args(x_bits, w_bits, bias_bits)
+        N, H, W, Cin = x.shape
+        Cout = w.shape[0]
+        idx = np.ascontiguousarray(flat_index, np.int64)
+        y = np.empty(idx.shape, np.float64)
+        a = np.empty_like(y) if with_abs else None
+        rc = self.lib.upconv_oracle_at(x.ctypes.data, w.ctypes.data,
+                                       None if b is None else b.ctypes.data,
+                                       N, H, W, Cin, Cout, idx.ctypes.data, idx.size,
+                                       y.ctypes.data, None if a is None else a.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"upconv_oracle_at rejected its arguments (rc={rc})")
+        return (y, a) if with_abs else y
+
+
+def build_upconv(source: str = UPCONV_SOURCE, out: str = UPCONV_LIB_PATH,
+                 force: bool = False) -> str:
+    return build(source=source, out=out, force=force)
+
+
+def upconv() -> UpconvOracle:
+    """The upsample+conv oracle built from ``upconv_oracle.c``."""
+    global _upconv_default
+    with _lock:
+        if _upconv_default is None:
+            _upconv_default = UpconvOracle(build_upconv())
+        return _upconv_default

@@ -78,3 +78,18 @@ def test_general_workloads_draw_whole_rows_deterministically():
     assert np.array_equal(a["x_bits"], b["x_bits"])
     assert {x.name for x in wl.GENERAL_WORKLOADS} <= set(wl.BY_NAME)
     assert all(x.general or x.D > 1 for x in wl.GENERAL_WORKLOADS)
+
+
+def test_upconv_inputs_are_seeded_and_scaled():
+    a = wl.make_upconv_case(1, 8, 4, 64, 128, 3)
+    b = wl.make_upconv_case(1, 8, 4, 64, 128, 3)
+    for k in ("x_bits", "w_bits", "bias_bits"):
+        assert np.array_equal(a[k], b[k]), k
+    assert a["x_bits"].shape == (1, 8, 4, 64) and a["w_bits"].shape == (128, 64, 3, 3)
+    bound = 1.0 / np.sqrt(9 * 64)
+    w = wl.bf16_bits_to_f32(a["w_bits"])
+    assert np.abs(w).max() <= bound * (1 + 2 ** -8) and np.abs(w).max() > 0.9 * bound
+    assert wl.make_upconv_case(1, 2, 2, 64, 128, 3, bias=False)["bias_bits"] is None
+    big = wl.UPCONV_BY_NAME["upconv_c512_256x256"]
+    assert (big.N, big.H, big.W, big.Cin, big.Cout) == (1, 256, 256, 512, 512)
+    assert big.flops == 2 * 512 * 512 * 512 * 4 * 512
