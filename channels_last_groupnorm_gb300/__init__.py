@@ -21,4 +21,6 @@ from .gnsilu import (  # noqa: F401
     gn_silu_workspace_bytes,
     residual_gate_add,
     status_string,
+    upconv_fold,
+    upsample_conv_nhwc,
 )

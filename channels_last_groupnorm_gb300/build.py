@@ -14,8 +14,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libgnsilu.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_static.cu", "rga_kernels.cu"]
-HEADERS = ["gn_internal.h", "gn_ptx.cuh"]
+SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_static.cu", "rga_kernels.cu", "upconv_kernels.cu"]
+HEADERS = ["gn_internal.h", "gn_ptx.cuh", "tc_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

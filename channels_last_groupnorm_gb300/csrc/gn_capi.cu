@@ -446,10 +446,13 @@ int gn_device_status(int clear)
         return GN_ERR_DEVICE;
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return GN_ERR_CUDA;
-    unsigned int st = 0;
+    unsigned int st = 0, st_uc = 0;
     if (gn::read_device_status(&st) != cudaSuccess) return GN_ERR_CUDA;
+    if (gn::read_upconv_status(&st_uc) != cudaSuccess) return GN_ERR_CUDA;
+    st |= st_uc;
     if (clear) {
         if (gn::clear_device_status() != cudaSuccess) return GN_ERR_CUDA;
+        if (gn::clear_upconv_status() != cudaSuccess) return GN_ERR_CUDA;
         std::lock_guard<std::mutex> lock(g_mu);
         for (auto &kv : g_workspaces) {
             if (kv.first.first == dev && kv.second.ptr && cudaMemset(kv.second.ptr, 0, 256) != cudaSuccess)
@@ -534,6 +537,79 @@ int gn_residual_gate_add(const void *residual, const void *update, const void *g
     return GN_OK;
 }
 
-int gn_abi_version(void) { return 3; }
+// ---- fused nearest-2x upsample + 3x3 convolution ----------------------------
+int64_t gn_upconv_folded_bytes(int64_t Cin, int64_t Cout)
+{
+    if (Cin < 1 || Cout < 1 || Cin > (1 << 20) || Cout > (1 << 20)) return -1;
+    return 16 * Cin * Cout * 2;
+}
+
+namespace {
+
+int upconv_channels_ok(int64_t Cin, int64_t Cout)
+{
+    return Cin >= 64 && Cin <= 8192 && Cin % 64 == 0 && Cout >= 128 && Cout <= 8192 && Cout % 128 == 0;
+}
+
+}  // namespace
+
+int gn_upconv_fold(const void *w, void *wf, int64_t Cin, int64_t Cout, void *stream)
+{
+    if (!w || !wf) return GN_ERR_NULL;
+    if (!upconv_channels_ok(Cin, Cout)) return GN_ERR_CHANNELS;
+    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(w) % 2 || addr(wf) % 16) return GN_ERR_ALIGN;
+    if (ranges_overlap(w, static_cast<size_t>(9 * Cin * Cout * 2), wf,
+                       static_cast<size_t>(gn_upconv_folded_bytes(Cin, Cout))))
+        return GN_ERR_ALIAS;
+    int dev = -1;
+    DeviceInfo d;
+    const int rc = current_device(&dev, &d);
+    if (rc != GN_OK) return rc;
+    const cudaError_t e = gn::launch_upconv_fold(w, wf, static_cast<int>(Cin), static_cast<int>(Cout), d.sm_count,
+                                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    g_launches.fetch_add(1);
+    return GN_OK;
+}
+
+int gn_upconv_nhwc(const void *x, const void *wf, const void *bias, void *y, int64_t N, int64_t H, int64_t W,
+                   int64_t Cin, int64_t Cout, void *stream)
+{
+    if (!x || !wf || !y) return GN_ERR_NULL;
+    if (N < 0 || H < 1 || W < 1 || H > (1 << 20) || W > (1 << 20)) return GN_ERR_SHAPE;
+    if (!upconv_channels_ok(Cin, Cout)) return GN_ERR_CHANNELS;
+    if (N > 0 && (N > (1 << 20) || N * H * W > INT64_MAX / (4 * 2 * std::max(Cin, Cout)))) return GN_ERR_SHAPE;
+    gn::UpconvTiling t;
+    if (N > 0 && !gn::upconv_tiling(N, H, W, &t)) return GN_ERR_SHAPE;
+    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(x) % 16 || addr(wf) % 16 || addr(y) % 16 || (bias && addr(bias) % 4)) return GN_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(N * H * W * Cin * 2);
+    const size_t yb = static_cast<size_t>(N * 4 * H * W * Cout * 2);
+    if (ranges_overlap(y, yb, x, xb) || ranges_overlap(y, yb, wf, static_cast<size_t>(gn_upconv_folded_bytes(Cin, Cout))) ||
+        (bias && ranges_overlap(y, yb, bias, static_cast<size_t>(2 * Cout))))
+        return GN_ERR_ALIAS;
+    int dev = -1;
+    DeviceInfo d;
+    const int rc = current_device(&dev, &d);
+    if (rc != GN_OK) return rc;
+    if (N == 0) return GN_OK;
+    cudaError_t e = cudaSuccess;
+    const int r = gn::launch_upconv(x, wf, bias, y, static_cast<int>(N), static_cast<int>(H), static_cast<int>(W),
+                                    static_cast<int>(Cin), static_cast<int>(Cout), wait_timeout_ns(),
+                                    static_cast<cudaStream_t>(stream), &e);
+    if (r == 1) return GN_ERR_SHAPE;
+    if (r != 0) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    g_launches.fetch_add(1);
+    return GN_OK;
+}
+
+int gn_abi_version(void) { return 4; }
 
 }  // extern "C"

@@ -131,4 +131,22 @@ cudaError_t launch_selftest_wait(int mode, uint64_t timeout_ns, int *done, int b
 cudaError_t read_device_status(unsigned int *status);
 cudaError_t clear_device_status();
 
+// ---- fused nearest-2x upsample + 3x3 convolution (upconv_kernels.cu) ----
+// The pixel box of one 128-pixel output tile of one parity: BW columns x BH
+// rows x BNI images, and the tile counts along each axis.
+struct UpconvTiling {
+    int BW, BH, BNI;
+    int tiles_w, tiles_h, tiles_n;
+};
+// false when (H, W) admits no such tiling: W a multiple of 128, or W a power
+// of two below 128 with H a multiple of 128 / W or a power of two below it.
+bool upconv_tiling(int64_t N, int64_t H, int64_t W, UpconvTiling *t);
+cudaError_t launch_upconv_fold(const void *w, void *wf, int Cin, int Cout, int sm_count, cudaStream_t s);
+// 0 = launched; 1 = shape not tileable; 2 = tensor-map encoding failed;
+// 3 = the launch failed (*err holds the CUDA error).
+int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int N, int H, int W, int Cin,
+                  int Cout, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err);
+cudaError_t read_upconv_status(unsigned int *status);
+cudaError_t clear_upconv_status();
+
 }  // namespace gn

@@ -1,0 +1,461 @@
+// upconv_kernels.cu -- the decoder's up-sampler, nearest-2x upsample fused
+// with the following 3x3 convolution (padding 1), on the sm_103a tensor
+// cores (tcgen05.mma, accumulators in tensor memory, operands staged by TMA).
+//
+// Operation (sglang PR #33451, "FLUX.2 VAE decoder fast path behind
+// quality=high", section "Modifications", item 2): with x channels-last
+// [N][H][W][Cin] and the convolution weight w [Cout][Cin][3][3],
+//   y[n][P][Q][co] = bias[co] + sum_{ky,kx} sum_ci u[n][P+ky-1][Q+kx-1][ci] w[co][ci][ky][kx],
+//   u[n][p][q] = x[n][p/2][q/2] inside the 2H x 2W image, 0 outside.
+// Nearest upsampling copies each input pixel into a 2x2 block, so an output
+// pixel P = 2i + a, Q = 2j + b (parity (a, b)) reads only the 2x2 input
+// window rows i + a - 1 + r, columns j + b - 1 + s (r, s in {0, 1}), and each
+// window tap carries the sum of the 3x3 taps whose upsampled pixel falls on
+// it: kernel row ky belongs to window row r exactly when
+// floor((a + ky - 1) / 2) = r + a - 1, and likewise for columns.  These are
+// the summed taps of the equivalent transposed convolution (kernel 4,
+// stride 2, padding 1) that the page describes.  Per parity the convolution
+// is then a GEMM with K = 4 Cin:
+//   Y_ab[pixel, co] = sum_{r,s,ci} x[n][i+a-1+r][j+b-1+s][ci] * Wf_ab[co][r][s][ci].
+//
+// upconv_fold_kernel computes Wf (fp32 sums of bf16 taps, rounded once to
+// bf16) into [4 parities][Cout][4 taps][Cin].  upconv_kernel computes one
+// 128-pixel x BN-channel output tile of one parity per CTA:
+//   warp 0 (one thread)  TMA producer: per K step of 64 input channels of one
+//                        tap, a 4-D box {64 ch, BW, BH, BNI} of x at the
+//                        tap's shifted coordinates (out-of-image rows and
+//                        columns are zero-filled by the copy engine, which is
+//                        the convolution's padding) and the matching
+//                        {64, BN} box of Wf, into a STAGES-deep ring;
+//   warp 1               allocates BN tensor-memory columns; one thread
+//                        issues four tcgen05.mma (M=128, N=BN, K=16) per K
+//                        step and commits each ring slot back to the producer;
+//   warps 2-5            epilogue: tcgen05.ld of the fp32 accumulator (one
+//                        pixel per thread), + bias, round to bf16, store to
+//                        y at (2i + a, 2j + b).
+// Every wait is bounded (a timeout sets a device status word and the CTA
+// drains its copies and frees its tensor memory before it returns).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "gn_internal.h"
+#include "gn_ptx.cuh"
+#include "tc_ptx.cuh"
+
+namespace gn {
+
+__device__ unsigned int g_uc_status;
+
+namespace {
+
+constexpr int kBM = 128;                                // output pixels per tile (MMA M)
+constexpr int kBK = 64;                                 // input channels per K step
+constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KB
+constexpr int kUcThreads = 192;
+constexpr uint32_t kSleepNs = 20000;
+
+struct UcArgs {
+    int N, H, W, Cin, Cout;
+    int BW, BH, BNI;            // the pixel box of one tile: BW x BH x BNI = 128
+    int tiles_w, tiles_h;
+    int co_tiles, chunks, ksteps;
+    const __nv_bfloat16 *bias;  // [Cout] or null
+    __nv_bfloat16 *y;
+    uint64_t timeout_ns;
+};
+
+template <int BN, int STAGES>
+struct UcLayout {
+    static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * kBK * 2;
+    static constexpr uint32_t kStage = kABytes + kBBytes;
+    static constexpr uint32_t kRing = kStage * STAGES;
+    // after the ring: full[STAGES], empty[STAGES], acc (8 B each), tmem slot, abort flag
+    static constexpr uint32_t kBars = kRing;
+    static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 1);
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kConsumed = kAbort + 4;
+    static constexpr uint32_t kBytes = kConsumed + 4;
+    static constexpr uint32_t kDynamic = kBytes + 1024;  // slack to align the ring to 1024 B
+};
+
+__device__ __forceinline__ bool uc_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    const uint64_t deadline = global_ns() + timeout_ns;
+#pragma unroll 1
+    for (;;) {
+        if (mbar_wait_sleep(bar, parity, kSleepNs)) return true;
+        if (*abort) return false;
+        if (global_ns() > deadline) {
+            *abort = 1;
+            atomicOr(&g_uc_status, 1u);
+            return false;
+        }
+    }
+}
+
+// A wait during teardown after an abort: bounded, but not cut short by the
+// abort flag (the copies and MMAs it waits for are still in flight).
+__device__ __forceinline__ void uc_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t deadline = global_ns() + timeout_ns;
+#pragma unroll 1
+    while (!mbar_wait_sleep(bar, parity, kSleepNs)) {
+        if (global_ns() > deadline) return;
+    }
+}
+
+__device__ __forceinline__ int floor_half(int v) { return (v + 2) / 2 - 1; }   // floor(v / 2) for v >= -2
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Wf[p][co][t][ci], p = 2a + b, t = 2r + s: the sum of w[co][ci][ky][kx] over
+// the 3x3 taps that land on window tap (r, s) of parity (a, b).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) upconv_fold_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                          __nv_bfloat16 *__restrict__ wf, int Cin, int Cout)
+{
+    const int64_t total = 16LL * Cout * Cin;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int ci = static_cast<int>(idx % Cin);
+        int64_t t = idx / Cin;
+        const int tap = static_cast<int>(t % 4);
+        t /= 4;
+        const int co = static_cast<int>(t % Cout);
+        const int p = static_cast<int>(t / Cout);
+        const int a = p >> 1, b = p & 1, r = tap >> 1, s = tap & 1;
+        const __nv_bfloat16 *src = w + (static_cast<int64_t>(co) * Cin + ci) * 9;
+        float acc = 0.f;
+        for (int ky = 0; ky < 3; ++ky) {
+            if (floor_half(a + ky - 1) != r + a - 1) continue;
+            for (int kx = 0; kx < 3; ++kx) {
+                if (floor_half(b + kx - 1) != s + b - 1) continue;
+                acc += __bfloat162float(src[ky * 3 + kx]);
+            }
+        }
+        wf[idx] = __float2bfloat16_rn(acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the implicit-GEMM convolution, one output tile per CTA
+// ---------------------------------------------------------------------------
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kUcThreads, 1)
+    upconv_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                  const UcArgs args)
+{
+    using L = UcLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t bar_full = base + L::kBars;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_acc = bar_empty + 8 * STAGES;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + L::kTmemSlot);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + L::kAbort);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // tile coordinates: Cout tile fastest, then parity, then the pixel tile
+    int rest = blockIdx.x;
+    const int co_t = rest % args.co_tiles;
+    rest /= args.co_tiles;
+    const int parity = rest & 3;
+    rest >>= 2;
+    const int tw = rest % args.tiles_w;
+    rest /= args.tiles_w;
+    const int th = rest % args.tiles_h;
+    const int tn = rest / args.tiles_h;
+    const int pa = parity >> 1, pb = parity & 1;
+    const int i0 = th * args.BH, j0 = tw * args.BW, n0 = tn * args.BNI, co0 = co_t * BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_acc, 1);
+        *abort = (*reinterpret_cast<volatile unsigned int *>(&g_uc_status) != 0u) ? 1 : 0;
+        mbar_init_fence();
+        prefetch_tensormap(&map_x);
+        prefetch_tensormap(&map_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(base + L::kTmemSlot, BN);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort != 0;
+
+    int issued = 0;       // producer: K steps whose loads were issued
+    int consumed = 0;     // MMA thread: K steps whose loads were consumed
+    if (!skip && warp == 0 && lane == 0) {
+        // ---- producer ----
+        for (int kt = 0; kt < args.ksteps; ++kt) {
+            const int s = kt % STAGES;
+            if (kt >= STAGES && !uc_wait(bar_empty + 8 * s, ((kt / STAGES) - 1) & 1, abort, args.timeout_ns)) break;
+            const int tap = kt / args.chunks;
+            const int c0 = (kt - tap * args.chunks) * kBK;
+            const int r = tap >> 1, sx = tap & 1;
+            const uint32_t sa = base + s * L::kStage;
+            mbar_arrive_expect_tx(bar_full + 8 * s, L::kStage);
+            tma_load_4d(sa, &map_x, c0, j0 + sx + pb - 1, i0 + r + pa - 1, n0, bar_full + 8 * s);
+            tma_load_2d(sa + kABytes, &map_w, kt * kBK, parity * args.Cout + co0, bar_full + 8 * s);
+            issued = kt + 1;
+        }
+    } else if (!skip && warp == 1 && lane == 0) {
+        // ---- MMA issue ----
+        constexpr uint32_t idesc = umma_idesc_bf16_f32(kBM, BN);
+        for (int kt = 0; kt < args.ksteps; ++kt) {
+            const int s = kt % STAGES;
+            if (!uc_wait(bar_full + 8 * s, (kt / STAGES) & 1, abort, args.timeout_ns)) break;
+            tc_fence_after_sync();
+            const uint32_t sa = base + s * L::kStage;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                umma_f16(tmem, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sa + kABytes + kk * 32), idesc,
+                         (kt > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(bar_empty + 8 * s);
+            consumed = kt + 1;
+        }
+        umma_commit(bar_acc);   // arrives once every MMA above has completed
+    } else if (warp >= 2) {
+        // ---- epilogue: thread <-> tile pixel (TMEM lane) ----
+        const int quad = warp & 3;
+        const int m = quad * 32 + lane;
+        const bool done = !skip && uc_wait(bar_acc, 0, abort, args.timeout_ns);
+        tc_fence_after_sync();
+        // warp-uniform, as the tensor-memory loads below are warp-collective
+        if (__all_sync(0xffffffffu, done && !*abort)) {
+            const int wi = m % args.BW;
+            const int hi = (m / args.BW) % args.BH;
+            const int n = n0 + m / (args.BW * args.BH);
+            const bool valid = n < args.N;
+            const int64_t P = 2LL * (i0 + hi) + pa, Q = 2LL * (j0 + wi) + pb;
+            __nv_bfloat16 *dst =
+                args.y + ((static_cast<int64_t>(n) * 2 * args.H + P) * 2 * args.W + Q) * args.Cout + co0;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(c), v);
+                tmem_wait_ld();
+                if (valid) {
+                    uint32_t o[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        float lo = __uint_as_float(v[2 * q]), hi2 = __uint_as_float(v[2 * q + 1]);
+                        if (args.bias) {
+                            const __nv_bfloat162 bb =
+                                *reinterpret_cast<const __nv_bfloat162 *>(args.bias + co0 + c + 2 * q);
+                            lo += __low2float(bb);
+                            hi2 += __high2float(bb);
+                        }
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi2);
+                        o[q] = *reinterpret_cast<const uint32_t *>(&h);
+                    }
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                }
+            }
+        }
+    }
+
+    // ---- teardown: drain what is still in flight, then free tensor memory ----
+    volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
+    if (warp == 1 && lane == 0) *consumed_sh = consumed;
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort && !skip) {
+        if (warp == 0 && lane == 0) {
+            // loads issued but never consumed still write into the ring
+            for (int kt = *consumed_sh; kt < issued; ++kt)
+                uc_drain(bar_full + 8 * (kt % STAGES), (kt / STAGES) & 1, args.timeout_ns);
+        }
+        if (warp == 1 && lane == 0) {
+            // the accumulator commit arrives once every issued MMA is done
+            uc_drain(bar_acc, 0, args.timeout_ns);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, BN);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library itself).
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_variant(const CUtensorMap &mx, const CUtensorMap &mw, const UcArgs &a, int blocks,
+                           cudaStream_t s)
+{
+    using L = UcLayout<BN, STAGES>;
+    static_assert(L::kDynamic <= 227 * 1024, "upconv ring does not fit in shared memory");
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(upconv_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(L::kDynamic));
+    });
+    if (attr != cudaSuccess) return attr;
+    upconv_kernel<BN, STAGES><<<blocks, kUcThreads, L::kDynamic, s>>>(mx, mw, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool upconv_tiling(int64_t N, int64_t H, int64_t W, UpconvTiling *t)
+{
+    if (N < 1 || H < 1 || W < 1) return false;
+    const auto pow2 = [](int64_t v) { return v > 0 && (v & (v - 1)) == 0; };
+    UpconvTiling r{};
+    if (W >= kBM) {
+        if (W % kBM != 0) return false;
+        r.BW = kBM;
+        r.BH = 1;
+        r.BNI = 1;
+    } else {
+        if (!pow2(W)) return false;
+        r.BW = static_cast<int>(W);
+        const int64_t rows = kBM / W;
+        if (H >= rows) {
+            if (H % rows != 0) return false;
+            r.BH = static_cast<int>(rows);
+            r.BNI = 1;
+        } else {
+            if (!pow2(H)) return false;
+            r.BH = static_cast<int>(H);
+            r.BNI = static_cast<int>(kBM / (W * H));
+        }
+    }
+    r.tiles_w = static_cast<int>(W / r.BW);
+    r.tiles_h = static_cast<int>(H / r.BH);
+    r.tiles_n = static_cast<int>((N + r.BNI - 1) / r.BNI);
+    *t = r;
+    return true;
+}
+
+cudaError_t launch_upconv_fold(const void *w, void *wf, int Cin, int Cout, int sm_count, cudaStream_t s)
+{
+    const int64_t total = 16LL * Cout * Cin;
+    const int64_t want = (total + 255) / 256;
+    const int blocks = static_cast<int>(want < 4LL * sm_count ? want : 4LL * sm_count);
+    upconv_fold_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w),
+                                              static_cast<__nv_bfloat16 *>(wf), Cin, Cout);
+    return cudaGetLastError();
+}
+
+int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int N, int H, int W, int Cin,
+                  int Cout, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err)
+{
+    *err = cudaSuccess;
+    UpconvTiling t;
+    if (!upconv_tiling(N, H, W, &t)) return 1;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return 2;
+    const int BN = (Cout % 256 == 0) ? 256 : 128;
+
+    CUtensorMap mx, mw;
+    {
+        // x as a 4-D tensor {Cin, W, H, N} (innermost first), boxes of
+        // {64 channels, BW, BH, BNI} pixels, 128-byte swizzle, zero fill
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(Cin), static_cast<cuuint64_t>(W),
+                                    static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(Cin) * 2, static_cast<cuuint64_t>(W) * Cin * 2,
+                                       static_cast<cuuint64_t>(H) * W * Cin * 2};
+        const cuuint32_t box[4] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(t.BW),
+                                   static_cast<cuuint32_t>(t.BH), static_cast<cuuint32_t>(t.BNI)};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return 2;
+    }
+    {
+        // folded weights as a 2-D tensor {4 Cin, 4 Cout}, boxes of {64, BN}
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4) * Cin, static_cast<cuuint64_t>(4) * Cout};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(4) * Cin * 2};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(BN)};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(wf), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return 2;
+    }
+    UcArgs a;
+    a.N = N;
+    a.H = H;
+    a.W = W;
+    a.Cin = Cin;
+    a.Cout = Cout;
+    a.BW = t.BW;
+    a.BH = t.BH;
+    a.BNI = t.BNI;
+    a.tiles_w = t.tiles_w;
+    a.tiles_h = t.tiles_h;
+    a.co_tiles = Cout / BN;
+    a.chunks = Cin / kBK;
+    a.ksteps = 4 * a.chunks;
+    a.bias = static_cast<const __nv_bfloat16 *>(bias);
+    a.y = static_cast<__nv_bfloat16 *>(y);
+    a.timeout_ns = timeout_ns;
+    const int64_t blocks = static_cast<int64_t>(t.tiles_n) * t.tiles_h * t.tiles_w * 4 * a.co_tiles;
+    if (blocks > 0x7fffffffLL) return 1;
+    *err = (BN == 256) ? launch_variant<256, 4>(mx, mw, a, static_cast<int>(blocks), s)
+                       : launch_variant<128, 6>(mx, mw, a, static_cast<int>(blocks), s);
+    return *err == cudaSuccess ? 0 : 3;
+}
+
+cudaError_t read_upconv_status(unsigned int *status)
+{
+    return cudaMemcpyFromSymbol(status, g_uc_status, sizeof(unsigned int));
+}
+
+cudaError_t clear_upconv_status()
+{
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_uc_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace gn

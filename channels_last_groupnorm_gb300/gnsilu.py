@@ -64,6 +64,9 @@ EXPORTS = {
                                ctypes.c_void_p]),
     "gn_residual_gate_add": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 2
                              + [ctypes.c_int, ctypes.c_void_p]),
+    "gn_upconv_folded_bytes": (ctypes.c_int64, [ctypes.c_int64] * 2),
+    "gn_upconv_fold": (ctypes.c_int, [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 2 + [ctypes.c_void_p]),
+    "gn_upconv_nhwc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]),
     "gn_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                 ctypes.c_int, ctypes.c_void_p]),
     "gn_silu_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4),
@@ -360,3 +363,79 @@ def residual_gate_add(residual, update, gate, out=None, stream=None):
                                       rows, D, FORMAT[str(dt).replace("torch.", "")],
                                       _stream_handle(residual.device, stream))
     return out if _finish(rc, "gn_residual_gate_add") else None
+
+
+# ---------------------------------------------------------------------------
+# fused nearest-2x upsample + 3x3 convolution
+# ---------------------------------------------------------------------------
+def raw_gn_upconv_fold(w, wf, Cin, Cout, stream=0) -> int:
+    return lib().gn_upconv_fold(w, wf, Cin, Cout, stream or None)
+
+
+def raw_gn_upconv_nhwc(x, wf, bias, y, N, H, W, Cin, Cout, stream=0) -> int:
+    return lib().gn_upconv_nhwc(x, wf, bias or None, y, N, H, W, Cin, Cout, stream or None)
+
+
+def gn_upconv_folded_bytes(Cin: int, Cout: int) -> int:
+    return int(lib().gn_upconv_folded_bytes(Cin, Cout))
+
+
+def upconv_fold(weight, stream=None):
+    """Summed 2x2-window taps of a Conv2d(Cin, Cout, 3, padding=1) weight
+    (bf16 CUDA tensor [Cout, Cin, 3, 3]) for ``upsample_conv_nhwc``: a bf16
+    tensor [4, Cout, 4 * Cin].  None when the weight is not supported (not a
+    contiguous bf16 CUDA tensor of that shape, Cin not a multiple of 64,
+    Cout not a multiple of 128)."""
+    lib()
+    torch = _torch()
+    if not (isinstance(weight, torch.Tensor) and weight.is_cuda and weight.dtype == torch.bfloat16
+            and weight.dim() == 4 and tuple(weight.shape[2:]) == (3, 3) and weight.is_contiguous()):
+        return None
+    if _grad_blocked(weight):
+        return None
+    Cout, Cin = weight.shape[:2]
+    if gn_upconv_folded_bytes(Cin, Cout) < 0:
+        return None
+    wf = torch.empty((4, Cout, 4 * Cin), dtype=torch.bfloat16, device=weight.device)
+    with torch.cuda.device(weight.device):
+        rc = raw_gn_upconv_fold(weight.data_ptr(), wf.data_ptr(), Cin, Cout,
+                                _stream_handle(weight.device, stream))
+    return wf if _finish(rc, "gn_upconv_fold") else None
+
+
+def upsample_conv_nhwc(x, folded, bias=None, out=None, stream=None):
+    """``conv2d(interpolate(x, scale_factor=2, mode="nearest"), w, bias,
+    padding=1)`` for a channels_last bf16 CUDA tensor x (N, Cin, H, W) and
+    the folded weight from ``upconv_fold(w)``.  Returns y (N, Cout, 2H, 2W)
+    in channels_last, or None when the input is not supported (layout,
+    dtype, channel counts, or an (H, W) the kernel's tiles do not cover)."""
+    lib()
+    torch = _torch()
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 4):
+        return None
+    if not x.is_contiguous(memory_format=torch.channels_last):
+        return None
+    N, Cin, H, W = x.shape
+    if not (isinstance(folded, torch.Tensor) and folded.is_cuda and folded.dtype == torch.bfloat16
+            and folded.dim() == 3 and folded.shape[0] == 4 and folded.shape[2] == 4 * Cin
+            and folded.is_contiguous() and folded.device == x.device):
+        return None
+    Cout = folded.shape[1]
+    if bias is not None and not (isinstance(bias, torch.Tensor) and bias.is_cuda and bias.dtype == torch.bfloat16
+                                 and bias.numel() == Cout and bias.is_contiguous()
+                                 and bias.device == x.device):
+        return None
+    if _grad_blocked(x, folded, bias):
+        return None
+    shape = (N, Cout, 2 * H, 2 * W)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=x.device, memory_format=torch.channels_last)
+    elif not (tuple(out.shape) == shape and out.dtype == torch.bfloat16 and out.device == x.device
+              and out.is_contiguous(memory_format=torch.channels_last)):
+        return None
+    if N == 0:
+        return out
+    with torch.cuda.device(x.device):
+        rc = raw_gn_upconv_nhwc(x.data_ptr(), folded.data_ptr(), 0 if bias is None else bias.data_ptr(),
+                                out.data_ptr(), N, H, W, Cin, Cout, _stream_handle(x.device, stream))
+    return out if _finish(rc, "gn_upconv_nhwc") else None

@@ -256,11 +256,64 @@ int gn_silu_rows_static(const void *x_bf16, const float *gamma, const float *bet
 int gn_residual_gate_add(const void *residual, const void *update, const void *gate, void *out,
                          int64_t rows, int64_t D, int format, void *stream);
 
+/* ---- fused nearest-2x upsample + 3x3 convolution ---------------------------
+ * The decoder's up-sampler (sglang PR #33451, "FLUX.2 VAE decoder fast path
+ * behind quality=high", section "Modifications", item 2): a nearest-neighbour
+ * 2x upsample followed by a 3x3 convolution with padding 1,
+ *
+ *   y[n][P][Q][co] = bias[co] + sum_{ky,kx,ci} u[n][P+ky-1][Q+kx-1][ci] * w[co][ci][ky][kx]
+ *   u[n][p][q][ci] = x[n][p/2][q/2][ci] inside the 2H x 2W image, 0 outside,
+ *
+ * evaluated without materialising u: an output pixel of parity (P mod 2,
+ * Q mod 2) sees a 2x2 input window whose taps are sums of the 3x3 taps (the
+ * transposed convolution with kernel 4, stride 2, padding 1 that the page
+ * names).  Two calls: gn_upconv_fold() turns the weight into those summed
+ * taps once (fp32 sums rounded to bf16), gn_upconv_nhwc() runs the
+ * convolution on the tensor cores (fp32 accumulation, bf16 output).  The
+ * summed taps are rounded to bf16, so the result differs from the unfused
+ * evaluation by rounding: per output at most about 2^-8 of the sum of
+ * |x * w| over its 9 Cin terms plus 2^-8 |y|.
+ */
+
+/* Bytes of the folded weight: [4 parities][Cout][4 taps][Cin] bf16
+ * (16 Cin Cout 2 bytes), or -1 if Cin or Cout is out of range. */
+int64_t gn_upconv_folded_bytes(int64_t Cin, int64_t Cout);
+
+/* Fold the convolution weight.
+ *   w  : DEVICE [Cout][Cin][3][3] bf16 (the convolution's own layout),
+ *        2-byte aligned.
+ *   wf : DEVICE, gn_upconv_folded_bytes(Cin, Cout) bytes, 16-byte aligned,
+ *        not overlapping w; row p Cout + co holds the 4 Cin summed taps of
+ *        output channel co for parity p = 2 (P mod 2) + (Q mod 2), taps
+ *        ordered (r, s, ci) with window row r and column s in {0, 1}.
+ *   Cin a multiple of 64 in [64, 8192]; Cout a multiple of 128 in [128, 8192].
+ * Asynchronous on `stream`.  Errors: GN_ERR_NULL, GN_ERR_CHANNELS,
+ * GN_ERR_ALIGN, GN_ERR_ALIAS, GN_ERR_DEVICE, GN_ERR_CUDA. */
+int gn_upconv_fold(const void *w_bf16, void *wf_bf16, int64_t Cin, int64_t Cout, void *stream);
+
+/* The upsample + convolution.
+ *   x    : DEVICE [N][H][W][Cin] bf16 (channels-last), 16-byte aligned.
+ *   wf   : DEVICE folded weight from gn_upconv_fold(), 16-byte aligned.
+ *   bias : DEVICE [Cout] bf16, 4-byte aligned, or NULL for none.
+ *   y    : DEVICE [N][2H][2W][Cout] bf16 (channels-last), 16-byte aligned,
+ *          overlapping none of the inputs.
+ *   N >= 0 (0: nothing to do); Cin and Cout as for gn_upconv_fold();
+ *   W a multiple of 128, or a power of two below 128 with H either a
+ *   multiple of 128 / W or a power of two below it (tiles of 128 output
+ *   pixels of one parity never straddle a row or image edge).
+ * Asynchronous on `stream`; the caller owns every buffer.  Errors:
+ * GN_ERR_NULL, GN_ERR_SHAPE (N < 0, H or W < 1 or not tileable as above,
+ * sizes overflow), GN_ERR_CHANNELS, GN_ERR_ALIGN, GN_ERR_ALIAS,
+ * GN_ERR_DEVICE, GN_ERR_CUDA.  A bounded wait that expires inside the kernel
+ * is reported by gn_device_status() as GN_ERR_KERNEL. */
+int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf16, void *y_bf16, int64_t N,
+                   int64_t H, int64_t W, int64_t Cin, int64_t Cout, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gn_status_string(int status);
 
-/* ABI version of this header: 3 (2 lacked gn_residual_gate_add; 1 also
- * gn_silu_rows_any and gn_silu_ndhwc). */
+/* ABI version of this header: 4 (3 lacked the gn_upconv_* calls; 2 also
+ * gn_residual_gate_add; 1 also gn_silu_rows_any and gn_silu_ndhwc). */
 int gn_abi_version(void);
 
 #ifdef __cplusplus

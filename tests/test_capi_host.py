@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert gs.gn_abi_version() == 3
+    assert gs.gn_abi_version() == 4
     for code in range(13):
         s = gs.status_string(code)
         assert s.startswith("GN_"), (code, s)
@@ -245,3 +245,79 @@ def test_residual_gate_valid_arguments_without_a_device():
 def test_residual_gate_binding_returns_none_for_cpu_tensors():
     r = torch.zeros(2, 16, dtype=torch.bfloat16)
     assert gs.residual_gate_add(r, r.clone(), torch.ones(16, dtype=torch.bfloat16)) is None
+
+
+WF = 0x50000000
+BIAS = 0x60000000
+
+
+def upconv(**kw):
+    a = dict(x=X, wf=WF, bias=BIAS, y=Y, N=1, H=16, W=16, Cin=64, Cout=128)
+    a.update(kw)
+    return gs.raw_gn_upconv_nhwc(a["x"], a["wf"], a["bias"], a["y"], a["N"], a["H"], a["W"], a["Cin"],
+                                 a["Cout"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=0), gs.GN_ERR_NULL),
+    (dict(wf=0), gs.GN_ERR_NULL),
+    (dict(y=0), gs.GN_ERR_NULL),
+    (dict(N=-1), gs.GN_ERR_SHAPE),
+    (dict(H=0), gs.GN_ERR_SHAPE),
+    (dict(W=0), gs.GN_ERR_SHAPE),
+    (dict(W=96), gs.GN_ERR_SHAPE),            # below 128 and not a power of two
+    (dict(W=192), gs.GN_ERR_SHAPE),           # above 128, not a multiple of it
+    (dict(W=16, H=12), gs.GN_ERR_SHAPE),      # H not a multiple of 128 / W = 8
+    (dict(W=32, H=3), gs.GN_ERR_SHAPE),       # H below 128 / W and not a power of two
+    (dict(Cin=32), gs.GN_ERR_CHANNELS),
+    (dict(Cin=96), gs.GN_ERR_CHANNELS),
+    (dict(Cout=64), gs.GN_ERR_CHANNELS),
+    (dict(Cout=320), gs.GN_ERR_CHANNELS),
+    (dict(Cin=16384), gs.GN_ERR_CHANNELS),
+    (dict(x=X + 8), gs.GN_ERR_ALIGN),
+    (dict(wf=WF + 8), gs.GN_ERR_ALIGN),
+    (dict(y=Y + 8), gs.GN_ERR_ALIGN),
+    (dict(bias=BIAS + 2), gs.GN_ERR_ALIGN),
+    (dict(y=X + 1024), gs.GN_ERR_ALIAS),
+    (dict(y=WF - 4096), gs.GN_ERR_ALIAS),
+    (dict(y=BIAS - 4096), gs.GN_ERR_ALIAS),
+])
+def test_upconv_rejects(kw, code):
+    assert upconv(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(w=0), gs.GN_ERR_NULL),
+    (dict(wf=0), gs.GN_ERR_NULL),
+    (dict(Cin=0), gs.GN_ERR_CHANNELS),
+    (dict(Cout=100), gs.GN_ERR_CHANNELS),
+    (dict(w=X + 1), gs.GN_ERR_ALIGN),
+    (dict(wf=WF + 4), gs.GN_ERR_ALIGN),
+    (dict(wf=X + 64), gs.GN_ERR_ALIAS),
+])
+def test_upconv_fold_rejects(kw, code):
+    a = dict(w=X, wf=WF, Cin=64, Cout=128)
+    a.update(kw)
+    assert gs.raw_gn_upconv_fold(a["w"], a["wf"], a["Cin"], a["Cout"]) == code
+
+
+def test_upconv_folded_bytes():
+    assert gs.gn_upconv_folded_bytes(512, 512) == 16 * 512 * 512 * 2
+    assert gs.gn_upconv_folded_bytes(0, 128) == -1
+
+
+@no_gpu
+def test_upconv_valid_arguments_without_a_device():
+    assert upconv() == gs.GN_ERR_DEVICE
+    assert upconv(bias=0) == gs.GN_ERR_DEVICE
+    assert upconv(N=3, H=8, W=8) == gs.GN_ERR_DEVICE       # images grouped in one tile
+    assert upconv(N=1, H=4, W=256, Cout=256) == gs.GN_ERR_DEVICE
+    assert upconv(N=0) == gs.GN_ERR_DEVICE
+    assert gs.raw_gn_upconv_fold(X, WF, 64, 128) == gs.GN_ERR_DEVICE
+
+
+def test_upconv_bindings_return_none_for_cpu_tensors():
+    x = torch.zeros(1, 64, 8, 8, dtype=torch.bfloat16).to(memory_format=torch.channels_last)
+    w = torch.zeros(128, 64, 3, 3, dtype=torch.bfloat16)
+    assert gs.upconv_fold(w) is None
+    assert gs.upsample_conv_nhwc(x, torch.zeros(4, 128, 256, dtype=torch.bfloat16)) is None
