@@ -599,7 +599,7 @@ int gn_upconv_nhwc(const void *x, const void *wf, const void *bias, void *y, int
     if (N == 0) return GN_OK;
     cudaError_t e = cudaSuccess;
     const int r = gn::launch_upconv(x, wf, bias, y, static_cast<int>(N), static_cast<int>(H), static_cast<int>(W),
-                                    static_cast<int>(Cin), static_cast<int>(Cout), wait_timeout_ns(),
+                                    static_cast<int>(Cin), static_cast<int>(Cout), d.sm_count, wait_timeout_ns(),
                                     static_cast<cudaStream_t>(stream), &e);
     if (r == 1) return GN_ERR_SHAPE;
     if (r != 0) {

@@ -145,7 +145,7 @@ cudaError_t launch_upconv_fold(const void *w, void *wf, int Cin, int Cout, int s
 // 0 = launched; 1 = shape not tileable; 2 = tensor-map encoding failed;
 // 3 = the launch failed (*err holds the CUDA error).
 int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int N, int H, int W, int Cin,
-                  int Cout, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err);
+                  int Cout, int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err);
 cudaError_t read_upconv_status(unsigned int *status);
 cudaError_t clear_upconv_status();
 

@@ -19,20 +19,26 @@
 //   Y_ab[pixel, co] = sum_{r,s,ci} x[n][i+a-1+r][j+b-1+s][ci] * Wf_ab[co][r][s][ci].
 //
 // upconv_fold_kernel computes Wf (fp32 sums of bf16 taps, rounded once to
-// bf16) into [4 parities][Cout][4 taps][Cin].  upconv_kernel computes one
-// 128-pixel x BN-channel output tile of one parity per CTA:
+// bf16) into [4 parities][Cout][4 taps][Cin].  upconv_kernel is persistent
+// (one CTA per SM) and walks output tiles of 128 pixels of one parity x BN
+// output channels:
 //   warp 0 (one thread)  TMA producer: per K step of 64 input channels of one
 //                        tap, a 4-D box {64 ch, BW, BH, BNI} of x at the
 //                        tap's shifted coordinates (out-of-image rows and
 //                        columns are zero-filled by the copy engine, which is
 //                        the convolution's padding) and the matching
-//                        {64, BN} box of Wf, into a STAGES-deep ring;
-//   warp 1               allocates BN tensor-memory columns; one thread
-//                        issues four tcgen05.mma (M=128, N=BN, K=16) per K
-//                        step and commits each ring slot back to the producer;
+//                        {64, BN} box of Wf, into a STAGES-deep ring that
+//                        runs on across tile boundaries;
+//   warp 1               allocates 2 BN tensor-memory columns (two
+//                        accumulators); one thread issues four tcgen05.mma
+//                        (M=128, N=BN, K=16) per K step into the tile's
+//                        accumulator and commits each ring slot back to the
+//                        producer and each finished accumulator to the
+//                        epilogue;
 //   warps 2-5            epilogue: tcgen05.ld of the fp32 accumulator (one
-//                        pixel per thread), + bias, round to bf16, store to
-//                        y at (2i + a, 2j + b).
+//                        pixel per thread), hand the accumulator back, + bias,
+//                        round to bf16, store to y at (2i + a, 2j + b) -- while
+//                        the MMAs of the next tile run into the other one.
 // Every wait is bounded (a timeout sets a device status word and the CTA
 // drains its copies and frees its tensor memory before it returns).
 #include <cuda.h>
@@ -63,6 +69,7 @@ struct UcArgs {
     int BW, BH, BNI;            // the pixel box of one tile: BW x BH x BNI = 128
     int tiles_w, tiles_h;
     int co_tiles, chunks, ksteps;
+    int tiles;                  // output tiles in all
     const __nv_bfloat16 *bias;  // [Cout] or null
     __nv_bfloat16 *y;
     uint64_t timeout_ns;
@@ -73,14 +80,43 @@ struct UcLayout {
     static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * kBK * 2;
     static constexpr uint32_t kStage = kABytes + kBBytes;
     static constexpr uint32_t kRing = kStage * STAGES;
-    // after the ring: full[STAGES], empty[STAGES], acc (8 B each), tmem slot, abort flag
+    static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators (double buffer)
+    // after the ring, 8-byte mbarriers: full[STAGES], empty[STAGES],
+    // acc_full[2], acc_empty[2], drain; then the TMEM slot, the abort flag
+    // and the MMA thread's consumed-step count
     static constexpr uint32_t kBars = kRing;
-    static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 1);
+    static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kConsumed = kAbort + 4;
     static constexpr uint32_t kBytes = kConsumed + 4;
     static constexpr uint32_t kDynamic = kBytes + 1024;  // slack to align the ring to 1024 B
 };
+
+// Tile t -> coordinates: the Cout tile varies fastest, then the parity, then
+// the pixel tile, so CTAs working at the same time share x rows and the
+// folded weights in L2.
+struct TileCoord {
+    int parity, i0, j0, n0, co0;
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord tile_coord(int t, const UcArgs &a)
+{
+    TileCoord c;
+    const int co_t = t % a.co_tiles;
+    t /= a.co_tiles;
+    c.parity = t & 3;
+    t >>= 2;
+    const int tw = t % a.tiles_w;
+    t /= a.tiles_w;
+    const int th = t % a.tiles_h;
+    const int tn = t / a.tiles_h;
+    c.i0 = th * a.BH;
+    c.j0 = tw * a.BW;
+    c.n0 = tn * a.BNI;
+    c.co0 = co_t * BN;
+    return c;
+}
 
 __device__ __forceinline__ bool uc_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns)
 {
@@ -145,7 +181,10 @@ __global__ void __launch_bounds__(256) upconv_fold_kernel(const __nv_bfloat16 *_
 }
 
 // ---------------------------------------------------------------------------
-// the implicit-GEMM convolution, one output tile per CTA
+// the implicit-GEMM convolution: a persistent CTA per SM walks the tiles
+// t = blockIdx.x, + gridDim.x, ...; the ring of operand stages runs across
+// tile boundaries and the two tensor-memory accumulators alternate, so the
+// epilogue of one tile overlaps the MMAs of the next.
 // ---------------------------------------------------------------------------
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kUcThreads, 1)
@@ -159,38 +198,33 @@ __global__ void __launch_bounds__(kUcThreads, 1)
     uint8_t *const gbase = smem_raw + (base - raw);
     const uint32_t bar_full = base + L::kBars;
     const uint32_t bar_empty = bar_full + 8 * STAGES;
-    const uint32_t bar_acc = bar_empty + 8 * STAGES;
+    const uint32_t bar_acc_full = bar_empty + 8 * STAGES;   // [2]
+    const uint32_t bar_acc_empty = bar_acc_full + 16;       // [2]
+    const uint32_t bar_drain = bar_acc_empty + 16;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + L::kTmemSlot);
     volatile int *abort = reinterpret_cast<volatile int *>(gbase + L::kAbort);
+    volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // tile coordinates: Cout tile fastest, then parity, then the pixel tile
-    int rest = blockIdx.x;
-    const int co_t = rest % args.co_tiles;
-    rest /= args.co_tiles;
-    const int parity = rest & 3;
-    rest >>= 2;
-    const int tw = rest % args.tiles_w;
-    rest /= args.tiles_w;
-    const int th = rest % args.tiles_h;
-    const int tn = rest / args.tiles_h;
-    const int pa = parity >> 1, pb = parity & 1;
-    const int i0 = th * args.BH, j0 = tw * args.BW, n0 = tn * args.BNI, co0 = co_t * BN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        mbar_init(bar_acc, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_acc_full + 8 * b, 1);
+            mbar_init(bar_acc_empty + 8 * b, 4);   // one arrival per epilogue warp
+        }
+        mbar_init(bar_drain, 1);
         *abort = (*reinterpret_cast<volatile unsigned int *>(&g_uc_status) != 0u) ? 1 : 0;
+        *consumed_sh = 0;
         mbar_init_fence();
         prefetch_tensormap(&map_x);
         prefetch_tensormap(&map_w);
     }
     if (warp == 1) {
-        tmem_alloc(base + L::kTmemSlot, BN);
+        tmem_alloc(base + L::kTmemSlot, L::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -199,102 +233,134 @@ __global__ void __launch_bounds__(kUcThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const bool skip = *abort != 0;
 
-    int issued = 0;       // producer: K steps whose loads were issued
-    int consumed = 0;     // MMA thread: K steps whose loads were consumed
+    int issued = 0;   // producer: ring steps whose loads were issued
     if (!skip && warp == 0 && lane == 0) {
         // ---- producer ----
-        for (int kt = 0; kt < args.ksteps; ++kt) {
-            const int s = kt % STAGES;
-            if (kt >= STAGES && !uc_wait(bar_empty + 8 * s, ((kt / STAGES) - 1) & 1, abort, args.timeout_ns)) break;
-            const int tap = kt / args.chunks;
-            const int c0 = (kt - tap * args.chunks) * kBK;
-            const int r = tap >> 1, sx = tap & 1;
-            const uint32_t sa = base + s * L::kStage;
-            mbar_arrive_expect_tx(bar_full + 8 * s, L::kStage);
-            tma_load_4d(sa, &map_x, c0, j0 + sx + pb - 1, i0 + r + pa - 1, n0, bar_full + 8 * s);
-            tma_load_2d(sa + kABytes, &map_w, kt * kBK, parity * args.Cout + co0, bar_full + 8 * s);
-            issued = kt + 1;
+        int q = 0;    // ring step, counted across tiles
+        bool go = true;
+        for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x) {
+            const TileCoord tc = tile_coord<BN>(t, args);
+            const int pa = tc.parity >> 1, pb = tc.parity & 1;
+            const int wrow = tc.parity * args.Cout + tc.co0;
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (q >= STAGES && !uc_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                const int tap = kt / args.chunks;
+                const int c0 = (kt - tap * args.chunks) * kBK;
+                const int r = tap >> 1, sx = tap & 1;
+                const uint32_t sa = base + s * L::kStage;
+                mbar_arrive_expect_tx(bar_full + 8 * s, L::kStage);
+                tma_load_4d(sa, &map_x, c0, tc.j0 + sx + pb - 1, tc.i0 + r + pa - 1, tc.n0, bar_full + 8 * s);
+                tma_load_2d(sa + kABytes, &map_w, kt * kBK, wrow, bar_full + 8 * s);
+                issued = q + 1;
+            }
         }
     } else if (!skip && warp == 1 && lane == 0) {
         // ---- MMA issue ----
         constexpr uint32_t idesc = umma_idesc_bf16_f32(kBM, BN);
-        for (int kt = 0; kt < args.ksteps; ++kt) {
-            const int s = kt % STAGES;
-            if (!uc_wait(bar_full + 8 * s, (kt / STAGES) & 1, abort, args.timeout_ns)) break;
+        int q = 0;
+        int lt = 0;   // this CTA's tile count
+        bool go = true;
+        for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x, ++lt) {
+            const int buf = lt & 1;
+            // the epilogue has drained this accumulator (tile lt - 2)
+            if (lt >= 2 && !uc_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
             tc_fence_after_sync();
-            const uint32_t sa = base + s * L::kStage;
+            const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (!uc_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sa = base + s * L::kStage;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                umma_f16(tmem, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sa + kABytes + kk * 32), idesc,
-                         (kt > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    umma_f16(d, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sa + kABytes + kk * 32), idesc,
+                             (kt > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(bar_empty + 8 * s);
+                *consumed_sh = q + 1;
             }
-            umma_commit(bar_empty + 8 * s);
-            consumed = kt + 1;
+            if (go) umma_commit(bar_acc_full + 8 * buf);
         }
-        umma_commit(bar_acc);   // arrives once every MMA above has completed
-    } else if (warp >= 2) {
+        umma_commit(bar_drain);   // arrives once every MMA issued above has completed
+    } else if (!skip && warp >= 2) {
         // ---- epilogue: thread <-> tile pixel (TMEM lane) ----
         const int quad = warp & 3;
         const int m = quad * 32 + lane;
-        const bool done = !skip && uc_wait(bar_acc, 0, abort, args.timeout_ns);
-        tc_fence_after_sync();
-        // warp-uniform, as the tensor-memory loads below are warp-collective
-        if (__all_sync(0xffffffffu, done && !*abort)) {
-            const int wi = m % args.BW;
-            const int hi = (m / args.BW) % args.BH;
-            const int n = n0 + m / (args.BW * args.BH);
+        const int wi = m % args.BW;
+        const int hi = (m / args.BW) % args.BH;
+        const int ni = m / (args.BW * args.BH);
+        int lt = 0;
+        for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
+            const int buf = lt & 1;
+            const bool done = uc_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            tc_fence_after_sync();
+            // warp-uniform, as the tensor-memory loads below are warp-collective
+            if (!__all_sync(0xffffffffu, done && !*abort)) break;
+            const TileCoord tc = tile_coord<BN>(t, args);
+            const int pa = tc.parity >> 1, pb = tc.parity & 1;
+            const int n = tc.n0 + ni;
             const bool valid = n < args.N;
-            const int64_t P = 2LL * (i0 + hi) + pa, Q = 2LL * (j0 + wi) + pb;
+            const int64_t P = 2LL * (tc.i0 + hi) + pa, Q = 2LL * (tc.j0 + wi) + pb;
             __nv_bfloat16 *dst =
-                args.y + ((static_cast<int64_t>(n) * 2 * args.H + P) * 2 * args.W + Q) * args.Cout + co0;
+                args.y + ((static_cast<int64_t>(n) * 2 * args.H + P) * 2 * args.W + Q) * args.Cout + tc.co0;
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(c), v);
+                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
                 tmem_wait_ld();
+                if (c + 32 == BN) {
+                    // every column of this accumulator is in registers: hand it back
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
+                }
                 if (valid) {
                     uint32_t o[16];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        float lo = __uint_as_float(v[2 * q]), hi2 = __uint_as_float(v[2 * q + 1]);
+                    for (int k = 0; k < 16; ++k) {
+                        float lo = __uint_as_float(v[2 * k]), hi2 = __uint_as_float(v[2 * k + 1]);
                         if (args.bias) {
                             const __nv_bfloat162 bb =
-                                *reinterpret_cast<const __nv_bfloat162 *>(args.bias + co0 + c + 2 * q);
+                                *reinterpret_cast<const __nv_bfloat162 *>(args.bias + tc.co0 + c + 2 * k);
                             lo += __low2float(bb);
                             hi2 += __high2float(bb);
                         }
                         const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi2);
-                        o[q] = *reinterpret_cast<const uint32_t *>(&h);
+                        o[k] = *reinterpret_cast<const uint32_t *>(&h);
                     }
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    for (int k = 0; k < 4; ++k) d4[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
                 }
             }
         }
     }
 
     // ---- teardown: drain what is still in flight, then free tensor memory ----
-    volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
-    if (warp == 1 && lane == 0) *consumed_sh = consumed;
     tc_fence_before_sync();
     __syncthreads();
     if (*abort && !skip) {
         if (warp == 0 && lane == 0) {
             // loads issued but never consumed still write into the ring
-            for (int kt = *consumed_sh; kt < issued; ++kt)
-                uc_drain(bar_full + 8 * (kt % STAGES), (kt / STAGES) & 1, args.timeout_ns);
+            for (int q = *consumed_sh; q < issued; ++q)
+                uc_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
         }
-        if (warp == 1 && lane == 0) {
-            // the accumulator commit arrives once every issued MMA is done
-            uc_drain(bar_acc, 0, args.timeout_ns);
-        }
+        if (warp == 1 && lane == 0) uc_drain(bar_drain, 0, args.timeout_ns);
         __syncthreads();
     }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem, BN);
+        tmem_dealloc(tmem, L::kTmemCols);
     }
 }
 
@@ -387,7 +453,7 @@ cudaError_t launch_upconv_fold(const void *w, void *wf, int Cin, int Cout, int s
 }
 
 int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int N, int H, int W, int Cin,
-                  int Cout, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err)
+                  int Cout, int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err)
 {
     *err = cudaSuccess;
     UpconvTiling t;
@@ -440,10 +506,13 @@ int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int 
     a.bias = static_cast<const __nv_bfloat16 *>(bias);
     a.y = static_cast<__nv_bfloat16 *>(y);
     a.timeout_ns = timeout_ns;
-    const int64_t blocks = static_cast<int64_t>(t.tiles_n) * t.tiles_h * t.tiles_w * 4 * a.co_tiles;
-    if (blocks > 0x7fffffffLL) return 1;
-    *err = (BN == 256) ? launch_variant<256, 4>(mx, mw, a, static_cast<int>(blocks), s)
-                       : launch_variant<128, 6>(mx, mw, a, static_cast<int>(blocks), s);
+    const int64_t tiles = static_cast<int64_t>(t.tiles_n) * t.tiles_h * t.tiles_w * 4 * a.co_tiles;
+    if (tiles > 0x7fffffffLL) return 1;
+    a.tiles = static_cast<int>(tiles);
+    // persistent: one CTA per SM (each holds all 512 tensor-memory columns or half of them)
+    const int blocks = static_cast<int>(tiles < sm_count ? tiles : sm_count);
+    *err = (BN == 256) ? launch_variant<256, 4>(mx, mw, a, blocks, s)
+                       : launch_variant<128, 6>(mx, mw, a, blocks, s);
     return *err == cudaSuccess ? 0 : 3;
 }
 
