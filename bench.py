@@ -15,6 +15,11 @@ write y once) per step, summed over ranks, divided by the slowest rank's
 time.  ``e2e`` repeats the measurement through the C ABI from pinned host
 buffers with the host<->device copies inside the timed region.
 
+``--workload upconv_*`` measures the fused nearest-2x upsample + 3x3 conv
+of the decoder's up-samplers instead (TFLOP/s against the measured bf16
+tensor peak), ``--workload rga_*`` the residual-gate update; the default
+run adds both to its sweep.
+
 Under torchrun each rank runs its own replica on its own GPU (the
 operation has no cross-GPU exchange); rank 0 prints the line.
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead.
@@ -37,8 +42,11 @@ if ROOT not in sys.path:
 METRIC = "NHWC GroupNorm+SiLU µs/call and HBM GB/s (% of GB300 peak), bf16 G=32"
 DEFAULT_WORKLOAD = "gn_silu_c512_128x128"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+UPCONV_METRIC = "fused nearest-2x upsample + 3x3 conv, bf16 in/out, fp32 accumulate: us/call and TFLOP/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh"]
+UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "gn_internal.h"]
 
 
 # ---------------------------------------------------------------------------
@@ -72,6 +80,17 @@ def barrier():
 # ---------------------------------------------------------------------------
 # peaks, clocks, traffic
 # ---------------------------------------------------------------------------
+def tensor_peak():
+    """Measured dense bf16 TFLOP/s (cuBLAS burst) of the GB300s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "of measured (burst)", float(d.get("bf16_tflops_sustained", 0)) or None
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_BF16_TFLOPS, "of fallback", None
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -138,22 +157,22 @@ class ClockSampler:
                                    default=None)}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, "channels_last_groupnorm_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, variant: str):
+def recorded_traffic(workload: str, variant: str, sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources."""
     try:
         lines = open(TRAFFIC_FILE).read().splitlines()
     except OSError:
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(sources)
     for line in lines:
         parts = line.split()
         if len(parts) == 4 and not line.startswith("#"):
@@ -477,6 +496,185 @@ def measure_rga(w, fmt, steps, device, stream, peak):
             "l2": f"{nsets} rotating buffer sets of {set_bytes >> 20} MiB", "launch": "cuda-graph"}
 
 
+def upconv_device_inputs(w, device):
+    import numpy as np
+    import torch
+    from channels_last_groupnorm_gb300 import workloads as wl
+    c = wl.make_upconv_inputs(w)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+    x = dev(c["x_bits"]).reshape(w.N, w.H, w.W, w.Cin)
+    wt = dev(c["w_bits"]).reshape(w.Cout, w.Cin, 3, 3).contiguous()
+    b = dev(c["bias_bits"]) if c["bias_bits"] is not None else None
+    return c, x, wt, b
+
+
+def measure_upconv(w, steps, device, stream, peak, cudnn_context=True):
+    """gn_upconv_nhwc on one decoder up-sampler workload: the weight is
+    folded once (gn_upconv_fold, untimed: it is per model, not per call),
+    then a CUDA graph of `steps` calls is replayed over rotating (x, y)
+    sets that together exceed twice L2.  TFLOP/s counts the folded
+    evaluation's multiply-adds (2 x 4 Cin per output element)."""
+    import torch
+    import torch.nn.functional as F
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    _, x0, wt, b = upconv_device_inputs(w, device)
+    wf = gs.upconv_fold(wt)
+    if wf is None:
+        raise RuntimeError("upconv_fold rejected the workload's weight")
+    set_bytes = 2 * (x0.numel() + w.out_pixels * w.Cout)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    nsets = buffer_sets_for(set_bytes, l2, cap=8)
+    sets = [(x0.clone(), torch.empty((w.N, 2 * w.H, 2 * w.W, w.Cout), dtype=torch.bfloat16, device=device))
+            for _ in range(nsets)]
+    h = stream.cuda_stream
+    bptr = b.data_ptr() if b is not None else 0
+
+    def call(i):
+        x, y = sets[i]
+        rc = gs.raw_gn_upconv_nhwc(x.data_ptr(), wf.data_ptr(), bptr, y.data_ptr(), w.N, w.H, w.W, w.Cin, w.Cout,
+                                   stream=h)
+        if rc != 0:
+            raise RuntimeError(gs.status_string(rc))
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            call(i % nsets)
+        torch.cuda.synchronize()
+        per, _ = time_calls(call, nsets, max(10, steps // 2), stream)
+        graph = capture_steps(call, nsets, steps, stream)
+        graph.replay()
+        elapsed = time_graph(graph, stream)
+        del graph
+    if gs.gn_device_status(False) != 0:
+        raise RuntimeError("a bounded wait expired inside the upconv kernel")
+    us = elapsed * 1e6 / steps
+    tflops = w.flops / (us * 1e-6) / 1e12
+    launch_us = statistics.mean(per) * 1e3
+    out = {"workload": w.name, "us_per_call": round(us, 2), "tflops": round(tflops, 1),
+           "frac": round(tflops / peak, 3), "launch_us_mean": round(launch_us, 2),
+           "tflops_per_launch": round(w.flops / (launch_us * 1e-6) / 1e12, 1),
+           "l2": f"{nsets} rotating (x, y) sets of {set_bytes >> 20} MiB", "launch": "cuda-graph"}
+    if cudnn_context:
+        # context only: PyTorch's own (cuDNN) upsample + conv2d on the same channels_last tensors
+        xc = x0.permute(0, 3, 1, 2)
+
+        def unfused(_):
+            F.conv2d(F.interpolate(xc, scale_factor=2, mode="nearest"), wt, b, padding=1)
+        with torch.cuda.stream(stream):
+            unfused(0)
+            torch.cuda.synchronize()
+            pt, _ = time_calls(unfused, 1, 10, stream)
+        out["torch_interpolate_conv2d_us"] = round(statistics.median(pt) * 1e3, 1)
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
+def upconv_cpu_baseline(w, budget_s=10.0):
+    """The fp64 oracle on sampled outputs of the workload, in the metric's
+    unit (folded multiply-adds per second), on the host's cores."""
+    import numpy as np
+    import oracle
+    from channels_last_groupnorm_gb300 import workloads as wl
+    c = wl.make_upconv_inputs(w)
+    orc = oracle.upconv()
+    total = w.out_pixels * w.Cout
+    rng = np.random.default_rng(0)
+    count = 256
+    while True:
+        idx = rng.integers(0, total, count)
+        t0 = time.perf_counter()
+        orc.at(c["x_bits"], c["w_bits"], c["bias_bits"], idx)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or count >= 1 << 22:
+            break
+        count *= 4
+    rate = count * 2 * 4 * w.Cin / dt / 1e12
+    return {"value": round(rate, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{count} randomly chosen outputs of {w.name} (of {total}), each a direct fp64 sum over "
+                      f"its 9 Cin upsampled-window terms, counted at the folded 4 Cin multiply-adds"}
+
+
+def run_upconv(args, w, device, rank, world):
+    """One upsample + conv workload on its own: the line reports its TFLOP/s
+    against the measured bf16 tensor peak."""
+    import torch
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind, sustained = tensor_peak()
+    sampler = ClockSampler(device.index or 0) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    r = measure_upconv(w, args.steps, device, stream, peak, cudnn_context=not args.no_sweep)
+    clocks = sampler.stop() if sampler else None
+    elapsed_s = r["us_per_call"] * 1e-6 * args.steps
+    total_elapsed, total_flops = reduce_timing(elapsed_s, float(w.flops) * args.steps,
+                                               device=device if world > 1 else None)
+    value = total_flops / total_elapsed / 1e12
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_upconv_e2e(w, max(3, args.steps // 10), device, stream)
+    line = {
+        "metric": UPCONV_METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["us_per_call"] / 1e3, 6),
+        "us_per_call": r["us_per_call"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "accumulate": "f32", "data": "synthetic (seeded numpy PCG64; x~N(0,1), "
+        "w, bias ~U(-1/sqrt(9Cin), 1/sqrt(9Cin)), bf16)",
+        "config": {**w.describe(), "l2": r["l2"], "launch": r["launch"],
+                   "flops_per_step": "2 * N*2H*2W * Cout * 4 Cin (folded taps)"},
+        "roofline": {"bound": "tensor", "achieved": r["tflops_per_launch"], "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(r["tflops_per_launch"] / peak, 4), "peak_kind": peak_kind,
+                     "peak_sustained": sustained,
+                     "traffic": recorded_traffic(w.name, "upconv", UPCONV_SOURCES),
+                     "kernel": "upconv_kernel", "algorithmic_flops_per_launch": w.flops,
+                     "launch_us_mean": r["launch_us_mean"]},
+        "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+    }
+    if "torch_interpolate_conv2d_us" in r:
+        line["context"] = {"torch_interpolate_conv2d_us": r["torch_interpolate_conv2d_us"],
+                           "note": "PyTorch's upsample + conv2d (cuDNN) on the same tensors, same GPU"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = upconv_cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_upconv_e2e(w, steps, device, stream):
+    """The same call end to end from pinned host buffers: x copied in, the
+    kernel, y copied back, all inside the timed region (the folded weight
+    stays resident, as a model's weights do)."""
+    import torch
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    _, x0, wt, b = upconv_device_inputs(w, device)
+    wf = gs.upconv_fold(wt)
+    hx = x0.cpu().pin_memory()
+    hy = torch.empty((w.N, 2 * w.H, 2 * w.W, w.Cout), dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(x0)
+    dy = torch.empty((w.N, 2 * w.H, 2 * w.W, w.Cout), dtype=torch.bfloat16, device=device)
+    h = stream.cuda_stream
+    bptr = b.data_ptr() if b is not None else 0
+
+    def step(_):
+        dx.copy_(hx, non_blocking=True)
+        rc = gs.raw_gn_upconv_nhwc(dx.data_ptr(), wf.data_ptr(), bptr, dy.data_ptr(), w.N, w.H, w.W, w.Cin,
+                                   w.Cout, stream=h)
+        if rc != 0:
+            raise RuntimeError(gs.status_string(rc))
+        hy.copy_(dy, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step(0)
+        torch.cuda.synchronize()
+        _, elapsed = time_calls(step, 1, steps, stream)
+    us = elapsed * 1e6 / steps
+    return {"value": round(w.flops / (us * 1e-6) / 1e12, 1), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": 2 * x0.numel(), "d2h_bytes_per_step": 2 * dy.numel(),
+            "us_per_call": round(us, 1)}
+
+
 def run_ours(args):
     import torch
     from channels_last_groupnorm_gb300 import build as gnbuild
@@ -495,6 +693,9 @@ def run_ours(args):
     gs.lib()
     if args.workload in wl.RGA_BY_NAME:
         run_rga(args, wl.RGA_BY_NAME[args.workload], device, rank, world)
+        return
+    if args.workload in wl.UPCONV_BY_NAME:
+        run_upconv(args, wl.UPCONV_BY_NAME[args.workload], device, rank, world)
         return
     w = wl.BY_NAME[args.workload]
     variant_id = {"auto": 0, "two_pass": 1, "fused": 2}[args.variant]
@@ -561,6 +762,9 @@ def run_ours(args):
         line["sweep"] = sweep(variant_id, device, stream, peak, launch=args.launch)
         line["residual_gate"] = [measure_rga(rw, fmt, 50, device, stream, peak)
                                  for rw in wl.RGA_WORKLOADS for fmt in ("bf16", "fp16")]
+        tpeak = tensor_peak()[0]
+        line["upsample_conv"] = [measure_upconv(uw, 20, device, stream, tpeak)
+                                 for uw in wl.UPCONV_WORKLOADS[1:]]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -596,6 +800,19 @@ def run_reference(args):
         return
     import oracle
     from channels_last_groupnorm_gb300 import workloads as wl
+    if args.workload in wl.UPCONV_BY_NAME:
+        uw = wl.UPCONV_BY_NAME[args.workload]
+        # warm-up: one untimed sample; then the timed sample sized to ~10 s per step budget
+        upconv_cpu_baseline(uw, budget_s=2.0)
+        cb = upconv_cpu_baseline(uw, budget_s=min(40.0, 100.0 / max(1, args.steps)))
+        print(json.dumps({
+            "impl": "reference", "metric": UPCONV_METRIC, "value": cb["value"], "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": uw.describe(),
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
     w = wl.BY_NAME[args.workload]
     case = wl.make_inputs(w)
     orc = oracle.get()
