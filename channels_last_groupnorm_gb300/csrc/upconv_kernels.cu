@@ -46,6 +46,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "gn_internal.h"
@@ -69,7 +70,7 @@ struct UcArgs {
     int BW, BH, BNI;            // the pixel box of one tile: BW x BH x BNI = 128
     int tiles_w, tiles_h;
     int co_tiles, chunks, ksteps;
-    int tiles;                  // output tiles in all
+    int tiles;                  // output tiles in all (tile pairs for the pair kernel)
     const __nv_bfloat16 *bias;  // [Cout] or null
     __nv_bfloat16 *y;
     uint64_t timeout_ns;
@@ -365,6 +366,242 @@ __global__ void __launch_bounds__(kUcThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// The same convolution on CTA pairs (a cluster of two CTAs on two SMs): one
+// tcgen05.mma.cta_group::2 of M = 256, N = 256 covers two pixel tiles (one
+// per CTA) of the same parity and 256 output channels.  Each CTA stages its
+// own A tile (16 KB per K step) and HALF of B (128 channels, 16 KB), so per
+// SM the operand traffic through shared memory and L2 is two thirds of the
+// single-CTA kernel's for the same MMA work.
+//   full[s]       in the even CTA: expects both CTAs' bytes of ring step s
+//                 (the odd CTA's copies signal it across the pair)
+//   empty[s]      in both CTAs: the pair MMA's commit arrives on both
+//   acc_full[b]   in both CTAs: the pair MMA's commit at the end of a tile
+//   acc_empty[b]  in the even CTA: one arrival per epilogue warp of both CTAs
+// ---------------------------------------------------------------------------
+template <int STAGES>
+struct PairLayout {
+    static constexpr uint32_t kBHalf = 128u * kBK * 2;   // 16 KB
+    static constexpr uint32_t kStage = kABytes + kBHalf;
+    static constexpr uint32_t kRing = kStage * STAGES;
+    static constexpr uint32_t kTmemCols = 512;          // two 256-column accumulators
+    static constexpr uint32_t kBars = kRing;
+    static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kConsumed = kAbort + 4;
+    static constexpr uint32_t kBytes = kConsumed + 4;
+    static constexpr uint32_t kDynamic = kBytes + 1024;
+};
+
+// Pair tile T -> this CTA's tile: the 256-channel tile varies fastest, then
+// the parity, then the pixel-tile pair; CTA `rank` takes pixel tile
+// 2 pp + rank (a tile past the last one lies beyond the batch: its loads
+// read zeros and its stores are skipped).
+__device__ __forceinline__ TileCoord pair_tile_coord(int T, int rank, const UcArgs &a)
+{
+    TileCoord c;
+    const int co_t = T % a.co_tiles;
+    T /= a.co_tiles;
+    c.parity = T & 3;
+    int pt = 2 * (T >> 2) + rank;
+    const int tw = pt % a.tiles_w;
+    pt /= a.tiles_w;
+    const int th = pt % a.tiles_h;
+    const int tn = pt / a.tiles_h;
+    c.i0 = th * a.BH;
+    c.j0 = tw * a.BW;
+    c.n0 = tn * a.BNI;
+    c.co0 = co_t * 256;
+    return c;
+}
+
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
+    upconv_pair_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                       const UcArgs args)
+{
+    using L = PairLayout<STAGES>;
+    constexpr int BN = 256;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t bar_full = base + L::kBars;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_acc_full = bar_empty + 8 * STAGES;   // [2]
+    const uint32_t bar_acc_empty = bar_acc_full + 16;       // [2]
+    const uint32_t bar_drain = bar_acc_empty + 16;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + L::kTmemSlot);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + L::kAbort);
+    volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_acc_full + 8 * b, 1);
+            mbar_init(bar_acc_empty + 8 * b, 8);   // 4 epilogue warps x 2 CTAs
+        }
+        mbar_init(bar_drain, 1);
+        *abort = (*reinterpret_cast<volatile unsigned int *>(&g_uc_status) != 0u) ? 1 : 0;
+        *consumed_sh = 0;
+        mbar_init_fence();
+        prefetch_tensormap(&map_x);
+        prefetch_tensormap(&map_w);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(base + L::kTmemSlot, L::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    cluster_sync_all();   // both CTAs' barriers are initialised before any signal crosses the pair
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort != 0;
+    const uint32_t full_lead = mapa_shared(bar_full, 0);
+    const uint32_t acc_empty_lead = mapa_shared(bar_acc_empty, 0);
+
+    int issued = 0;
+    if (!skip && warp == 0 && lane == 0) {
+        // ---- producer (both CTAs): own A tile, own half of B ----
+        int q = 0;
+        bool go = true;
+        for (int T = pair; go && T < args.tiles; T += npairs) {
+            const TileCoord tc = pair_tile_coord(T, rank, args);
+            const int pa = tc.parity >> 1, pb = tc.parity & 1;
+            const int wrow = tc.parity * args.Cout + tc.co0 + rank * 128;
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (q >= STAGES && !uc_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                const int tap = kt / args.chunks;
+                const int c0 = (kt - tap * args.chunks) * kBK;
+                const int r = tap >> 1, sx = tap & 1;
+                const uint32_t sa = base + s * L::kStage;
+                if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * L::kStage);
+                tma_load_4d_pair(sa, &map_x, c0, tc.j0 + sx + pb - 1, tc.i0 + r + pa - 1, tc.n0, full_lead + 8 * s);
+                tma_load_2d_pair(sa + kABytes, &map_w, kt * kBK, wrow, full_lead + 8 * s);
+                issued = q + 1;
+            }
+        }
+    } else if (!skip && leader && warp == 1 && lane == 0) {
+        // ---- MMA issue (even CTA only) ----
+        constexpr uint32_t idesc = umma_idesc_bf16_f32(2 * kBM, BN);
+        int q = 0;
+        int lt = 0;
+        bool go = true;
+        for (int T = pair; go && T < args.tiles; T += npairs, ++lt) {
+            const int buf = lt & 1;
+            if (lt >= 2 && !uc_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
+            tc_fence_after_sync();
+            const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (!uc_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sa = base + s * L::kStage;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    umma_f16_pair(d, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sa + kABytes + kk * 32),
+                                  idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit_pair(bar_empty + 8 * s, 0x3);
+                *consumed_sh = q + 1;
+            }
+            if (go) umma_commit_pair(bar_acc_full + 8 * buf, 0x3);
+        }
+        umma_commit_pair(bar_drain, 0x1);
+    } else if (!skip && warp >= 2) {
+        // ---- epilogue (both CTAs): thread <-> own pixel (TMEM lane), 256 channels ----
+        const int quad = warp & 3;
+        const int m = quad * 32 + lane;
+        const int wi = m % args.BW;
+        const int hi = (m / args.BW) % args.BH;
+        const int ni = m / (args.BW * args.BH);
+        int lt = 0;
+        for (int T = pair; T < args.tiles; T += npairs, ++lt) {
+            const int buf = lt & 1;
+            const bool done = uc_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            tc_fence_after_sync();
+            if (!__all_sync(0xffffffffu, done && !*abort)) break;
+            const TileCoord tc = pair_tile_coord(T, rank, args);
+            const int pa = tc.parity >> 1, pb = tc.parity & 1;
+            const int n = tc.n0 + ni;
+            const bool valid = n < args.N;
+            const int64_t P = 2LL * (tc.i0 + hi) + pa, Q = 2LL * (tc.j0 + wi) + pb;
+            __nv_bfloat16 *dst =
+                args.y + ((static_cast<int64_t>(n) * 2 * args.H + P) * 2 * args.W + Q) * args.Cout + tc.co0;
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
+                tmem_wait_ld();
+                if (c + 32 == BN) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acc_empty_lead + 8 * buf);
+                }
+                if (valid) {
+                    uint32_t o[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        float lo = __uint_as_float(v[2 * k]), hi2 = __uint_as_float(v[2 * k + 1]);
+                        if (args.bias) {
+                            const __nv_bfloat162 bb =
+                                *reinterpret_cast<const __nv_bfloat162 *>(args.bias + tc.co0 + c + 2 * k);
+                            lo += __low2float(bb);
+                            hi2 += __high2float(bb);
+                        }
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi2);
+                        o[k] = *reinterpret_cast<const uint32_t *>(&h);
+                    }
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) d4[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                }
+            }
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort && !skip) {
+        if (leader && warp == 0 && lane == 0) {
+            for (int q = *consumed_sh; q < issued; ++q)
+                uc_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
+        }
+        if (leader && warp == 1 && lane == 0) uc_drain(bar_drain, 0, args.timeout_ns);
+        if (!leader && warp == 0 && lane == 0) {
+            // this CTA's copies signal the even CTA's barriers: give them time to land
+            const uint64_t until = global_ns() + 200000;
+            while (global_ns() < until) __nanosleep(1000);
+        }
+        __syncthreads();
+    }
+    __syncwarp();
+    cluster_sync_all();   // neither CTA leaves while the pair's MMAs or signals may touch it
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem, L::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 namespace {
@@ -407,6 +644,50 @@ cudaError_t launch_variant(const CUtensorMap &mx, const CUtensorMap &mw, const U
     if (attr != cudaSuccess) return attr;
     upconv_kernel<BN, STAGES><<<blocks, kUcThreads, L::kDynamic, s>>>(mx, mw, a);
     return cudaGetLastError();
+}
+
+template <int STAGES>
+cudaError_t launch_pair(const CUtensorMap &mx, const CUtensorMap &mw, const UcArgs &a, int sm_count, cudaStream_t s)
+{
+    using L = PairLayout<STAGES>;
+    static_assert(L::kDynamic <= 227 * 1024, "upconv pair ring does not fit in shared memory");
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    static int max_clusters = 0;
+    std::call_once(once, [sm_count] {
+        attr = cudaFuncSetAttribute(upconv_pair_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(L::kDynamic));
+        if (attr != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (sm_count / 2));
+        cfg.blockDim = dim3(kUcThreads);
+        cfg.dynamicSmemBytes = L::kDynamic;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, upconv_pair_kernel<STAGES>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            max_clusters = sm_count / 2;
+        }
+    });
+    if (attr != cudaSuccess) return attr;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    const int pairs = a.tiles < max_clusters ? a.tiles : max_clusters;
+    upconv_pair_kernel<STAGES><<<2 * pairs, kUcThreads, L::kDynamic, s>>>(mx, mw, a);
+    return cudaGetLastError();
+}
+
+bool pair_kernel_enabled()
+{
+    static const bool on = [] {
+        const char *v = std::getenv("GN_UPCONV_PAIR");
+        return !(v && v[0] == '0');
+    }();
+    return on;
 }
 
 }  // namespace
@@ -461,6 +742,7 @@ int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int 
     EncodeTiledFn enc = encode_fn();
     if (!enc) return 2;
     const int BN = (Cout % 256 == 0) ? 256 : 128;
+    const bool use_pair = BN == 256 && pair_kernel_enabled();
 
     CUtensorMap mx, mw;
     {
@@ -480,9 +762,10 @@ int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int 
     }
     {
         // folded weights as a 2-D tensor {4 Cin, 4 Cout}, boxes of {64, BN}
+        // channels (a CTA pair: 128 channels, the half of B one CTA stages)
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4) * Cin, static_cast<cuuint64_t>(4) * Cout};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(4) * Cin * 2};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(BN)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(use_pair ? 128 : BN)};
         const cuuint32_t es[2] = {1, 1};
         if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(wf), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -506,9 +789,14 @@ int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int 
     a.bias = static_cast<const __nv_bfloat16 *>(bias);
     a.y = static_cast<__nv_bfloat16 *>(y);
     a.timeout_ns = timeout_ns;
-    const int64_t tiles = static_cast<int64_t>(t.tiles_n) * t.tiles_h * t.tiles_w * 4 * a.co_tiles;
+    const int64_t pixel_tiles = static_cast<int64_t>(t.tiles_n) * t.tiles_h * t.tiles_w;
+    const int64_t tiles = (use_pair ? (pixel_tiles + 1) / 2 : pixel_tiles) * 4 * a.co_tiles;
     if (tiles > 0x7fffffffLL) return 1;
     a.tiles = static_cast<int>(tiles);
+    if (use_pair) {
+        *err = launch_pair<6>(mx, mw, a, sm_count, s);
+        return *err == cudaSuccess ? 0 : 3;
+    }
     // persistent: one CTA per SM (each holds all 512 tensor-memory columns or half of them)
     const int blocks = static_cast<int>(tiles < sm_count ? tiles : sm_count);
     *err = (BN == 256) ? launch_variant<256, 4>(mx, mw, a, blocks, s)

@@ -175,3 +175,31 @@ def test_unsupported_inputs_return_none():
     with pytest.warns(UserWarning):
         assert gs.upconv_fold(torch.zeros(100, 64, 3, 3, dtype=torch.bfloat16, device=dev)) is None
     assert gs.upconv_fold(w.float()) is None
+
+
+def test_single_sm_schedule_matches_oracle():
+    """The single-CTA schedule (taken when the CTA-pair kernel is switched
+    off with GN_UPCONV_PAIR=0, and always for Cout not a multiple of 256) on
+    a 256-channel case, in a child process (the switch is read once)."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import numpy as np, torch, oracle\n"
+        "from channels_last_groupnorm_gb300 import gnsilu as gs, workloads as wl\n"
+        "c = wl.make_upconv_case(2, 8, 16, 128, 512, 41)\n"
+        "d = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).cuda().view(torch.bfloat16)\n"
+        "x = d(c['x_bits']).reshape(2, 8, 16, 128).permute(0, 3, 1, 2)\n"
+        "wf = gs.upconv_fold(d(c['w_bits']).reshape(512, 128, 3, 3).contiguous())\n"
+        "y = gs.upsample_conv_nhwc(x, wf, d(c['bias_bits']))\n"
+        "torch.cuda.synchronize()\n"
+        "assert gs.gn_device_status(False) == 0\n"
+        "ref, ab = oracle.upconv().forward(c['x_bits'], c['w_bits'], c['bias_bits'], with_abs=True)\n"
+        "err = np.abs(y.permute(0, 2, 3, 1).float().cpu().numpy().astype(np.float64) - ref)\n"
+        "assert np.all(err <= 2.0 ** -8 * (ab + np.abs(ref))), err.max()\n"
+        "print('ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, GN_UPCONV_PAIR="0", PYTHONPATH=root)
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
