@@ -567,6 +567,25 @@ def measure_upconv(w, steps, device, stream, peak, cudnn_context=True):
             torch.cuda.synchronize()
             pt, _ = time_calls(unfused, 1, 10, stream)
         out["torch_interpolate_conv2d_us"] = round(statistics.median(pt) * 1e3, 1)
+        # the page's own formulation: ConvTranspose2d(k4, s2, p1) with the summed 4x4 taps
+        # (kernel row k of the transposed conv sums 3x3 rows (2,), (1, 2), (0, 1), (0,))
+        rows = ((2,), (1, 2), (0, 1), (0,))
+        wt32 = wt.float()
+        w4 = torch.zeros((w.Cin, w.Cout, 4, 4), dtype=torch.float32, device=device)
+        for k1, r1 in enumerate(rows):
+            for k2, r2 in enumerate(rows):
+                for ky in r1:
+                    for kx in r2:
+                        w4[:, :, k1, k2] += wt32[:, :, ky, kx].t()
+        w4 = w4.to(torch.bfloat16)
+
+        def transposed(_):
+            F.conv_transpose2d(xc, w4, b, stride=2, padding=1)
+        with torch.cuda.stream(stream):
+            transposed(0)
+            torch.cuda.synchronize()
+            pt, _ = time_calls(transposed, 1, 10, stream)
+        out["torch_conv_transpose2d_us"] = round(statistics.median(pt) * 1e3, 1)
     del sets
     torch.cuda.empty_cache()
     return out
@@ -634,7 +653,9 @@ def run_upconv(args, w, device, rank, world):
     }
     if "torch_interpolate_conv2d_us" in r:
         line["context"] = {"torch_interpolate_conv2d_us": r["torch_interpolate_conv2d_us"],
-                           "note": "PyTorch's upsample + conv2d (cuDNN) on the same tensors, same GPU"}
+                           "torch_conv_transpose2d_us": r.get("torch_conv_transpose2d_us"),
+                           "note": "PyTorch (cuDNN) on the same tensors and GPU: upsample + conv2d, and "
+                                   "the summed-tap ConvTranspose2d(k4, s2, p1) the page runs"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = upconv_cpu_baseline(w)
     if rank == 0:
