@@ -311,3 +311,68 @@ def make_upconv_case(N: int, H: int, W: int, Cin: int, Cout: int, index: int,
 
 def make_upconv_inputs(w: UpconvWorkload) -> dict:
     return make_upconv_case(w.N, w.H, w.W, w.Cin, w.Cout, w.index, w.bias)
+
+
+# ---------------------------------------------------------------------------
+# Single-head attention of the VAE mid-block with the output projection
+# folded into the value projection (sglang PR #33451, "FLUX.2 VAE decoder
+# fast path behind quality=high", section "Modifications", item 2, attention
+# bullet).  Width D = 512 (one head of the decoder's 512 channels); S = the
+# latent's pixel count: 64^2 = 4096 for a 512^2 decode, 128^2 = 16384 for
+# 1024^2, plus a small full-oracle case.  Values: q, k, xn (the GroupNorm
+# output) and residual ~ N(0, 1); the value / output projection weights and
+# biases ~ U(-b, b), b = 1/sqrt(D) (PyTorch's default Linear initialisation),
+# drawn in fp32 and rounded to bf16.
+# Seeds: 10000 + index (q), 11000 (k), 12000 (xn), 13000 (residual),
+# 14000 (wv), 14500 (bv), 15000 (wo), 15500 (bo).
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    index: int
+    S: int
+    D: int = 512
+    residual: bool = True
+    note: str = ""
+
+    @property
+    def flops(self) -> int:
+        """Multiply-adds x 2 of the folded evaluation: the value projection,
+        the scores, and the attention-weighted sum."""
+        return 2 * self.S * self.D * self.D + 4 * self.S * self.S * self.D
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "S": self.S, "D": self.D, "heads": 1, "residual": self.residual,
+                "values": "q, k, xn, residual ~ N(0,1); W, b ~ U(-1/sqrt(D), 1/sqrt(D))"}
+
+
+ATTN_WORKLOADS = [
+    AttnWorkload("attn_s256_d512", 0, 256, note="small, full oracle"),
+    AttnWorkload("attn_s4096_d512", 1, 4096, note="FLUX.2 VAE mid-block at a 512^2 decode (64^2 latent)"),
+    AttnWorkload("attn_s16384_d512", 2, 16384, note="FLUX.2 VAE mid-block at a 1024^2 decode (128^2 latent)"),
+]
+
+ATTN_BY_NAME = {w.name: w for w in ATTN_WORKLOADS}
+
+
+def make_attn_case(S: int, D: int, index: int, residual: bool = True) -> dict:
+    """bf16 bit patterns: q, k, xn, residual [S, D]; wv, wo [D, D] (Linear
+    layout [out][in]); bv, bo [D].  residual is None when not asked for."""
+    b = 1.0 / np.sqrt(D)
+
+    def normal(seed, shape):
+        return f32_to_bf16_bits(np.random.default_rng(seed).standard_normal(shape, dtype=np.float32)).reshape(shape)
+
+    def uniform(seed, shape):
+        v = np.random.default_rng(seed).uniform(-b, b, shape).astype(np.float32)
+        return f32_to_bf16_bits(v).reshape(shape)
+    out = {"q": normal(10000 + index, (S, D)), "k": normal(11000 + index, (S, D)),
+           "xn": normal(12000 + index, (S, D)),
+           "residual": normal(13000 + index, (S, D)) if residual else None,
+           "wv": uniform(14000 + index, (D, D)), "bv": uniform(14500 + index, (D,)),
+           "wo": uniform(15000 + index, (D, D)), "bo": uniform(15500 + index, (D,))}
+    return out
+
+
+def make_attn_inputs(w: AttnWorkload) -> dict:
+    return make_attn_case(w.S, w.D, w.index, w.residual)

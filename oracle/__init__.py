@@ -19,7 +19,10 @@ which writes out the two roundings of the eager evaluation; ``rga()``
 returns it.  ``upconv()`` returns the oracle of the decoder's fused
 nearest-2x upsample + 3x3 convolution (``upconv_oracle.c``; the sglang PR
 #33451 page, section "Modifications", item 2), which evaluates the upsample
-and the convolution as defined, in fp64.
+and the convolution as defined, in fp64.  ``attn()`` returns the oracle of
+the decoder's single-head attention block with its value and output
+projections (``attn_oracle.c``; same page, item 2, attention bullet),
+evaluated unfolded, in fp64.
 
 Parity pins: the oracle is checked against brute force on tiny tensors, a
 library special case (``torch.nn.functional.group_norm`` in float64), closed
@@ -321,3 +324,82 @@ def upconv() -> UpconvOracle:
         if _upconv_default is None:
             _upconv_default = UpconvOracle(build_upconv())
         return _upconv_default
+
+
+# ---------------------------------------------------------------------------
+# single-head attention block oracle (attn_oracle.c): value projection,
+# softmax attention, output projection (+ residual), unfolded, fp64
+# ---------------------------------------------------------------------------
+ATTN_SOURCE = os.path.join(_HERE, "attn_oracle.c")
+ATTN_LIB_PATH = os.path.join(BUILD_DIR, "libattn_oracle.so")
+_attn_default = None
+
+
+class AttnOracle:
+    """ctypes view of one compiled attention oracle library."""
+
+    def __init__(self, lib_path: str):
+        self.lib = ctypes.CDLL(lib_path)
+        f = self.lib.attn_oracle_forward
+        f.restype = ctypes.c_int
+        f.argtypes = [_p] * 8 + [_i64, _i64, _p, _p]
+        f = self.lib.attn_oracle_rows
+        f.restype = ctypes.c_int
+        f.argtypes = [_p] * 8 + [_i64, _i64, _p, _i64, _p, _p]
+
+    @staticmethod
+    def _args(q, k, xn, wv, bv, wo, bo, residual):
+        u = lambda a: np.ascontiguousarray(a).view(np.uint16)  # noqa: E731
+        q, k, xn, wv, bv, wo, bo = (u(a) for a in (q, k, xn, wv, bv, wo, bo))
+        S, D = q.shape
+        if k.shape != (S, D) or xn.shape != (S, D) or wv.shape != (D, D) or wo.shape != (D, D):
+            raise ValueError("q, k, xn must be [S, D] and wv, wo [D, D] bf16 bits")
+        bv, bo = bv.reshape(-1), bo.reshape(-1)
+        if bv.shape != (D,) or bo.shape != (D,):
+            raise ValueError("bv, bo must be [D] bf16 bits")
+        r = None
+        if residual is not None:
+            r = u(residual)
+            if r.shape != (S, D):
+                raise ValueError("residual must be [S, D] bf16 bits")
+        return q, k, xn, wv, bv, wo, bo, r, S, D
+
+    def forward(self, q, k, xn, wv, bv, wo, bo, residual=None, with_mag: bool = False):
+        """out float64 [S, D] (and the magnitudes if asked)."""
+        q, k, xn, wv, bv, wo, bo, r, S, D = self._args(q, k, xn, wv, bv, wo, bo, residual)
+        out = np.empty((S, D), np.float64)
+        mag = np.empty_like(out) if with_mag else None
+        rc = self.lib.attn_oracle_forward(q.ctypes.data, k.ctypes.data, xn.ctypes.data, wv.ctypes.data,
+                                          bv.ctypes.data, wo.ctypes.data, bo.ctypes.data,
+                                          None if r is None else r.ctypes.data, S, D, out.ctypes.data,
+                                          None if mag is None else mag.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"attn_oracle_forward rejected its arguments (rc={rc})")
+        return (out, mag) if with_mag else out
+
+    def rows(self, q, k, xn, wv, bv, wo, bo, residual, rows, with_mag: bool = False):
+        """out (and magnitudes) for the given query rows, float64 [len(rows), D]."""
+        q, k, xn, wv, bv, wo, bo, r, S, D = self._args(q, k, xn, wv, bv, wo, bo, residual)
+        idx = np.ascontiguousarray(rows, np.int64)
+        out = np.empty((idx.size, D), np.float64)
+        mag = np.empty_like(out) if with_mag else None
+        rc = self.lib.attn_oracle_rows(q.ctypes.data, k.ctypes.data, xn.ctypes.data, wv.ctypes.data,
+                                       bv.ctypes.data, wo.ctypes.data, bo.ctypes.data,
+                                       None if r is None else r.ctypes.data, S, D, idx.ctypes.data, idx.size,
+                                       out.ctypes.data, None if mag is None else mag.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"attn_oracle_rows rejected its arguments (rc={rc})")
+        return (out, mag) if with_mag else out
+
+
+def build_attn(source: str = ATTN_SOURCE, out: str = ATTN_LIB_PATH, force: bool = False) -> str:
+    return build(source=source, out=out, force=force)
+
+
+def attn() -> AttnOracle:
+    """The attention-block oracle built from ``attn_oracle.c``."""
+    global _attn_default
+    with _lock:
+        if _attn_default is None:
+            _attn_default = AttnOracle(build_attn())
+        return _attn_default
