@@ -4,14 +4,17 @@ evaluates the upsample and the convolution as defined (sglang PR #33451,
 "FLUX.2 VAE decoder fast path behind quality=high", section "Modifications",
 item 2).
 
-Acceptance bound, per output, derived from the arithmetic: the summed taps
-are rounded to bf16 (relative error <= 2^-9 each, so the products they enter
-err by <= 2^-9 of the sum of |x * w| over their constituent 3x3 taps), the
-tensor cores accumulate in fp32 (<= K 2^-24 of the same sum, K = 4 Cin <=
-2048 here: 2^-13), and the result is rounded to bf16 (2^-9 |y|):
-    |y_gpu - y_ref| <= 2^-8 (S + |y_ref|),   S = |bias| + sum |u * w|
+Acceptance bound, per output, derived from the arithmetic (bf16 keeps 8
+significant bits: one rounding errs by at most u = 2^-8 relative): the
+summed taps are rounded to bf16 (so the products they enter err by at most
+2^-8 of the sum of |x * w| over their constituent 3x3 taps), the tensor
+cores accumulate in fp32 (at most K 2^-24 of the same sum, K = 4 Cin <=
+2048 here: 2^-13), and the result is rounded to bf16 (2^-8 |y|); together
+less than
+    |y_gpu - y_ref| <= 2^-7 (S + |y_ref|),   S = |bias| + sum |u * w|
 (S is returned by the oracle).  Wrong indexing or a wrong tap moves outputs
-by about |y| (~0.6 here), far above the bound (~0.04).
+by about |y| (~0.6 here), far above the bound (~0.08); the rms check below
+is tighter still.
 """
 import numpy as np
 import pytest
@@ -26,7 +29,7 @@ from tests import upconv_pins as up
 
 pytestmark = pytest.mark.gpu
 
-BOUND = 2.0 ** -8
+BOUND = 2.0 ** -7
 
 
 @pytest.fixture(scope="module", autouse=True)
