@@ -6,6 +6,8 @@ Build the library with ``python -m channels_last_groupnorm_gb300.build``.
 """
 from .gnsilu import (  # noqa: F401
     GnError,
+    attention_folded,
+    attn_fold,
     VARIANT_AUTO,
     VARIANT_FUSED,
     VARIANT_TWO_PASS,

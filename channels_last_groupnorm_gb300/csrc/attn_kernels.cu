@@ -1,0 +1,557 @@
+// attn_kernels.cu -- the VAE mid-block's single-head attention with the
+// output projection folded into the value projection, on the sm_103a tensor
+// cores.
+//
+// Operation (sglang PR #33451, "FLUX.2 VAE decoder fast path behind
+// quality=high", section "Modifications", item 2, attention bullet): with
+// the query / key projections q, k [S][D], the GroupNorm output xn [S][D]
+// and the value / output projections (wv, bv), (wo, bo),
+//   out = softmax(q k^T / sqrt(D)) (xn wv^T + bv) wo^T + bo + residual
+//       = softmax(q k^T / sqrt(D)) (xn W'^T + b') + residual,
+//   W' = wo wv, b' = wo bv + bo,
+// the second form being exact because every softmax row sums to 1.  This
+// file evaluates the second form:
+//   attn_fold_kernel   W' (fp32 sums over D, rounded once to bf16) and b'
+//                      (fp32), once per weight;
+//   gemm_kernel        C = alpha A B^T (+ a per-row or per-column bias, + a
+//                      bf16 residual), A [M][K] and B [N][K] bf16 K-major,
+//                      fp32 accumulation in tensor memory, fp32 or bf16 out;
+//                      run three times: V'^T = W' xn^T + b' ([D][S], bf16),
+//                      the scores q k^T / sqrt(D) ([S][S], fp32), and
+//                      out = P V' + residual ([S][D], bf16);
+//   softmax_rows_kernel  P = softmax of each score row, rounded to bf16.
+// The scores are materialised: for D = 512 an fp32 128 x 512 output block
+// alone fills the 512 tensor-memory columns of an SM, so a single-pass
+// (flash) kernel would need its output split across CTAs and the scores
+// computed twice; the three GEMMs run at tensor-core rate and the softmax
+// at HBM rate instead.
+//
+// gemm_kernel is persistent (one CTA per SM): warp 0 issues TMA tile loads
+// (128-byte swizzle) into a STAGES-deep ring, warp 1 owns 2 BN tensor-memory
+// columns and issues tcgen05.mma (M = 128, N = BN, K = 16), warps 2-5 drain
+// the two accumulators alternately (tcgen05.ld, epilogue, 16-byte stores)
+// while the next tile's MMAs run.  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "gn_internal.h"
+#include "gn_ptx.cuh"
+#include "tc_ptx.cuh"
+
+namespace gn {
+
+__device__ unsigned int g_at_status;
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kSleepNs = 20000;
+
+struct GemmArgs {
+    int M, N, K;
+    int n_tiles, tiles, ksteps;
+    float alpha;
+    const float *bias_m;            // [M] or null
+    const float *bias_n;            // [N] or null
+    const __nv_bfloat16 *residual;  // [M][N] bf16 or null
+    void *c;                        // [M][N] fp32 or bf16
+    int out_f32;
+    uint64_t timeout_ns;
+};
+
+template <int BN, int STAGES>
+struct GemmLayout {
+    static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * kBK * 2;
+    static constexpr uint32_t kStage = kABytes + kBBytes;
+    static constexpr uint32_t kRing = kStage * STAGES;
+    static constexpr uint32_t kTmemCols = 2 * BN;
+    static constexpr uint32_t kBars = kRing;
+    static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kConsumed = kAbort + 4;
+    static constexpr uint32_t kBytes = kConsumed + 4;
+    static constexpr uint32_t kDynamic = kBytes + 1024;
+};
+
+__device__ __forceinline__ bool at_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    const uint64_t deadline = global_ns() + timeout_ns;
+#pragma unroll 1
+    for (;;) {
+        if (mbar_wait_sleep(bar, parity, kSleepNs)) return true;
+        if (*abort) return false;
+        if (global_ns() > deadline) {
+            *abort = 1;
+            atomicOr(&g_at_status, 1u);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void at_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t deadline = global_ns() + timeout_ns;
+#pragma unroll 1
+    while (!mbar_wait_sleep(bar, parity, kSleepNs)) {
+        if (global_ns() > deadline) return;
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// W'[e][i] = sum_c wo[e][c] wv[c][i] (fp32, rounded once to bf16) and
+// b'[e] = sum_c wo[e][c] bv[c] + bo[e] (fp32), one thread per output.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) attn_fold_kernel(const __nv_bfloat16 *__restrict__ wv,
+                                                        const __nv_bfloat16 *__restrict__ bv,
+                                                        const __nv_bfloat16 *__restrict__ wo,
+                                                        const __nv_bfloat16 *__restrict__ bo,
+                                                        __nv_bfloat16 *__restrict__ wf, float *__restrict__ bf,
+                                                        int D)
+{
+    const int64_t total = static_cast<int64_t>(D) * (D + 1);
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int e = static_cast<int>(idx / (D + 1));
+        const int i = static_cast<int>(idx % (D + 1));   // i == D: the bias
+        const __nv_bfloat16 *wrow = wo + static_cast<int64_t>(e) * D;
+        float acc = 0.f;
+        if (i < D) {
+            for (int c = 0; c < D; ++c)
+                acc = fmaf(__bfloat162float(wrow[c]), __bfloat162float(wv[static_cast<int64_t>(c) * D + i]), acc);
+            wf[static_cast<int64_t>(e) * D + i] = __float2bfloat16_rn(acc);
+        } else {
+            for (int c = 0; c < D; ++c) acc = fmaf(__bfloat162float(wrow[c]), __bfloat162float(bv[c]), acc);
+            bf[e] = acc + __bfloat162float(bo[e]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// P[r][j] = exp(s[r][j] - max_j s[r][.]) / sum_j exp(...), rounded to bf16;
+// one CTA per row, the row staged once in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kSoftmaxThreads = 512;
+
+__global__ void __launch_bounds__(kSoftmaxThreads) softmax_rows_kernel(const float *__restrict__ s,
+                                                                       __nv_bfloat16 *__restrict__ p, int S)
+{
+    extern __shared__ float4 row4[];
+    __shared__ float red[kSoftmaxThreads / 32];
+    __shared__ float bcast;
+    const int r = blockIdx.x;
+    const float4 *src = reinterpret_cast<const float4 *>(s + static_cast<int64_t>(r) * S);
+    const int n4 = S / 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    float mx = -INFINITY;
+    for (int i = threadIdx.x; i < n4; i += kSoftmaxThreads) {
+        const float4 v = __ldcs(src + i);
+        row4[i] = v;
+        mx = fmaxf(fmaxf(mx, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (warp == 0) {
+        float v = lane < kSoftmaxThreads / 32 ? red[lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) bcast = v;
+    }
+    __syncthreads();
+    const float m = bcast;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float mb = m * kLog2e;
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < n4; i += kSoftmaxThreads) {
+        float4 v = row4[i];
+        v.x = exp2f(fmaf(v.x, kLog2e, -mb));
+        v.y = exp2f(fmaf(v.y, kLog2e, -mb));
+        v.z = exp2f(fmaf(v.z, kLog2e, -mb));
+        v.w = exp2f(fmaf(v.w, kLog2e, -mb));
+        row4[i] = v;
+        sum += (v.x + v.y) + (v.z + v.w);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    if (warp == 0) {
+        float v = lane < kSoftmaxThreads / 32 ? red[lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) bcast = 1.0f / v;
+    }
+    __syncthreads();
+    const float inv = bcast;
+    uint2 *dst = reinterpret_cast<uint2 *>(p + static_cast<int64_t>(r) * S);
+    for (int i = threadIdx.x; i < n4; i += kSoftmaxThreads) {
+        const float4 v = row4[i];
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x * inv, v.y * inv);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v.z * inv, v.w * inv);
+        dst[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// C = alpha A B^T (+ bias, + residual): persistent, one CTA per SM; tile t:
+// the N tile varies fastest.
+// ---------------------------------------------------------------------------
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const GemmArgs args)
+{
+    using L = GemmLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t bar_full = base + L::kBars;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
+    const uint32_t bar_acc_empty = bar_acc_full + 16;
+    const uint32_t bar_drain = bar_acc_empty + 16;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + L::kTmemSlot);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + L::kAbort);
+    volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_acc_full + 8 * b, 1);
+            mbar_init(bar_acc_empty + 8 * b, 4);
+        }
+        mbar_init(bar_drain, 1);
+        *abort = (*reinterpret_cast<volatile unsigned int *>(&g_at_status) != 0u) ? 1 : 0;
+        *consumed_sh = 0;
+        mbar_init_fence();
+        prefetch_tensormap(&map_a);
+        prefetch_tensormap(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(base + L::kTmemSlot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort != 0;
+
+    int issued = 0;
+    if (!skip && warp == 0 && lane == 0) {
+        int q = 0;
+        bool go = true;
+        for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x) {
+            const int m0 = (t / args.n_tiles) * kBM, n0 = (t % args.n_tiles) * BN;
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (q >= STAGES && !at_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                const uint32_t sa = base + s * L::kStage;
+                mbar_arrive_expect_tx(bar_full + 8 * s, L::kStage);
+                tma_load_2d(sa, &map_a, kt * kBK, m0, bar_full + 8 * s);
+                tma_load_2d(sa + kABytes, &map_b, kt * kBK, n0, bar_full + 8 * s);
+                issued = q + 1;
+            }
+        }
+    } else if (!skip && warp == 1 && lane == 0) {
+        constexpr uint32_t idesc = umma_idesc_bf16_f32(kBM, BN);
+        int q = 0, lt = 0;
+        bool go = true;
+        for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x, ++lt) {
+            const int buf = lt & 1;
+            if (lt >= 2 && !at_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
+            tc_fence_after_sync();
+            const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (!at_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sa = base + s * L::kStage;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    umma_f16(d, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sa + kABytes + kk * 32), idesc,
+                             (kt > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(bar_empty + 8 * s);
+                *consumed_sh = q + 1;
+            }
+            if (go) umma_commit(bar_acc_full + 8 * buf);
+        }
+        umma_commit(bar_drain);
+    } else if (!skip && warp >= 2) {
+        const int quad = warp & 3;
+        const int row_in_tile = quad * 32 + lane;
+        int lt = 0;
+        for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
+            const int buf = lt & 1;
+            const bool done = at_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            tc_fence_after_sync();
+            if (!__all_sync(0xffffffffu, done && !*abort)) break;
+            const int m = (t / args.n_tiles) * kBM + row_in_tile;
+            const int n0 = (t % args.n_tiles) * BN;
+            const float bm = args.bias_m ? args.bias_m[m] : 0.f;
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
+                tmem_wait_ld();
+                if (c + 32 == BN) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
+                }
+                float f[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) f[k] = fmaf(__uint_as_float(v[k]), args.alpha, bm);
+                if (args.bias_n) {
+                    const float4 *b4 = reinterpret_cast<const float4 *>(args.bias_n + n0 + c);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float4 b = __ldg(b4 + k);
+                        f[4 * k] += b.x;
+                        f[4 * k + 1] += b.y;
+                        f[4 * k + 2] += b.z;
+                        f[4 * k + 3] += b.w;
+                    }
+                }
+                const int64_t at = static_cast<int64_t>(m) * args.N + n0 + c;
+                if (args.residual) {
+                    const uint4 *r4 = reinterpret_cast<const uint4 *>(args.residual + at);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 rr = r4[k];
+                        const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            f[8 * k + 2 * h] += __uint_as_float(w[h] << 16);
+                            f[8 * k + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                        }
+                    }
+                }
+                if (args.out_f32) {
+                    float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(args.c) + at);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) d4[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+                } else {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.c) + at);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const __nv_bfloat162 hb = __floats2bfloat162_rn(f[8 * k + 2 * h], f[8 * k + 2 * h + 1]);
+                            o[h] = *reinterpret_cast<const uint32_t *>(&hb);
+                        }
+                        d4[k] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort && !skip) {
+        if (warp == 0 && lane == 0) {
+            for (int q = *consumed_sh; q < issued; ++q)
+                at_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
+        }
+        if (warp == 1 && lane == 0) at_drain(bar_drain, 0, args.timeout_ns);
+        __syncthreads();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// A bf16 [rows][K] K-major operand, boxes of {64, box_rows}, 128-byte swizzle.
+bool encode_kmajor(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows)
+{
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_gemm_variant(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &a, int sm_count,
+                                cudaStream_t s)
+{
+    using L = GemmLayout<BN, STAGES>;
+    static_assert(L::kDynamic <= 227 * 1024, "gemm ring does not fit in shared memory");
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(gemm_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(L::kDynamic));
+    });
+    if (attr != cudaSuccess) return attr;
+    const int blocks = a.tiles < sm_count ? a.tiles : sm_count;
+    gemm_kernel<BN, STAGES><<<blocks, kGemmThreads, L::kDynamic, s>>>(ma, mb, a);
+    return cudaGetLastError();
+}
+
+// C[M][N] = alpha A[M][K] B[N][K]^T (+ bias_m[M], + bias_n[N], + residual)
+int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float alpha, const float *bias_m,
+             const float *bias_n, const void *residual, bool out_f32, int sm_count, uint64_t timeout_ns,
+             cudaStream_t s, cudaError_t *err)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return 2;
+    const int BN = (N % 256 == 0) ? 256 : 128;
+    CUtensorMap ma, mb;
+    if (!encode_kmajor(enc, &ma, A, M, K, kBM) || !encode_kmajor(enc, &mb, B, N, K, BN)) return 2;
+    GemmArgs a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.n_tiles = N / BN;
+    a.tiles = (M / kBM) * a.n_tiles;
+    a.ksteps = K / kBK;
+    a.alpha = alpha;
+    a.bias_m = bias_m;
+    a.bias_n = bias_n;
+    a.residual = static_cast<const __nv_bfloat16 *>(residual);
+    a.c = C;
+    a.out_f32 = out_f32 ? 1 : 0;
+    a.timeout_ns = timeout_ns;
+    *err = (BN == 256) ? launch_gemm_variant<256, 4>(ma, mb, a, sm_count, s)
+                       : launch_gemm_variant<128, 6>(ma, mb, a, sm_count, s);
+    return *err == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fold(const void *wv, const void *bv, const void *wo, const void *bo, void *wf, float *bf,
+                             int D, int sm_count, cudaStream_t s)
+{
+    const int64_t total = static_cast<int64_t>(D) * (D + 1);
+    const int64_t want = (total + 255) / 256;
+    const int blocks = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
+    attn_fold_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(wv),
+                                            static_cast<const __nv_bfloat16 *>(bv),
+                                            static_cast<const __nv_bfloat16 *>(wo),
+                                            static_cast<const __nv_bfloat16 *>(bo), static_cast<__nv_bfloat16 *>(wf),
+                                            bf, D);
+    return cudaGetLastError();
+}
+
+size_t attn_workspace_bytes(int64_t S, int64_t D)
+{
+    // V'^T [D][S] bf16 | scores [S][S] fp32 | P [S][S] bf16, each 256-byte aligned
+    const auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    return up(static_cast<size_t>(2 * D * S)) + up(static_cast<size_t>(4 * S * S)) + up(static_cast<size_t>(2 * S * S));
+}
+
+int launch_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
+                       const void *residual, void *out, int S, int D, void *workspace, int sm_count,
+                       uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches)
+{
+    const auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *vt = ws;                                                        // [D][S] bf16
+    float *scores = reinterpret_cast<float *>(ws + up(static_cast<size_t>(2) * D * S));   // [S][S] fp32
+    void *p = ws + up(static_cast<size_t>(2) * D * S) + up(static_cast<size_t>(4) * S * S);  // [S][S] bf16
+    *launches = 0;
+    // V'^T = W' xn^T + b' (b' per row of V'^T)
+    int r = run_gemm(wf, xn, vt, D, S, D, 1.0f, bf, nullptr, nullptr, false, sm_count, timeout_ns, s, err);
+    if (r) return r;
+    ++*launches;
+    // scores = q k^T / sqrt(D)
+    r = run_gemm(q, k, scores, S, S, D, 1.0f / sqrtf(static_cast<float>(D)), nullptr, nullptr, nullptr, true,
+                 sm_count, timeout_ns, s, err);
+    if (r) return r;
+    ++*launches;
+    // P = softmax(scores) row by row (the row is staged in up to 128 KB of shared memory)
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(softmax_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    4 * kAttnMaxS);
+    });
+    if (attr != cudaSuccess) {
+        *err = attr;
+        return 3;
+    }
+    softmax_rows_kernel<<<S, kSoftmaxThreads, static_cast<size_t>(4) * S, s>>>(scores,
+                                                                              static_cast<__nv_bfloat16 *>(p), S);
+    *err = cudaGetLastError();
+    if (*err != cudaSuccess) return 3;
+    ++*launches;
+    // out = P V' + residual
+    r = run_gemm(p, vt, out, S, D, S, 1.0f, nullptr, nullptr, residual, false, sm_count, timeout_ns, s, err);
+    if (r) return r;
+    ++*launches;
+    return 0;
+}
+
+cudaError_t read_attn_status(unsigned int *status)
+{
+    return cudaMemcpyFromSymbol(status, g_at_status, sizeof(unsigned int));
+}
+
+cudaError_t clear_attn_status()
+{
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_at_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace gn

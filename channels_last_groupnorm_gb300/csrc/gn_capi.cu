@@ -446,13 +446,15 @@ int gn_device_status(int clear)
         return GN_ERR_DEVICE;
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return GN_ERR_CUDA;
-    unsigned int st = 0, st_uc = 0;
+    unsigned int st = 0, st_uc = 0, st_at = 0;
     if (gn::read_device_status(&st) != cudaSuccess) return GN_ERR_CUDA;
     if (gn::read_upconv_status(&st_uc) != cudaSuccess) return GN_ERR_CUDA;
-    st |= st_uc;
+    if (gn::read_attn_status(&st_at) != cudaSuccess) return GN_ERR_CUDA;
+    st |= st_uc | st_at;
     if (clear) {
         if (gn::clear_device_status() != cudaSuccess) return GN_ERR_CUDA;
         if (gn::clear_upconv_status() != cudaSuccess) return GN_ERR_CUDA;
+        if (gn::clear_attn_status() != cudaSuccess) return GN_ERR_CUDA;
         std::lock_guard<std::mutex> lock(g_mu);
         for (auto &kv : g_workspaces) {
             if (kv.first.first == dev && kv.second.ptr && cudaMemset(kv.second.ptr, 0, 256) != cudaSuccess)
@@ -610,6 +612,92 @@ int gn_upconv_nhwc(const void *x, const void *wf, const void *bias, void *y, int
     return GN_OK;
 }
 
-int gn_abi_version(void) { return 4; }
+// ---- single-head attention with the output projection folded into V --------
+namespace {
+
+bool attn_width_ok(int64_t D) { return D >= 128 && D <= 1024 && D % 128 == 0; }
+
+bool attn_tokens_ok(int64_t S) { return S >= 128 && S <= gn::kAttnMaxS && S % 128 == 0; }
+
+}  // namespace
+
+int gn_attn_fold(const void *wv, const void *bv, const void *wo, const void *bo, void *wf, float *bf, int64_t D,
+                 void *stream)
+{
+    if (!wv || !bv || !wo || !bo || !wf || !bf) return GN_ERR_NULL;
+    if (!attn_width_ok(D)) return GN_ERR_CHANNELS;
+    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(wv) % 2 || addr(bv) % 2 || addr(wo) % 2 || addr(bo) % 2 || addr(wf) % 16 || addr(bf) % 16)
+        return GN_ERR_ALIGN;
+    const size_t wb = static_cast<size_t>(2 * D * D), bb = static_cast<size_t>(4 * D);
+    for (const void *in : {wv, wo})
+        if (ranges_overlap(wf, wb, in, wb) || ranges_overlap(bf, bb, in, wb)) return GN_ERR_ALIAS;
+    for (const void *in : {bv, bo})
+        if (ranges_overlap(wf, wb, in, static_cast<size_t>(2 * D)) ||
+            ranges_overlap(bf, bb, in, static_cast<size_t>(2 * D)))
+            return GN_ERR_ALIAS;
+    if (ranges_overlap(wf, wb, bf, bb)) return GN_ERR_ALIAS;
+    int dev = -1;
+    DeviceInfo d;
+    const int rc = current_device(&dev, &d);
+    if (rc != GN_OK) return rc;
+    const cudaError_t e = gn::launch_attn_fold(wv, bv, wo, bo, wf, bf, static_cast<int>(D), d.sm_count,
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    g_launches.fetch_add(1);
+    return GN_OK;
+}
+
+size_t gn_attn_workspace_bytes(int64_t S, int64_t D)
+{
+    if (!attn_tokens_ok(S) || !attn_width_ok(D)) return 0;
+    return gn::attn_workspace_bytes(S, D);
+}
+
+int gn_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
+                   const void *residual, void *out, int64_t S, int64_t D, void *workspace, size_t workspace_bytes,
+                   void *stream)
+{
+    if (!q || !k || !xn || !wf || !bf || !out || !workspace) return GN_ERR_NULL;
+    if (!attn_tokens_ok(S)) return GN_ERR_SHAPE;
+    if (!attn_width_ok(D)) return GN_ERR_CHANNELS;
+    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(q) % 16 || addr(k) % 16 || addr(xn) % 16 || addr(wf) % 16 || addr(bf) % 16 || addr(out) % 16 ||
+        addr(workspace) % 256 || (residual && addr(residual) % 16))
+        return GN_ERR_ALIGN;
+    const size_t need = gn::attn_workspace_bytes(S, D);
+    if (workspace_bytes < need) return GN_ERR_WORKSPACE;
+    const size_t act = static_cast<size_t>(2 * S * D);
+    const struct {
+        const void *p;
+        size_t n;
+    } ins[] = {{q, act}, {k, act}, {xn, act}, {wf, static_cast<size_t>(2 * D * D)}, {bf, static_cast<size_t>(4 * D)}};
+    for (const auto &in : ins)
+        if (ranges_overlap(out, act, in.p, in.n) || ranges_overlap(workspace, need, in.p, in.n)) return GN_ERR_ALIAS;
+    if (ranges_overlap(out, act, workspace, need)) return GN_ERR_ALIAS;
+    if (residual && residual != out &&
+        (ranges_overlap(out, act, residual, act) || ranges_overlap(workspace, need, residual, act)))
+        return GN_ERR_ALIAS;
+    int dev = -1;
+    DeviceInfo d;
+    const int rc = current_device(&dev, &d);
+    if (rc != GN_OK) return rc;
+    cudaError_t e = cudaSuccess;
+    int launches = 0;
+    const int r = gn::launch_attn_folded(q, k, xn, wf, bf, residual, out, static_cast<int>(S), static_cast<int>(D),
+                                         workspace, d.sm_count, wait_timeout_ns(), static_cast<cudaStream_t>(stream),
+                                         &e, &launches);
+    g_launches.fetch_add(static_cast<uint64_t>(launches));
+    if (r != 0) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    return GN_OK;
+}
+
+int gn_abi_version(void) { return 5; }
 
 }  // extern "C"

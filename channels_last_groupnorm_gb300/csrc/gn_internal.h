@@ -149,4 +149,17 @@ int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int 
 cudaError_t read_upconv_status(unsigned int *status);
 cudaError_t clear_upconv_status();
 
+// ---- single-head attention with the output projection folded into V (attn_kernels.cu) ----
+constexpr int kAttnMaxS = 32768;   // a score row (fp32) is staged in shared memory
+cudaError_t launch_attn_fold(const void *wv, const void *bv, const void *wo, const void *bo, void *wf, float *bf,
+                             int D, int sm_count, cudaStream_t s);
+size_t attn_workspace_bytes(int64_t S, int64_t D);
+// 0 = launched (*launches kernels); 2 = tensor-map encoding failed; 3 = a
+// launch failed (*err holds the CUDA error).
+int launch_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
+                       const void *residual, void *out, int S, int D, void *workspace, int sm_count,
+                       uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches);
+cudaError_t read_attn_status(unsigned int *status);
+cudaError_t clear_attn_status();
+
 }  // namespace gn

@@ -67,6 +67,10 @@ EXPORTS = {
     "gn_upconv_folded_bytes": (ctypes.c_int64, [ctypes.c_int64] * 2),
     "gn_upconv_fold": (ctypes.c_int, [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 2 + [ctypes.c_void_p]),
     "gn_upconv_nhwc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]),
+    "gn_attn_fold": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int64, ctypes.c_void_p]),
+    "gn_attn_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 2),
+    "gn_attn_folded": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int64] * 2
+                       + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gn_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                 ctypes.c_int, ctypes.c_void_p]),
     "gn_silu_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4),
@@ -439,3 +443,87 @@ def upsample_conv_nhwc(x, folded, bias=None, out=None, stream=None):
         rc = raw_gn_upconv_nhwc(x.data_ptr(), folded.data_ptr(), 0 if bias is None else bias.data_ptr(),
                                 out.data_ptr(), N, H, W, Cin, Cout, _stream_handle(x.device, stream))
     return out if _finish(rc, "gn_upconv_nhwc") else None
+
+
+# ---------------------------------------------------------------------------
+# single-head attention with the output projection folded into V
+# ---------------------------------------------------------------------------
+def raw_gn_attn_fold(wv, bv, wo, bo, wf, bf, D, stream=0) -> int:
+    return lib().gn_attn_fold(wv, bv, wo, bo, wf, bf, D, stream or None)
+
+
+def raw_gn_attn_folded(q, k, xn, wf, bf, residual, out, S, D, workspace, workspace_bytes, stream=0) -> int:
+    return lib().gn_attn_folded(q, k, xn, wf, bf, residual or None, out, S, D, workspace, workspace_bytes,
+                                stream or None)
+
+
+def gn_attn_workspace_bytes(S: int, D: int) -> int:
+    return int(lib().gn_attn_workspace_bytes(S, D))
+
+
+def attn_fold(wv, bv, wo, bo, stream=None):
+    """Fold an attention block's value projection (wv [D, D], bv [D]) and
+    output projection (wo, bo) -- bf16 CUDA tensors, Linear layout -- into
+    (W' bf16 [D, D], b' fp32 [D]).  None when not supported."""
+    lib()
+    torch = _torch()
+    ts = (wv, bv, wo, bo)
+    if not all(isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+               for t in ts):
+        return None
+    if _grad_blocked(*ts) or wv.dim() != 2 or wv.shape[0] != wv.shape[1]:
+        return None
+    D = wv.shape[0]
+    if wo.shape != wv.shape or bv.numel() != D or bo.numel() != D or not all(t.device == wv.device for t in ts):
+        return None
+    wf = torch.empty((D, D), dtype=torch.bfloat16, device=wv.device)
+    bf = torch.empty((D,), dtype=torch.float32, device=wv.device)
+    with torch.cuda.device(wv.device):
+        rc = raw_gn_attn_fold(wv.data_ptr(), bv.data_ptr(), wo.data_ptr(), bo.data_ptr(), wf.data_ptr(),
+                              bf.data_ptr(), D, _stream_handle(wv.device, stream))
+    return (wf, bf) if _finish(rc, "gn_attn_fold") else None
+
+
+def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, stream=None):
+    """``softmax(q k^T / sqrt(D)) (xn W'^T + b') + residual`` for bf16 CUDA
+    tensors q, k, xn (and residual) of shape [S, D] and the folded weight
+    from ``attn_fold``; equal to the unfolded single-head attention block
+    (value projection, attention, output projection, residual).  Returns
+    out [S, D] bf16, or None when not supported (S not a multiple of 128 in
+    [128, 32768], D not a multiple of 128 in [128, 1024], layouts, dtypes)."""
+    lib()
+    torch = _torch()
+    ts = (q, k, xn)
+    if not all(isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 2
+               and t.is_contiguous() for t in ts):
+        return None
+    S, D = q.shape
+    if k.shape != q.shape or xn.shape != q.shape or not all(t.device == q.device for t in ts):
+        return None
+    if not (isinstance(wf, torch.Tensor) and wf.is_cuda and wf.dtype == torch.bfloat16 and wf.shape == (D, D)
+            and wf.is_contiguous() and isinstance(bf, torch.Tensor) and bf.dtype == torch.float32
+            and bf.numel() == D and bf.is_contiguous() and wf.device == q.device and bf.device == q.device):
+        return None
+    if residual is not None and not (isinstance(residual, torch.Tensor) and residual.shape == q.shape
+                                     and residual.dtype == torch.bfloat16 and residual.is_contiguous()
+                                     and residual.device == q.device):
+        return None
+    if _grad_blocked(q, k, xn, wf, bf, residual):
+        return None
+    need = gn_attn_workspace_bytes(S, D)
+    if need == 0:
+        warnings.warn("attention_folded: unsupported S or D", stacklevel=2)
+        return None
+    if out is None:
+        out = torch.empty_like(q)
+    elif not (out.shape == q.shape and out.dtype == torch.bfloat16 and out.is_contiguous()
+              and out.device == q.device):
+        return None
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = raw_gn_attn_folded(q.data_ptr(), k.data_ptr(), xn.data_ptr(), wf.data_ptr(), bf.data_ptr(),
+                                0 if residual is None else residual.data_ptr(), out.data_ptr(), S, D,
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_handle(q.device, stream))
+    return out if _finish(rc, "gn_attn_folded") else None

@@ -271,8 +271,8 @@ int gn_residual_gate_add(const void *residual, const void *update, const void *g
  * taps once (fp32 sums rounded to bf16), gn_upconv_nhwc() runs the
  * convolution on the tensor cores (fp32 accumulation, bf16 output).  The
  * summed taps are rounded to bf16, so the result differs from the unfused
- * evaluation by rounding: per output at most about 2^-8 of the sum of
- * |x * w| over its 9 Cin terms plus 2^-8 |y|.
+ * evaluation by rounding: per output less than 2^-7 of the sum of
+ * |x * w| over its 9 Cin terms plus 2^-7 |y|.
  */
 
 /* Bytes of the folded weight: [4 parities][Cout][4 taps][Cin] bf16
@@ -309,11 +309,61 @@ int gn_upconv_fold(const void *w_bf16, void *wf_bf16, int64_t Cin, int64_t Cout,
 int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf16, void *y_bf16, int64_t N,
                    int64_t H, int64_t W, int64_t Cin, int64_t Cout, void *stream);
 
+/* ---- single-head attention with the output projection folded into V -------
+ * The VAE mid-block attention after its GroupNorm and its query / key
+ * projections (sglang PR #33451, "FLUX.2 VAE decoder fast path behind
+ * quality=high", section "Modifications", item 2, attention bullet):
+ *
+ *   out = softmax(q k^T / sqrt(D)) (xn wv^T + bv) wo^T + bo + residual
+ *       = softmax(q k^T / sqrt(D)) (xn W'^T + b') + residual,
+ *   W' = wo wv,  b' = wo bv + bo
+ *
+ * (exact because every softmax row sums to 1).  gn_attn_fold() forms W'
+ * (fp32 sums rounded once to bf16) and b' (fp32) once per weight;
+ * gn_attn_folded() evaluates the second form with three tensor-core GEMMs
+ * (fp32 accumulation) and a row softmax; the scores are kept in fp32 and
+ * the softmax weights rounded to bf16 before the weighted sum.
+ */
+
+/* Fold the value projection (wv [D][D], bv [D]) and the output projection
+ * (wo [D][D], bo [D]) -- DEVICE bf16, PyTorch Linear layout [out][in],
+ * 2-byte aligned -- into wf (DEVICE bf16 [D][D], 16-byte aligned) and bf
+ * (DEVICE fp32 [D], 16-byte aligned); the outputs overlap no input.
+ * D a multiple of 128 in [128, 1024].  Asynchronous on `stream`.  Errors:
+ * GN_ERR_NULL, GN_ERR_CHANNELS, GN_ERR_ALIGN, GN_ERR_ALIAS, GN_ERR_DEVICE,
+ * GN_ERR_CUDA. */
+int gn_attn_fold(const void *wv_bf16, const void *bv_bf16, const void *wo_bf16, const void *bo_bf16,
+                 void *wf_bf16, float *bf, int64_t D, void *stream);
+
+/* Workspace bytes gn_attn_folded() needs for S tokens of width D (the
+ * folded value rows, the fp32 scores and the bf16 softmax weights:
+ * 2 D S + 6 S^2 bytes, rounded up), or 0 if S or D is out of range. */
+size_t gn_attn_workspace_bytes(int64_t S, int64_t D);
+
+/* The folded attention.
+ *   q, k, xn  : DEVICE bf16 [S][D], 16-byte aligned (query / key
+ *               projections and the GroupNorm output).
+ *   wf, bf    : from gn_attn_fold().
+ *   residual  : DEVICE bf16 [S][D] added to the result, or NULL; may equal
+ *               out (in place) but not overlap it otherwise.
+ *   out       : DEVICE bf16 [S][D], 16-byte aligned, overlapping no input.
+ *   workspace : DEVICE, >= gn_attn_workspace_bytes(S, D), 256-byte aligned,
+ *               caller-owned, overlapping nothing else.
+ *   S a multiple of 128 in [128, 32768]; D as for gn_attn_fold().
+ * Asynchronous on `stream`.  Errors: GN_ERR_NULL, GN_ERR_SHAPE (S),
+ * GN_ERR_CHANNELS (D), GN_ERR_ALIGN, GN_ERR_ALIAS, GN_ERR_WORKSPACE,
+ * GN_ERR_DEVICE, GN_ERR_CUDA; a bounded wait that expires inside a kernel
+ * is reported by gn_device_status() as GN_ERR_KERNEL. */
+int gn_attn_folded(const void *q_bf16, const void *k_bf16, const void *xn_bf16, const void *wf_bf16, const float *bf,
+                   const void *residual_bf16, void *out_bf16, int64_t S, int64_t D, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gn_status_string(int status);
 
-/* ABI version of this header: 4 (3 lacked the gn_upconv_* calls; 2 also
- * gn_residual_gate_add; 1 also gn_silu_rows_any and gn_silu_ndhwc). */
+/* ABI version of this header: 5 (4 lacked the gn_attn_* calls; 3 also the
+ * gn_upconv_* calls; 2 also gn_residual_gate_add; 1 also gn_silu_rows_any
+ * and gn_silu_ndhwc). */
 int gn_abi_version(void);
 
 #ifdef __cplusplus

@@ -1,0 +1,136 @@
+"""Single-head attention with the output projection folded into V on the
+GPU (gn_attn_fold + gn_attn_folded: three tcgen05 GEMMs and a row softmax)
+against the fp64 oracle of the UNFOLDED block (value projection, softmax
+attention, output projection, residual; sglang PR #33451, "FLUX.2 VAE
+decoder fast path behind quality=high", section "Modifications", item 2,
+attention bullet).
+
+Acceptance bound, per output, derived from the arithmetic (one bf16
+rounding errs by at most u = 2^-8 relative): the folded weight, the folded
+value rows and the softmax weights are each rounded to bf16 once (each
+perturbs the output by at most 2^-8 of the magnitude M = |bo| + |residual| +
+sum_c |wo| sum_j a_j (|bv| + sum_i |xn wv|) that the oracle returns), fp32
+scores and accumulations add far less, and the output is rounded to bf16
+(2^-8 |y|); together less than
+    |y_gpu - y_ref| <= 2^-6 M + 2^-7 |y_ref|.
+The rms check below (rms error < 2^-7 of the rms output) is what a dropped
+bias or a mis-scaled softmax would fail first.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from channels_last_groupnorm_gb300 import build as gnbuild
+from channels_last_groupnorm_gb300 import gnsilu as gs
+from channels_last_groupnorm_gb300 import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gnbuild.build()
+    gs.lib()
+    yield
+    gu.assert_clean_device()
+
+
+def dev(bits):
+    if bits is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def run(c, residual_in_place=False):
+    wf, bf = gs.attn_fold(dev(c["wv"]), dev(c["bv"]), dev(c["wo"]), dev(c["bo"]))
+    res = dev(c["residual"])
+    out = res if residual_in_place else None
+    y = gs.attention_folded(dev(c["q"]), dev(c["k"]), dev(c["xn"]), wf, bf, residual=res, out=out)
+    assert y is not None, "the CUDA path rejected a supported input"
+    torch.cuda.synchronize()
+    assert gs.gn_device_status(False) == 0
+    return y
+
+
+def check(got, ref, mag, what):
+    err = np.abs(got - ref)
+    bound = 2.0 ** -6 * mag + 2.0 ** -7 * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside the bound; worst err "
+                           f"{err.max():.3e}")
+    rel = np.sqrt(np.mean(err ** 2)) / max(np.sqrt(np.mean(ref ** 2)), 1e-30)
+    assert rel < 2.0 ** -7, f"{what}: rms error {rel:.3e} of the rms output"
+
+
+def oracle_args(c):
+    return (c["q"], c["k"], c["xn"], c["wv"], c["bv"], c["wo"], c["bo"], c["residual"])
+
+
+@pytest.mark.parametrize("S,D,residual", [(256, 512, True), (256, 512, False), (384, 128, True),
+                                          (128, 256, True), (640, 384, False)])
+def test_matches_oracle(S, D, residual):
+    c = wl.make_attn_case(S, D, S + D, residual)
+    y = run(c).float().cpu().numpy().astype(np.float64)
+    ref, mag = oracle.attn().forward(*oracle_args(c), with_mag=True)
+    check(y, ref, mag, f"S={S} D={D} residual={residual}")
+
+
+def test_in_place_on_the_residual():
+    c = wl.make_attn_case(256, 512, 3)
+    ref, mag = oracle.attn().forward(*oracle_args(c), with_mag=True)
+    y = run(c, residual_in_place=True).float().cpu().numpy().astype(np.float64)
+    check(y, ref, mag, "in place")
+
+
+def test_fold_matches_the_weight_product():
+    D = 512
+    c = wl.make_attn_case(128, D, 21)
+    wf, bf = gs.attn_fold(dev(c["wv"]), dev(c["bv"]), dev(c["wo"]), dev(c["bo"]))
+    torch.cuda.synchronize()
+    v = lambda n: wl.bf16_bits_to_f32(c[n]).astype(np.float64).reshape(np.shape(c[n]))  # noqa: E731
+    w_want = v("wo") @ v("wv")
+    b_want = v("wo") @ v("bv") + v("bo")
+    w_abs = np.abs(v("wo")) @ np.abs(v("wv"))
+    b_abs = np.abs(v("wo")) @ np.abs(v("bv")) + np.abs(v("bo"))
+    wg = wf.float().cpu().numpy().astype(np.float64)
+    bg = bf.cpu().numpy().astype(np.float64)
+    # one bf16 rounding (2^-8 relative) after an fp32 sum of D products
+    # (at most D 2^-24 = 2^-15 of the sum of their magnitudes)
+    assert np.all(np.abs(wg - w_want) <= 2.0 ** -8 * np.abs(w_want) + 2.0 ** -14 * w_abs)
+    assert np.all(np.abs(bg - b_want) <= 2.0 ** -14 * b_abs)
+
+
+@pytest.mark.parametrize("name,rows", [("attn_s4096_d512", 48), ("attn_s16384_d512", 24)])
+def test_decoder_shapes_sampled(name, rows):
+    """The FLUX.2 mid-block shapes in full, sampled query rows (first, last,
+    tile edges, random) against the oracle row by row."""
+    w = wl.ATTN_BY_NAME[name]
+    c = wl.make_attn_inputs(w)
+    y = run(c)
+    idx = np.unique(np.concatenate([[0, 1, 127, 128, w.S - 1],
+                                    np.random.default_rng(7).integers(0, w.S, rows)]))
+    got = y[torch.from_numpy(idx).cuda()].float().cpu().numpy().astype(np.float64)
+    ref, mag = oracle.attn().rows(*oracle_args(c), idx, with_mag=True)
+    check(got, ref, mag, name)
+
+
+def test_deterministic():
+    c = wl.make_attn_case(512, 512, 5)
+    a = run(c).cpu()
+    b = run(c).cpu()
+    assert torch.equal(a, b)
+
+
+def test_unsupported_inputs_return_none():
+    q = torch.zeros(256, 512, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(512, 512, dtype=torch.bfloat16, device="cuda")
+    wf, bf = gs.attn_fold(w, q[0], w.clone(), q[1])
+    assert gs.attention_folded(q.float(), q, q, wf, bf) is None                 # fp32
+    q100 = torch.zeros(100, 512, dtype=torch.bfloat16, device="cuda")
+    with pytest.warns(UserWarning):
+        assert gs.attention_folded(q100, q100, q100, wf, bf) is None           # S not a multiple of 128
+    assert gs.attention_folded(q.t(), q, q, wf, bf) is None                    # not contiguous

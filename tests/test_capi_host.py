@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert gs.gn_abi_version() == 4
+    assert gs.gn_abi_version() == 5
     for code in range(13):
         s = gs.status_string(code)
         assert s.startswith("GN_"), (code, s)
@@ -321,3 +321,75 @@ def test_upconv_bindings_return_none_for_cpu_tensors():
     w = torch.zeros(128, 64, 3, 3, dtype=torch.bfloat16)
     assert gs.upconv_fold(w) is None
     assert gs.upsample_conv_nhwc(x, torch.zeros(4, 128, 256, dtype=torch.bfloat16)) is None
+
+
+AQ, AK, AX, AW, AB, AR, AO, AWS = (0x70000000 + i * 0x02000000 for i in range(8))
+
+
+def attn(**kw):
+    a = dict(q=AQ, k=AK, xn=AX, wf=AW, bf=AB, residual=AR, out=AO, S=256, D=512, ws=AWS,
+             ws_bytes=gs.gn_attn_workspace_bytes(256, 512))
+    a.update(kw)
+    return gs.raw_gn_attn_folded(a["q"], a["k"], a["xn"], a["wf"], a["bf"], a["residual"], a["out"], a["S"],
+                                 a["D"], a["ws"], a["ws_bytes"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), gs.GN_ERR_NULL),
+    (dict(k=0), gs.GN_ERR_NULL),
+    (dict(xn=0), gs.GN_ERR_NULL),
+    (dict(wf=0), gs.GN_ERR_NULL),
+    (dict(bf=0), gs.GN_ERR_NULL),
+    (dict(out=0), gs.GN_ERR_NULL),
+    (dict(ws=0), gs.GN_ERR_NULL),
+    (dict(S=0), gs.GN_ERR_SHAPE),
+    (dict(S=100), gs.GN_ERR_SHAPE),
+    (dict(S=65536), gs.GN_ERR_SHAPE),
+    (dict(D=64), gs.GN_ERR_CHANNELS),
+    (dict(D=320), gs.GN_ERR_CHANNELS),
+    (dict(D=2048), gs.GN_ERR_CHANNELS),
+    (dict(q=AQ + 8), gs.GN_ERR_ALIGN),
+    (dict(residual=AR + 8), gs.GN_ERR_ALIGN),
+    (dict(ws=AWS + 16), gs.GN_ERR_ALIGN),
+    (dict(ws_bytes=1024), gs.GN_ERR_WORKSPACE),
+    (dict(out=AQ + 256), gs.GN_ERR_ALIAS),
+    (dict(out=AWS + 1024), gs.GN_ERR_ALIAS),
+    (dict(residual=AO + 256), gs.GN_ERR_ALIAS),
+    (dict(ws=AX), gs.GN_ERR_ALIAS),
+])
+def test_attn_rejects(kw, code):
+    assert attn(**kw) == code
+
+
+def test_attn_workspace_bytes():
+    assert gs.gn_attn_workspace_bytes(256, 512) == 2 * 512 * 256 + 6 * 256 * 256
+    assert gs.gn_attn_workspace_bytes(100, 512) == 0
+    assert gs.gn_attn_workspace_bytes(256, 96) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(wv=0), gs.GN_ERR_NULL),
+    (dict(bf=0), gs.GN_ERR_NULL),
+    (dict(D=100), gs.GN_ERR_CHANNELS),
+    (dict(wf=AW + 8), gs.GN_ERR_ALIGN),
+    (dict(wv=AQ + 1), gs.GN_ERR_ALIGN),
+    (dict(wf=AQ), gs.GN_ERR_ALIAS),
+])
+def test_attn_fold_rejects(kw, code):
+    a = dict(wv=AQ, bv=AK, wo=AX, bo=AR, wf=AW, bf=AB, D=512)
+    a.update(kw)
+    assert gs.raw_gn_attn_fold(a["wv"], a["bv"], a["wo"], a["bo"], a["wf"], a["bf"], a["D"]) == code
+
+
+@no_gpu
+def test_attn_valid_arguments_without_a_device():
+    assert attn() == gs.GN_ERR_DEVICE
+    assert attn(residual=0) == gs.GN_ERR_DEVICE
+    assert attn(residual=AO) == gs.GN_ERR_DEVICE        # in place on the residual
+    assert gs.raw_gn_attn_fold(AQ, AK, AX, AR, AW, AB, 512) == gs.GN_ERR_DEVICE
+
+
+def test_attn_bindings_return_none_for_cpu_tensors():
+    t = torch.zeros(256, 512, dtype=torch.bfloat16)
+    assert gs.attn_fold(torch.zeros(512, 512, dtype=torch.bfloat16), t[0], t[:512].clone(), t[1]) is None
+    assert gs.attention_folded(t, t, t, torch.zeros(512, 512, dtype=torch.bfloat16), torch.zeros(512)) is None
