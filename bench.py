@@ -17,8 +17,9 @@ buffers with the host<->device copies inside the timed region.
 
 ``--workload upconv_*`` measures the fused nearest-2x upsample + 3x3 conv
 of the decoder's up-samplers instead (TFLOP/s against the measured bf16
-tensor peak), ``--workload rga_*`` the residual-gate update; the default
-run adds both to its sweep.
+tensor peak), ``--workload attn_*`` the mid-block attention with the output
+projection folded into V, ``--workload rga_*`` the residual-gate update;
+the default run adds all three to its sweep.
 
 Under torchrun each rank runs its own replica on its own GPU (the
 operation has no cross-GPU exchange); rank 0 prints the line.
@@ -44,6 +45,8 @@ DEFAULT_WORKLOAD = "gn_silu_c512_128x128"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 UPCONV_METRIC = "fused nearest-2x upsample + 3x3 conv, bf16 in/out, fp32 accumulate: us/call and TFLOP/s"
+ATTN_METRIC = ("single-head attention, output projection folded into V, bf16 in/out, fp32 scores and "
+               "accumulation: us/call and TFLOP/s")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh"]
 UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "gn_internal.h"]
@@ -696,6 +699,143 @@ def measure_upconv_e2e(w, steps, device, stream):
             "us_per_call": round(us, 1)}
 
 
+def attn_device_inputs(w, device):
+    import numpy as np
+    import torch
+    from channels_last_groupnorm_gb300 import workloads as wl
+    c = wl.make_attn_inputs(w)
+
+    def dev(bits):
+        if bits is None:
+            return None
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+    return c, {n: dev(c[n]) for n in c}
+
+
+def measure_attn(w, steps, device, stream, peak, torch_context=True):
+    """gn_attn_folded on one mid-block attention workload: the weights are
+    folded once (gn_attn_fold, untimed: per model), then a CUDA graph of
+    `steps` calls is replayed (each call writes and reads 6 S^2 bytes of
+    scores and softmax weights, far more than L2).  TFLOP/s counts the
+    folded evaluation: 2 S D^2 (value rows) + 4 S^2 D (scores, weighted
+    sum)."""
+    import torch
+    import torch.nn.functional as F
+    from channels_last_groupnorm_gb300 import gnsilu as gs
+    _, t = attn_device_inputs(w, device)
+    wf, bf = gs.attn_fold(t["wv"], t["bv"], t["wo"], t["bo"])
+    out = torch.empty_like(t["q"])
+    need = gs.gn_attn_workspace_bytes(w.S, w.D)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    h = stream.cuda_stream
+    rptr = t["residual"].data_ptr() if t["residual"] is not None else 0
+
+    def call(_):
+        rc = gs.raw_gn_attn_folded(t["q"].data_ptr(), t["k"].data_ptr(), t["xn"].data_ptr(), wf.data_ptr(),
+                                   bf.data_ptr(), rptr, out.data_ptr(), w.S, w.D, ws.data_ptr(), need, stream=h)
+        if rc != 0:
+            raise RuntimeError(gs.status_string(rc))
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call(0)
+        torch.cuda.synchronize()
+        per, _ = time_calls(call, 1, max(5, steps // 2), stream)
+        graph = capture_steps(call, 1, steps, stream)
+        graph.replay()
+        elapsed = time_graph(graph, stream)
+        del graph
+    if gs.gn_device_status(False) != 0:
+        raise RuntimeError("a bounded wait expired inside the attention kernels")
+    us = elapsed * 1e6 / steps
+    launch_us = statistics.mean(per) * 1e3
+    r = {"workload": w.name, "us_per_call": round(us, 2), "tflops": round(w.flops / (us * 1e-6) / 1e12, 1),
+         "frac": round(w.flops / (us * 1e-6) / 1e12 / peak, 3), "launch_us_mean": round(launch_us, 2),
+         "tflops_per_call_events": round(w.flops / (launch_us * 1e-6) / 1e12, 1),
+         "kernels_per_call": 4, "workspace_bytes": need, "launch": "cuda-graph"}
+    if torch_context:
+        # context only: the stock block (value projection, SDPA, output projection, residual) in PyTorch
+        def stock(_):
+            v = F.linear(t["xn"], t["wv"], t["bv"])
+            o = F.scaled_dot_product_attention(t["q"][None, None], t["k"][None, None], v[None, None])[0, 0]
+            y = F.linear(o, t["wo"], t["bo"])
+            if t["residual"] is not None:
+                y = y + t["residual"]
+            return y
+        with torch.cuda.stream(stream):
+            stock(0)
+            torch.cuda.synchronize()
+            pt, _ = time_calls(stock, 1, 5, stream)
+        r["torch_linear_sdpa_linear_us"] = round(statistics.median(pt) * 1e3, 1)
+    del ws
+    torch.cuda.empty_cache()
+    return r
+
+
+def attn_cpu_baseline(w, budget_s=10.0):
+    """The fp64 oracle on sampled query rows, in the metric's unit (folded
+    multiply-adds per second): the value projection of all S rows, then the
+    sampled rows' attention."""
+    import numpy as np
+    import oracle
+    from channels_last_groupnorm_gb300 import workloads as wl
+    c = wl.make_attn_inputs(w)
+    orc = oracle.attn()
+    args = (c["q"], c["k"], c["xn"], c["wv"], c["bv"], c["wo"], c["bo"], c["residual"])
+    rows = 4
+    while True:
+        idx = np.random.default_rng(0).integers(0, w.S, rows)
+        t0 = time.perf_counter()
+        orc.rows(*args, idx)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or rows >= w.S:
+            break
+        rows = min(w.S, rows * 4)
+    flops = 2 * w.S * w.D * w.D + rows * 4 * w.S * w.D
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows} query rows of {w.name} (of {w.S}) after the value projection of all rows, fp64, "
+                      f"unfolded; counted at the folded multiply-adds of that work"}
+
+
+def run_attn(args, w, device, rank, world):
+    import torch
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind, sustained = tensor_peak()
+    sampler = ClockSampler(device.index or 0) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    r = measure_attn(w, args.steps, device, stream, peak, torch_context=not args.no_sweep)
+    clocks = sampler.stop() if sampler else None
+    elapsed_s = r["us_per_call"] * 1e-6 * args.steps
+    total_elapsed, total_flops = reduce_timing(elapsed_s, float(w.flops) * args.steps,
+                                               device=device if world > 1 else None)
+    line = {
+        "metric": ATTN_METRIC, "value": round(total_flops / total_elapsed / 1e12, 1), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(r["us_per_call"] / 1e3, 6), "us_per_call": r["us_per_call"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "accumulate": "f32", "data": "synthetic (seeded numpy PCG64; q, k, xn, residual ~N(0,1); "
+        "W, b ~U(-1/sqrt(D), 1/sqrt(D)); bf16)",
+        "config": {**w.describe(), "launch": r["launch"], "workspace_bytes": r["workspace_bytes"],
+                   "flops_per_step": "2 S D^2 + 4 S^2 D (folded value rows, scores, weighted sum)"},
+        "roofline": {"bound": "tensor", "achieved": r["tflops_per_call_events"], "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(r["tflops_per_call_events"] / peak, 4),
+                     "peak_kind": peak_kind, "peak_sustained": sustained, "traffic": None,
+                     "kernel": "whole call: 3 gemm_kernel launches + softmax_rows_kernel (shares in the "
+                               "committed ncu launch list)",
+                     "algorithmic_flops_per_launch": w.flops, "launch_us_mean": r["launch_us_mean"]},
+        "e2e": None, "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    if "torch_linear_sdpa_linear_us" in r:
+        line["context"] = {"torch_linear_sdpa_linear_us": r["torch_linear_sdpa_linear_us"],
+                           "note": "PyTorch's stock block (value Linear, SDPA, output Linear, residual) on the "
+                                   "same tensors and GPU"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = attn_cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import torch
     from channels_last_groupnorm_gb300 import build as gnbuild
@@ -717,6 +857,9 @@ def run_ours(args):
         return
     if args.workload in wl.UPCONV_BY_NAME:
         run_upconv(args, wl.UPCONV_BY_NAME[args.workload], device, rank, world)
+        return
+    if args.workload in wl.ATTN_BY_NAME:
+        run_attn(args, wl.ATTN_BY_NAME[args.workload], device, rank, world)
         return
     w = wl.BY_NAME[args.workload]
     variant_id = {"auto": 0, "two_pass": 1, "fused": 2}[args.variant]
@@ -786,6 +929,8 @@ def run_ours(args):
         tpeak = tensor_peak()[0]
         line["upsample_conv"] = [measure_upconv(uw, 20, device, stream, tpeak)
                                  for uw in wl.UPCONV_WORKLOADS[1:]]
+        line["attention_folded"] = [measure_attn(aw, 10, device, stream, tpeak)
+                                    for aw in wl.ATTN_WORKLOADS[1:]]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -821,6 +966,18 @@ def run_reference(args):
         return
     import oracle
     from channels_last_groupnorm_gb300 import workloads as wl
+    if args.workload in wl.ATTN_BY_NAME:
+        aw = wl.ATTN_BY_NAME[args.workload]
+        attn_cpu_baseline(aw, budget_s=2.0)
+        cb = attn_cpu_baseline(aw, budget_s=min(40.0, 100.0 / max(1, args.steps)))
+        print(json.dumps({
+            "impl": "reference", "metric": ATTN_METRIC, "value": cb["value"], "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": aw.describe(),
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
     if args.workload in wl.UPCONV_BY_NAME:
         uw = wl.UPCONV_BY_NAME[args.workload]
         # warm-up: one untimed sample; then the timed sample sized to ~10 s per step budget

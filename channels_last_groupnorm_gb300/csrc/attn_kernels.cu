@@ -76,7 +76,10 @@ struct GemmLayout {
     static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kConsumed = kAbort + 4;
-    static constexpr uint32_t kBytes = kConsumed + 4;
+    // fp32 epilogue staging: per epilogue warp 32 rows x 32 floats, rows padded to 36
+    static constexpr uint32_t kStaging = (kConsumed + 4 + 15) & ~15u;
+    static constexpr uint32_t kStagingRow = 36;
+    static constexpr uint32_t kBytes = kStaging + 4 * 32 * kStagingRow * 4;
     static constexpr uint32_t kDynamic = kBytes + 1024;
 };
 
@@ -306,6 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (!skip && warp >= 2) {
         const int quad = warp & 3;
         const int row_in_tile = quad * 32 + lane;
+        float *const stage = reinterpret_cast<float *>(gbase + L::kStaging) + (warp - 2) * 32 * L::kStagingRow;
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
@@ -356,9 +360,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
                 if (args.out_f32) {
-                    float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(args.c) + at);
+                    // through shared memory, so that each store instruction of the
+                    // warp writes four whole 128-byte row segments
+                    float4 *mine = reinterpret_cast<float4 *>(stage + lane * L::kStagingRow);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) d4[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+                    for (int k = 0; k < 8; ++k) mine[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+                    __syncwarp();
+                    float *crow = static_cast<float *>(args.c) +
+                                  static_cast<int64_t>(m - row_in_tile + quad * 32) * args.N + n0 + c;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = (lane >> 3) + 4 * i;
+                        const float4 val = reinterpret_cast<const float4 *>(stage + r * L::kStagingRow)[lane & 7];
+                        reinterpret_cast<float4 *>(crow + static_cast<int64_t>(r) * args.N)[lane & 7] = val;
+                    }
+                    __syncwarp();
                 } else {
                     uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.c) + at);
 #pragma unroll
