@@ -28,9 +28,11 @@
 //
 // gemm_kernel is persistent (one CTA per SM): warp 0 issues TMA tile loads
 // (128-byte swizzle) into a STAGES-deep ring, warp 1 owns 2 BN tensor-memory
-// columns and issues tcgen05.mma (M = 128, N = BN, K = 16), warps 2-5 drain
-// the two accumulators alternately (tcgen05.ld, epilogue, 16-byte stores)
-// while the next tile's MMAs run.  Every wait is bounded.
+// columns and issues tcgen05.mma (M = 128, N = BN, K = 16), warps 2-9 (two
+// per tensor-memory lane quarter, each half of the columns) drain the two
+// accumulators alternately (tcgen05.ld, epilogue; fp32 results pass through
+// a shared-memory tile so that each store writes whole 128-byte row
+// segments) while the next tile's MMAs run.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -51,7 +53,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 320;   // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t kSleepNs = 20000;
 
 struct GemmArgs {
@@ -76,10 +78,10 @@ struct GemmLayout {
     static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kConsumed = kAbort + 4;
-    // fp32 epilogue staging: per epilogue warp 32 rows x 32 floats, rows padded to 36
+    // fp32 epilogue staging: per epilogue warp 32 rows x 32 floats (4 KB), the
+    // 16-byte chunks of row r stored at chunk index c ^ (r & 7)
     static constexpr uint32_t kStaging = (kConsumed + 4 + 15) & ~15u;
-    static constexpr uint32_t kStagingRow = 36;
-    static constexpr uint32_t kBytes = kStaging + 4 * 32 * kStagingRow * 4;
+    static constexpr uint32_t kBytes = kStaging + 8 * 32 * 32 * 4;
     static constexpr uint32_t kDynamic = kBytes + 1024;
 };
 
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
-            mbar_init(bar_acc_empty + 8 * b, 4);
+            mbar_init(bar_acc_empty + 8 * b, 8);   // one arrival per epilogue warp
         }
         mbar_init(bar_drain, 1);
         *abort = (*reinterpret_cast<volatile unsigned int *>(&g_at_status) != 0u) ? 1 : 0;
@@ -307,9 +309,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         umma_commit(bar_drain);
     } else if (!skip && warp >= 2) {
+        // two warps per tensor-memory lane quarter, each draining half the columns
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row_in_tile = quad * 32 + lane;
-        float *const stage = reinterpret_cast<float *>(gbase + L::kStaging) + (warp - 2) * 32 * L::kStagingRow;
+        float4 *const stage = reinterpret_cast<float4 *>(gbase + L::kStaging) + (warp - 2) * 32 * 8;
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
@@ -322,11 +326,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
                 tmem_wait_ld();
-                if (c + 32 == BN) {
+                if (c + 32 == (half + 1) * (BN / 2)) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
@@ -362,16 +366,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (args.out_f32) {
                     // through shared memory, so that each store instruction of the
                     // warp writes four whole 128-byte row segments
-                    float4 *mine = reinterpret_cast<float4 *>(stage + lane * L::kStagingRow);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) mine[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+                    for (int k = 0; k < 8; ++k)
+                        stage[lane * 8 + (k ^ (lane & 7))] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
                     __syncwarp();
                     float *crow = static_cast<float *>(args.c) +
                                   static_cast<int64_t>(m - row_in_tile + quad * 32) * args.N + n0 + c;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int r = (lane >> 3) + 4 * i;
-                        const float4 val = reinterpret_cast<const float4 *>(stage + r * L::kStagingRow)[lane & 7];
+                        const float4 val = stage[r * 8 + ((lane & 7) ^ (r & 7))];
                         reinterpret_cast<float4 *>(crow + static_cast<int64_t>(r) * args.N)[lane & 7] = val;
                     }
                     __syncwarp();
