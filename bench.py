@@ -50,6 +50,7 @@ ATTN_METRIC = ("single-head attention, output projection folded into V, bf16 in/
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh"]
 UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "gn_internal.h"]
+ATTN_SOURCES = ["attn_kernels.cu", "tc_ptx.cuh", "gn_internal.h"]
 
 
 # ---------------------------------------------------------------------------
@@ -820,9 +821,10 @@ def run_attn(args, w, device, rank, world):
                    "flops_per_step": "2 S D^2 + 4 S^2 D (folded value rows, scores, weighted sum)"},
         "roofline": {"bound": "tensor", "achieved": r["tflops_per_call_events"], "peak": peak,
                      "unit": "TFLOP/s", "frac": round(r["tflops_per_call_events"] / peak, 4),
-                     "peak_kind": peak_kind, "peak_sustained": sustained, "traffic": None,
+                     "peak_kind": peak_kind, "peak_sustained": sustained,
+                     "traffic": recorded_traffic(w.name, "attn", ATTN_SOURCES),
                      "kernel": "whole call: 3 gemm_kernel launches + softmax_rows_kernel (shares in the "
-                               "committed ncu launch list)",
+                               "committed ncu launch list); traffic = DRAM bytes of the four per call",
                      "algorithmic_flops_per_launch": w.flops, "launch_us_mean": r["launch_us_mean"]},
         "e2e": None, "gpu_launches": 4 * args.steps, "clocks": clocks,
     }
