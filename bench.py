@@ -48,9 +48,9 @@ UPCONV_METRIC = "fused nearest-2x upsample + 3x3 conv, bf16 in/out, fp32 accumul
 ATTN_METRIC = ("single-head attention, output projection folded into V, bf16 in/out, fp32 scores and "
                "accumulation: us/call and TFLOP/s")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh"]
-UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "gn_internal.h"]
-ATTN_SOURCES = ["attn_kernels.cu", "tc_ptx.cuh", "gn_internal.h"]
+KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh", "capi_util.h", "rga_kernels.cu"]
+UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
+ATTN_SOURCES = ["attn_kernels.cu", "tc_ptx.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
 
 
 # ---------------------------------------------------------------------------
@@ -716,8 +716,8 @@ def attn_device_inputs(w, device):
 def measure_attn(w, steps, device, stream, peak, torch_context=True):
     """gn_attn_folded on one mid-block attention workload: the weights are
     folded once (gn_attn_fold, untimed: per model), then a CUDA graph of
-    `steps` calls is replayed (each call writes and reads 6 S^2 bytes of
-    scores and softmax weights, far more than L2).  TFLOP/s counts the
+    `steps` calls is replayed (each call writes and reads the 2 S^2 bytes of
+    softmax weights, more than L2 at S = 16384).  TFLOP/s counts the
     folded evaluation: 2 S D^2 (value rows) + 4 S^2 D (scores, weighted
     sum)."""
     import torch
@@ -753,7 +753,7 @@ def measure_attn(w, steps, device, stream, peak, torch_context=True):
     r = {"workload": w.name, "us_per_call": round(us, 2), "tflops": round(w.flops / (us * 1e-6) / 1e12, 1),
          "frac": round(w.flops / (us * 1e-6) / 1e12 / peak, 3), "launch_us_mean": round(launch_us, 2),
          "tflops_per_call_events": round(w.flops / (launch_us * 1e-6) / 1e12, 1),
-         "kernels_per_call": 4, "workspace_bytes": need, "launch": "cuda-graph"}
+         "kernels_per_call": 5, "workspace_bytes": need, "launch": "cuda-graph"}
     if torch_context:
         # context only: the stock block (value projection, SDPA, output projection, residual) in PyTorch
         def stock(_):
@@ -823,10 +823,10 @@ def run_attn(args, w, device, rank, world):
                      "unit": "TFLOP/s", "frac": round(r["tflops_per_call_events"] / peak, 4),
                      "peak_kind": peak_kind, "peak_sustained": sustained,
                      "traffic": recorded_traffic(w.name, "attn", ATTN_SOURCES),
-                     "kernel": "whole call: 3 gemm_kernel launches + softmax_rows_kernel (shares in the "
-                               "committed ncu launch list); traffic = DRAM bytes of the four per call",
+                     "kernel": "whole call: 4 gemm_kernel launches + softmax_stats_kernel (shares in the "
+                               "committed ncu launch list); traffic = DRAM bytes of the five per call",
                      "algorithmic_flops_per_launch": w.flops, "launch_us_mean": r["launch_us_mean"]},
-        "e2e": None, "gpu_launches": 4 * args.steps, "clocks": clocks,
+        "e2e": None, "gpu_launches": 5 * args.steps, "clocks": clocks,
     }
     if "torch_linear_sdpa_linear_us" in r:
         line["context"] = {"torch_linear_sdpa_linear_us": r["torch_linear_sdpa_linear_us"],

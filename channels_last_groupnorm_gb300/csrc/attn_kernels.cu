@@ -15,16 +15,19 @@
 //                      (fp32), once per weight;
 //   gemm_kernel        C = alpha A B^T (+ a per-row or per-column bias, + a
 //                      bf16 residual), A [M][K] and B [N][K] bf16 K-major,
-//                      fp32 accumulation in tensor memory, fp32 or bf16 out;
-//                      run three times: V'^T = W' xn^T + b' ([D][S], bf16),
-//                      the scores q k^T / sqrt(D) ([S][S], fp32), and
+//                      fp32 accumulation in tensor memory; its epilogue can
+//                      instead reduce each row segment of alpha A B^T to a
+//                      softmax (max, sum of exp) record, or write the softmax
+//                      weights exp(alpha A B^T - max) / sum as bf16.  Run four
+//                      times: V'^T = W' xn^T + b' ([D][S], bf16); the scores
+//                      q k^T / sqrt(D) reduced to per-row-segment records;
+//                      the scores again, written as P ([S][S], bf16); and
 //                      out = P V' + residual ([S][D], bf16);
-//   softmax_rows_kernel  P = softmax of each score row, rounded to bf16.
-// The scores are materialised: for D = 512 an fp32 128 x 512 output block
-// alone fills the 512 tensor-memory columns of an SM, so a single-pass
-// (flash) kernel would need its output split across CTAs and the scores
-// computed twice; the three GEMMs run at tensor-core rate and the softmax
-// at HBM rate instead.
+//   softmax_stats_kernel  merges each row's records into (max, 1 / sum).
+// The fp32 scores are never stored: computing them twice costs 2 S^2 D
+// tensor-core flops, far cheaper than writing and re-reading 4 S^2 bytes.
+// (A single-pass, flash-style kernel does not fit D = 512 well: an fp32
+// 128 x 512 output block alone fills the 512 tensor-memory columns of an SM.)
 //
 // gemm_kernel is persistent (one CTA per SM): warp 0 issues TMA tile loads
 // (128-byte swizzle) into a STAGES-deep ring, warp 1 owns 2 BN tensor-memory
@@ -40,7 +43,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "gn_internal.h"
+#include "tc_internal.h"
 #include "gn_ptx.cuh"
 #include "tc_ptx.cuh"
 
@@ -65,8 +68,19 @@ struct GemmArgs {
     const __nv_bfloat16 *residual;  // [M][N] bf16 or null
     void *c;                        // [M][N] fp32 or bf16
     int out_f32;
+    int mode;                       // kGemmPlain, kGemmRowStats or kGemmSoftmax
+    float2 *stats;                  // kGemmRowStats: [M][2 n_tiles] (max, sum of exp) per row segment
+    const float2 *row_ml;           // kGemmSoftmax: [M] (row max, 1 / row sum of exp)
     uint64_t timeout_ns;
 };
+
+// Epilogue modes: the plain product (+ bias, + residual); per-row softmax
+// statistics of alpha A B^T over each half tile (nothing else is written);
+// the softmax weights exp(alpha A B^T - max) / sum, rounded to bf16.
+constexpr int kGemmPlain = 0;
+constexpr int kGemmRowStats = 1;
+constexpr int kGemmSoftmax = 2;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int BN, int STAGES>
 struct GemmLayout {
@@ -143,72 +157,32 @@ __global__ void __launch_bounds__(256) attn_fold_kernel(const __nv_bfloat16 *__r
 }
 
 // ---------------------------------------------------------------------------
-// P[r][j] = exp(s[r][j] - max_j s[r][.]) / sum_j exp(...), rounded to bf16;
-// one CTA per row, the row staged once in shared memory.
+// Row softmax statistics: merge a row's `parts` (max, sum of exp) segment
+// records into (max, 1 / sum), one warp per row, in a fixed order.
 // ---------------------------------------------------------------------------
-constexpr int kSoftmaxThreads = 512;
-
-__global__ void __launch_bounds__(kSoftmaxThreads) softmax_rows_kernel(const float *__restrict__ s,
-                                                                       __nv_bfloat16 *__restrict__ p, int S)
+__device__ __forceinline__ float2 merge_ml(float2 a, float2 b)
 {
-    extern __shared__ float4 row4[];
-    __shared__ float red[kSoftmaxThreads / 32];
-    __shared__ float bcast;
-    const int r = blockIdx.x;
-    const float4 *src = reinterpret_cast<const float4 *>(s + static_cast<int64_t>(r) * S);
-    const int n4 = S / 4;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float m = fmaxf(a.x, b.x);
+    if (m == -INFINITY) return make_float2(m, 0.f);
+    return make_float2(m, a.y * exp2f((a.x - m) * kLog2e) + b.y * exp2f((b.x - m) * kLog2e));
+}
 
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < n4; i += kSoftmaxThreads) {
-        const float4 v = __ldcs(src + i);
-        row4[i] = v;
-        mx = fmaxf(fmaxf(mx, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
-    }
+__global__ void __launch_bounds__(256) softmax_stats_kernel(const float2 *__restrict__ parts_in, int parts,
+                                                            float2 *__restrict__ row_ml, int rows)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const float2 *p = parts_in + static_cast<int64_t>(warp) * parts;
+    float2 acc = make_float2(-INFINITY, 0.f);
+    for (int i = lane; i < parts; i += 32) acc = merge_ml(acc, p[i]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    if (warp == 0) {
-        float v = lane < kSoftmaxThreads / 32 ? red[lane] : -INFINITY;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (lane == 0) bcast = v;
+    for (int o = 16; o > 0; o >>= 1) {
+        float2 other;
+        other.x = __shfl_xor_sync(0xffffffffu, acc.x, o);
+        other.y = __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc = merge_ml(acc, other);
     }
-    __syncthreads();
-    const float m = bcast;
-    constexpr float kLog2e = 1.4426950408889634f;
-    const float mb = m * kLog2e;
-    float sum = 0.f;
-    for (int i = threadIdx.x; i < n4; i += kSoftmaxThreads) {
-        float4 v = row4[i];
-        v.x = exp2f(fmaf(v.x, kLog2e, -mb));
-        v.y = exp2f(fmaf(v.y, kLog2e, -mb));
-        v.z = exp2f(fmaf(v.z, kLog2e, -mb));
-        v.w = exp2f(fmaf(v.w, kLog2e, -mb));
-        row4[i] = v;
-        sum += (v.x + v.y) + (v.z + v.w);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = sum;
-    __syncthreads();
-    if (warp == 0) {
-        float v = lane < kSoftmaxThreads / 32 ? red[lane] : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) bcast = 1.0f / v;
-    }
-    __syncthreads();
-    const float inv = bcast;
-    uint2 *dst = reinterpret_cast<uint2 *>(p + static_cast<int64_t>(r) * S);
-    for (int i = threadIdx.x; i < n4; i += kSoftmaxThreads) {
-        const float4 v = row4[i];
-        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x * inv, v.y * inv);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(v.z * inv, v.w * inv);
-        dst[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
-    }
+    if (lane == 0) row_ml[warp] = make_float2(acc.x, 1.0f / acc.y);
 }
 
 // ---------------------------------------------------------------------------
@@ -323,6 +297,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int m = (t / args.n_tiles) * kBM + row_in_tile;
             const int n0 = (t % args.n_tiles) * BN;
             const float bm = args.bias_m ? args.bias_m[m] : 0.f;
+            float run_m = -INFINITY, run_l = 0.f;   // kGemmRowStats: this row segment's running max / sum
+            float2 ml = make_float2(0.f, 0.f);
+            if (args.mode == kGemmSoftmax) ml = args.row_ml[m];
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
 #pragma unroll 1
@@ -338,6 +315,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int k = 0; k < 32; ++k) f[k] = fmaf(__uint_as_float(v[k]), args.alpha, bm);
+                if (args.mode == kGemmRowStats) {
+                    float cmax = f[0];
+#pragma unroll
+                    for (int k = 1; k < 32; ++k) cmax = fmaxf(cmax, f[k]);
+                    const float m_new = fmaxf(run_m, cmax);
+                    const float mb = m_new * kLog2e;
+                    float acc = run_l * exp2f(fmaf(run_m, kLog2e, -mb));
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc += exp2f(fmaf(f[k], kLog2e, -mb));
+                    run_l = acc;
+                    run_m = m_new;
+                    continue;
+                }
+                if (args.mode == kGemmSoftmax) {
+                    const float mb = ml.x * kLog2e;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) f[k] = exp2f(fmaf(f[k], kLog2e, -mb)) * ml.y;
+                }
                 if (args.bias_n) {
                     const float4 *b4 = reinterpret_cast<const float4 *>(args.bias_n + n0 + c);
 #pragma unroll
@@ -380,7 +375,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     __syncwarp();
                 } else {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.c) + at);
+                    // bf16: the same staging, 64 bytes per row; each store
+                    // instruction writes eight whole 64-byte row segments
+                    uint4 *stage4 = reinterpret_cast<uint4 *>(stage);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint32_t o[4];
@@ -389,10 +386,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             const __nv_bfloat162 hb = __floats2bfloat162_rn(f[8 * k + 2 * h], f[8 * k + 2 * h + 1]);
                             o[h] = *reinterpret_cast<const uint32_t *>(&hb);
                         }
-                        d4[k] = make_uint4(o[0], o[1], o[2], o[3]);
+                        stage4[lane * 4 + (k ^ (lane & 3))] = make_uint4(o[0], o[1], o[2], o[3]);
                     }
+                    __syncwarp();
+                    __nv_bfloat16 *crow = static_cast<__nv_bfloat16 *>(args.c) +
+                                          static_cast<int64_t>(m - row_in_tile + quad * 32) * args.N + n0 + c;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = (lane >> 2) + 8 * i;
+                        const uint4 val = stage4[r * 4 + ((lane & 3) ^ (r & 3))];
+                        reinterpret_cast<uint4 *>(crow + static_cast<int64_t>(r) * args.N)[lane & 3] = val;
+                    }
+                    __syncwarp();
                 }
             }
+            if (args.mode == kGemmRowStats)
+                args.stats[static_cast<int64_t>(m) * (2 * args.n_tiles) + 2 * (t % args.n_tiles) + half] =
+                    make_float2(run_m, run_l);
         }
     }
 
@@ -469,14 +479,17 @@ cudaError_t launch_gemm_variant(const CUtensorMap &ma, const CUtensorMap &mb, co
     return cudaGetLastError();
 }
 
-// C[M][N] = alpha A[M][K] B[N][K]^T (+ bias_m[M], + bias_n[N], + residual)
+int gemm_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
+
+// C[M][N] = alpha A[M][K] B[N][K]^T (+ bias_m[M], + bias_n[N], + residual),
+// or the softmax statistics / weights of alpha A B^T (mode)
 int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float alpha, const float *bias_m,
-             const float *bias_n, const void *residual, bool out_f32, int sm_count, uint64_t timeout_ns,
-             cudaStream_t s, cudaError_t *err)
+             const float *bias_n, const void *residual, bool out_f32, int mode, float2 *stats,
+             const float2 *row_ml, int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return 2;
-    const int BN = (N % 256 == 0) ? 256 : 128;
+    const int BN = gemm_bn(N);
     CUtensorMap ma, mb;
     if (!encode_kmajor(enc, &ma, A, M, K, kBM) || !encode_kmajor(enc, &mb, B, N, K, BN)) return 2;
     GemmArgs a;
@@ -492,6 +505,9 @@ int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float a
     a.residual = static_cast<const __nv_bfloat16 *>(residual);
     a.c = C;
     a.out_f32 = out_f32 ? 1 : 0;
+    a.mode = mode;
+    a.stats = stats;
+    a.row_ml = row_ml;
     a.timeout_ns = timeout_ns;
     *err = (BN == 256) ? launch_gemm_variant<256, 4>(ma, mb, a, sm_count, s)
                        : launch_gemm_variant<128, 6>(ma, mb, a, sm_count, s);
@@ -514,50 +530,67 @@ cudaError_t launch_attn_fold(const void *wv, const void *bv, const void *wo, con
     return cudaGetLastError();
 }
 
-size_t attn_workspace_bytes(int64_t S, int64_t D)
+namespace {
+
+size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// workspace: V'^T [D][S] bf16 | segment statistics [S][2 S/128] float2 (room
+// for the 128-wide tiles) | row (max, 1/sum) [S] float2 | P [S][S] bf16
+struct AttnWorkspace {
+    size_t vt, stats, row_ml, p, total;
+};
+
+AttnWorkspace attn_layout(int64_t S, int64_t D)
 {
-    // V'^T [D][S] bf16 | scores [S][S] fp32 | P [S][S] bf16, each 256-byte aligned
-    const auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
-    return up(static_cast<size_t>(2 * D * S)) + up(static_cast<size_t>(4 * S * S)) + up(static_cast<size_t>(2 * S * S));
+    AttnWorkspace w;
+    w.vt = 0;
+    w.stats = w.vt + up256(static_cast<size_t>(2 * D * S));
+    w.row_ml = w.stats + up256(static_cast<size_t>(8 * S * 2 * (S / 128)));
+    w.p = w.row_ml + up256(static_cast<size_t>(8 * S));
+    w.total = w.p + up256(static_cast<size_t>(2 * S * S));
+    return w;
 }
+
+}  // namespace
+
+size_t attn_workspace_bytes(int64_t S, int64_t D) { return attn_layout(S, D).total; }
 
 int launch_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
                        const void *residual, void *out, int S, int D, void *workspace, int sm_count,
                        uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches)
 {
-    const auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    const AttnWorkspace lay = attn_layout(S, D);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    void *vt = ws;                                                        // [D][S] bf16
-    float *scores = reinterpret_cast<float *>(ws + up(static_cast<size_t>(2) * D * S));   // [S][S] fp32
-    void *p = ws + up(static_cast<size_t>(2) * D * S) + up(static_cast<size_t>(4) * S * S);  // [S][S] bf16
+    void *vt = ws + lay.vt;
+    float2 *stats = reinterpret_cast<float2 *>(ws + lay.stats);
+    float2 *row_ml = reinterpret_cast<float2 *>(ws + lay.row_ml);
+    void *p = ws + lay.p;
+    const float scale = 1.0f / sqrtf(static_cast<float>(D));
     *launches = 0;
     // V'^T = W' xn^T + b' (b' per row of V'^T)
-    int r = run_gemm(wf, xn, vt, D, S, D, 1.0f, bf, nullptr, nullptr, false, sm_count, timeout_ns, s, err);
+    int r = run_gemm(wf, xn, vt, D, S, D, 1.0f, bf, nullptr, nullptr, false, kGemmPlain, nullptr, nullptr,
+                     sm_count, timeout_ns, s, err);
     if (r) return r;
     ++*launches;
-    // scores = q k^T / sqrt(D)
-    r = run_gemm(q, k, scores, S, S, D, 1.0f / sqrtf(static_cast<float>(D)), nullptr, nullptr, nullptr, true,
+    // pass 1 over the scores q k^T / sqrt(D): per-row (max, sum of exp) of each half tile
+    r = run_gemm(q, k, nullptr, S, S, D, scale, nullptr, nullptr, nullptr, false, kGemmRowStats, stats, nullptr,
                  sm_count, timeout_ns, s, err);
     if (r) return r;
     ++*launches;
-    // P = softmax(scores) row by row (the row is staged in up to 128 KB of shared memory)
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(softmax_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    4 * kAttnMaxS);
-    });
-    if (attr != cudaSuccess) {
-        *err = attr;
-        return 3;
-    }
-    softmax_rows_kernel<<<S, kSoftmaxThreads, static_cast<size_t>(4) * S, s>>>(scores,
-                                                                              static_cast<__nv_bfloat16 *>(p), S);
+    // the rows' (max, 1 / sum)
+    const int parts = 2 * (S / gemm_bn(S));
+    softmax_stats_kernel<<<(S + 7) / 8, 256, 0, s>>>(stats, parts, row_ml, S);
     *err = cudaGetLastError();
     if (*err != cudaSuccess) return 3;
     ++*launches;
+    // pass 2: the scores again, written as softmax weights P (bf16)
+    r = run_gemm(q, k, p, S, S, D, scale, nullptr, nullptr, nullptr, false, kGemmSoftmax, nullptr, row_ml,
+                 sm_count, timeout_ns, s, err);
+    if (r) return r;
+    ++*launches;
     // out = P V' + residual
-    r = run_gemm(p, vt, out, S, D, S, 1.0f, nullptr, nullptr, residual, false, sm_count, timeout_ns, s, err);
+    r = run_gemm(p, vt, out, S, D, S, 1.0f, nullptr, nullptr, residual, false, kGemmPlain, nullptr, nullptr,
+                 sm_count, timeout_ns, s, err);
     if (r) return r;
     ++*launches;
     return 0;

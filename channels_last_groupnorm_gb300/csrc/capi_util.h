@@ -1,0 +1,28 @@
+// capi_util.h -- what the two C-ABI translation units share: the current
+// device (checked to be an sm_103 part, kernel attributes set once), the
+// bound on every in-kernel wait, the overlap test used by the aliasing
+// checks, and the library-wide kernel-launch counter.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace gn_capi {
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;      // max dynamic shared memory per block
+    int smem_per_sm = 0;
+    int coop = 0;
+    int major = 0, minor = 0;
+};
+
+// GN_OK with the device's properties, or GN_ERR_DEVICE / GN_ERR_CUDA.
+int current_device(int *dev_out, DeviceInfo *info_out);
+// Timeout of every bounded wait inside the kernels (GN_WAIT_TIMEOUT_MS, default 2000).
+uint64_t wait_timeout_ns();
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb);
+void count_launches(uint64_t n);
+
+}  // namespace gn_capi

@@ -17,24 +17,29 @@
 #include <utility>
 
 #include "../../include/gnsilu.h"
+#include "capi_util.h"
 #include "gn_internal.h"
+#include "tc_internal.h"
+
+namespace gn_capi {
+
+std::atomic<uint64_t> g_launches{0};
+
+void count_launches(uint64_t n) { g_launches.fetch_add(n); }
+
+}  // namespace gn_capi
 
 namespace {
 
 using gn::Args;
 using gn::Geom;
+using gn_capi::DeviceInfo;
+using gn_capi::g_launches;
+using gn_capi::current_device;
+using gn_capi::ranges_overlap;
+using gn_capi::wait_timeout_ns;
 
-std::atomic<uint64_t> g_launches{0};
 std::mutex g_mu;
-
-struct DeviceInfo {
-    bool ready = false;
-    int sm_count = 0;
-    int smem_optin = 0;      // max dynamic shared memory per block
-    int smem_per_sm = 0;
-    int coop = 0;
-    int major = 0, minor = 0;
-};
 std::map<int, DeviceInfo> g_devices;
 
 struct Workspace {
@@ -52,12 +57,6 @@ uint64_t env_u64(const char *name, uint64_t dflt)
     return (end && *end == '\0') ? static_cast<uint64_t>(r) : dflt;
 }
 
-// Timeout of every bounded wait inside the kernels.
-uint64_t wait_timeout_ns()
-{
-    static const uint64_t t = env_u64("GN_WAIT_TIMEOUT_MS", 2000) * 1000000ull;
-    return t;
-}
 
 // L2 eviction hints of the bulk copies (bit meanings in gn_internal.h).
 uint32_t l2_hints()
@@ -66,11 +65,6 @@ uint32_t l2_hints()
     return h;
 }
 
-bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
-{
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + nb && b0 < a0 + na;
-}
 
 // Channel counts an entry point serves: the power-of-two entries take the
 // page's contract (C a power of two in [8, 2048]); the general entries take
@@ -114,37 +108,6 @@ int validate(const void *x, const float *gamma, const float *beta, const void *y
     return GN_OK;
 }
 
-// Current device, checked to be an sm_103 part; kernel attributes set once.
-int current_device(int *dev_out, DeviceInfo *info_out)
-{
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GN_ERR_DEVICE;
-    }
-    std::lock_guard<std::mutex> lock(g_mu);
-    DeviceInfo &d = g_devices[dev];
-    if (!d.ready) {
-        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) ||
-            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) ||
-            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) ||
-            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ||
-            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ||
-            cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev)) {
-            cudaGetLastError();
-            return GN_ERR_DEVICE;
-        }
-        if (d.major != 10 || d.minor != 3) return GN_ERR_DEVICE;
-        if (gn::prepare_kernels(static_cast<uint32_t>(d.smem_optin)) != cudaSuccess) {
-            cudaGetLastError();
-            return GN_ERR_CUDA;
-        }
-        d.ready = true;
-    }
-    *dev_out = dev;
-    *info_out = d;
-    return GN_OK;
-}
 
 struct Plan {
     Geom g{};
@@ -366,6 +329,55 @@ int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N
 
 }  // namespace
 
+namespace gn_capi {
+
+// Timeout of every bounded wait inside the kernels.
+uint64_t wait_timeout_ns()
+{
+    static const uint64_t t = env_u64("GN_WAIT_TIMEOUT_MS", 2000) * 1000000ull;
+    return t;
+}
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Current device, checked to be an sm_103 part; kernel attributes set once.
+int current_device(int *dev_out, DeviceInfo *info_out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ||
+            cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev)) {
+            cudaGetLastError();
+            return GN_ERR_DEVICE;
+        }
+        if (d.major != 10 || d.minor != 3) return GN_ERR_DEVICE;
+        if (gn::prepare_kernels(static_cast<uint32_t>(d.smem_optin)) != cudaSuccess) {
+            cudaGetLastError();
+            return GN_ERR_CUDA;
+        }
+        d.ready = true;
+    }
+    *dev_out = dev;
+    *info_out = d;
+    return GN_OK;
+}
+
+}  // namespace gn_capi
+
 extern "C" {
 
 int gn_silu_rows_ex(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16, int64_t N,
@@ -536,165 +548,6 @@ int gn_residual_gate_add(const void *residual, const void *update, const void *g
         return GN_ERR_CUDA;
     }
     g_launches.fetch_add(1);
-    return GN_OK;
-}
-
-// ---- fused nearest-2x upsample + 3x3 convolution ----------------------------
-int64_t gn_upconv_folded_bytes(int64_t Cin, int64_t Cout)
-{
-    if (Cin < 1 || Cout < 1 || Cin > (1 << 20) || Cout > (1 << 20)) return -1;
-    return 16 * Cin * Cout * 2;
-}
-
-namespace {
-
-int upconv_channels_ok(int64_t Cin, int64_t Cout)
-{
-    return Cin >= 64 && Cin <= 8192 && Cin % 64 == 0 && Cout >= 128 && Cout <= 8192 && Cout % 128 == 0;
-}
-
-}  // namespace
-
-int gn_upconv_fold(const void *w, void *wf, int64_t Cin, int64_t Cout, void *stream)
-{
-    if (!w || !wf) return GN_ERR_NULL;
-    if (!upconv_channels_ok(Cin, Cout)) return GN_ERR_CHANNELS;
-    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
-    if (addr(w) % 2 || addr(wf) % 16) return GN_ERR_ALIGN;
-    if (ranges_overlap(w, static_cast<size_t>(9 * Cin * Cout * 2), wf,
-                       static_cast<size_t>(gn_upconv_folded_bytes(Cin, Cout))))
-        return GN_ERR_ALIAS;
-    int dev = -1;
-    DeviceInfo d;
-    const int rc = current_device(&dev, &d);
-    if (rc != GN_OK) return rc;
-    const cudaError_t e = gn::launch_upconv_fold(w, wf, static_cast<int>(Cin), static_cast<int>(Cout), d.sm_count,
-                                                 static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return GN_ERR_CUDA;
-    }
-    g_launches.fetch_add(1);
-    return GN_OK;
-}
-
-int gn_upconv_nhwc(const void *x, const void *wf, const void *bias, void *y, int64_t N, int64_t H, int64_t W,
-                   int64_t Cin, int64_t Cout, void *stream)
-{
-    if (!x || !wf || !y) return GN_ERR_NULL;
-    if (N < 0 || H < 1 || W < 1 || H > (1 << 20) || W > (1 << 20)) return GN_ERR_SHAPE;
-    if (!upconv_channels_ok(Cin, Cout)) return GN_ERR_CHANNELS;
-    if (N > 0 && (N > (1 << 20) || N * H * W > INT64_MAX / (4 * 2 * std::max(Cin, Cout)))) return GN_ERR_SHAPE;
-    gn::UpconvTiling t;
-    if (N > 0 && !gn::upconv_tiling(N, H, W, &t)) return GN_ERR_SHAPE;
-    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
-    if (addr(x) % 16 || addr(wf) % 16 || addr(y) % 16 || (bias && addr(bias) % 4)) return GN_ERR_ALIGN;
-    const size_t xb = static_cast<size_t>(N * H * W * Cin * 2);
-    const size_t yb = static_cast<size_t>(N * 4 * H * W * Cout * 2);
-    if (ranges_overlap(y, yb, x, xb) || ranges_overlap(y, yb, wf, static_cast<size_t>(gn_upconv_folded_bytes(Cin, Cout))) ||
-        (bias && ranges_overlap(y, yb, bias, static_cast<size_t>(2 * Cout))))
-        return GN_ERR_ALIAS;
-    int dev = -1;
-    DeviceInfo d;
-    const int rc = current_device(&dev, &d);
-    if (rc != GN_OK) return rc;
-    if (N == 0) return GN_OK;
-    cudaError_t e = cudaSuccess;
-    const int r = gn::launch_upconv(x, wf, bias, y, static_cast<int>(N), static_cast<int>(H), static_cast<int>(W),
-                                    static_cast<int>(Cin), static_cast<int>(Cout), d.sm_count, wait_timeout_ns(),
-                                    static_cast<cudaStream_t>(stream), &e);
-    if (r == 1) return GN_ERR_SHAPE;
-    if (r != 0) {
-        cudaGetLastError();
-        return GN_ERR_CUDA;
-    }
-    g_launches.fetch_add(1);
-    return GN_OK;
-}
-
-// ---- single-head attention with the output projection folded into V --------
-namespace {
-
-bool attn_width_ok(int64_t D) { return D >= 128 && D <= 1024 && D % 128 == 0; }
-
-bool attn_tokens_ok(int64_t S) { return S >= 128 && S <= gn::kAttnMaxS && S % 128 == 0; }
-
-}  // namespace
-
-int gn_attn_fold(const void *wv, const void *bv, const void *wo, const void *bo, void *wf, float *bf, int64_t D,
-                 void *stream)
-{
-    if (!wv || !bv || !wo || !bo || !wf || !bf) return GN_ERR_NULL;
-    if (!attn_width_ok(D)) return GN_ERR_CHANNELS;
-    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
-    if (addr(wv) % 2 || addr(bv) % 2 || addr(wo) % 2 || addr(bo) % 2 || addr(wf) % 16 || addr(bf) % 16)
-        return GN_ERR_ALIGN;
-    const size_t wb = static_cast<size_t>(2 * D * D), bb = static_cast<size_t>(4 * D);
-    for (const void *in : {wv, wo})
-        if (ranges_overlap(wf, wb, in, wb) || ranges_overlap(bf, bb, in, wb)) return GN_ERR_ALIAS;
-    for (const void *in : {bv, bo})
-        if (ranges_overlap(wf, wb, in, static_cast<size_t>(2 * D)) ||
-            ranges_overlap(bf, bb, in, static_cast<size_t>(2 * D)))
-            return GN_ERR_ALIAS;
-    if (ranges_overlap(wf, wb, bf, bb)) return GN_ERR_ALIAS;
-    int dev = -1;
-    DeviceInfo d;
-    const int rc = current_device(&dev, &d);
-    if (rc != GN_OK) return rc;
-    const cudaError_t e = gn::launch_attn_fold(wv, bv, wo, bo, wf, bf, static_cast<int>(D), d.sm_count,
-                                               static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return GN_ERR_CUDA;
-    }
-    g_launches.fetch_add(1);
-    return GN_OK;
-}
-
-size_t gn_attn_workspace_bytes(int64_t S, int64_t D)
-{
-    if (!attn_tokens_ok(S) || !attn_width_ok(D)) return 0;
-    return gn::attn_workspace_bytes(S, D);
-}
-
-int gn_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
-                   const void *residual, void *out, int64_t S, int64_t D, void *workspace, size_t workspace_bytes,
-                   void *stream)
-{
-    if (!q || !k || !xn || !wf || !bf || !out || !workspace) return GN_ERR_NULL;
-    if (!attn_tokens_ok(S)) return GN_ERR_SHAPE;
-    if (!attn_width_ok(D)) return GN_ERR_CHANNELS;
-    const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
-    if (addr(q) % 16 || addr(k) % 16 || addr(xn) % 16 || addr(wf) % 16 || addr(bf) % 16 || addr(out) % 16 ||
-        addr(workspace) % 256 || (residual && addr(residual) % 16))
-        return GN_ERR_ALIGN;
-    const size_t need = gn::attn_workspace_bytes(S, D);
-    if (workspace_bytes < need) return GN_ERR_WORKSPACE;
-    const size_t act = static_cast<size_t>(2 * S * D);
-    const struct {
-        const void *p;
-        size_t n;
-    } ins[] = {{q, act}, {k, act}, {xn, act}, {wf, static_cast<size_t>(2 * D * D)}, {bf, static_cast<size_t>(4 * D)}};
-    for (const auto &in : ins)
-        if (ranges_overlap(out, act, in.p, in.n) || ranges_overlap(workspace, need, in.p, in.n)) return GN_ERR_ALIAS;
-    if (ranges_overlap(out, act, workspace, need)) return GN_ERR_ALIAS;
-    if (residual && residual != out &&
-        (ranges_overlap(out, act, residual, act) || ranges_overlap(workspace, need, residual, act)))
-        return GN_ERR_ALIAS;
-    int dev = -1;
-    DeviceInfo d;
-    const int rc = current_device(&dev, &d);
-    if (rc != GN_OK) return rc;
-    cudaError_t e = cudaSuccess;
-    int launches = 0;
-    const int r = gn::launch_attn_folded(q, k, xn, wf, bf, residual, out, static_cast<int>(S), static_cast<int>(D),
-                                         workspace, d.sm_count, wait_timeout_ns(), static_cast<cudaStream_t>(stream),
-                                         &e, &launches);
-    g_launches.fetch_add(static_cast<uint64_t>(launches));
-    if (r != 0) {
-        cudaGetLastError();
-        return GN_ERR_CUDA;
-    }
     return GN_OK;
 }
 

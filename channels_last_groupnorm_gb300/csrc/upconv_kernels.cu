@@ -49,7 +49,7 @@
 #include <cstdlib>
 #include <mutex>
 
-#include "gn_internal.h"
+#include "tc_internal.h"
 #include "gn_ptx.cuh"
 #include "tc_ptx.cuh"
 

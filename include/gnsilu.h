@@ -320,9 +320,10 @@ int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf1
  *
  * (exact because every softmax row sums to 1).  gn_attn_fold() forms W'
  * (fp32 sums rounded once to bf16) and b' (fp32) once per weight;
- * gn_attn_folded() evaluates the second form with three tensor-core GEMMs
- * (fp32 accumulation) and a row softmax; the scores are kept in fp32 and
- * the softmax weights rounded to bf16 before the weighted sum.
+ * gn_attn_folded() evaluates the second form on the tensor cores (fp32
+ * accumulation): the folded value rows, then the fp32 scores twice -- once
+ * reduced to each row's softmax maximum and sum, once written as softmax
+ * weights rounded to bf16 -- and the weighted sum.
  */
 
 /* Fold the value projection (wv [D][D], bv [D]) and the output projection
@@ -335,9 +336,11 @@ int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf1
 int gn_attn_fold(const void *wv_bf16, const void *bv_bf16, const void *wo_bf16, const void *bo_bf16,
                  void *wf_bf16, float *bf, int64_t D, void *stream);
 
-/* Workspace bytes gn_attn_folded() needs for S tokens of width D (the
- * folded value rows, the fp32 scores and the bf16 softmax weights:
- * 2 D S + 6 S^2 bytes, rounded up), or 0 if S or D is out of range. */
+/* Workspace bytes gn_attn_folded() needs for S tokens of width D: the
+ * folded value rows (2 D S bytes), per-row-segment softmax records
+ * (16 S^2 / 128 bytes), the rows' softmax statistics (8 S) and the bf16
+ * softmax weights (2 S^2), each rounded up to 256 bytes; 0 if S or D is out
+ * of range. */
 size_t gn_attn_workspace_bytes(int64_t S, int64_t D);
 
 /* The folded attention.

@@ -362,7 +362,12 @@ def test_attn_rejects(kw, code):
 
 
 def test_attn_workspace_bytes():
-    assert gs.gn_attn_workspace_bytes(256, 512) == 2 * 512 * 256 + 6 * 256 * 256
+    def up(v):
+        return (v + 255) // 256 * 256
+    S, D = 256, 512
+    # folded value rows, per-row-segment softmax records (room for 128-wide tiles), row stats, P
+    want = up(2 * D * S) + up(8 * S * 2 * (S // 128)) + up(8 * S) + up(2 * S * S)
+    assert gs.gn_attn_workspace_bytes(S, D) == want
     assert gs.gn_attn_workspace_bytes(100, 512) == 0
     assert gs.gn_attn_workspace_bytes(256, 96) == 0
 
