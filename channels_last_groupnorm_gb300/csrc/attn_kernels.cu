@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "tc_internal.h"
@@ -186,6 +187,130 @@ __global__ void __launch_bounds__(256) softmax_stats_kernel(const float2 *__rest
 }
 
 // ---------------------------------------------------------------------------
+// The epilogue of one finished accumulator for one warp: its 32 rows
+// (m_warp0 + lane, tensor-memory lanes of its quarter from `tbase`) and one
+// half of the BN columns; hands the accumulator back with one arrival on
+// `acc_empty` (in the peer CTA when `remote`) once the last columns are in
+// registers.
+// ---------------------------------------------------------------------------
+template <int BN>
+__device__ __forceinline__ void gemm_epilogue(const GemmArgs &args, uint32_t tbase, int m_warp0, int n0, int n_t,
+                                              int half, int lane, float4 *stage, uint32_t acc_empty, bool remote)
+{
+    const int m = m_warp0 + lane;
+    const float bm = args.bias_m ? args.bias_m[m] : 0.f;
+    float run_m = -INFINITY, run_l = 0.f;   // kGemmRowStats: this row segment's running max / sum
+    float2 ml = make_float2(0.f, 0.f);
+    if (args.mode == kGemmSoftmax) ml = args.row_ml[m];
+#pragma unroll 1
+    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
+        tmem_wait_ld();
+        if (c + 32 == (half + 1) * (BN / 2)) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (remote)
+                    mbar_arrive_cluster(acc_empty);
+                else
+                    mbar_arrive(acc_empty);
+            }
+        }
+        float f[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) f[k] = fmaf(__uint_as_float(v[k]), args.alpha, bm);
+        if (args.mode == kGemmRowStats) {
+            float cmax = f[0];
+#pragma unroll
+            for (int k = 1; k < 32; ++k) cmax = fmaxf(cmax, f[k]);
+            const float m_new = fmaxf(run_m, cmax);
+            const float mb = m_new * kLog2e;
+            float acc = run_l * exp2f(fmaf(run_m, kLog2e, -mb));
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc += exp2f(fmaf(f[k], kLog2e, -mb));
+            run_l = acc;
+            run_m = m_new;
+            continue;
+        }
+        if (args.mode == kGemmSoftmax) {
+            const float mb = ml.x * kLog2e;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) f[k] = exp2f(fmaf(f[k], kLog2e, -mb)) * ml.y;
+        }
+        if (args.bias_n) {
+            const float4 *b4 = reinterpret_cast<const float4 *>(args.bias_n + n0 + c);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float4 b = __ldg(b4 + k);
+                f[4 * k] += b.x;
+                f[4 * k + 1] += b.y;
+                f[4 * k + 2] += b.z;
+                f[4 * k + 3] += b.w;
+            }
+        }
+        const int64_t at = static_cast<int64_t>(m) * args.N + n0 + c;
+        if (args.residual) {
+            const uint4 *r4 = reinterpret_cast<const uint4 *>(args.residual + at);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 rr = r4[k];
+                const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    f[8 * k + 2 * h] += __uint_as_float(w[h] << 16);
+                    f[8 * k + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                }
+            }
+        }
+        if (args.out_f32) {
+            // through shared memory, so that each store instruction of the
+            // warp writes four whole 128-byte row segments
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                stage[lane * 8 + (k ^ (lane & 7))] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+            __syncwarp();
+            float *crow = static_cast<float *>(args.c) +
+                          static_cast<int64_t>(m_warp0) * args.N + n0 + c;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = (lane >> 3) + 4 * i;
+                const float4 val = stage[r * 8 + ((lane & 7) ^ (r & 7))];
+                reinterpret_cast<float4 *>(crow + static_cast<int64_t>(r) * args.N)[lane & 7] = val;
+            }
+            __syncwarp();
+        } else {
+            // bf16: the same staging, 64 bytes per row; each store
+            // instruction writes eight whole 64-byte row segments
+            uint4 *stage4 = reinterpret_cast<uint4 *>(stage);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const __nv_bfloat162 hb = __floats2bfloat162_rn(f[8 * k + 2 * h], f[8 * k + 2 * h + 1]);
+                    o[h] = *reinterpret_cast<const uint32_t *>(&hb);
+                }
+                stage4[lane * 4 + (k ^ (lane & 3))] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            __syncwarp();
+            __nv_bfloat16 *crow = static_cast<__nv_bfloat16 *>(args.c) +
+                                  static_cast<int64_t>(m_warp0) * args.N + n0 + c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = (lane >> 2) + 8 * i;
+                const uint4 val = stage4[r * 4 + ((lane & 3) ^ (r & 3))];
+                reinterpret_cast<uint4 *>(crow + static_cast<int64_t>(r) * args.N)[lane & 3] = val;
+            }
+            __syncwarp();
+        }
+    }
+    if (args.mode == kGemmRowStats)
+        args.stats[static_cast<int64_t>(m) * (2 * args.n_tiles) + 2 * n_t + half] =
+            make_float2(run_m, run_l);
+}
+
+// ---------------------------------------------------------------------------
 // C = alpha A B^T (+ bias, + residual): persistent, one CTA per SM; tile t:
 // the N tile varies fastest.
 // ---------------------------------------------------------------------------
@@ -286,7 +411,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // two warps per tensor-memory lane quarter, each draining half the columns
         const int quad = warp & 3;
         const int half = (warp - 2) >> 2;
-        const int row_in_tile = quad * 32 + lane;
         float4 *const stage = reinterpret_cast<float4 *>(gbase + L::kStaging) + (warp - 2) * 32 * 8;
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
@@ -294,115 +418,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const bool done = at_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
-            const int m = (t / args.n_tiles) * kBM + row_in_tile;
-            const int n0 = (t % args.n_tiles) * BN;
-            const float bm = args.bias_m ? args.bias_m[m] : 0.f;
-            float run_m = -INFINITY, run_l = 0.f;   // kGemmRowStats: this row segment's running max / sum
-            float2 ml = make_float2(0.f, 0.f);
-            if (args.mode == kGemmSoftmax) ml = args.row_ml[m];
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
-#pragma unroll 1
-            for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
-                tmem_wait_ld();
-                if (c + 32 == (half + 1) * (BN / 2)) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
-                }
-                float f[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) f[k] = fmaf(__uint_as_float(v[k]), args.alpha, bm);
-                if (args.mode == kGemmRowStats) {
-                    float cmax = f[0];
-#pragma unroll
-                    for (int k = 1; k < 32; ++k) cmax = fmaxf(cmax, f[k]);
-                    const float m_new = fmaxf(run_m, cmax);
-                    const float mb = m_new * kLog2e;
-                    float acc = run_l * exp2f(fmaf(run_m, kLog2e, -mb));
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) acc += exp2f(fmaf(f[k], kLog2e, -mb));
-                    run_l = acc;
-                    run_m = m_new;
-                    continue;
-                }
-                if (args.mode == kGemmSoftmax) {
-                    const float mb = ml.x * kLog2e;
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) f[k] = exp2f(fmaf(f[k], kLog2e, -mb)) * ml.y;
-                }
-                if (args.bias_n) {
-                    const float4 *b4 = reinterpret_cast<const float4 *>(args.bias_n + n0 + c);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float4 b = __ldg(b4 + k);
-                        f[4 * k] += b.x;
-                        f[4 * k + 1] += b.y;
-                        f[4 * k + 2] += b.z;
-                        f[4 * k + 3] += b.w;
-                    }
-                }
-                const int64_t at = static_cast<int64_t>(m) * args.N + n0 + c;
-                if (args.residual) {
-                    const uint4 *r4 = reinterpret_cast<const uint4 *>(args.residual + at);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint4 rr = r4[k];
-                        const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            f[8 * k + 2 * h] += __uint_as_float(w[h] << 16);
-                            f[8 * k + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
-                        }
-                    }
-                }
-                if (args.out_f32) {
-                    // through shared memory, so that each store instruction of the
-                    // warp writes four whole 128-byte row segments
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        stage[lane * 8 + (k ^ (lane & 7))] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
-                    __syncwarp();
-                    float *crow = static_cast<float *>(args.c) +
-                                  static_cast<int64_t>(m - row_in_tile + quad * 32) * args.N + n0 + c;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int r = (lane >> 3) + 4 * i;
-                        const float4 val = stage[r * 8 + ((lane & 7) ^ (r & 7))];
-                        reinterpret_cast<float4 *>(crow + static_cast<int64_t>(r) * args.N)[lane & 7] = val;
-                    }
-                    __syncwarp();
-                } else {
-                    // bf16: the same staging, 64 bytes per row; each store
-                    // instruction writes eight whole 64-byte row segments
-                    uint4 *stage4 = reinterpret_cast<uint4 *>(stage);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t o[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const __nv_bfloat162 hb = __floats2bfloat162_rn(f[8 * k + 2 * h], f[8 * k + 2 * h + 1]);
-                            o[h] = *reinterpret_cast<const uint32_t *>(&hb);
-                        }
-                        stage4[lane * 4 + (k ^ (lane & 3))] = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                    __syncwarp();
-                    __nv_bfloat16 *crow = static_cast<__nv_bfloat16 *>(args.c) +
-                                          static_cast<int64_t>(m - row_in_tile + quad * 32) * args.N + n0 + c;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = (lane >> 2) + 8 * i;
-                        const uint4 val = stage4[r * 4 + ((lane & 3) ^ (r & 3))];
-                        reinterpret_cast<uint4 *>(crow + static_cast<int64_t>(r) * args.N)[lane & 3] = val;
-                    }
-                    __syncwarp();
-                }
-            }
-            if (args.mode == kGemmRowStats)
-                args.stats[static_cast<int64_t>(m) * (2 * args.n_tiles) + 2 * (t % args.n_tiles) + half] =
-                    make_float2(run_m, run_l);
+            gemm_epilogue<BN>(args, tbase, (t / args.n_tiles) * kBM + quad * 32, (t % args.n_tiles) * BN,
+                              t % args.n_tiles, half, lane, stage, bar_acc_empty + 8 * buf, false);
         }
     }
 
@@ -420,6 +439,172 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The same GEMM on CTA pairs (a cluster of two CTAs): one
+// tcgen05.mma.cta_group::2 of M = 256 (128 rows per CTA), N = 256 per pair
+// tile; each CTA stages its own A rows and half of the B rows, so per SM the
+// operand traffic is 2/3 of the single-CTA kernel's.  Barriers as in the
+// upsample-conv pair kernel: `full` in the even CTA counts both CTAs' bytes,
+// the pair MMA's commits arrive on both CTAs' `empty` / `acc_full`, and all
+// sixteen epilogue warps arrive on the even CTA's `acc_empty`.
+// ---------------------------------------------------------------------------
+template <int STAGES>
+struct GemmPairLayout {
+    static constexpr uint32_t kBHalf = 128u * kBK * 2;
+    static constexpr uint32_t kStage = kABytes + kBHalf;   // 32 KB
+    static constexpr uint32_t kRing = kStage * STAGES;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kBars = kRing;
+    static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kConsumed = kAbort + 4;
+    static constexpr uint32_t kStaging = (kConsumed + 4 + 15) & ~15u;
+    static constexpr uint32_t kBytes = kStaging + 8 * 32 * 32 * 4;
+    static constexpr uint32_t kDynamic = kBytes + 1024;
+};
+
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                     const GemmArgs args)
+{
+    using L = GemmPairLayout<STAGES>;
+    constexpr int BN = 256;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t bar_full = base + L::kBars;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
+    const uint32_t bar_acc_empty = bar_acc_full + 16;
+    const uint32_t bar_drain = bar_acc_empty + 16;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + L::kTmemSlot);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + L::kAbort);
+    volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_acc_full + 8 * b, 1);
+            mbar_init(bar_acc_empty + 8 * b, 16);   // 8 epilogue warps x 2 CTAs
+        }
+        mbar_init(bar_drain, 1);
+        *abort = (*reinterpret_cast<volatile unsigned int *>(&g_at_status) != 0u) ? 1 : 0;
+        *consumed_sh = 0;
+        mbar_init_fence();
+        prefetch_tensormap(&map_a);
+        prefetch_tensormap(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(base + L::kTmemSlot, L::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    cluster_sync_all();   // both CTAs' barriers are initialised before any signal crosses the pair
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort != 0;
+    const uint32_t full_lead = mapa_shared(bar_full, 0);
+    const uint32_t acc_empty_lead = mapa_shared(bar_acc_empty, 0);
+
+    int issued = 0;
+    if (!skip && warp == 0 && lane == 0) {
+        int q = 0;
+        bool go = true;
+        for (int T = pair; go && T < args.tiles; T += npairs) {
+            const int m0 = (2 * (T / args.n_tiles) + rank) * kBM;
+            const int nrow = (T % args.n_tiles) * BN + rank * 128;
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (q >= STAGES && !at_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                const uint32_t sa = base + s * L::kStage;
+                if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * L::kStage);
+                tma_load_2d_pair(sa, &map_a, kt * kBK, m0, full_lead + 8 * s);
+                tma_load_2d_pair(sa + kABytes, &map_b, kt * kBK, nrow, full_lead + 8 * s);
+                issued = q + 1;
+            }
+        }
+    } else if (!skip && leader && warp == 1 && lane == 0) {
+        constexpr uint32_t idesc = umma_idesc_bf16_f32(2 * kBM, BN);
+        int q = 0, lt = 0;
+        bool go = true;
+        for (int T = pair; go && T < args.tiles; T += npairs, ++lt) {
+            const int buf = lt & 1;
+            if (lt >= 2 && !at_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
+            tc_fence_after_sync();
+            const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+            for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
+                const int s = q % STAGES;
+                if (!at_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sa = base + s * L::kStage;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    umma_f16_pair(d, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sa + kABytes + kk * 32),
+                                  idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit_pair(bar_empty + 8 * s, 0x3);
+                *consumed_sh = q + 1;
+            }
+            if (go) umma_commit_pair(bar_acc_full + 8 * buf, 0x3);
+        }
+        umma_commit_pair(bar_drain, 0x1);
+    } else if (!skip && warp >= 2) {
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        float4 *const stage = reinterpret_cast<float4 *>(gbase + L::kStaging) + (warp - 2) * 32 * 8;
+        int lt = 0;
+        for (int T = pair; T < args.tiles; T += npairs, ++lt) {
+            const int buf = lt & 1;
+            const bool done = at_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            tc_fence_after_sync();
+            if (!__all_sync(0xffffffffu, done && !*abort)) break;
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
+            gemm_epilogue<BN>(args, tbase, (2 * (T / args.n_tiles) + rank) * kBM + quad * 32,
+                              (T % args.n_tiles) * BN, T % args.n_tiles, half, lane, stage,
+                              acc_empty_lead + 8 * buf, true);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort && !skip) {
+        if (leader && warp == 0 && lane == 0) {
+            for (int q = *consumed_sh; q < issued; ++q)
+                at_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
+        }
+        if (leader && warp == 1 && lane == 0) at_drain(bar_drain, 0, args.timeout_ns);
+        if (!leader && warp == 0 && lane == 0) {
+            // this CTA's copies signal the even CTA's barriers: give them time to land
+            const uint64_t until = global_ns() + 200000;
+            while (global_ns() < until) __nanosleep(1000);
+        }
+        __syncthreads();
+    }
+    __syncwarp();
+    cluster_sync_all();   // neither CTA leaves while the pair's MMAs or signals may touch it
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem, L::kTmemCols);
     }
 }
 
@@ -481,6 +666,51 @@ cudaError_t launch_gemm_variant(const CUtensorMap &ma, const CUtensorMap &mb, co
 
 int gemm_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
 
+bool gemm_pair_enabled()
+{
+    static const bool on = [] {
+        const char *v = std::getenv("GN_GEMM_PAIR");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
+template <int STAGES>
+cudaError_t launch_gemm_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &a, int sm_count,
+                             cudaStream_t s)
+{
+    using L = GemmPairLayout<STAGES>;
+    static_assert(L::kDynamic <= 227 * 1024, "gemm pair ring does not fit in shared memory");
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    static int max_clusters = 0;
+    std::call_once(once, [sm_count] {
+        attr = cudaFuncSetAttribute(gemm_pair_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(L::kDynamic));
+        if (attr != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (sm_count / 2));
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = L::kDynamic;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_pair_kernel<STAGES>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            max_clusters = sm_count / 2;
+        }
+    });
+    if (attr != cudaSuccess) return attr;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    const int pairs = a.tiles < max_clusters ? a.tiles : max_clusters;
+    gemm_pair_kernel<STAGES><<<2 * pairs, kGemmThreads, L::kDynamic, s>>>(ma, mb, a);
+    return cudaGetLastError();
+}
+
 // C[M][N] = alpha A[M][K] B[N][K]^T (+ bias_m[M], + bias_n[N], + residual),
 // or the softmax statistics / weights of alpha A B^T (mode)
 int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float alpha, const float *bias_m,
@@ -490,14 +720,18 @@ int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float a
     EncodeTiledFn enc = encode_fn();
     if (!enc) return 2;
     const int BN = gemm_bn(N);
+    // CTA pairs take 256-row x 256-column tiles (each CTA 128 rows and half the columns' B rows);
+    // they pay off once a tile has 16 or more K steps (at S = 16384 the weighted sum, K = S,
+    // runs 199 -> 173 us on pairs, while the 8-step score passes run slower)
+    const bool pair = BN == 256 && M % 256 == 0 && K / kBK >= 16 && gemm_pair_enabled();
     CUtensorMap ma, mb;
-    if (!encode_kmajor(enc, &ma, A, M, K, kBM) || !encode_kmajor(enc, &mb, B, N, K, BN)) return 2;
+    if (!encode_kmajor(enc, &ma, A, M, K, kBM) || !encode_kmajor(enc, &mb, B, N, K, pair ? 128 : BN)) return 2;
     GemmArgs a;
     a.M = M;
     a.N = N;
     a.K = K;
     a.n_tiles = N / BN;
-    a.tiles = (M / kBM) * a.n_tiles;
+    a.tiles = (M / (pair ? 2 * kBM : kBM)) * a.n_tiles;
     a.ksteps = K / kBK;
     a.alpha = alpha;
     a.bias_m = bias_m;
@@ -509,6 +743,10 @@ int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float a
     a.stats = stats;
     a.row_ml = row_ml;
     a.timeout_ns = timeout_ns;
+    if (pair) {
+        *err = launch_gemm_pair<6>(ma, mb, a, sm_count, s);
+        return *err == cudaSuccess ? 0 : 3;
+    }
     *err = (BN == 256) ? launch_gemm_variant<256, 4>(ma, mb, a, sm_count, s)
                        : launch_gemm_variant<128, 6>(ma, mb, a, sm_count, s);
     return *err == cudaSuccess ? 0 : 3;

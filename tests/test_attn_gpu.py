@@ -71,7 +71,8 @@ def oracle_args(c):
 
 
 @pytest.mark.parametrize("S,D,residual", [(256, 512, True), (256, 512, False), (384, 128, True),
-                                          (128, 256, True), (640, 384, False)])
+                                          (128, 256, True), (640, 384, False),
+                                          (1024, 512, True)])   # weighted sum on CTA pairs (K = S >= 1024)
 def test_matches_oracle(S, D, residual):
     c = wl.make_attn_case(S, D, S + D, residual)
     y = run(c).float().cpu().numpy().astype(np.float64)
@@ -134,3 +135,32 @@ def test_unsupported_inputs_return_none():
     with pytest.warns(UserWarning):
         assert gs.attention_folded(q100, q100, q100, wf, bf) is None           # S not a multiple of 128
     assert gs.attention_folded(q.t(), q, q, wf, bf) is None                    # not contiguous
+
+
+def test_single_cta_gemm_schedule_matches_oracle():
+    """The single-CTA GEMM schedule (taken for row counts that are not a
+    multiple of 256, for fewer than 16 K steps, and for every GEMM with
+    GN_GEMM_PAIR=0) on a shape whose weighted sum the CTA-pair schedule
+    would otherwise take, in a child process."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import numpy as np, torch, oracle\n"
+        "from channels_last_groupnorm_gb300 import gnsilu as gs, workloads as wl\n"
+        "c = wl.make_attn_case(1024, 512, 77)\n"
+        "d = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).cuda().view(torch.bfloat16)\n"
+        "wf, bf = gs.attn_fold(d(c['wv']), d(c['bv']), d(c['wo']), d(c['bo']))\n"
+        "y = gs.attention_folded(d(c['q']), d(c['k']), d(c['xn']), wf, bf, residual=d(c['residual']))\n"
+        "torch.cuda.synchronize()\n"
+        "assert gs.gn_device_status(False) == 0\n"
+        "ref, mag = oracle.attn().forward(c['q'], c['k'], c['xn'], c['wv'], c['bv'], c['wo'], c['bo'],\n"
+        "                                 c['residual'], with_mag=True)\n"
+        "err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)\n"
+        "assert np.all(err <= 2.0 ** -6 * mag + 2.0 ** -7 * np.abs(ref)), err.max()\n"
+        "print('ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, GN_GEMM_PAIR="0", PYTHONPATH=root)
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
