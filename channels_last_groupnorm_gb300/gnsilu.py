@@ -13,6 +13,10 @@ C > 2048, not channels_last), so callers can fall back to their own path.
 ``gn_silu_rows_any`` and ``gn_silu_ndhwc`` take any C that is a multiple of 8
 up to 2048 (any channels per group) and 5D channels-last input, the range of
 the page's existing general kernel (same section, item 1, third bullet).
+``residual_gate_add``, ``upconv_fold`` / ``upsample_conv_nhwc`` and
+``attn_fold`` / ``attention_folded`` bind the residual-gate update, the
+fused nearest-2x upsample + 3x3 conv and the folded single-head attention
+the same way.
 """
 from __future__ import annotations
 

@@ -1,5 +1,6 @@
 /*
- * gnsilu.h -- C ABI of libgnsilu: channels-last GroupNorm (+SiLU) on GB300.
+ * gnsilu.h -- C ABI of libgnsilu: channels-last GroupNorm (+SiLU) on GB300,
+ * and the decoder operations next to it.
  *
  * The operation (sglang PR #33451, "FLUX.2 VAE decoder fast path behind
  * quality=high", section "Modifications", item 1): x is bf16 in (N, L, C)
@@ -24,6 +25,14 @@
  * to any multiple of 8 up to 2048 (any channels per group, e.g. C = 320 or
  * 960) and add 5D channels-last input: the range the page's existing
  * general kernel serves (same section, item 1, third bullet).
+ *
+ * The library also carries the neighbouring decoder operations the pages
+ * describe, each declared further down with its own definition and
+ * contract: the residual-gate update residual + gate * update
+ * (gn_residual_gate_add), the fused nearest-2x upsample + 3x3 convolution
+ * (gn_upconv_fold, gn_upconv_nhwc) and the single-head attention with its
+ * output projection folded into V (gn_attn_fold, gn_attn_folded); the last
+ * two run on the tensor cores.
  *
  * Memory and streams: every pointer argument is a DEVICE pointer owned by
  * the caller; the library never frees caller memory.  x and y are bf16
