@@ -35,10 +35,13 @@
 //                        accumulator and commits each ring slot back to the
 //                        producer and each finished accumulator to the
 //                        epilogue;
-//   warps 2-5            epilogue: tcgen05.ld of the fp32 accumulator (one
-//                        pixel per thread), hand the accumulator back, + bias,
-//                        round to bf16, store to y at (2i + a, 2j + b) -- while
-//                        the MMAs of the next tile run into the other one.
+//   warps 2-9            epilogue, two warps per tensor-memory lane quarter
+//                        (each half of the channels): tcgen05.ld of the fp32
+//                        accumulator (one pixel per thread), hand the
+//                        accumulator back, + bias, round to bf16, and through a
+//                        small shared-memory tile store to y at (2i + a, 2j + b)
+//                        in 64-byte channel runs -- while the MMAs of the next
+//                        tile run into the other accumulator.
 // Every wait is bounded (a timeout sets a device status word and the CTA
 // drains its copies and frees its tensor memory before it returns).
 #include <cuda.h>
@@ -62,7 +65,7 @@ namespace {
 constexpr int kBM = 128;                                // output pixels per tile (MMA M)
 constexpr int kBK = 64;                                 // input channels per K step
 constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KB
-constexpr int kUcThreads = 192;
+constexpr int kUcThreads = 320;   // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t kSleepNs = 20000;
 
 struct UcArgs {
@@ -89,7 +92,8 @@ struct UcLayout {
     static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kConsumed = kAbort + 4;
-    static constexpr uint32_t kBytes = kConsumed + 4;
+    static constexpr uint32_t kStaging = (kConsumed + 4 + 15) & ~15u;   // 8 epilogue warps x 2 KB
+    static constexpr uint32_t kBytes = kStaging + 8 * 2048;
     static constexpr uint32_t kDynamic = kBytes + 1024;  // slack to align the ring to 1024 B
 };
 
@@ -182,6 +186,75 @@ __global__ void __launch_bounds__(256) upconv_fold_kernel(const __nv_bfloat16 *_
 }
 
 // ---------------------------------------------------------------------------
+// The epilogue of one finished accumulator for one warp: the 32 pixels of
+// its tensor-memory lane quarter and one half of the BN channels.  Each
+// 32-channel chunk gets the bias, is rounded to bf16 and goes through a
+// swizzled 2 KB shared-memory tile, so that each store instruction writes
+// eight pixels' 64-byte channel runs (instead of 32 pixels' 16 bytes); the
+// accumulator is handed back (one arrival on `acc_empty`, in the peer CTA
+// when `remote`) once the warp's last columns are in registers.
+// ---------------------------------------------------------------------------
+template <int BN>
+__device__ __forceinline__ void upconv_epilogue(const UcArgs &args, const TileCoord &tc, uint32_t tbase, int quad,
+                                                int half, int lane, uint4 *stage, uint32_t acc_empty, bool remote)
+{
+    const int pa = tc.parity >> 1, pb = tc.parity & 1;
+    // this lane stores pixels (lane >> 2) + 8 i of the warp's 32, 16 bytes each
+    __nv_bfloat16 *rowp[4];
+    bool rowv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = quad * 32 + (lane >> 2) + 8 * i;
+        const int wi = m % args.BW;
+        const int hi = (m / args.BW) % args.BH;
+        const int n = tc.n0 + m / (args.BW * args.BH);
+        rowv[i] = n < args.N;
+        const int64_t P = 2LL * (tc.i0 + hi) + pa, Q = 2LL * (tc.j0 + wi) + pb;
+        rowp[i] = args.y + ((static_cast<int64_t>(rowv[i] ? n : 0) * 2 * args.H + P) * 2 * args.W + Q) * args.Cout +
+                  tc.co0;
+    }
+#pragma unroll 1
+    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
+        tmem_wait_ld();
+        if (c + 32 == (half + 1) * (BN / 2)) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (remote)
+                    mbar_arrive_cluster(acc_empty);
+                else
+                    mbar_arrive(acc_empty);
+            }
+        }
+        uint32_t o[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            float lo = __uint_as_float(v[2 * k]), hi2 = __uint_as_float(v[2 * k + 1]);
+            if (args.bias) {
+                const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162 *>(args.bias + tc.co0 + c + 2 * k);
+                lo += __low2float(bb);
+                hi2 += __high2float(bb);
+            }
+            const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi2);
+            o[k] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            stage[lane * 4 + (k ^ (lane & 3))] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = (lane >> 2) + 8 * i;
+            const uint4 val = stage[r * 4 + ((lane & 3) ^ (r & 3))];
+            if (rowv[i]) reinterpret_cast<uint4 *>(rowp[i] + c)[lane & 3] = val;
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
 // the implicit-GEMM convolution: a persistent CTA per SM walks the tiles
 // t = blockIdx.x, + gridDim.x, ...; the ring of operand stages runs across
 // tile boundaries and the two tensor-memory accumulators alternate, so the
@@ -215,7 +288,7 @@ __global__ void __launch_bounds__(kUcThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
-            mbar_init(bar_acc_empty + 8 * b, 4);   // one arrival per epilogue warp
+            mbar_init(bar_acc_empty + 8 * b, 8);   // one arrival per epilogue warp
         }
         mbar_init(bar_drain, 1);
         *abort = (*reinterpret_cast<volatile unsigned int *>(&g_uc_status) != 0u) ? 1 : 0;
@@ -291,12 +364,10 @@ __global__ void __launch_bounds__(kUcThreads, 1)
         }
         umma_commit(bar_drain);   // arrives once every MMA issued above has completed
     } else if (!skip && warp >= 2) {
-        // ---- epilogue: thread <-> tile pixel (TMEM lane) ----
+        // ---- epilogue: two warps per tensor-memory lane quarter, each half the columns ----
         const int quad = warp & 3;
-        const int m = quad * 32 + lane;
-        const int wi = m % args.BW;
-        const int hi = (m / args.BW) % args.BH;
-        const int ni = m / (args.BW * args.BH);
+        const int half = (warp - 2) >> 2;
+        uint4 *const stage = reinterpret_cast<uint4 *>(gbase + L::kStaging) + (warp - 2) * 128;
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
@@ -304,45 +375,10 @@ __global__ void __launch_bounds__(kUcThreads, 1)
             tc_fence_after_sync();
             // warp-uniform, as the tensor-memory loads below are warp-collective
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
-            const TileCoord tc = tile_coord<BN>(t, args);
-            const int pa = tc.parity >> 1, pb = tc.parity & 1;
-            const int n = tc.n0 + ni;
-            const bool valid = n < args.N;
-            const int64_t P = 2LL * (tc.i0 + hi) + pa, Q = 2LL * (tc.j0 + wi) + pb;
-            __nv_bfloat16 *dst =
-                args.y + ((static_cast<int64_t>(n) * 2 * args.H + P) * 2 * args.W + Q) * args.Cout + tc.co0;
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
-                tmem_wait_ld();
-                if (c + 32 == BN) {
-                    // every column of this accumulator is in registers: hand it back
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
-                }
-                if (valid) {
-                    uint32_t o[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float lo = __uint_as_float(v[2 * k]), hi2 = __uint_as_float(v[2 * k + 1]);
-                        if (args.bias) {
-                            const __nv_bfloat162 bb =
-                                *reinterpret_cast<const __nv_bfloat162 *>(args.bias + tc.co0 + c + 2 * k);
-                            lo += __low2float(bb);
-                            hi2 += __high2float(bb);
-                        }
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi2);
-                        o[k] = *reinterpret_cast<const uint32_t *>(&h);
-                    }
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) d4[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                }
-            }
+            upconv_epilogue<BN>(args, tile_coord<BN>(t, args), tbase, quad, half, lane, stage,
+                                bar_acc_empty + 8 * buf, false);
         }
     }
 
@@ -388,7 +424,8 @@ struct PairLayout {
     static constexpr uint32_t kTmemSlot = kBars + 8 * (2 * STAGES + 5);
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kConsumed = kAbort + 4;
-    static constexpr uint32_t kBytes = kConsumed + 4;
+    static constexpr uint32_t kStaging = (kConsumed + 4 + 15) & ~15u;   // 8 epilogue warps x 2 KB
+    static constexpr uint32_t kBytes = kStaging + 8 * 2048;
     static constexpr uint32_t kDynamic = kBytes + 1024;
 };
 
@@ -446,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
-            mbar_init(bar_acc_empty + 8 * b, 8);   // 4 epilogue warps x 2 CTAs
+            mbar_init(bar_acc_empty + 8 * b, 16);   // 8 epilogue warps x 2 CTAs
         }
         mbar_init(bar_drain, 1);
         *abort = (*reinterpret_cast<volatile unsigned int *>(&g_uc_status) != 0u) ? 1 : 0;
@@ -524,56 +561,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
         }
         umma_commit_pair(bar_drain, 0x1);
     } else if (!skip && warp >= 2) {
-        // ---- epilogue (both CTAs): thread <-> own pixel (TMEM lane), 256 channels ----
+        // ---- epilogue (both CTAs): own pixels, 256 channels, two warps per lane quarter ----
         const int quad = warp & 3;
-        const int m = quad * 32 + lane;
-        const int wi = m % args.BW;
-        const int hi = (m / args.BW) % args.BH;
-        const int ni = m / (args.BW * args.BH);
+        const int half = (warp - 2) >> 2;
+        uint4 *const stage = reinterpret_cast<uint4 *>(gbase + L::kStaging) + (warp - 2) * 128;
         int lt = 0;
         for (int T = pair; T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
             const bool done = uc_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
-            const TileCoord tc = pair_tile_coord(T, rank, args);
-            const int pa = tc.parity >> 1, pb = tc.parity & 1;
-            const int n = tc.n0 + ni;
-            const bool valid = n < args.N;
-            const int64_t P = 2LL * (tc.i0 + hi) + pa, Q = 2LL * (tc.j0 + wi) + pb;
-            __nv_bfloat16 *dst =
-                args.y + ((static_cast<int64_t>(n) * 2 * args.H + P) * 2 * args.W + Q) * args.Cout + tc.co0;
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), v);
-                tmem_wait_ld();
-                if (c + 32 == BN) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(acc_empty_lead + 8 * buf);
-                }
-                if (valid) {
-                    uint32_t o[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float lo = __uint_as_float(v[2 * k]), hi2 = __uint_as_float(v[2 * k + 1]);
-                        if (args.bias) {
-                            const __nv_bfloat162 bb =
-                                *reinterpret_cast<const __nv_bfloat162 *>(args.bias + tc.co0 + c + 2 * k);
-                            lo += __low2float(bb);
-                            hi2 += __high2float(bb);
-                        }
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi2);
-                        o[k] = *reinterpret_cast<const uint32_t *>(&h);
-                    }
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) d4[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                }
-            }
+            upconv_epilogue<BN>(args, pair_tile_coord(T, rank, args), tbase, quad, half, lane, stage,
+                                acc_empty_lead + 8 * buf, true);
         }
     }
 
