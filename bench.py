@@ -49,8 +49,8 @@ ATTN_METRIC = ("single-head attention, output projection folded into V, bf16 in/
                "accumulation: us/call and TFLOP/s")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh", "capi_util.h", "rga_kernels.cu"]
-UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
-ATTN_SOURCES = ["attn_kernels.cu", "tc_ptx.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
+UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
+ATTN_SOURCES = ["attn_kernels.cu", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
 
 
 # ---------------------------------------------------------------------------

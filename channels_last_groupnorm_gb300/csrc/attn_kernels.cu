@@ -46,6 +46,7 @@
 
 #include "tc_internal.h"
 #include "gn_ptx.cuh"
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace gn {
@@ -58,7 +59,6 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kGemmThreads = 320;   // producer warp, MMA warp, 8 epilogue warps
-constexpr uint32_t kSleepNs = 20000;
 
 struct GemmArgs {
     int M, N, K;
@@ -100,31 +100,7 @@ struct GemmLayout {
     static constexpr uint32_t kDynamic = kBytes + 1024;
 };
 
-__device__ __forceinline__ bool at_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    const uint64_t deadline = global_ns() + timeout_ns;
-#pragma unroll 1
-    for (;;) {
-        if (mbar_wait_sleep(bar, parity, kSleepNs)) return true;
-        if (*abort) return false;
-        if (global_ns() > deadline) {
-            *abort = 1;
-            atomicOr(&g_at_status, 1u);
-            return false;
-        }
-    }
-}
 
-__device__ __forceinline__ void at_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
-{
-    const uint64_t deadline = global_ns() + timeout_ns;
-#pragma unroll 1
-    while (!mbar_wait_sleep(bar, parity, kSleepNs)) {
-        if (global_ns() > deadline) return;
-    }
-}
 
 }  // namespace
 
@@ -368,7 +344,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int m0 = (t / args.n_tiles) * kBM, n0 = (t % args.n_tiles) * BN;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !at_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_at_status)) {
                     go = false;
                     break;
                 }
@@ -385,12 +361,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool go = true;
         for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
-            if (lt >= 2 && !at_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_at_status)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!at_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_at_status)) {
                     go = false;
                     break;
                 }
@@ -415,7 +391,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
-            const bool done = at_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_at_status);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
             const uint32_t tbase =
@@ -430,9 +406,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (*abort && !skip) {
         if (warp == 0 && lane == 0) {
             for (int q = *consumed_sh; q < issued; ++q)
-                at_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
+                tc::drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
         }
-        if (warp == 1 && lane == 0) at_drain(bar_drain, 0, args.timeout_ns);
+        if (warp == 1 && lane == 0) tc::drain(bar_drain, 0, args.timeout_ns);
         __syncthreads();
     }
     if (warp == 1) {
@@ -528,7 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const int nrow = (T % args.n_tiles) * BN + rank * 128;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !at_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_at_status)) {
                     go = false;
                     break;
                 }
@@ -545,12 +521,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         bool go = true;
         for (int T = pair; go && T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            if (lt >= 2 && !at_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_at_status)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!at_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_at_status)) {
                     go = false;
                     break;
                 }
@@ -574,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         int lt = 0;
         for (int T = pair; T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            const bool done = at_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_at_status);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
             const uint32_t tbase =
@@ -590,9 +566,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (*abort && !skip) {
         if (leader && warp == 0 && lane == 0) {
             for (int q = *consumed_sh; q < issued; ++q)
-                at_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
+                tc::drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
         }
-        if (leader && warp == 1 && lane == 0) at_drain(bar_drain, 0, args.timeout_ns);
+        if (leader && warp == 1 && lane == 0) tc::drain(bar_drain, 0, args.timeout_ns);
         if (!leader && warp == 0 && lane == 0) {
             // this CTA's copies signal the even CTA's barriers: give them time to land
             const uint64_t until = global_ns() + 200000;
@@ -613,29 +589,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 // ---------------------------------------------------------------------------
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
 
 // A bf16 [rows][K] K-major operand, boxes of {64, box_rows}, 128-byte swizzle.
-bool encode_kmajor(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows)
+bool encode_kmajor(tc::EncodeTiledFn enc, CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows)
 {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
@@ -688,21 +644,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap &ma, const CUtensorMap &mb, const
         attr = cudaFuncSetAttribute(gemm_pair_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(L::kDynamic));
         if (attr != cudaSuccess) return;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (sm_count / 2));
-        cfg.blockDim = dim3(kGemmThreads);
-        cfg.dynamicSmemBytes = L::kDynamic;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_pair_kernel<STAGES>, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            max_clusters = sm_count / 2;
-        }
+        max_clusters = tc::pair_clusters(gemm_pair_kernel<STAGES>, kGemmThreads, L::kDynamic, sm_count);
     });
     if (attr != cudaSuccess) return attr;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
@@ -717,7 +659,7 @@ int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float a
              const float *bias_n, const void *residual, bool out_f32, int mode, float2 *stats,
              const float2 *row_ml, int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err)
 {
-    EncodeTiledFn enc = encode_fn();
+    tc::EncodeTiledFn enc = tc::encode_fn();
     if (!enc) return 2;
     const int BN = gemm_bn(N);
     // CTA pairs take 256-row x 256-column tiles (each CTA 128 rows and half the columns' B rows);

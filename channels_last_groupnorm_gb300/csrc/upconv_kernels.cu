@@ -54,6 +54,7 @@
 
 #include "tc_internal.h"
 #include "gn_ptx.cuh"
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace gn {
@@ -66,7 +67,6 @@ constexpr int kBM = 128;                                // output pixels per til
 constexpr int kBK = 64;                                 // input channels per K step
 constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KB
 constexpr int kUcThreads = 320;   // producer warp, MMA warp, 8 epilogue warps
-constexpr uint32_t kSleepNs = 20000;
 
 struct UcArgs {
     int N, H, W, Cin, Cout;
@@ -123,33 +123,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const UcArgs &a)
     return c;
 }
 
-__device__ __forceinline__ bool uc_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    const uint64_t deadline = global_ns() + timeout_ns;
-#pragma unroll 1
-    for (;;) {
-        if (mbar_wait_sleep(bar, parity, kSleepNs)) return true;
-        if (*abort) return false;
-        if (global_ns() > deadline) {
-            *abort = 1;
-            atomicOr(&g_uc_status, 1u);
-            return false;
-        }
-    }
-}
 
-// A wait during teardown after an abort: bounded, but not cut short by the
-// abort flag (the copies and MMAs it waits for are still in flight).
-__device__ __forceinline__ void uc_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
-{
-    const uint64_t deadline = global_ns() + timeout_ns;
-#pragma unroll 1
-    while (!mbar_wait_sleep(bar, parity, kSleepNs)) {
-        if (global_ns() > deadline) return;
-    }
-}
 
 __device__ __forceinline__ int floor_half(int v) { return (v + 2) / 2 - 1; }   // floor(v / 2) for v >= -2
 
@@ -318,7 +292,7 @@ __global__ void __launch_bounds__(kUcThreads, 1)
             const int wrow = tc.parity * args.Cout + tc.co0;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !uc_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) {
                     go = false;
                     break;
                 }
@@ -341,12 +315,12 @@ __global__ void __launch_bounds__(kUcThreads, 1)
         for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
             // the epilogue has drained this accumulator (tile lt - 2)
-            if (lt >= 2 && !uc_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!uc_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_uc_status)) {
                     go = false;
                     break;
                 }
@@ -371,7 +345,7 @@ __global__ void __launch_bounds__(kUcThreads, 1)
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
-            const bool done = uc_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_uc_status);
             tc_fence_after_sync();
             // warp-uniform, as the tensor-memory loads below are warp-collective
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
@@ -389,9 +363,9 @@ __global__ void __launch_bounds__(kUcThreads, 1)
         if (warp == 0 && lane == 0) {
             // loads issued but never consumed still write into the ring
             for (int q = *consumed_sh; q < issued; ++q)
-                uc_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
+                tc::drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
         }
-        if (warp == 1 && lane == 0) uc_drain(bar_drain, 0, args.timeout_ns);
+        if (warp == 1 && lane == 0) tc::drain(bar_drain, 0, args.timeout_ns);
         __syncthreads();
     }
     if (warp == 1) {
@@ -516,7 +490,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
             const int wrow = tc.parity * args.Cout + tc.co0 + rank * 128;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !uc_wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) {
                     go = false;
                     break;
                 }
@@ -538,12 +512,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
         bool go = true;
         for (int T = pair; go && T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            if (lt >= 2 && !uc_wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!uc_wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_uc_status)) {
                     go = false;
                     break;
                 }
@@ -568,7 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
         int lt = 0;
         for (int T = pair; T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            const bool done = uc_wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_uc_status);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
             const uint32_t tbase =
@@ -584,9 +558,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
     if (*abort && !skip) {
         if (leader && warp == 0 && lane == 0) {
             for (int q = *consumed_sh; q < issued; ++q)
-                uc_drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
+                tc::drain(bar_full + 8 * (q % STAGES), (q / STAGES) & 1, args.timeout_ns);
         }
-        if (leader && warp == 1 && lane == 0) uc_drain(bar_drain, 0, args.timeout_ns);
+        if (leader && warp == 1 && lane == 0) tc::drain(bar_drain, 0, args.timeout_ns);
         if (!leader && warp == 0 && lane == 0) {
             // this CTA's copies signal the even CTA's barriers: give them time to land
             const uint64_t until = global_ns() + 200000;
@@ -607,28 +581,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
 // ---------------------------------------------------------------------------
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, looked up once through the runtime (the
-// library does not link the driver library itself).
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
 
 template <int BN, int STAGES>
 cudaError_t launch_variant(const CUtensorMap &mx, const CUtensorMap &mw, const UcArgs &a, int blocks,
@@ -659,21 +611,7 @@ cudaError_t launch_pair(const CUtensorMap &mx, const CUtensorMap &mw, const UcAr
         attr = cudaFuncSetAttribute(upconv_pair_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(L::kDynamic));
         if (attr != cudaSuccess) return;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (sm_count / 2));
-        cfg.blockDim = dim3(kUcThreads);
-        cfg.dynamicSmemBytes = L::kDynamic;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, upconv_pair_kernel<STAGES>, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            max_clusters = sm_count / 2;
-        }
+        max_clusters = tc::pair_clusters(upconv_pair_kernel<STAGES>, kUcThreads, L::kDynamic, sm_count);
     });
     if (attr != cudaSuccess) return attr;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
@@ -740,7 +678,7 @@ int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int 
     *err = cudaSuccess;
     UpconvTiling t;
     if (!upconv_tiling(N, H, W, &t)) return 1;
-    EncodeTiledFn enc = encode_fn();
+    tc::EncodeTiledFn enc = tc::encode_fn();
     if (!enc) return 2;
     const int BN = (Cout % 256 == 0) ? 256 : 128;
     const bool use_pair = BN == 256 && pair_kernel_enabled();

@@ -72,7 +72,8 @@ def oracle_args(c):
 
 @pytest.mark.parametrize("S,D,residual", [(256, 512, True), (256, 512, False), (384, 128, True),
                                           (128, 256, True), (640, 384, False),
-                                          (1024, 512, True)])   # weighted sum on CTA pairs (K = S >= 1024)
+                                          (1024, 512, True),    # weighted sum on CTA pairs (K = S >= 1024)
+                                          (256, 1024, False)])  # the widest D the entry takes
 def test_matches_oracle(S, D, residual):
     c = wl.make_attn_case(S, D, S + D, residual)
     y = run(c).float().cpu().numpy().astype(np.float64)

@@ -90,6 +90,8 @@ SMALL = [
     (1, 1, 256, 64, 128, True),      # a single input row (every tap row but one is padding)
     (2, 16, 8, 192, 256, True),      # Cin 192: three K chunks per tap
     (1, 1, 1, 64, 128, True),        # one input pixel, one tile mostly outside the image
+    (2, 2, 128, 64, 256, False),     # W = 128, two images, CTA pairs, no bias
+    (3, 1, 128, 128, 512, True),     # odd number of pixel tiles: the last pair's second tile is past the batch
 ]
 
 
