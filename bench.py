@@ -340,8 +340,12 @@ def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, s
 
 
 def measure_e2e(w, variant_id, steps, warmup, device, stream):
-    """Through the C ABI from pinned host buffers: H2D of x, gamma, beta, the
-    call, D2H of y, every step, all inside the timed region."""
+    """Through the C ABI from pinned host buffers: every step copies x,
+    gamma and beta in, makes the call and copies y out, all inside the timed
+    region.  The steps are pipelined the way a streaming caller runs them:
+    copies in and out go on two copy streams with two device buffer sets,
+    so step i's call overlaps step i+1's copy in and step i-1's copy out;
+    the region runs from the first copy in to the last copy out."""
     import numpy as np
     import torch
     from channels_last_groupnorm_gb300 import gnsilu as gs
@@ -352,28 +356,55 @@ def measure_e2e(w, variant_id, steps, warmup, device, stream):
     hg = torch.from_numpy(case["gamma"]).pin_memory()
     hb = torch.from_numpy(case["beta"]).pin_memory()
     hy = torch.empty_like(hx).pin_memory()
-    dx = torch.empty_like(hx, device=device)
-    dg = torch.empty_like(hg, device=device)
-    db = torch.empty_like(hb, device=device)
-    dy = torch.empty_like(hx, device=device)
+    dx = [torch.empty_like(hx, device=device) for _ in range(2)]
+    dg = [torch.empty_like(hg, device=device) for _ in range(2)]
+    db = [torch.empty_like(hb, device=device) for _ in range(2)]
+    dy = [torch.empty_like(hx, device=device) for _ in range(2)]
+    s_in = torch.cuda.Stream(device)
+    s_out = torch.cuda.Stream(device)
     h = stream.cuda_stream
     entry = raw_entry(w)
 
-    def step(_):
-        dx.copy_(hx, non_blocking=True)
-        dg.copy_(hg, non_blocking=True)
-        db.copy_(hb, non_blocking=True)
-        rc = entry(dx.data_ptr(), dg.data_ptr(), db.data_ptr(), dy.data_ptr(),
-                   w.N, w.L, w.C, w.G, w.eps, 1, variant=variant_id, stream=h)
-        if rc != 0:
-            raise RuntimeError(gs.status_string(rc))
-        hy.copy_(dy, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for i in range(max(3, warmup)):
-            step(i)
+    def run(n, timed):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_k = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        per, elapsed = time_calls(step, 1, steps, stream)
+        if timed:
+            barrier()
+            torch.cuda.synchronize()
+        t0.record(s_in)
+        for i in range(n):
+            k = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_k[i - 2])      # the call two steps back has read this set
+                dx[k].copy_(hx, non_blocking=True)
+                dg[k].copy_(hg, non_blocking=True)
+                db[k].copy_(hb, non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])      # y of two steps back has left the device
+            rc = entry(dx[k].data_ptr(), dg[k].data_ptr(), db[k].data_ptr(), dy[k].data_ptr(),
+                       w.N, w.L, w.C, w.G, w.eps, 1, variant=variant_id, stream=h)
+            if rc != 0:
+                raise RuntimeError(gs.status_string(rc))
+            ev_k[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_k[i])
+                hy.copy_(dy[k], non_blocking=True)
+                ev_out[i].record(s_out)
+        t1.record(s_out)
+        torch.cuda.synchronize()
+        if timed:
+            barrier()
+        return t0.elapsed_time(t1) / 1e3
+
+    run(max(3, warmup), False)
+    elapsed = run(steps, True)
     h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
     d2h = hy.numel() * 2
     return elapsed, h2d, d2h
