@@ -620,8 +620,6 @@ cudaError_t launch_gemm_variant(const CUtensorMap &ma, const CUtensorMap &mb, co
     return cudaGetLastError();
 }
 
-int gemm_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
-
 bool gemm_pair_enabled()
 {
     static const bool on = [] {
@@ -630,6 +628,41 @@ bool gemm_pair_enabled()
     }();
     return on;
 }
+
+// The three GEMM schedules and a rough cost model to choose among them:
+// time ~ rounds of tiles over the SMs (or SM pairs) x the per-SM work of one
+// tile / its tensor-pipe efficiency (CTA pairs ~0.93, single CTA 128x256
+// ~0.80, 128x128 ~0.70).  CTA pairs need 16 or more K steps per tile to pay
+// off (at S = 16384 the weighted sum, K = S, runs 199 -> 173 us on pairs,
+// while the 8-step score passes run slower).  Problems with few tiles take
+// the 128-wide tiles so that more SMs work (the weighted sum at S = 4096
+// has 32 pair tiles for 76 pairs).
+enum GemmSchedule { kPair256 = 0, kSingle256 = 1, kSingle128 = 2 };
+
+GemmSchedule choose_gemm(int M, int N, int K, int sm_count)
+{
+    const auto cost = [sm_count](int64_t units, bool pair, double area_over_eff) {
+        const int64_t slots = pair ? sm_count / 2 : sm_count;
+        return static_cast<double>((units + slots - 1) / slots) * area_over_eff;
+    };
+    GemmSchedule best = kSingle128;
+    double best_cost = cost(static_cast<int64_t>(M / 128) * (N / 128), false, 128.0 * 128.0 / 0.70);
+    if (N % 256 == 0) {
+        const double c = cost(static_cast<int64_t>(M / 128) * (N / 256), false, 128.0 * 256.0 / 0.80);
+        if (c <= best_cost) {
+            best = kSingle256;
+            best_cost = c;
+        }
+        if (M % 256 == 0 && K / kBK >= 16 && gemm_pair_enabled()) {
+            const double cp = cost(static_cast<int64_t>(M / 256) * (N / 256), true, 128.0 * 256.0 / 0.93);
+            if (cp < best_cost) best = kPair256;
+        }
+    }
+    return best;
+}
+
+int schedule_bn(GemmSchedule g) { return g == kSingle128 ? 128 : 256; }
+
 
 template <int STAGES>
 cudaError_t launch_gemm_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &a, int sm_count,
@@ -661,11 +694,10 @@ int run_gemm(const void *A, const void *B, void *C, int M, int N, int K, float a
 {
     tc::EncodeTiledFn enc = tc::encode_fn();
     if (!enc) return 2;
-    const int BN = gemm_bn(N);
-    // CTA pairs take 256-row x 256-column tiles (each CTA 128 rows and half the columns' B rows);
-    // they pay off once a tile has 16 or more K steps (at S = 16384 the weighted sum, K = S,
-    // runs 199 -> 173 us on pairs, while the 8-step score passes run slower)
-    const bool pair = BN == 256 && M % 256 == 0 && K / kBK >= 16 && gemm_pair_enabled();
+    const GemmSchedule sched = choose_gemm(M, N, K, sm_count);
+    const int BN = schedule_bn(sched);
+    // CTA pairs take 256-row x 256-column tiles (each CTA 128 rows and half the columns' B rows)
+    const bool pair = sched == kPair256;
     CUtensorMap ma, mb;
     if (!encode_kmajor(enc, &ma, A, M, K, kBM) || !encode_kmajor(enc, &mb, B, N, K, pair ? 128 : BN)) return 2;
     GemmArgs a;
@@ -758,7 +790,7 @@ int launch_attn_folded(const void *q, const void *k, const void *xn, const void 
     if (r) return r;
     ++*launches;
     // the rows' (max, 1 / sum)
-    const int parts = 2 * (S / gemm_bn(S));
+    const int parts = 2 * (S / schedule_bn(choose_gemm(S, S, D, sm_count)));   // as pass 1 runs
     softmax_stats_kernel<<<(S + 7) / 8, 256, 0, s>>>(stats, parts, row_ml, S);
     *err = cudaGetLastError();
     if (*err != cudaSuccess) return 3;
