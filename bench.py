@@ -4,8 +4,9 @@
                     [--workload NAME] [--variant auto|fused|two_pass] [--no-sweep]
 
 A step is one call of the whole path (pass 1, finalize, pass 2) on one
-synthetic bf16 activation of the workload (default: N=1 C=512 H=W=128, the
-FLUX.2 VAE mid-block GroupNorm shape).  Inputs are seeded (see
+synthetic bf16 activation of the workload (default: N=1 C=256 H=W=1024, the
+FLUX.2 VAE up-block GroupNorm shape, 512 MiB: the largest configuration).
+Inputs are seeded (see
 ``channels_last_groupnorm_gb300/workloads.py``) and already resident in HBM;
 consecutive steps rotate over enough buffer sets that no step finds its
 input in L2.  The timed steps are captured once into a CUDA graph and
@@ -41,7 +42,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "NHWC GroupNorm+SiLU µs/call and HBM GB/s (% of GB300 peak), bf16 G=32"
-DEFAULT_WORKLOAD = "gn_silu_c512_128x128"
+DEFAULT_WORKLOAD = "gn_silu_c256_1024x1024"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 UPCONV_METRIC = "fused nearest-2x upsample + 3x3 conv, bf16 in/out, fp32 accumulate: us/call and TFLOP/s"
@@ -264,8 +265,16 @@ def raw_entry(w):
     return gs.raw_gn_silu_rows_any if (w.general or w.D > 1) else gs.raw_gn_silu_rows_ex
 
 
+def line_config(w, silu, world):
+    """The `config` of a GroupNorm line; both arms print the same one."""
+    return {**w.describe(), "silu": bool(silu),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (rotating buffer sets of x + y that together exceed twice L2)",
+            "bytes_per_step": "N*L*C*4 (x read once, y written once)"}
+
+
 def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, sampler=None,
-                     seeded=True, launch="graph", hot_l2=False):
+                     seeded=True, launch="graph", hot_l2=False, apply_silu=True):
     """Device-resident timing of one workload.  Returns a dict."""
     import torch
     from channels_last_groupnorm_gb300 import gnsilu as gs
@@ -290,10 +299,11 @@ def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, s
     ys = [torch.empty_like(x0) for _ in range(nsets)]
     h = stream.cuda_stream
     entry = raw_entry(w)
+    silu = 1 if apply_silu else 0
 
     def call(i):
         rc = entry(xs[i].data_ptr(), gamma.data_ptr(), beta.data_ptr(), ys[i].data_ptr(), w.N, w.L,
-                   w.C, w.G, w.eps, 1, variant=variant_id, stream=h)
+                   w.C, w.G, w.eps, silu, variant=variant_id, stream=h)
         if rc != 0:
             raise RuntimeError(f"{entry.__name__} failed: {gs.status_string(rc)}")
 
@@ -428,64 +438,98 @@ def cpu_model() -> str:
     return ""
 
 
-def cpu_baseline(w, budget_s=12.0):
-    """The fp64 oracle on this host's cores, on the full workload tensor,
-    repeated until about `budget_s` of CPU time has passed; plus a short
-    single-thread run."""
-    import oracle
-    from channels_last_groupnorm_gb300 import workloads as wl
-    case = wl.make_inputs(w)
-    orc = oracle.get()
-    cores = orc.max_threads()
+def time_oracle(orc, case, w, silu, budget_s, max_calls, nthreads=0):
+    """Mean seconds per full oracle call, over calls until `budget_s` has
+    passed (at least one, at most `max_calls`)."""
     t0 = time.perf_counter()
     calls = 0
     while True:
-        orc.forward(case["x_bits"], case["gamma"], case["beta"], w.G, w.eps, True)
+        orc.forward(case["x_bits"], case["gamma"], case["beta"], w.G, w.eps, silu, nthreads=nthreads)
         calls += 1
-        if time.perf_counter() - t0 >= budget_s or calls >= 50:
+        if time.perf_counter() - t0 >= budget_s or calls >= max_calls:
             break
-    dt = (time.perf_counter() - t0) / calls
-    t1 = time.perf_counter()
-    calls1 = 0
-    while True:
-        orc.forward(case["x_bits"], case["gamma"], case["beta"], w.G, w.eps, True, nthreads=1)
-        calls1 += 1
-        if time.perf_counter() - t1 >= budget_s / 4 or calls1 >= 20:
-            break
-    dt1 = (time.perf_counter() - t1) / calls1
-    return {"value": 4.0 * w.elements / dt / 1e9, "unit": "GB/s", "cores": cores,
-            "kind": "oracle", "us_per_call": dt * 1e6, "cpu_model": cpu_model(),
+    return (time.perf_counter() - t0) / calls, calls
+
+
+def cpu_baseline(w, budget_s=10.0, case=None):
+    """The fp64 oracle on this host's cores, on the full workload tensor,
+    repeated until about `budget_s` of CPU time has passed; plus a
+    single-thread run."""
+    import oracle
+    from channels_last_groupnorm_gb300 import workloads as wl
+    case = case or wl.make_inputs(w)
+    orc = oracle.get()
+    cores = orc.max_threads()
+    dt, calls = time_oracle(orc, case, w, True, budget_s, 50)
+    dt1, calls1 = time_oracle(orc, case, w, True, budget_s / 4, 20, nthreads=1)
+    return {"value": round(4.0 * w.elements / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "us_per_call": round(dt * 1e6, 1), "cpu_model": cpu_model(),
             "one_thread": {"value": round(4.0 * w.elements / dt1 / 1e9, 4), "unit": "GB/s",
                            "us_per_call": round(dt1 * 1e6, 1), "calls": calls1},
             "sample": f"{calls} full calls of the fp64 oracle on the {w.name} tensor "
-                      f"({w.elements} elements), {cores} OpenMP threads"}
+                      f"({w.elements} elements), {cores} OpenMP threads; {calls1} on one thread"}
+
+
+def cpu_baselines(budget_s=1.0):
+    """The fp64 oracle on every configuration (and both SiLU settings of the
+    one run with and without it), all host cores and one thread: one full
+    call or more each, µs/call and GB/s at 4 B/elem."""
+    import oracle
+    from channels_last_groupnorm_gb300 import workloads as wl
+    orc = oracle.get()
+    cores = orc.max_threads()
+    out = []
+    for w in wl.WORKLOADS:
+        case = wl.make_inputs(w)
+        for silu in w.silu_modes:
+            dt, _ = time_oracle(orc, case, w, silu, budget_s, 20)
+            dt1, _ = time_oracle(orc, case, w, silu, budget_s / 2, 5, nthreads=1)
+            out.append({"workload": w.name, "silu": silu, "cores": cores,
+                        "us": round(dt * 1e6, 1), "gbs": round(4.0 * w.elements / dt / 1e9, 3),
+                        "us_1t": round(dt1 * 1e6, 1), "gbs_1t": round(4.0 * w.elements / dt1 / 1e9, 3)})
+        del case
+    return out
 
 
 def sweep(variant_id, device, stream, peak, launch="graph"):
-    """Every workload shape, the general-channel ones included: us/call and
-    effective bandwidth at 4 B/elem (read once + write once) and 6 B/elem
-    (two-pass byte count)."""
+    """Every workload shape (and SiLU setting), the general-channel ones
+    included: us/call and effective bandwidth at 4 B/elem (read once + write
+    once) and 6 B/elem (two-pass byte count)."""
     from channels_last_groupnorm_gb300 import workloads as wl
     out = []
     for w in wl.WORKLOADS + wl.GENERAL_WORKLOADS:
-        r = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24),
-                             launch=launch)
-        us = statistics.median(r["per_step_ms"]) * 1e3
-        gbs4 = 4.0 * w.elements / (us * 1e-6) / 1e9
-        gbs6 = 6.0 * w.elements / (us * 1e-6) / 1e9
-        hot = None
-        if w.elements <= 1 << 25:
-            # the small shapes also with one buffer set: x and y stay in L2
-            rh = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24),
-                                  launch=launch, hot_l2=True)
-            hot = round(statistics.median(rh["per_step_ms"]) * 1e3, 2)
-        out.append({"workload": w.name, "C": w.C, "variant": r["variant"],
-                    "us_per_call": round(us, 2), "us_per_call_hot_l2": hot,
-                    "gbs_4B": round(gbs4, 1), "gbs_6B": round(gbs6, 1),
-                    "frac_4B": round(gbs4 / peak, 3), "frac_6B": round(gbs6 / peak, 3),
-                    "pages_h200_us": w.pages_us_h200,
-                    "l2": f"{r['nsets']} rotating buffer sets of {r['set_bytes'] >> 20} MiB",
-                    "launch": r["launch"]})
+        for silu in w.silu_modes:
+            r = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24),
+                                 launch=launch, apply_silu=silu)
+            us = statistics.median(r["per_step_ms"]) * 1e3
+            gbs4 = 4.0 * w.elements / (us * 1e-6) / 1e9
+            gbs6 = 6.0 * w.elements / (us * 1e-6) / 1e9
+            hot = None
+            if w.elements <= 1 << 25:
+                # the small shapes also with one buffer set: x and y stay in L2
+                rh = measure_workload(w, variant_id, 30, 5, device, stream, seeded=(w.elements <= 1 << 24),
+                                      launch=launch, hot_l2=True, apply_silu=silu)
+                hot = round(statistics.median(rh["per_step_ms"]) * 1e3, 2)
+            out.append({"workload": w.name, "C": w.C, "silu": silu, "variant": r["variant"],
+                        "us_per_call": round(us, 2), "us_per_call_hot_l2": hot,
+                        "gbs_4B": round(gbs4, 1), "gbs_6B": round(gbs6, 1),
+                        "frac_4B": round(gbs4 / peak, 3), "frac_6B": round(gbs6 / peak, 3),
+                        "pages_h200_us": w.pages_us_h200,
+                        "l2": f"{r['nsets']} rotating buffer sets of {r['set_bytes'] >> 20} MiB",
+                        "launch": r["launch"]})
+    return out
+
+
+def compact_sweep(rows):
+    """One short string per swept shape, so the figures survive a reader
+    that keeps only the end of the line."""
+    out = []
+    for r in rows:
+        name = r["workload"].replace("gn_silu_", "").replace("gn_", "")
+        out.append(f"{name}{'' if r['silu'] else ' nosilu'} {r['variant']} {r['us_per_call']}us "
+                   f"4B={r['frac_4B']} 6B={r['frac_6B']}"
+                   + (f" hotL2={r['us_per_call_hot_l2']}us" if r["us_per_call_hot_l2"] else "")
+                   + (f" h200={r['pages_h200_us']}us" if r["pages_h200_us"] else ""))
     return out
 
 
@@ -929,19 +973,18 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_call": round(ms_per_step * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
-        "data": "synthetic (seeded numpy PCG64; x~N(0,1) bf16, gamma~U(0.5,1.5), beta~N(0,0.1))",
-        "config": {**w.describe(), "silu": True, "variant": r["variant"],
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: {r['nsets']} rotating buffer sets of "
-                         f"{r['set_bytes'] >> 20} MiB (x+y)",
-                   "bytes_per_step": "N*L*C*4 (x read once, y written once)",
-                   "launch": r["launch"]},
+        "data": (f"synthetic (seeded numpy PCG64; x~N({w.x_mean},{w.x_std}) bf16, gamma~U(0.5,1.5), "
+                 "beta~N(0,0.1))"),
+        "config": line_config(w, True, world),
+        "schedule": {"variant": r["variant"], "launch": r["launch"],
+                     "buffer_sets": f"{r['nsets']} rotating buffer sets of {r['set_bytes'] >> 20} MiB (x+y)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic,
                      "kernel": "gn_fused_kernel" if r["variant"] == "fused"
                                else "pass1+finalize+pass2",
                      "algorithmic_bytes_per_launch": alg_bytes,
+                     "achieved_6B": round(1.5 * achieved, 1), "frac_6B": round(1.5 * achieved / peak, 4),
                      "launch_us_mean": round(launch_ms * 1e3, 3),
                      "launch_us_median": round(statistics.median(per) * 1e3, 3)},
         "e2e": e2e,
@@ -956,16 +999,20 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0 and not args.no_sweep:
-        line["sweep"] = sweep(variant_id, device, stream, peak, launch=args.launch)
+        tpeak = tensor_peak()[0]
         line["residual_gate"] = [measure_rga(rw, fmt, 50, device, stream, peak)
                                  for rw in wl.RGA_WORKLOADS for fmt in ("bf16", "fp16")]
-        tpeak = tensor_peak()[0]
         line["upsample_conv"] = [measure_upconv(uw, 20, device, stream, tpeak)
                                  for uw in wl.UPCONV_WORKLOADS[1:]]
         line["attention_folded"] = [measure_attn(aw, 10, device, stream, tpeak)
                                     for aw in wl.ATTN_WORKLOADS[1:]]
+        rows = sweep(variant_id, device, stream, peak, launch=args.launch)
+        line["sweep"] = rows
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baselines"] = cpu_baselines()
+        line["gn_sweep"] = compact_sweep(rows)
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -1049,7 +1096,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": w.describe(),
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": line_config(w, True, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

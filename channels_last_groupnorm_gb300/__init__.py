@@ -14,6 +14,8 @@ from .gnsilu import (  # noqa: F401
     gn_abi_version,
     gn_device_status,
     gn_kernel_launch_count,
+    gn_library_workspaces,
+    gn_release_workspaces,
     gn_silu_ndhwc,
     gn_silu_nhwc,
     gn_silu_pick_variant,
@@ -21,6 +23,7 @@ from .gnsilu import (  # noqa: F401
     gn_silu_rows_any,
     gn_silu_rows_ex,
     gn_silu_workspace_bytes,
+    new_workspace,
     residual_gate_add,
     status_string,
     upconv_fold,

@@ -52,6 +52,8 @@
 namespace gn {
 
 __device__ unsigned int g_at_status;
+// the host-visible copy of g_at_status (mapped page-locked host memory; null until set)
+__device__ unsigned int *g_at_status_host;
 
 namespace {
 
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int m0 = (t / args.n_tiles) * kBM, n0 = (t % args.n_tiles) * BN;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_at_status)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host)) {
                     go = false;
                     break;
                 }
@@ -361,12 +363,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool go = true;
         for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
-            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_at_status)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_at_status)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host)) {
                     go = false;
                     break;
                 }
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
-            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_at_status);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
             const uint32_t tbase =
@@ -504,7 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const int nrow = (T % args.n_tiles) * BN + rank * 128;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_at_status)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host)) {
                     go = false;
                     break;
                 }
@@ -521,12 +523,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         bool go = true;
         for (int T = pair; go && T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_at_status)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_at_status)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host)) {
                     go = false;
                     break;
                 }
@@ -550,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         int lt = 0;
         for (int T = pair; T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_at_status);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_at_status, g_at_status_host);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
             const uint32_t tbase =
@@ -817,6 +819,11 @@ cudaError_t clear_attn_status()
 {
     const unsigned int zero = 0;
     return cudaMemcpyToSymbol(g_at_status, &zero, sizeof(unsigned int));
+}
+
+cudaError_t set_attn_status_host(unsigned int *host_word)
+{
+    return cudaMemcpyToSymbol(g_at_status_host, &host_word, sizeof(host_word));
 }
 
 }  // namespace gn

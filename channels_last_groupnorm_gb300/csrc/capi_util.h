@@ -24,5 +24,15 @@ int current_device(int *dev_out, DeviceInfo *info_out);
 uint64_t wait_timeout_ns();
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb);
 void count_launches(uint64_t n);
+// True once a kernel on device `dev` has given up a bounded wait and the
+// status has not been cleared since (read from mapped host memory, no
+// synchronisation).
+bool kernel_status_raised(int dev);
+// Every check gn_silu_rows_ex() makes before it launches anything, for the
+// automatic schedule and a caller workspace: GN_OK with the workspace bytes
+// the call needs, or the status the call would return.
+int check_rows_call(const void *x, const float *gamma, const float *beta, const void *y, int64_t N, int64_t L,
+                    int64_t C, int64_t G, float eps, const float *mean_out, const float *rstd_out,
+                    size_t *workspace_need);
 
 }  // namespace gn_capi

@@ -42,11 +42,27 @@ using gn_capi::wait_timeout_ns;
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
 
+// Library-owned workspaces, one per (device, stream) on which calls without
+// a caller workspace arrive, at most kMaxStreamWorkspaces per device: the
+// least recently used one is freed when a further stream arrives, so that a
+// caller that creates streams per request does not leak one per stream.
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
+    uint64_t last_use = 0;
 };
+constexpr int kMaxStreamWorkspaces = 8;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+uint64_t g_workspace_clock = 0;
+
+// Host-visible copies of the kernels' sticky status, one word per device
+// index, in page-locked host memory mapped into every device (registered
+// on the first call that sets up a device).  A kernel whose bounded wait
+// expires sets its device's word; every entry point reads it before it
+// launches anything, without synchronising.
+constexpr int kStatusWords = 16384;
+alignas(65536) unsigned int g_status_words[kStatusWords];
+bool g_status_registered = false;
 
 uint64_t env_u64(const char *name, uint64_t dflt)
 {
@@ -239,20 +255,44 @@ size_t workspace_bytes_any(int64_t N, int64_t L, int64_t C, int64_t G, const Dev
     return a.ws_bytes > b.ws_bytes ? a.ws_bytes : b.ws_bytes;
 }
 
-// Library-owned workspace of (device, stream), grown on demand.
+// Frees one library workspace once no kernel can still be using it.
+int free_workspace(Workspace &w)
+{
+    if (!w.ptr) return GN_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(w.ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_CUDA;
+    }
+    w.ptr = nullptr;
+    w.bytes = 0;
+    return GN_OK;
+}
+
+// Library-owned workspace of (device, stream), grown on demand; a new
+// stream beyond kMaxStreamWorkspaces on the device takes the place of the
+// least recently used one.
 int library_workspace(int dev, cudaStream_t stream, size_t bytes, void **ptr)
 {
     std::lock_guard<std::mutex> lock(g_mu);
-    Workspace &w = g_workspaces[{dev, stream}];
-    if (w.bytes < bytes) {
-        if (w.ptr) {
-            if (cudaFree(w.ptr) != cudaSuccess) {   // synchronises: no kernel still uses it
-                cudaGetLastError();
-                return GN_ERR_CUDA;
-            }
-            w.ptr = nullptr;
-            w.bytes = 0;
+    auto it = g_workspaces.find({dev, stream});
+    if (it == g_workspaces.end()) {
+        int count = 0;
+        auto lru = g_workspaces.end();
+        for (auto j = g_workspaces.begin(); j != g_workspaces.end(); ++j) {
+            if (j->first.first != dev) continue;
+            ++count;
+            if (lru == g_workspaces.end() || j->second.last_use < lru->second.last_use) lru = j;
         }
+        if (count >= kMaxStreamWorkspaces) {
+            if (free_workspace(lru->second) != GN_OK) return GN_ERR_CUDA;
+            g_workspaces.erase(lru);
+        }
+        it = g_workspaces.emplace(std::make_pair(dev, stream), Workspace{}).first;
+    }
+    Workspace &w = it->second;
+    w.last_use = ++g_workspace_clock;
+    if (w.bytes < bytes) {
+        if (free_workspace(w) != GN_OK) return GN_ERR_CUDA;
         const size_t want = bytes + bytes / 4;   // headroom for nearby shapes
         void *p = nullptr;
         if (cudaMalloc(&p, want) != cudaSuccess || cudaMemset(p, 0, want) != cudaSuccess) {
@@ -267,19 +307,31 @@ int library_workspace(int dev, cudaStream_t stream, size_t bytes, void **ptr)
     return GN_OK;
 }
 
-int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N, int64_t L, int64_t C,
-        int64_t G, float eps, int apply_silu, float *mean_out, float *rstd_out, void *workspace,
-        size_t workspace_bytes, int variant, void *stream, bool general = false)
+// Every check a GroupNorm call makes before it launches: arguments, device,
+// the sticky kernel status, and the schedule.
+int plan_call(const void *x, const float *gamma, const float *beta, const void *y, int64_t N, int64_t L, int64_t C,
+              int64_t G, float eps, const float *mean_out, const float *rstd_out, const void *workspace, int variant,
+              bool general, int *dev, DeviceInfo *d, Plan *p)
 {
     int rc = validate(x, gamma, beta, y, N, L, C, G, eps, mean_out, rstd_out, general);
     if (rc != GN_OK) return rc;
     if (variant < GN_VARIANT_AUTO || variant > GN_VARIANT_FUSED) return GN_ERR_VARIANT;
     if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256) return GN_ERR_ALIGN;
+    if ((rc = current_device(dev, d)) != GN_OK) return rc;
+    if (gn_capi::kernel_status_raised(*dev)) return GN_ERR_KERNEL;
+    return resolve_variant(variant, N, L, C, G, *d, p);
+}
+
+int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N, int64_t L, int64_t C,
+        int64_t G, float eps, int apply_silu, float *mean_out, float *rstd_out, void *workspace,
+        size_t workspace_bytes, int variant, void *stream, bool general = false)
+{
     int dev = -1;
     DeviceInfo d;
-    if ((rc = current_device(&dev, &d)) != GN_OK) return rc;
     Plan p;
-    if ((rc = resolve_variant(variant, N, L, C, G, d, &p)) != GN_OK) return rc;
+    int rc = plan_call(x, gamma, beta, y, N, L, C, G, eps, mean_out, rstd_out, workspace, variant, general, &dev,
+                       &d, &p);
+    if (rc != GN_OK) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = workspace;
     if (ws) {
@@ -331,6 +383,26 @@ int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N
 
 namespace gn_capi {
 
+int check_rows_call(const void *x, const float *gamma, const float *beta, const void *y, int64_t N, int64_t L,
+                    int64_t C, int64_t G, float eps, const float *mean_out, const float *rstd_out,
+                    size_t *workspace_need)
+{
+    int dev = -1;
+    DeviceInfo d;
+    Plan p;
+    const int rc = plan_call(x, gamma, beta, y, N, L, C, G, eps, mean_out, rstd_out, nullptr, GN_VARIANT_AUTO,
+                             false, &dev, &d, &p);
+    if (rc != GN_OK) return rc;
+    *workspace_need = workspace_bytes_any(N, L, C, G, d);
+    return GN_OK;
+}
+
+bool kernel_status_raised(int dev)
+{
+    if (dev < 0 || dev >= kStatusWords) return false;
+    return reinterpret_cast<volatile unsigned int *>(g_status_words)[dev] != 0u;
+}
+
 // Timeout of every bounded wait inside the kernels.
 uint64_t wait_timeout_ns()
 {
@@ -364,8 +436,26 @@ int current_device(int *dev_out, DeviceInfo *info_out)
             cudaGetLastError();
             return GN_ERR_DEVICE;
         }
-        if (d.major != 10 || d.minor != 3) return GN_ERR_DEVICE;
+        if (d.major != 10 || d.minor != 3 || dev >= kStatusWords) return GN_ERR_DEVICE;
         if (gn::prepare_kernels(static_cast<uint32_t>(d.smem_optin)) != cudaSuccess) {
+            cudaGetLastError();
+            return GN_ERR_CUDA;
+        }
+        // map this device's status word (registering the words once) and
+        // hand its device address to the three kernel files
+        if (!g_status_registered) {
+            if (cudaHostRegister(g_status_words, sizeof(g_status_words),
+                                 cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
+                cudaGetLastError();
+                return GN_ERR_CUDA;
+            }
+            g_status_registered = true;
+        }
+        void *word = nullptr;
+        if (cudaHostGetDevicePointer(&word, &g_status_words[dev], 0) != cudaSuccess || !word ||
+            gn::set_device_status_host(static_cast<unsigned int *>(word)) != cudaSuccess ||
+            gn::set_upconv_status_host(static_cast<unsigned int *>(word)) != cudaSuccess ||
+            gn::set_attn_status_host(static_cast<unsigned int *>(word)) != cudaSuccess) {
             cudaGetLastError();
             return GN_ERR_CUDA;
         }
@@ -463,10 +553,12 @@ int gn_device_status(int clear)
     if (gn::read_upconv_status(&st_uc) != cudaSuccess) return GN_ERR_CUDA;
     if (gn::read_attn_status(&st_at) != cudaSuccess) return GN_ERR_CUDA;
     st |= st_uc | st_at;
+    if (gn_capi::kernel_status_raised(dev)) st |= 1u;
     if (clear) {
         if (gn::clear_device_status() != cudaSuccess) return GN_ERR_CUDA;
         if (gn::clear_upconv_status() != cudaSuccess) return GN_ERR_CUDA;
         if (gn::clear_attn_status() != cudaSuccess) return GN_ERR_CUDA;
+        if (dev < kStatusWords) reinterpret_cast<volatile unsigned int *>(g_status_words)[dev] = 0u;
         std::lock_guard<std::mutex> lock(g_mu);
         for (auto &kv : g_workspaces) {
             if (kv.first.first == dev && kv.second.ptr && cudaMemset(kv.second.ptr, 0, 256) != cudaSuccess)
@@ -474,6 +566,39 @@ int gn_device_status(int clear)
         }
     }
     return st ? GN_ERR_KERNEL : GN_OK;
+}
+
+int gn_release_workspaces(void)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GN_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto it = g_workspaces.begin(); it != g_workspaces.end();) {
+        if (it->first.first != dev) {
+            ++it;
+            continue;
+        }
+        if (free_workspace(it->second) != GN_OK) return GN_ERR_CUDA;
+        it = g_workspaces.erase(it);
+    }
+    return GN_OK;
+}
+
+int gn_library_workspaces(void)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -GN_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    int count = 0;
+    for (const auto &kv : g_workspaces)
+        if (kv.first.first == dev && kv.second.ptr) ++count;
+    return count;
 }
 
 int gn_selftest_bounded_wait(int mode, int timeout_ms, int *done, int blocks, void *stream)
@@ -536,6 +661,7 @@ int gn_residual_gate_add(const void *residual, const void *update, const void *g
     DeviceInfo d;
     const int rc = current_device(&dev, &d);
     if (rc != GN_OK) return rc;
+    if (gn_capi::kernel_status_raised(dev)) return GN_ERR_KERNEL;
     if (rows == 0) return GN_OK;
     // enough resident threads to keep HBM busy, but no more blocks than vectors need
     const int64_t nvec = rows * (D / 8);
@@ -551,6 +677,6 @@ int gn_residual_gate_add(const void *residual, const void *update, const void *g
     return GN_OK;
 }
 
-int gn_abi_version(void) { return 5; }
+int gn_abi_version(void) { return 6; }
 
 }  // extern "C"

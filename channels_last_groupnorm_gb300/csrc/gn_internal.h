@@ -130,5 +130,7 @@ cudaError_t prepare_kernels(uint32_t max_smem);
 cudaError_t launch_selftest_wait(int mode, uint64_t timeout_ns, int *done, int blocks, cudaStream_t s);
 cudaError_t read_device_status(unsigned int *status);
 cudaError_t clear_device_status();
+// Device address of the mapped host word that mirrors the status (current device).
+cudaError_t set_device_status_host(unsigned int *host_word);
 
 }  // namespace gn

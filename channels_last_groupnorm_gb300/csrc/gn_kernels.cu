@@ -43,6 +43,8 @@ namespace gn {
 
 // Sticky device-side status: bit 0 = a bounded wait expired.
 __device__ unsigned int g_status;
+// Its host-visible copy (mapped page-locked host memory; null until set).
+__device__ unsigned int *g_status_host;
 
 // ---------------------------------------------------------------------------
 // packed fp32 pairs (sm_100+ f32x2 arithmetic)
@@ -231,6 +233,7 @@ __device__ __forceinline__ void record_timeout(const Ctl &ctl)
 {
     *ctl.abort = 1;
     atomicOr(&g_status, 1u);
+    raise_host_status(g_status_host);
 }
 
 // Waiting threads sleep in the try_wait (up to kWaitSleepNs per round)
@@ -1447,6 +1450,11 @@ cudaError_t clear_device_status()
 {
     const unsigned int zero = 0;
     return cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned int));
+}
+
+cudaError_t set_device_status_host(unsigned int *host_word)
+{
+    return cudaMemcpyToSymbol(g_status_host, &host_word, sizeof(host_word));
 }
 
 }  // namespace gn

@@ -19,6 +19,18 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// Sets the host-visible copy of the sticky kernel status: a word of
+// page-locked host memory mapped into the device (null until the library
+// has mapped it).  The host reads it before every launch, without
+// synchronising, so a bounded wait that expired makes later calls fail.
+__device__ __forceinline__ void raise_host_status(unsigned int *host_word)
+{
+    if (host_word) {
+        *reinterpret_cast<volatile unsigned int *>(host_word) = 1u;
+        __threadfence_system();
+    }
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {

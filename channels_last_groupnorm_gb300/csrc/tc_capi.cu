@@ -51,6 +51,7 @@ int gn_upconv_fold(const void *w, void *wf, int64_t Cin, int64_t Cout, void *str
     DeviceInfo d;
     const int rc = current_device(&dev, &d);
     if (rc != GN_OK) return rc;
+    if (gn_capi::kernel_status_raised(dev)) return GN_ERR_KERNEL;
     const cudaError_t e = gn::launch_upconv_fold(w, wf, static_cast<int>(Cin), static_cast<int>(Cout), d.sm_count,
                                                  static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
@@ -81,6 +82,7 @@ int gn_upconv_nhwc(const void *x, const void *wf, const void *bias, void *y, int
     DeviceInfo d;
     const int rc = current_device(&dev, &d);
     if (rc != GN_OK) return rc;
+    if (gn_capi::kernel_status_raised(dev)) return GN_ERR_KERNEL;
     if (N == 0) return GN_OK;
     cudaError_t e = cudaSuccess;
     const int r = gn::launch_upconv(x, wf, bias, y, static_cast<int>(N), static_cast<int>(H), static_cast<int>(W),
@@ -124,6 +126,7 @@ int gn_attn_fold(const void *wv, const void *bv, const void *wo, const void *bo,
     DeviceInfo d;
     const int rc = current_device(&dev, &d);
     if (rc != GN_OK) return rc;
+    if (gn_capi::kernel_status_raised(dev)) return GN_ERR_KERNEL;
     const cudaError_t e = gn::launch_attn_fold(wv, bv, wo, bo, wf, bf, static_cast<int>(D), d.sm_count,
                                                static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
@@ -168,6 +171,7 @@ int gn_attn_folded(const void *q, const void *k, const void *xn, const void *wf,
     DeviceInfo d;
     const int rc = current_device(&dev, &d);
     if (rc != GN_OK) return rc;
+    if (gn_capi::kernel_status_raised(dev)) return GN_ERR_KERNEL;
     cudaError_t e = cudaSuccess;
     int launches = 0;
     const int r = gn::launch_attn_folded(q, k, xn, wf, bf, residual, out, static_cast<int>(S), static_cast<int>(D),

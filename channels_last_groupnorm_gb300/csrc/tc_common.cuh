@@ -19,10 +19,10 @@ namespace tc {
 constexpr uint32_t kSleepNs = 20000;
 
 // Bounded wait on an mbarrier phase.  False once `timeout_ns` pass (the
-// CTA's abort flag and the kernel file's status word are then set), or at
-// once when another thread of the CTA has aborted.
+// CTA's abort flag, the kernel file's status word and its host-visible copy
+// are then set), or at once when another thread of the CTA has aborted.
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns,
-                                     unsigned int *status)
+                                     unsigned int *status, unsigned int *host_status)
 {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
@@ -34,6 +34,7 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int
         if (global_ns() > deadline) {
             *abort = 1;
             atomicOr(status, 1u);
+            raise_host_status(host_status);
             return false;
         }
     }

@@ -26,6 +26,8 @@ int launch_upconv(const void *x, const void *wf, const void *bias, void *y, int 
                   int Cout, int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err);
 cudaError_t read_upconv_status(unsigned int *status);
 cudaError_t clear_upconv_status();
+// Device address of the mapped host word that mirrors the status (current device).
+cudaError_t set_upconv_status_host(unsigned int *host_word);
 
 // ---- single-head attention with the output projection folded into V (attn_kernels.cu) ----
 constexpr int kAttnMaxS = 32768;   // the longest sequence gn_attn_folded takes
@@ -39,5 +41,7 @@ int launch_attn_folded(const void *q, const void *k, const void *xn, const void 
                        uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches);
 cudaError_t read_attn_status(unsigned int *status);
 cudaError_t clear_attn_status();
+// Device address of the mapped host word that mirrors the status (current device).
+cudaError_t set_attn_status_host(unsigned int *host_word);
 
 }  // namespace gn

@@ -60,6 +60,8 @@
 namespace gn {
 
 __device__ unsigned int g_uc_status;
+// the host-visible copy of g_uc_status (mapped page-locked host memory; null until set)
+__device__ unsigned int *g_uc_status_host;
 
 namespace {
 
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kUcThreads, 1)
             const int wrow = tc.parity * args.Cout + tc.co0;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host)) {
                     go = false;
                     break;
                 }
@@ -315,12 +317,12 @@ __global__ void __launch_bounds__(kUcThreads, 1)
         for (int t = blockIdx.x; go && t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
             // the epilogue has drained this accumulator (tile lt - 2)
-            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_uc_status)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host)) {
                     go = false;
                     break;
                 }
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(kUcThreads, 1)
         int lt = 0;
         for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++lt) {
             const int buf = lt & 1;
-            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_uc_status);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host);
             tc_fence_after_sync();
             // warp-uniform, as the tensor-memory loads below are warp-collective
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
@@ -490,7 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
             const int wrow = tc.parity * args.Cout + tc.co0 + rank * 128;
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) {
+                if (q >= STAGES && !tc::wait(bar_empty + 8 * s, ((q / STAGES) - 1) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host)) {
                     go = false;
                     break;
                 }
@@ -512,12 +514,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
         bool go = true;
         for (int T = pair; go && T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_uc_status)) break;
+            if (lt >= 2 && !tc::wait(bar_acc_empty + 8 * buf, ((lt >> 1) - 1) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host)) break;
             tc_fence_after_sync();
             const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
             for (int kt = 0; kt < args.ksteps; ++kt, ++q) {
                 const int s = q % STAGES;
-                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_uc_status)) {
+                if (!tc::wait(bar_full + 8 * s, (q / STAGES) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host)) {
                     go = false;
                     break;
                 }
@@ -542,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
         int lt = 0;
         for (int T = pair; T < args.tiles; T += npairs, ++lt) {
             const int buf = lt & 1;
-            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_uc_status);
+            const bool done = tc::wait(bar_acc_full + 8 * buf, (lt >> 1) & 1, abort, args.timeout_ns, &g_uc_status, g_uc_status_host);
             tc_fence_after_sync();
             if (!__all_sync(0xffffffffu, done && !*abort)) break;
             const uint32_t tbase =
@@ -752,6 +754,11 @@ cudaError_t clear_upconv_status()
 {
     const unsigned int zero = 0;
     return cudaMemcpyToSymbol(g_uc_status, &zero, sizeof(unsigned int));
+}
+
+cudaError_t set_upconv_status_host(unsigned int *host_word)
+{
+    return cudaMemcpyToSymbol(g_uc_status_host, &host_word, sizeof(host_word));
 }
 
 }  // namespace gn

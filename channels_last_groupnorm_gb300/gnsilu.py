@@ -8,8 +8,10 @@ raises.
 
 Unsupported inputs give ``None``, the contract of the sglang PR #33451 page
 ("FLUX.2 VAE decoder fast path behind quality=high", section
-"Modifications", item 2: non-CUDA, grad enabled, non-power-of-two C,
-C > 2048, not channels_last), so callers can fall back to their own path.
+"Modifications", item 1, second bullet: non-CUDA, grad enabled,
+non-power-of-two C, C > 2048, not channels_last), so callers can fall back
+to their own path.  A caller-given ``out`` or ``workspace`` of the wrong
+shape, dtype, device or layout is unsupported input too.
 ``gn_silu_rows_any`` and ``gn_silu_ndhwc`` take any C that is a multiple of 8
 up to 2048 (any channels per group) and 5D channels-last input, the range of
 the page's existing general kernel (same section, item 1, third bullet).
@@ -81,6 +83,8 @@ EXPORTS = {
     "gn_silu_pick_variant": (ctypes.c_int, [ctypes.c_int64] * 4),
     "gn_kernel_launch_count": (ctypes.c_uint64, []),
     "gn_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "gn_release_workspaces": (ctypes.c_int, []),
+    "gn_library_workspaces": (ctypes.c_int, []),
     "gn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gn_abi_version": (ctypes.c_int, []),
 }
@@ -170,6 +174,15 @@ def gn_abi_version() -> int:
     return int(lib().gn_abi_version())
 
 
+def gn_release_workspaces() -> int:
+    """Free the workspaces the library allocated on the current device."""
+    return int(lib().gn_release_workspaces())
+
+
+def gn_library_workspaces() -> int:
+    return int(lib().gn_library_workspaces())
+
+
 # ---------------------------------------------------------------------------
 # tensor entry points
 # ---------------------------------------------------------------------------
@@ -182,6 +195,12 @@ def _affine_ok(t, C, device) -> bool:
     torch = _torch()
     return (t is not None and t.is_cuda and t.device == device and t.dtype == torch.float32
             and t.dim() == 1 and t.numel() == C and t.is_contiguous())
+
+
+def _workspace_ok(ws, device) -> bool:
+    torch = _torch()
+    return (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.device == device and ws.dtype == torch.uint8
+            and ws.dim() == 1 and ws.is_contiguous())
 
 
 def _grad_blocked(*ts) -> bool:
@@ -254,11 +273,31 @@ def gn_silu_rows(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: boo
     return out if _finish(rc, "gn_silu_rows") else None
 
 
+def new_workspace(x, G: int = 32):
+    """A zero-filled workspace for ``gn_silu_rows_ex`` / ``gn_silu_rows_any``
+    on rows shaped like ``x`` (N, L, C): a uint8 tensor on x's device of
+    ``gn_silu_workspace_bytes`` bytes, or None if the shape is unsupported."""
+    torch = _torch()
+    N, L, C = x.shape
+    with torch.cuda.device(x.device):
+        need = gn_silu_workspace_bytes(N, L, C, G)
+    if need == 0:
+        return None
+    return torch.zeros(need, dtype=torch.uint8, device=x.device)
+
+
 def gn_silu_rows_ex(x, gamma, beta, G: int = 32, eps: float = 1e-6, apply_silu: bool = True,
                     out=None, variant: int = VARIANT_AUTO, workspace=None, stream=None):
     """``gn_silu_rows`` that also returns the fp32 statistics:
-    (y, mean [N, G], rstd [N, G]), or None when unsupported.  ``workspace``
-    is an optional uint8 CUDA tensor (see ``gn_silu_workspace_bytes``)."""
+    (y, mean [N, G], rstd [N, G]), or None when unsupported.
+
+    ``workspace``: None (the library's own), or a contiguous uint8 tensor on
+    x's device of at least ``gn_silu_workspace_bytes`` bytes whose first 256
+    bytes are zero before its first use -- ``new_workspace(x, G)`` makes one.
+    The kernels leave those bytes zero after every successful call, so the
+    same workspace serves any number of calls that do not overlap on the
+    GPU; after ``gn_device_status(True)`` clears a failure it must be zeroed
+    again."""
     return _rows_with_stats(raw_gn_silu_rows_ex, "gn_silu_rows_ex", x, gamma, beta, G, eps,
                             apply_silu, out, variant, workspace, stream)
 
@@ -310,11 +349,16 @@ def _rows_with_stats(raw, what, x, gamma, beta, G, eps, apply_silu, out, variant
         return None
     if out is None:
         out = torch.empty_like(x)
-    mean = torch.empty((N, G), dtype=torch.float32, device=x.device)
-    rstd = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    elif not (isinstance(out, torch.Tensor) and out.shape == x.shape and out.dtype == x.dtype
+              and out.device == x.device and out.is_contiguous()):
+        return None
     ws_ptr, ws_bytes = 0, 0
     if workspace is not None:
-        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        if not _workspace_ok(workspace, x.device):
+            return None
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    mean = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    rstd = torch.empty((N, G), dtype=torch.float32, device=x.device)
     with torch.cuda.device(x.device):
         rc = raw(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
                  N, L, C, G, eps, apply_silu, mean.data_ptr(), rstd.data_ptr(),
@@ -494,7 +538,9 @@ def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, 
     from ``attn_fold``; equal to the unfolded single-head attention block
     (value projection, attention, output projection, residual).  Returns
     out [S, D] bf16, or None when not supported (S not a multiple of 128 in
-    [128, 32768], D not a multiple of 128 in [128, 1024], layouts, dtypes)."""
+    [128, 32768], D not a multiple of 128 in [128, 1024], layouts, dtypes,
+    a ``workspace`` that is not a contiguous 1-D uint8 tensor on q's
+    device; a smaller one is replaced by a fresh one)."""
     lib()
     torch = _torch()
     ts = (q, k, xn)
@@ -523,11 +569,13 @@ def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, 
     elif not (out.shape == q.shape and out.dtype == torch.bfloat16 and out.is_contiguous()
               and out.device == q.device):
         return None
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
+    if workspace is not None and not _workspace_ok(workspace, q.device):
+        return None
+    if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
         rc = raw_gn_attn_folded(q.data_ptr(), k.data_ptr(), xn.data_ptr(), wf.data_ptr(), bf.data_ptr(),
                                 0 if residual is None else residual.data_ptr(), out.data_ptr(), S, D,
-                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                workspace.data_ptr(), workspace.numel(),
                                 _stream_handle(q.device, stream))
     return out if _finish(rc, "gn_attn_folded") else None

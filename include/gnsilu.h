@@ -19,7 +19,8 @@
  * statistics and one round-to-nearest-even rounding of y to bf16.
  *
  * Supported inputs (the page's "unsupported inputs are rejected" contract,
- * same section, item 2): C a power of two in [8, 2048], G >= 1 dividing C,
+ * same section, item 1, second bullet): C a power of two in [8, 2048],
+ * G >= 1 dividing C,
  * N, L >= 1.  Unsupported inputs return a non-zero status and touch nothing.
  * Two further entry points, gn_silu_rows_any() and gn_silu_ndhwc(), widen C
  * to any multiple of 8 up to 2048 (any channels per group, e.g. C = 320 or
@@ -42,13 +43,25 @@
  * enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
  * and the call returns without synchronising: a return of GN_OK means the
  * arguments were valid and the kernels were launched.  Faults that happen
- * later surface at the caller's next synchronisation, and the kernels'
- * own bounded-wait failures are reported by gn_device_status().
+ * later surface at the caller's next synchronisation.  Every wait inside a
+ * kernel is bounded; a kernel that gives up one records a sticky status in
+ * device memory and in a word of page-locked host memory mapped into the
+ * device.  From the moment that host word is set, every entry point that
+ * launches kernels returns GN_ERR_KERNEL without launching, until
+ * gn_device_status(1) clears it (calls enqueued before then return GN_OK,
+ * and their kernels return at once without writing any output).
  *
  * Thread safety: calls from several host threads are safe.  Calls on
  * different streams of one device that use the library's own workspace are
- * safe (the workspace is kept per device and stream); two calls that share
- * one caller-provided workspace must not overlap on the GPU.
+ * safe (the workspace is kept per device and stream, for up to eight streams
+ * per device; a further stream takes the place of the least recently used
+ * one, whose workspace is freed after a device synchronisation); two calls
+ * that share one caller-provided workspace must not overlap on the GPU.
+ *
+ * Device reset: the library keeps per-device state (kernel attributes, its
+ * workspaces, the mapped status word, the static scratch address).
+ * cudaDeviceReset() destroys what that state refers to; a process that
+ * resets a device must not call the library on that device afterwards.
  */
 #ifndef GNSILU_H
 #define GNSILU_H
@@ -78,7 +91,8 @@ enum gn_status_code {
     GN_ERR_DEVICE = 9,     /* no CUDA device, or the current device is not sm_103 */
     GN_ERR_VARIANT = 10,   /* unknown variant, or the fused variant cannot be
                               launched cooperatively for this shape */
-    GN_ERR_KERNEL = 11,    /* gn_device_status(): a kernel gave up a bounded wait */
+    GN_ERR_KERNEL = 11,    /* a kernel gave up a bounded wait and the status has not
+                              been cleared (gn_device_status(1)) since; nothing ran */
     GN_ERR_FORMAT = 12     /* gn_residual_gate_add(): unknown half format */
 };
 
@@ -111,7 +125,8 @@ int gn_silu_nhwc(const void *x_bf16, const float *gamma, const float *beta, void
  * rows entry, "as used by attention").  Uses a workspace the library
  * allocates on first use for each (device, stream) and grows when a larger
  * shape arrives; that first call allocates (cudaMalloc) and so should come
- * before any CUDA graph capture on the stream.
+ * before any CUDA graph capture on the stream.  gn_release_workspaces()
+ * frees these workspaces.
  */
 int gn_silu_rows(const void *x_bf16, const float *gamma, const float *beta, void *y_bf16,
                  int64_t N, int64_t L, int64_t C, int64_t G,
@@ -183,11 +198,23 @@ uint64_t gn_kernel_launch_count(void);
 /* Synchronises the current device, then returns GN_OK or GN_ERR_KERNEL if
  * one of this library's kernels gave up a bounded wait since the last clear
  * (GN_ERR_CUDA / GN_ERR_DEVICE if the device itself reports an error).
- * Kernels launched while that flag is set return at once without writing
- * any output.  clear != 0 resets the flag and re-zeroes the library's own
- * workspaces on this device; a caller-provided workspace must then be
- * re-zeroed by the caller. */
+ * While that flag is set the entry points return GN_ERR_KERNEL, and kernels
+ * enqueued before it was set return at once without writing any output.
+ * clear != 0 resets the flag (on the device and in host memory) and
+ * re-zeroes the library's own workspaces on this device; a caller-provided
+ * workspace must then be re-zeroed by the caller. */
 int gn_device_status(int clear);
+
+/* Synchronises the current device and frees every workspace the library
+ * allocated on it (those of gn_silu_rows, gn_silu_nhwc, gn_silu_ndhwc and of
+ * gn_silu_rows_ex / gn_silu_rows_any called without a workspace).  Later
+ * calls allocate again.  Must not be called while a stream of the device is
+ * being captured.  Returns GN_OK, GN_ERR_DEVICE or GN_ERR_CUDA. */
+int gn_release_workspaces(void);
+
+/* Number of workspaces the library currently holds on the current device
+ * (at most eight), or a negative status code. */
+int gn_library_workspaces(void);
 
 /* Diagnostic of the kernels' failure handling: launches `blocks` CTAs that
  * each wait for something nothing will ever do -- mode 0: an mbarrier phase
@@ -206,10 +233,12 @@ int gn_selftest_bounded_wait(int mode, int timeout_ms, int *done, int blocks, vo
  * entry point has no counterpart on the sglang PR #33451 page; it is a
  * deployment convenience of this library.)
  *
- * Who needs it: code running while a CUDA graph is captured in global
- * capture mode, where allocation calls are not allowed; plug-ins whose host
- * framework owns every byte of device memory; latency-critical paths that
- * cannot afford an allocator's implicit synchronisation.  gn_silu_rows()
+ * Who needs it: a plug-in inside a host framework that owns every byte of
+ * device memory through its own pool and accounting, and so may not
+ * allocate behind the framework's back; a latency-critical path that cannot
+ * afford the device-wide synchronisation and unbounded time of an
+ * allocation or a free; a process under a fixed device-memory budget that
+ * cannot count on an allocation succeeding mid-run.  gn_silu_rows()
  * allocates its workspace on first use, and gn_silu_rows_ex() needs one from
  * the caller; this entry point needs neither.
  *
@@ -219,10 +248,16 @@ int gn_selftest_bounded_wait(int mode, int timeout_ms, int *done, int blocks, vo
  * to cudaMalloc, cudaFree or any other allocating routine is made.
  *   - Shapes whose scratch need (gn_silu_workspace_bytes) exceeds
  *     GN_STATIC_SCRATCH_BYTES are refused with GN_ERR_WORKSPACE and nothing
- *     runs.  With C = 2048 that still covers N up to about 8 on a GB300.
+ *     runs.  The need is about 8 C N + 16 G N + 8 G max(N, 152) + 2 KB
+ *     on a GB300 (152 SMs): with C = 2048 and G = 32 that covers N up to
+ *     about 490.
+ *   - Every argument check runs before the array is touched: a refused
+ *     call (any non-zero status) writes nothing.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *     (cudaGetSymbolAddress) with that device current, and the first call
+ *     of the library on a device sets the device up (kernel attributes, the
+ *     mapped status word); make that first call before any stream capture
+ *     begins.
  *   - All calls on a device share the one array, which keeps the previous
  *     call's contents; each call clears the words that must start at zero
  *     (an asynchronous memset on `stream`).  Calls whose GPU work overlaps
@@ -373,9 +408,10 @@ int gn_attn_folded(const void *q_bf16, const void *k_bf16, const void *xn_bf16, 
 /* Human-readable name of a status code (static storage). */
 const char *gn_status_string(int status);
 
-/* ABI version of this header: 5 (4 lacked the gn_attn_* calls; 3 also the
- * gn_upconv_* calls; 2 also gn_residual_gate_add; 1 also gn_silu_rows_any
- * and gn_silu_ndhwc). */
+/* ABI version of this header: 6 (5 lacked gn_release_workspaces and
+ * gn_library_workspaces, and its entry points did not return GN_ERR_KERNEL;
+ * 4 also lacked the gn_attn_* calls; 3 also the gn_upconv_* calls; 2 also
+ * gn_residual_gate_add; 1 also gn_silu_rows_any and gn_silu_ndhwc). */
 int gn_abi_version(void);
 
 #ifdef __cplusplus

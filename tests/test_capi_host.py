@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert gs.gn_abi_version() == 5
+    assert gs.gn_abi_version() == 6
     for code in range(13):
         s = gs.status_string(code)
         assert s.startswith("GN_"), (code, s)
@@ -126,6 +126,39 @@ def test_valid_arguments_without_a_device_report_no_device():
     assert rows(y=X) == gs.GN_ERR_DEVICE          # in place is allowed
     assert gs.gn_silu_workspace_bytes(1, 4, 32, 32) == 0
     assert gs.gn_silu_pick_variant(1, 4, 32, 32) == -gs.GN_ERR_DEVICE
+
+
+@no_gpu
+def test_workspace_management_without_a_device():
+    assert gs.gn_release_workspaces() == gs.GN_ERR_DEVICE
+    assert gs.gn_library_workspaces() == -gs.GN_ERR_DEVICE
+
+
+def static(**kw):
+    a = dict(x=X, gamma=GAM, beta=BET, y=Y, N=1, L=4, C=32, G=32, eps=1e-6, apply_silu=1,
+             mean_out=None, rstd_out=None, stream=None)
+    a.update(kw)
+    return gs.lib().gn_silu_rows_static(a["x"], a["gamma"], a["beta"], a["y"], a["N"], a["L"], a["C"],
+                                        a["G"], a["eps"], a["apply_silu"], a["mean_out"], a["rstd_out"],
+                                        a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=0), gs.GN_ERR_NULL),
+    (dict(L=0), gs.GN_ERR_SHAPE),
+    (dict(C=24, G=8), gs.GN_ERR_CHANNELS),        # a general C: only the power-of-two contract here
+    (dict(y=Y + 2), gs.GN_ERR_ALIGN),
+    (dict(eps=-1.0), gs.GN_ERR_EPS),
+    (dict(y=X + 16), gs.GN_ERR_ALIAS),
+])
+def test_static_entry_checks_arguments_before_anything_else(kw, code):
+    # the same statuses, in the same order, as gn_silu_rows_ex; no device is touched
+    assert static(**kw) == code
+
+
+@no_gpu
+def test_static_entry_without_a_device():
+    assert static() == gs.GN_ERR_DEVICE
 
 
 def test_workspace_query_rejects_bad_shapes():

@@ -1,11 +1,15 @@
 """gn_silu_rows_static: the entry point for callers that cannot allocate
-device memory (code inside a CUDA graph capture, plug-ins whose host owns all
-device memory, paths that cannot risk an allocator's synchronisation).
+device memory -- a plug-in whose host framework owns all device memory and
+forbids allocations behind its back, a latency-critical path that cannot
+afford an allocation's device-wide synchronisation, a process under a fixed
+device-memory budget.
 
 It takes its scratch from a fixed array inside the library instead of a
 workspace.  Here it is called through the C ABI and its outputs are compared
-with those of the ordinary entry point (gn_silu_rows_ex), on two calls in a
-row so that the second call sees the scratch the first one left behind.
+with the fp64 oracle and with those of the ordinary entry point
+(gn_silu_rows_ex), on two calls in a row so that the second call sees the
+scratch the first one left behind; and a call on a stream the library has
+not seen before is checked to allocate nothing.
 
 This file is collected last on purpose; it passes alone in a fresh process
 and after the rest of the suite.
@@ -16,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from channels_last_groupnorm_gb300 import build as gnbuild
 from channels_last_groupnorm_gb300 import gnsilu as gs
 from channels_last_groupnorm_gb300 import workloads as wl
@@ -45,15 +50,16 @@ def call_static(x, gamma, beta, y, mean, rstd, G, eps, silu, stream):
 
 @pytest.mark.parametrize("shape,silu", [((1, 16384, 512, 32), True), ((2, 3001, 256, 32), False),
                                         ((3, 777, 2048, 32), True)])
-def test_static_matches_ordinary_entry_point_twice(shape, silu):
+def test_static_matches_oracle_and_ordinary_entry_point_twice(shape, silu):
     N, L, C, G = shape
     case = wl.make_case(N, L, C, seed=N * 7 + L + C, mean=0.3, std=1.4)
     x, gamma, beta = gu.device_inputs(case)
     stream = torch.cuda.current_stream()
-    y_ref, m_ref, r_ref = gu.run_rows_ex(x, gamma, beta, G, 1e-6, silu)
-    y_ref = gu.bf16_to_f64(y_ref)
-    m_ref = m_ref.cpu().numpy().astype(np.float64)
-    r_ref = r_ref.cpu().numpy().astype(np.float64)
+    y_orc, m_orc, r_orc = oracle.forward(case["x_bits"], case["gamma"], case["beta"], G, 1e-6, silu)
+    y_ex, m_ex, r_ex = gu.run_rows_ex(x, gamma, beta, G, 1e-6, silu)
+    y_ex = gu.bf16_to_f64(y_ex)
+    m_ex = m_ex.cpu().numpy().astype(np.float64)
+    r_ex = r_ex.cpu().numpy().astype(np.float64)
     for call in range(2):
         y = torch.full_like(x, float("nan"))
         mean = torch.full((N, G), float("nan"), device=x.device)
@@ -61,10 +67,41 @@ def test_static_matches_ordinary_entry_point_twice(shape, silu):
         rc = call_static(x, gamma, beta, y, mean, rstd, G, 1e-6, silu, stream)
         assert rc == gs.GN_OK, gs.status_string(rc)
         torch.cuda.synchronize()
-        gu.check_y(gu.bf16_to_f64(y), y_ref, f"static call {call}")
-        gu.check_stats(mean.cpu().numpy(), rstd.cpu().numpy(), m_ref, r_ref,
-                       f"static call {call}")
+        y_np = gu.bf16_to_f64(y)
+        m_np, r_np = mean.cpu().numpy(), rstd.cpu().numpy()
+        gu.check_y(y_np, y_orc, f"static call {call} against the oracle")
+        gu.check_stats(m_np, r_np, m_orc, r_orc, f"static call {call} against the oracle")
+        gu.check_y(y_np, y_ex, f"static call {call} against gn_silu_rows_ex")
+        gu.check_stats(m_np, r_np, m_ex, r_ex, f"static call {call} against gn_silu_rows_ex")
     assert gs.gn_device_status(False) == gs.GN_OK
+
+
+def test_static_call_on_a_new_stream_allocates_nothing():
+    # scale/shift of 128 x 2048 channels: a library workspace for this shape
+    # would take more than 2 MiB of device memory
+    N, L, C, G = 128, 8, 2048, 32
+    need = gs.gn_silu_workspace_bytes(N, L, C, G)
+    assert 2 << 20 < need <= STATIC_SCRATCH_BYTES
+    case = wl.make_case(N, L, C, seed=41)
+    x, gamma, beta = gu.device_inputs(case)
+    y = torch.empty_like(x)
+    mean = torch.empty((N, G), device=x.device)
+    rstd = torch.empty((N, G), device=x.device)
+    # first call of the library on this device from this test: sets the device up
+    assert call_static(x, gamma, beta, y, mean, rstd, G, 1e-6, True, torch.cuda.current_stream()) == gs.GN_OK
+    torch.cuda.synchronize()
+    fresh = torch.cuda.Stream()
+    workspaces = gs.gn_library_workspaces()
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _ in range(2):
+        assert call_static(x, gamma, beta, y, mean, rstd, G, 1e-6, True, fresh) == gs.GN_OK
+    fresh.synchronize()
+    assert gs.gn_library_workspaces() == workspaces
+    assert abs(torch.cuda.mem_get_info()[0] - free_before) < (1 << 20)
+    y_ref, m_ref, r_ref = oracle.forward(case["x_bits"], case["gamma"], case["beta"], G, 1e-6, True)
+    gu.check_y(gu.bf16_to_f64(y), y_ref, "static call on a new stream")
+    gu.check_stats(mean.cpu().numpy(), rstd.cpu().numpy(), m_ref, r_ref, "static call on a new stream")
 
 
 def test_static_refuses_shapes_beyond_its_scratch():
