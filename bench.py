@@ -49,7 +49,8 @@ UPCONV_METRIC = "fused nearest-2x upsample + 3x3 conv, bf16 in/out, fp32 accumul
 ATTN_METRIC = ("single-head attention, output projection folded into V, bf16 in/out, fp32 scores and "
                "accumulation: us/call and TFLOP/s")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-KERNEL_SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_internal.h", "gn_ptx.cuh", "capi_util.h", "rga_kernels.cu"]
+KERNEL_SOURCES = ["gn_kernels.cu", "gn_cluster.cu", "gn_capi.cu", "gn_internal.h", "gn_math.cuh", "gn_ptx.cuh",
+                  "capi_util.h", "rga_kernels.cu"]
 UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
 ATTN_SOURCES = ["attn_kernels.cu", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
 
@@ -341,7 +342,7 @@ def measure_workload(w, variant_id, steps, warmup, device, stream, soak_s=0.0, s
         raise RuntimeError(f"device status after timing: {gs.status_string(status)}")
     res = {"elapsed_s": elapsed, "per_step_ms": per, "nsets": nsets, "set_bytes": set_bytes,
            "launches": launches, "clocks": clocks, "launch": mode,
-           "variant": {1: "two_pass", 2: "fused"}.get(
+           "variant": {1: "two_pass", 2: "fused", 3: "cluster"}.get(
                gs.gn_silu_pick_variant(w.N, w.L, w.C, w.G) if variant_id == 0 else variant_id,
                "?")}
     del xs, ys
@@ -438,6 +439,18 @@ def cpu_model() -> str:
     return ""
 
 
+_ORACLE_CORES = None
+
+
+def oracle_cores(orc) -> int:
+    """The oracle's OpenMP thread count before anything set it to one
+    thread (a one-thread run changes the process-wide default)."""
+    global _ORACLE_CORES
+    if _ORACLE_CORES is None:
+        _ORACLE_CORES = orc.max_threads()
+    return _ORACLE_CORES
+
+
 def time_oracle(orc, case, w, silu, budget_s, max_calls, nthreads=0):
     """Mean seconds per full oracle call, over calls until `budget_s` has
     passed (at least one, at most `max_calls`)."""
@@ -459,8 +472,8 @@ def cpu_baseline(w, budget_s=10.0, case=None):
     from channels_last_groupnorm_gb300 import workloads as wl
     case = case or wl.make_inputs(w)
     orc = oracle.get()
-    cores = orc.max_threads()
-    dt, calls = time_oracle(orc, case, w, True, budget_s, 50)
+    cores = oracle_cores(orc)
+    dt, calls = time_oracle(orc, case, w, True, budget_s, 50, nthreads=cores)
     dt1, calls1 = time_oracle(orc, case, w, True, budget_s / 4, 20, nthreads=1)
     return {"value": round(4.0 * w.elements / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle", "us_per_call": round(dt * 1e6, 1), "cpu_model": cpu_model(),
@@ -477,12 +490,12 @@ def cpu_baselines(budget_s=1.0):
     import oracle
     from channels_last_groupnorm_gb300 import workloads as wl
     orc = oracle.get()
-    cores = orc.max_threads()
+    cores = oracle_cores(orc)
     out = []
     for w in wl.WORKLOADS:
         case = wl.make_inputs(w)
         for silu in w.silu_modes:
-            dt, _ = time_oracle(orc, case, w, silu, budget_s, 20)
+            dt, _ = time_oracle(orc, case, w, silu, budget_s, 20, nthreads=cores)
             dt1, _ = time_oracle(orc, case, w, silu, budget_s / 2, 5, nthreads=1)
             out.append({"workload": w.name, "silu": silu, "cores": cores,
                         "us": round(dt * 1e6, 1), "gbs": round(4.0 * w.elements / dt / 1e9, 3),
@@ -939,7 +952,7 @@ def run_ours(args):
         run_attn(args, wl.ATTN_BY_NAME[args.workload], device, rank, world)
         return
     w = wl.BY_NAME[args.workload]
-    variant_id = {"auto": 0, "two_pass": 1, "fused": 2}[args.variant]
+    variant_id = {"auto": 0, "two_pass": 1, "fused": 2, "cluster": 3}[args.variant]
     stream = torch.cuda.Stream(device)
     peak, peak_kind = hbm_peak()
 
@@ -981,8 +994,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic,
-                     "kernel": "gn_fused_kernel" if r["variant"] == "fused"
-                               else "pass1+finalize+pass2",
+                     "kernel": {"fused": "gn_fused_kernel", "cluster": "gn_cluster_kernel"}.get(
+                         r["variant"], "pass1+finalize+pass2"),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "achieved_6B": round(1.5 * achieved, 1), "frac_6B": round(1.5 * achieved / peak, 4),
                      "launch_us_mean": round(launch_ms * 1e3, 3),
@@ -1111,7 +1124,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--variant", choices=["auto", "fused", "two_pass"], default="auto")
+    ap.add_argument("--variant", choices=["auto", "fused", "two_pass", "cluster"], default="auto")
     ap.add_argument("--launch", choices=["graph", "stream"], default="graph",
                     help="submit the timed steps as one captured CUDA graph, or one stream "
                          "launch per step")

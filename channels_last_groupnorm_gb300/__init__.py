@@ -9,6 +9,7 @@ from .gnsilu import (  # noqa: F401
     attention_folded,
     attn_fold,
     VARIANT_AUTO,
+    VARIANT_CLUSTER,
     VARIANT_FUSED,
     VARIANT_TWO_PASS,
     gn_abi_version,

@@ -14,8 +14,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libgnsilu.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["gn_kernels.cu", "gn_capi.cu", "gn_static.cu", "rga_kernels.cu", "upconv_kernels.cu", "attn_kernels.cu", "tc_capi.cu"]
-HEADERS = ["gn_internal.h", "gn_ptx.cuh", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "capi_util.h"]
+SOURCES = ["gn_kernels.cu", "gn_cluster.cu", "gn_capi.cu", "gn_static.cu", "rga_kernels.cu", "upconv_kernels.cu", "attn_kernels.cu", "tc_capi.cu"]
+HEADERS = ["gn_internal.h", "gn_math.cuh", "gn_ptx.cuh", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "capi_util.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

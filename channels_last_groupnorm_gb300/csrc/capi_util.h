@@ -16,6 +16,9 @@ struct DeviceInfo {
     int smem_per_sm = 0;
     int coop = 0;
     int major = 0, minor = 0;
+    int cluster_cap[17] = {};   // co-resident clusters of each size (cluster schedule)
+    unsigned int *status_word = nullptr;   // the GroupNorm kernels' sticky status (device address)
+    unsigned int *status_host = nullptr;   // its mapped host copy (device address)
 };
 
 // GN_OK with the device's properties, or GN_ERR_DEVICE / GN_ERR_CUDA.

@@ -127,7 +127,8 @@ int validate(const void *x, const float *gamma, const float *beta, const void *y
 
 struct Plan {
     Geom g{};
-    int kind = 0;            // GN_VARIANT_TWO_PASS or GN_VARIANT_FUSED
+    gn::ClusterPlan cl{};    // the cluster schedule's layout (kind GN_VARIANT_CLUSTER)
+    int kind = 0;            // GN_VARIANT_TWO_PASS, GN_VARIANT_FUSED or GN_VARIANT_CLUSTER
     int grid = 0;
     size_t off_partial = 0, off_gstat = 0, off_st = 0, off_mean = 0, off_rstd = 0;
     size_t ws_bytes = 0;
@@ -229,8 +230,38 @@ bool fused_launchable(const Plan &p, const DeviceInfo &d)
     return blocks >= 1 && p.grid <= blocks * d.sm_count;
 }
 
+// Whether the automatic choice takes the cluster schedule's layout: one
+// round of clusters, and few enough 16-byte vectors per CTA that copying
+// its slice rows (16-64 bytes each, one request per row segment) costs less
+// than the fused schedule's grid barrier and global merge.  Measured on a
+// GB300 (graph of calls, inputs larger than L2): up to 2048 vectors per CTA
+// the cluster schedule takes 6.8-8.5 us against 10.6-11.6 us; at 4096 it
+// still wins with 32-byte or wider row segments (10.1-10.9 us against
+// 11.8-12.2) but not with 16-byte ones (14.3 against 12.1); at 8192 (C = 512,
+// 128 x 128) it loses (16.3 against 15.1).
+bool cluster_preferred(const gn::ClusterPlan &cp)
+{
+    const int64_t vectors = static_cast<int64_t>(cp.R) * (cp.SC / 8);
+    return cp.waves == 1 && (vectors <= 2048 || (vectors <= 4096 && cp.SC >= 16));
+}
+
+// The automatic choice: the cluster schedule where it is the faster one
+// (x read once, no grid barrier; cluster_preferred), else the fused
+// cooperative schedule when it can launch, else two passes.
 int resolve_variant(int variant, int64_t N, int64_t L, int64_t C, int64_t G, const DeviceInfo &d, Plan *out)
 {
+    if (variant == GN_VARIANT_CLUSTER || variant == GN_VARIANT_AUTO) {
+        gn::ClusterPlan cp;
+        const bool ok = gn::plan_cluster(N, L, static_cast<int>(C), static_cast<int>(G), d.cluster_cap,
+                                         d.smem_optin, &cp);
+        if (ok && (variant == GN_VARIANT_CLUSTER || cluster_preferred(cp))) {
+            *out = Plan{};
+            out->kind = GN_VARIANT_CLUSTER;
+            out->cl = cp;
+            return GN_OK;
+        }
+        if (variant == GN_VARIANT_CLUSTER) return GN_ERR_VARIANT;
+    }
     if (variant == GN_VARIANT_TWO_PASS) {
         *out = make_plan(N, L, C, G, GN_VARIANT_TWO_PASS, d);
         return out->g.ring >= 2 ? GN_OK : GN_ERR_VARIANT;
@@ -315,7 +346,7 @@ int plan_call(const void *x, const float *gamma, const float *beta, const void *
 {
     int rc = validate(x, gamma, beta, y, N, L, C, G, eps, mean_out, rstd_out, general);
     if (rc != GN_OK) return rc;
-    if (variant < GN_VARIANT_AUTO || variant > GN_VARIANT_FUSED) return GN_ERR_VARIANT;
+    if (variant < GN_VARIANT_AUTO || variant > GN_VARIANT_CLUSTER) return GN_ERR_VARIANT;
     if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256) return GN_ERR_ALIGN;
     if ((rc = current_device(dev, d)) != GN_OK) return rc;
     if (gn_capi::kernel_status_raised(*dev)) return GN_ERR_KERNEL;
@@ -333,12 +364,22 @@ int run(const void *x, const float *gamma, const float *beta, void *y, int64_t N
                        &d, &p);
     if (rc != GN_OK) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void *ws = workspace;
-    if (ws) {
-        if (workspace_bytes < workspace_bytes_any(N, L, C, G, d)) return GN_ERR_WORKSPACE;
-    } else if ((rc = library_workspace(dev, s, workspace_bytes_any(N, L, C, G, d), &ws)) != GN_OK) {
-        return rc;
+    if (workspace && workspace_bytes < workspace_bytes_any(N, L, C, G, d)) return GN_ERR_WORKSPACE;
+    if (p.kind == GN_VARIANT_CLUSTER) {
+        // everything stays in the clusters' shared memory: no workspace
+        const cudaError_t e = gn::launch_cluster(p.cl, static_cast<const uint16_t *>(x), static_cast<uint16_t *>(y),
+                                                 gamma, beta, mean_out, rstd_out, eps, apply_silu != 0, N, L,
+                                                 static_cast<int>(C), static_cast<int>(G), wait_timeout_ns(),
+                                                 d.status_word, d.status_host, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GN_ERR_CUDA;
+        }
+        g_launches.fetch_add(1);
+        return GN_OK;
     }
+    void *ws = workspace;
+    if (!ws && (rc = library_workspace(dev, s, workspace_bytes_any(N, L, C, G, d), &ws)) != GN_OK) return rc;
     uint8_t *base = static_cast<uint8_t *>(ws);
     Args a{};
     a.x = static_cast<const uint16_t *>(x);
@@ -437,12 +478,13 @@ int current_device(int *dev_out, DeviceInfo *info_out)
             return GN_ERR_DEVICE;
         }
         if (d.major != 10 || d.minor != 3 || dev >= kStatusWords) return GN_ERR_DEVICE;
-        if (gn::prepare_kernels(static_cast<uint32_t>(d.smem_optin)) != cudaSuccess) {
+        if (gn::prepare_kernels(static_cast<uint32_t>(d.smem_optin)) != cudaSuccess ||
+            gn::prepare_cluster_kernels(d.smem_optin, d.cluster_cap) != cudaSuccess) {
             cudaGetLastError();
             return GN_ERR_CUDA;
         }
         // map this device's status word (registering the words once) and
-        // hand its device address to the three kernel files
+        // hand its device address to the kernel files
         if (!g_status_registered) {
             if (cudaHostRegister(g_status_words, sizeof(g_status_words),
                                  cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
@@ -454,11 +496,13 @@ int current_device(int *dev_out, DeviceInfo *info_out)
         void *word = nullptr;
         if (cudaHostGetDevicePointer(&word, &g_status_words[dev], 0) != cudaSuccess || !word ||
             gn::set_device_status_host(static_cast<unsigned int *>(word)) != cudaSuccess ||
+            gn::device_status_address(&d.status_word) != cudaSuccess ||
             gn::set_upconv_status_host(static_cast<unsigned int *>(word)) != cudaSuccess ||
             gn::set_attn_status_host(static_cast<unsigned int *>(word)) != cudaSuccess) {
             cudaGetLastError();
             return GN_ERR_CUDA;
         }
+        d.status_host = static_cast<unsigned int *>(word);
         d.ready = true;
     }
     *dev_out = dev;

@@ -128,7 +128,32 @@ cudaError_t launch_fused(const Args &a, int grid, bool silu, cudaStream_t s);
 cudaError_t fused_blocks_per_sm(bool silu, uint32_t smem, int *blocks);
 cudaError_t prepare_kernels(uint32_t max_smem);
 cudaError_t launch_selftest_wait(int mode, uint64_t timeout_ns, int *done, int blocks, cudaStream_t s);
+// ---- cluster schedule for tensors that fit in shared memory (gn_cluster.cu) ----
+constexpr int kClusterMaxCtas = 16;   // largest cluster the schedule uses (non-portable above 8)
+struct ClusterPlan {
+    int SC;            // channels per slice: whole groups, a multiple of 8
+    int CL;            // CTAs per cluster
+    int R;             // rows per CTA
+    int BR;            // rows per tensor-map box (a multiple of 8, at most 256)
+    int boxes;         // boxes per CTA
+    int64_t units;     // clusters: (batch entry, slice) pairs
+    int waves;         // rounds of clusters the device runs one after another
+    uint32_t smem;     // dynamic shared memory per CTA
+};
+// Kernel attributes, and the co-resident clusters of each size 1..16
+// (cap[size]) at `max_smem` bytes of shared memory per CTA.
+cudaError_t prepare_cluster_kernels(int max_smem, int (&cap)[kClusterMaxCtas + 1]);
+// False when no cluster layout fits the shape.
+bool plan_cluster(int64_t N, int64_t L, int C, int G, const int (&cap)[kClusterMaxCtas + 1], int max_smem,
+                  ClusterPlan *out);
+cudaError_t launch_cluster(const ClusterPlan &p, const uint16_t *x, uint16_t *y, const float *gamma,
+                           const float *beta, float *mean, float *rstd, float eps, bool silu, int64_t N, int64_t L,
+                           int C, int G, uint64_t timeout_ns, unsigned int *status, unsigned int *status_host,
+                           cudaStream_t s);
+
 cudaError_t read_device_status(unsigned int *status);
+// Device address of the GroupNorm kernels' sticky status word (current device).
+cudaError_t device_status_address(unsigned int **word);
 cudaError_t clear_device_status();
 // Device address of the mapped host word that mirrors the status (current device).
 cudaError_t set_device_status_host(unsigned int *host_word);

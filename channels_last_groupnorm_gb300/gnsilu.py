@@ -47,6 +47,7 @@ GN_ERR_FORMAT = 12
 VARIANT_AUTO = 0
 VARIANT_TWO_PASS = 1
 VARIANT_FUSED = 2
+VARIANT_CLUSTER = 3
 
 # statuses that mean "this input is not supported" (the caller falls back)
 UNSUPPORTED = {GN_ERR_SHAPE, GN_ERR_CHANNELS, GN_ERR_ALIGN, GN_ERR_EPS, GN_ERR_ALIAS, GN_ERR_FORMAT}

@@ -90,7 +90,8 @@ enum gn_status_code {
     GN_ERR_CUDA = 8,       /* a CUDA runtime call or kernel launch failed */
     GN_ERR_DEVICE = 9,     /* no CUDA device, or the current device is not sm_103 */
     GN_ERR_VARIANT = 10,   /* unknown variant, or the fused variant cannot be
-                              launched cooperatively for this shape */
+                              launched cooperatively for this shape, or the
+                              cluster variant does not fit it */
     GN_ERR_KERNEL = 11,    /* a kernel gave up a bounded wait and the status has not
                               been cleared (gn_device_status(1)) since; nothing ran */
     GN_ERR_FORMAT = 12     /* gn_residual_gate_add(): unknown half format */
@@ -106,9 +107,20 @@ enum gn_half_format {
 enum gn_variant {
     GN_VARIANT_AUTO = 0,      /* the library picks (fused when it can launch) */
     GN_VARIANT_TWO_PASS = 1,  /* three launches: pass 1, finalize, pass 2 */
-    GN_VARIANT_FUSED = 2      /* one cooperative launch: pass 1, grid barrier,
+    GN_VARIANT_FUSED = 2,     /* one cooperative launch: pass 1, grid barrier,
                                  finalize, grid barrier, pass 2; x re-read from
                                  shared memory / L2 where it still sits there */
+    GN_VARIANT_CLUSTER = 3    /* one launch of thread-block clusters, each owning
+                                 a slice of whole groups of one batch entry: its
+                                 CTAs keep their rows in shared memory, merge the
+                                 group statistics over distributed shared memory
+                                 and write y; x is read from HBM once and no
+                                 workspace is used.  Only for tensors whose
+                                 slices fit the clusters' shared memory (about
+                                 2 MiB of one batch entry's slice per cluster):
+                                 GN_ERR_VARIANT otherwise.  GN_VARIANT_AUTO picks
+                                 it for small tensors (up to a few MiB), where it
+                                 is the fastest schedule */
 };
 
 /*

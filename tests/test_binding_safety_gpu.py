@@ -110,16 +110,23 @@ def test_library_workspaces_stay_bounded_over_many_streams():
     y = torch.empty_like(x)
     need = gs.gn_silu_workspace_bytes(N, L, C, G)
     assert need > (1 << 20)
+
+    def calls_on_new_streams(count):
+        for _ in range(count):
+            s = torch.cuda.Stream()
+            assert gs.gn_silu_rows(x, gamma, beta, G=G, out=y, stream=s) is not None
+            s.synchronize()
+            del s
+        assert 1 <= gs.gn_library_workspaces() <= 8
+
+    # a first round lets the driver set up whatever per-stream state it
+    # keeps for the streams PyTorch hands out (its pool is finite)
+    calls_on_new_streams(100)
     assert gs.gn_release_workspaces() == gs.GN_OK
     assert gs.gn_library_workspaces() == 0
     torch.cuda.synchronize()
     free_before = torch.cuda.mem_get_info()[0]
-    for _ in range(100):
-        s = torch.cuda.Stream()
-        assert gs.gn_silu_rows(x, gamma, beta, G=G, out=y, stream=s) is not None
-        s.synchronize()
-        del s
-    assert 1 <= gs.gn_library_workspaces() <= 8
+    calls_on_new_streams(100)
     torch.cuda.synchronize()
     grown = free_before - torch.cuda.mem_get_info()[0]
     assert grown <= 8 * (need + need // 4) + (16 << 20), grown

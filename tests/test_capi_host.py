@@ -99,7 +99,7 @@ def test_rows_rejects(kw, code):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(variant=3), gs.GN_ERR_VARIANT),
+    (dict(variant=4), gs.GN_ERR_VARIANT),
     (dict(variant=-1), gs.GN_ERR_VARIANT),
     (dict(workspace=0x40000010, workspace_bytes=1 << 20), gs.GN_ERR_ALIGN),
     (dict(mean_out=0x50000002), gs.GN_ERR_ALIGN),

@@ -21,7 +21,23 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 VARIANTS = [gs.VARIANT_FUSED, gs.VARIANT_TWO_PASS]
-VNAME = {gs.VARIANT_FUSED: "fused", gs.VARIANT_TWO_PASS: "two_pass"}
+ALL_VARIANTS = VARIANTS + [gs.VARIANT_CLUSTER]
+VNAME = {gs.VARIANT_FUSED: "fused", gs.VARIANT_TWO_PASS: "two_pass", gs.VARIANT_CLUSTER: "cluster"}
+
+
+def skip_unless_cluster_fits(N, L, C, G, variant):
+    """The explicit cluster variant is refused (GN_ERR_VARIANT) for shapes
+    whose slices do not fit the clusters' shared memory."""
+    if variant != gs.VARIANT_CLUSTER:
+        return
+    x = torch.zeros((N, L, C), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(C, device="cuda")
+    rc = gs.raw_gn_silu_rows_any(x.data_ptr(), g.data_ptr(), g.data_ptr(), x.data_ptr(), N, L, C, G, 1e-6, 1,
+                                 variant=gs.VARIANT_CLUSTER)
+    torch.cuda.synchronize()
+    assert rc in (gs.GN_OK, gs.GN_ERR_VARIANT), gs.status_string(rc)
+    if rc != gs.GN_OK:
+        pytest.skip("the cluster schedule does not fit this shape")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,9 +69,10 @@ GENERAL = [
 ]
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 @pytest.mark.parametrize("N,L,C,G", GENERAL)
 def test_general_channel_counts_every_output(N, L, C, G, variant):
+    skip_unless_cluster_fits(N, L, C, G, variant)
     case = wl.make_case(N, L, C, seed=N * 7919 + L * 13 + C * 3 + G, mean=0.4, std=1.6,
                         channel_offset=0.5)
     x, gamma, beta = gu.device_inputs(case)
@@ -68,11 +85,12 @@ def test_general_channel_counts_every_output(N, L, C, G, variant):
         gu.check_stats(mean.cpu().numpy(), rstd.cpu().numpy(), m_ref, r_ref, what)
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 @pytest.mark.parametrize("N,L,C", [(1, 16384, 256), (2, 3001, 512), (1, 999, 2048), (3, 77, 8)])
 def test_power_of_two_channels_match_the_pow2_entry_bitwise(N, L, C, variant):
     """For a power-of-two C both entry points run the same kernels with the
     same geometry, so every output and statistic is bitwise identical."""
+    skip_unless_cluster_fits(N, L, C, 32 if C >= 32 else C, variant)
     case = wl.make_case(N, L, C, seed=L + C, mean=-0.3, std=1.2)
     x, gamma, beta = gu.device_inputs(case)
     a = run_any(x, gamma, beta, 32 if C >= 32 else C, 1e-6, True, variant)

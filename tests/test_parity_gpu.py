@@ -3,7 +3,7 @@
 Elementwise on every output for the shapes the oracle finishes in seconds
 (including ragged tails, odd batch counts and every supported C), and on
 sampled outputs plus all group statistics at the full benchmark sizes, for
-both kernel schedules."""
+every kernel schedule (the cluster schedule wherever it fits the shape)."""
 import numpy as np
 import pytest
 import torch
@@ -17,7 +17,9 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 VARIANTS = [gs.VARIANT_FUSED, gs.VARIANT_TWO_PASS]
-VNAME = {gs.VARIANT_FUSED: "fused", gs.VARIANT_TWO_PASS: "two_pass", gs.VARIANT_AUTO: "auto"}
+ALL_VARIANTS = VARIANTS + [gs.VARIANT_CLUSTER]
+VNAME = {gs.VARIANT_FUSED: "fused", gs.VARIANT_TWO_PASS: "two_pass", gs.VARIANT_AUTO: "auto",
+         gs.VARIANT_CLUSTER: "cluster"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,8 +32,26 @@ def lib():
     gu.assert_clean_device()
 
 
+def fits_cluster(N, L, C, G):
+    """The cluster schedule takes this shape (its slices fit the clusters'
+    shared memory); the explicit variant is refused otherwise."""
+    return gs.gn_silu_pick_variant(N, L, C, G) == gs.VARIANT_CLUSTER or _cluster_accepts(N, L, C, G)
+
+
+def _cluster_accepts(N, L, C, G):
+    x = torch.zeros((N, L, C), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(C, device="cuda")
+    rc = gs.raw_gn_silu_rows_ex(x.data_ptr(), g.data_ptr(), g.data_ptr(), x.data_ptr(), N, L, C, G, 1e-6, 1,
+                                variant=gs.VARIANT_CLUSTER)
+    torch.cuda.synchronize()
+    assert rc in (gs.GN_OK, gs.GN_ERR_VARIANT), gs.status_string(rc)
+    return rc == gs.GN_OK
+
+
 def full_check(case, G, eps, silu, variant, what):
     x, gamma, beta = gu.device_inputs(case)
+    if variant == gs.VARIANT_CLUSTER and not fits_cluster(*x.shape, G):
+        pytest.skip("the cluster schedule does not fit this shape")
     y, mean, rstd = gu.run_rows_ex(x, gamma, beta, G, eps, silu, variant)
     y_ref, m_ref, r_ref = oracle.forward(case["x_bits"], case["gamma"], case["beta"], G, eps, silu)
     gu.check_y(gu.bf16_to_f64(y), y_ref, what)
@@ -42,7 +62,7 @@ def full_check(case, G, eps, silu, variant, what):
 # ---------------------------------------------------------------------------
 # the benchmark workloads
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 @pytest.mark.parametrize("index", [0, 1])
 def test_small_workloads_every_output(index, variant):
     w = wl.WORKLOADS[index]
@@ -50,9 +70,10 @@ def test_small_workloads_every_output(index, variant):
     full_check(case, w.G, w.eps, True, variant, f"{w.name} {VNAME[variant]}")
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 @pytest.mark.parametrize("silu", [True, False], ids=["silu", "nosilu"])
 def test_offset_stress_every_output(silu, variant):
+    # the cluster schedule takes this 64 MiB tensor in several rounds of clusters
     w = wl.WORKLOADS[2]
     case = wl.make_inputs(w)
     full_check(case, w.G, w.eps, silu, variant, f"{w.name} silu={silu} {VNAME[variant]}")
@@ -99,7 +120,7 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 @pytest.mark.parametrize("N,L,C,G", EDGE)
 def test_edge_shapes(N, L, C, G, variant):
     case = wl.make_case(N, L, C, seed=N * 1000003 + L * 31 + C + G, mean=0.5, std=1.7)
@@ -107,7 +128,7 @@ def test_edge_shapes(N, L, C, G, variant):
         full_check(case, G, 1e-6, silu, variant, f"N={N} L={L} C={C} G={G} {VNAME[variant]}")
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 def test_constant_input(variant):
     """var = 0: the mean is the constant exactly, rstd = 1/sqrt(eps) and
     y = beta (SiLU off)."""
@@ -120,7 +141,7 @@ def test_constant_input(variant):
                "constant")
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 def test_in_place(variant):
     case = wl.make_case(2, 5000, 512, 11, std=2.0)
     x, gamma, beta = gu.device_inputs(case)
@@ -129,7 +150,7 @@ def test_in_place(variant):
     gu.check_y(gu.bf16_to_f64(x), y_ref, "in place")
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAME[v])
+@pytest.mark.parametrize("variant", ALL_VARIANTS, ids=lambda v: VNAME[v])
 def test_no_writes_outside_y(variant):
     """y sits inside a larger poisoned buffer; only its own bytes change."""
     N, L, C = 1, 3333, 256
@@ -158,7 +179,7 @@ def test_variants_agree_closely():
 def test_repeated_calls_are_deterministic():
     case = wl.make_case(1, 50000, 256, 19)
     x, gamma, beta = gu.device_inputs(case)
-    for variant in VARIANTS:
+    for variant in ALL_VARIANTS:
         first = gu.run_rows_ex(x, gamma, beta, 32, 1e-6, True, variant)
         for _ in range(3):
             again = gu.run_rows_ex(x, gamma, beta, 32, 1e-6, True, variant)
@@ -186,3 +207,45 @@ def test_ring_reuse_is_race_free(N, L, C, variant):
     y_ref = oracle.apply_at(case["x_bits"], case["gamma"], case["beta"], 32, m_ref, r_ref, True, idx)
     gu.check_y(gu.bf16_to_f64(first[0].reshape(-1)[torch.from_numpy(idx).cuda()]), y_ref,
                "ring reuse sampled")
+
+
+# ---------------------------------------------------------------------------
+# the cluster schedule: where the automatic choice takes it, and where not
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("N,L,C", [(1, 4096, 128), (1, 1024, 512), (1, 4096, 512), (4, 1024, 512)])
+def test_small_tensors_take_the_cluster_schedule(N, L, C):
+    assert gs.gn_silu_pick_variant(N, L, C, 32) == gs.VARIANT_CLUSTER
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_automatic_choice_leaves_larger_shapes_to_the_fused_schedule(index):
+    w = wl.WORKLOADS[index]
+    assert gs.gn_silu_pick_variant(w.N, w.L, w.C, w.G) == gs.VARIANT_FUSED
+    assert fits_cluster(w.N, w.L, w.C, w.G)
+
+
+@pytest.mark.parametrize("index", [3, 4, 5])
+def test_large_workloads_do_not_fit_the_cluster_schedule(index):
+    w = wl.WORKLOADS[index]
+    assert gs.gn_silu_pick_variant(w.N, w.L, w.C, w.G) != gs.VARIANT_CLUSTER
+    x = torch.empty((w.N, w.L, w.C), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(w.C, device="cuda")
+    before = gs.gn_kernel_launch_count()
+    rc = gs.raw_gn_silu_rows_ex(x.data_ptr(), g.data_ptr(), g.data_ptr(), x.data_ptr(), w.N, w.L, w.C, w.G,
+                                w.eps, 1, variant=gs.VARIANT_CLUSTER)
+    assert rc == gs.GN_ERR_VARIANT
+    assert gs.gn_kernel_launch_count() == before
+
+
+@pytest.mark.parametrize("N,L,C,G", [(1, 4096, 128, 32), (1, 16384, 512, 32), (3, 777, 2048, 32),
+                                     (160, 33, 64, 32), (2, 513, 2048, 2048)])
+def test_cluster_schedule_matches_two_pass_closely(N, L, C, G):
+    """Same statistics as the two-pass schedule to fp32 rounding, outputs
+    within one bf16 rounding step."""
+    case = wl.make_case(N, L, C, seed=N + L + C + G, mean=-0.7, std=2.5)
+    x, gamma, beta = gu.device_inputs(case)
+    a = gu.run_rows_ex(x, gamma, beta, G, 1e-6, True, gs.VARIANT_CLUSTER)
+    b = gu.run_rows_ex(x, gamma, beta, G, 1e-6, True, gs.VARIANT_TWO_PASS)
+    np.testing.assert_allclose(a[1].cpu().numpy(), b[1].cpu().numpy(), rtol=2e-6, atol=2e-6)
+    np.testing.assert_allclose(a[2].cpu().numpy(), b[2].cpu().numpy(), rtol=2e-6)
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 0.02
