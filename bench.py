@@ -801,16 +801,20 @@ def attn_device_inputs(w, device):
     return c, {n: dev(c[n]) for n in c}
 
 
-def measure_attn(w, steps, device, stream, peak, torch_context=True):
-    """gn_attn_folded on one mid-block attention workload: the weights are
-    folded once (gn_attn_fold, untimed: per model), then a CUDA graph of
-    `steps` calls is replayed (each call writes and reads the 2 S^2 bytes of
-    softmax weights, more than L2 at S = 16384).  TFLOP/s counts the
-    folded evaluation: 2 S D^2 (value rows) + 4 S^2 D (scores, weighted
-    sum)."""
+def measure_attn(w, steps, device, stream, peak, torch_context=True, schedule=None):
+    """gn_attn_folded_ex on one mid-block attention workload: the weights
+    are folded once (gn_attn_fold, untimed: per model), then a CUDA graph of
+    `steps` calls is replayed.  ``schedule`` (default: the library's
+    automatic choice) is reported with the kernels one call launches: the
+    one-pass schedule keeps the scores on chip (2 launches), the
+    stored-weights one writes and reads the 2 S^2 bytes of softmax weights
+    (5 launches; more than L2 at S = 16384).  TFLOP/s counts the folded
+    evaluation: 2 S D^2 (value rows) + 4 S^2 D (scores, weighted sum)."""
     import torch
     import torch.nn.functional as F
     from channels_last_groupnorm_gb300 import gnsilu as gs
+    if schedule is None:
+        schedule = gs.ATTN_AUTO
     _, t = attn_device_inputs(w, device)
     wf, bf = gs.attn_fold(t["wv"], t["bv"], t["wo"], t["bo"])
     out = torch.empty_like(t["q"])
@@ -820,11 +824,18 @@ def measure_attn(w, steps, device, stream, peak, torch_context=True):
     rptr = t["residual"].data_ptr() if t["residual"] is not None else 0
 
     def call(_):
-        rc = gs.raw_gn_attn_folded(t["q"].data_ptr(), t["k"].data_ptr(), t["xn"].data_ptr(), wf.data_ptr(),
-                                   bf.data_ptr(), rptr, out.data_ptr(), w.S, w.D, ws.data_ptr(), need, stream=h)
+        rc = gs.raw_gn_attn_folded_ex(t["q"].data_ptr(), t["k"].data_ptr(), t["xn"].data_ptr(), wf.data_ptr(),
+                                      bf.data_ptr(), rptr, out.data_ptr(), w.S, w.D, ws.data_ptr(), need,
+                                      schedule, stream=h)
         if rc != 0:
             raise RuntimeError(gs.status_string(rc))
 
+    torch.cuda.synchronize()
+    before = gs.gn_kernel_launch_count()
+    with torch.cuda.stream(stream):
+        call(0)
+    torch.cuda.synchronize()
+    kernels = int(gs.gn_kernel_launch_count() - before)
     with torch.cuda.stream(stream):
         for _ in range(3):
             call(0)
@@ -841,7 +852,8 @@ def measure_attn(w, steps, device, stream, peak, torch_context=True):
     r = {"workload": w.name, "us_per_call": round(us, 2), "tflops": round(w.flops / (us * 1e-6) / 1e12, 1),
          "frac": round(w.flops / (us * 1e-6) / 1e12 / peak, 3), "launch_us_mean": round(launch_us, 2),
          "tflops_per_call_events": round(w.flops / (launch_us * 1e-6) / 1e12, 1),
-         "kernels_per_call": 5, "workspace_bytes": need, "launch": "cuda-graph"}
+         "kernels_per_call": kernels, "schedule": "one_pass" if kernels == 2 else "stored_weights",
+         "workspace_bytes": need, "launch": "cuda-graph"}
     if torch_context:
         # context only: the stock block (value projection, SDPA, output projection, residual) in PyTorch
         def stock(_):
@@ -906,15 +918,18 @@ def run_attn(args, w, device, rank, world):
         "accumulate": "f32", "data": "synthetic (seeded numpy PCG64; q, k, xn, residual ~N(0,1); "
         "W, b ~U(-1/sqrt(D), 1/sqrt(D)); bf16)",
         "config": {**w.describe(), "launch": r["launch"], "workspace_bytes": r["workspace_bytes"],
+                   "schedule": r["schedule"],
                    "flops_per_step": "2 S D^2 + 4 S^2 D (folded value rows, scores, weighted sum)"},
         "roofline": {"bound": "tensor", "achieved": r["tflops_per_call_events"], "peak": peak,
                      "unit": "TFLOP/s", "frac": round(r["tflops_per_call_events"] / peak, 4),
                      "peak_kind": peak_kind, "peak_sustained": sustained,
                      "traffic": recorded_traffic(w.name, "attn", ATTN_SOURCES),
-                     "kernel": "whole call: 4 gemm_kernel launches + softmax_stats_kernel (shares in the "
-                               "committed ncu launch list); traffic = DRAM bytes of the five per call",
+                     "kernel": ("whole call: the value-row gemm_kernel + attn_flash_kernel" if r["schedule"] == "one_pass"
+                                else "whole call: 4 gemm_kernel launches + softmax_stats_kernel")
+                               + " (shares in the committed ncu launch list); traffic = DRAM bytes of the "
+                               + f"{r['kernels_per_call']} per call",
                      "algorithmic_flops_per_launch": w.flops, "launch_us_mean": r["launch_us_mean"]},
-        "e2e": None, "gpu_launches": 5 * args.steps, "clocks": clocks,
+        "e2e": None, "gpu_launches": r["kernels_per_call"] * args.steps, "clocks": clocks,
     }
     if "torch_linear_sdpa_linear_us" in r:
         line["context"] = {"torch_linear_sdpa_linear_us": r["torch_linear_sdpa_linear_us"],

@@ -5,6 +5,9 @@ the C ABI of ``include/gnsilu.h``); ``gnsilu`` is its Python binding.
 Build the library with ``python -m channels_last_groupnorm_gb300.build``.
 """
 from .gnsilu import (  # noqa: F401
+    ATTN_AUTO,
+    ATTN_ONE_PASS,
+    ATTN_STORED_WEIGHTS,
     GnError,
     attention_folded,
     attn_fold,

@@ -587,6 +587,752 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// The softmax and the weighted sum in one pass over the keys, on CTA pairs,
+// for widths D <= 512 (see the file comment):
+//   out = softmax(q k^T / sqrt(D)) V' + residual,  given V'^T [D][S].
+// A cluster of two CTAs owns one tile of 128 query rows at a time
+// (persistent over the tiles).
+//  * CTA 0, the score CTA, keeps the tile's q rows in tensor memory (the
+//    A operand of its MMAs; its softmax warps load them, one row per
+//    thread), streams k in blocks of 128 keys (128-dimension chunks through
+//    a shared-memory ring) and has tcgen05.mma compute each block's scores
+//    into tensor memory (two buffers, so a block's MMAs run while the
+//    softmax warps read the one before).  Its four softmax warps (one
+//    tensor-memory lane quarter, one query row per thread) turn the scores
+//    into weights p = 2^(s log2e / sqrt(D) - m): m is a running maximum
+//    that moves only when a block's maximum exceeds it by more than 8
+//    (weights stay below 2^8, and the output is rarely rescaled).  The
+//    weights are rounded to bf16 and the rounded values summed into the row
+//    sum l.  They are written into a staging buffer, in the
+//    128-byte-swizzled K-major layout the output CTA's MMA reads, with each
+//    row's rescale factor 2^(m_old - m_new) and a flag when m moved; one
+//    thread then ships the block with bulk copies into the output CTA's
+//    shared memory (distributed shared memory), completing on the output
+//    CTA's mbarrier.
+//  * CTA 1, the output CTA, holds the 128 x D fp32 output in tensor memory
+//    (D <= 512 columns: which is why the scores live in the other CTA),
+//    streams V'^T in 64-key chunks and accumulates O += P V'.  Before a block
+//    that came with a rescale its MMA thread asks the eight epilogue warps
+//    to multiply O's rows by the factors (after the previous block's MMAs
+//    have completed); at the tile's end they write out = O / l + residual.
+//    A forwarder warp hands each weights buffer back to the score CTA as
+//    soon as the MMAs that read it have completed.
+//  * Per block both tensor pipes do 2 x 128 x 128 x D flops.
+//  * Tile t visits the key blocks starting at block t (the softmax does not
+//    depend on the order): clusters working at the same time then read
+//    different key and value rows, instead of all asking L2 for the same
+//    lines at once.
+// Every wait is bounded; a timeout records the sticky status and both CTAs
+// still meet at the final cluster barrier before either leaves.
+// ---------------------------------------------------------------------------
+// warps: 0 producer, 1 and 10 the two MMA issuers, 12 and 13 their waiters,
+// 2-9 softmax (score CTA: 2-5) / epilogue (output CTA), 11 the output CTA's
+// forwarder.  An issuing thread that touches shared memory (every mbarrier
+// wait does, and so does a plain load by any lane of its warp) stalls until
+// its own MMAs in flight have completed, about 0.5 us on a GB300 (measured),
+// which leaves the tensor pipe idle between chunks.  So a separate waiter
+// warp polls the mbarriers and passes each go-ahead (or a failure) to its
+// issuer with a named barrier, which does not stall the issuer; and two
+// issuers, on separate accumulators, keep the pipe fed while one waits for
+// its next operands.
+constexpr int kFlashThreads = 448;
+constexpr int kFlashKStages = 6;     // score CTA: 128-dimension chunks of key blocks in flight
+constexpr int kFlashVStages = 4;     // output CTA: 64 keys x D/2 of V'^T per stage
+constexpr float kFlashRescaleLog2 = 8.0f;
+constexpr int kFlashEnd = -1;        // mailbox: the tile is finished
+constexpr uint32_t kFlashPBytes = 32768u + 512u + 16u;   // one block's weights, factors and flags
+
+// barrier indices (8 bytes each)
+enum FlashBar {
+    // score CTA
+    kQFull = 0, kQFree = 1, kKFull = 2, kKEmpty = kKFull + kFlashKStages, kSFull = kKEmpty + kFlashKStages,
+    kSEmpty = kSFull + 2, kPEmpty = kSEmpty + 2, kSDrain = kPEmpty + 2,
+    // output CTA
+    kPFull = kSDrain + 1, kVFull = kPFull + 2, kVEmpty = kVFull + kFlashVStages, kPDone = kVEmpty + kFlashVStages,
+    kRescaleReq = kPDone + 2, kORescaled = kRescaleReq + 1, kOFull = kORescaled + 1, kOFree = kOFull + 1,
+    kLFull = kOFree + 1, kODrain = kLFull + 2, kFlashBars = kODrain + 1
+};
+
+struct FlashArgs {
+    int S, D, tiles, nblocks;
+    float scale_log2;                  // log2(e) / sqrt(D)
+    const __nv_bfloat16 *q;            // [S][D]
+    const __nv_bfloat16 *residual;     // [S][D] or null
+    __nv_bfloat16 *out;                // [S][D]
+    uint64_t timeout_ns;
+};
+
+// Shared-memory layout.  The score CTA uses q / kring, the output CTA
+// p / vring / alpha / flags / lsum / mailbox; the barriers and the small
+// words sit after both.  Both CTAs run the same kernel, so an offset names
+// the same place in either CTA (distributed shared memory addresses are
+// formed with mapa from the writer's own offsets).
+struct FlashLayout {
+    uint32_t kring, pstage, astage, fstage, lstage;      // score CTA
+    uint32_t p, vring, alpha, flags, lsum, mailbox;      // output CTA
+    uint32_t bars, tslot, abort, counters, total;
+};
+
+__host__ __device__ inline FlashLayout flash_layout(int D)
+{
+    FlashLayout l;
+    l.kring = 0;                                         // two [128 keys][64] bf16 boxes per stage
+    l.pstage = l.kring + kFlashKStages * 32768u;         // one block's weights, as the output CTA lays them out
+    l.astage = l.pstage + 32768u;                        // 128 rescale factors
+    l.fstage = l.astage + 512u;                          // 4 flags
+    l.lstage = l.fstage + 16u;                           // 128 row sums
+    const uint32_t score_end = l.lstage + 512u;
+    l.p = 0;                                             // two buffers of two [128][64] subtiles
+    l.vring = 2u * 32768u;
+    l.alpha = l.vring + kFlashVStages * static_cast<uint32_t>(D) * 64u;
+    l.flags = l.alpha + 2u * 128u * 4u;
+    l.lsum = l.flags + 2u * 4u * 4u;
+    l.mailbox = l.lsum + 2u * 128u * 4u;
+    const uint32_t out_end = l.mailbox + 16u;
+    l.bars = (score_end > out_end ? score_end : out_end);
+    l.bars = (l.bars + 15u) & ~15u;
+    l.tslot = l.bars + 8u * kFlashBars;
+    l.abort = l.tslot + 4u;
+    l.counters = l.abort + 4u;                           // issued / consumed copies, for the drain
+    l.total = l.counters + 32u;
+    return l;
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity, uint32_t sleep_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(sleep_ns)
+        : "memory");
+    return done != 0;
+}
+
+// tc::wait for a phase completed by arrivals from the other CTA: acquire at
+// cluster scope, so that what that CTA wrote before arriving is visible.
+__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+    if (*abort) return false;
+    const uint64_t deadline = global_ns() + timeout_ns;
+#pragma unroll 1
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity, tc::kSleepNs)) return true;
+        if (*abort) return false;
+        if (global_ns() > deadline) {
+            *abort = 1;
+            atomicOr(&g_at_status, 1u);
+            raise_host_status(g_at_status_host);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns)
+{
+    return tc::wait(bar, parity, abort, timeout_ns, &g_at_status, g_at_status_host);
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Bulk copy from this CTA's shared memory to the peer's (shared::cluster
+// addresses), completing `bytes` on the peer's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M = 128 rows, one per tensor-memory
+// lane, K packed two bf16 per 32-bit column) read from tensor memory.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// A barrier over `count` threads (named barrier `id`) that also returns
+// whether any of them passed pred = true.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "barrier.cta.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;"
+                 ::"r"(bar_cluster), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+          "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+          "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
+    attn_flash_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v, const FlashArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const FlashLayout lay = flash_layout(args.D);
+    const uint32_t bars = base + lay.bars;
+    const auto bar = [bars](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + lay.tslot);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + lay.abort);
+    volatile int *counters = reinterpret_cast<volatile int *>(gbase + lay.counters);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const bool scorer = rank == 0;
+    const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int D = args.D, half = D / 2, nb = args.nblocks;
+    // score CTA: two score buffers (columns 0-255) and the q rows (from 256);
+    // output CTA: the output, D columns
+    const uint32_t tmem_cols = scorer ? 512u : (D <= 128 ? 128u : (D <= 256 ? 256u : 512u));
+
+    if (threadIdx.x == 0) {
+        if (scorer) {
+            mbar_init(bar(kQFull), 4);               // the four softmax warps, once q is in tensor memory
+            mbar_init(bar(kQFree), 2);               // both issuers, after a tile's MMAs
+            for (int i = 0; i < kFlashKStages; ++i) {
+                mbar_init(bar(kKFull + i), 1);
+                mbar_init(bar(kKEmpty + i), 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(bar(kSFull + i), 1);
+                mbar_init(bar(kSEmpty + i), 4);      // the four softmax warps
+                mbar_init(bar(kPEmpty + i), 1);      // the output CTA's forwarder
+            }
+            mbar_init(bar(kSDrain), 2);
+        } else {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(bar(kPFull + i), 1);       // armed here (plus the bytes the score CTA copies)
+                mbar_init(bar(kPDone + i), 2);       // both issuers (one half of D each)
+                mbar_init(bar(kLFull + i), 1);
+            }
+            for (int i = 0; i < kFlashVStages; ++i) {
+                mbar_init(bar(kVFull + i), 1);
+                mbar_init(bar(kVEmpty + i), 1);
+            }
+            mbar_init(bar(kRescaleReq), 1);
+            mbar_init(bar(kORescaled), 8);           // the eight epilogue warps
+            mbar_init(bar(kOFull), 2);
+            mbar_init(bar(kOFree), 8);
+            mbar_init(bar(kODrain), 2);
+            // the first uses of the weights and row-sum buffers expect their bytes
+            for (int i = 0; i < 2; ++i) {
+                mbar_arrive_expect_tx(bar(kPFull + i), kFlashPBytes);
+                mbar_arrive_expect_tx(bar(kLFull + i), 512u);
+            }
+        }
+        *abort = (*reinterpret_cast<volatile unsigned int *>(&g_at_status) != 0u) ? 1 : 0;
+        for (int i = 0; i < 8; ++i) counters[i] = 0;
+        mbar_init_fence();
+        if (scorer) {
+            prefetch_tensormap(&map_q);
+            prefetch_tensormap(&map_k);
+        } else {
+            prefetch_tensormap(&map_v);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(base + lay.tslot, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    cluster_sync_all();   // both CTAs' barriers exist before anything crosses the pair
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort != 0;
+
+    if (scorer) {
+        if (!skip && warp == 0 && lane == 0) {
+            // ---- producer: k in 128-dimension chunks (two boxes each) ----
+            int kq = 0;
+            bool go = true;
+            for (int t = cl; go && t < args.tiles; t += ncl) {
+                for (int j = 0; go && j < nb; ++j) {
+                    for (int c = 0; c < D / 128; ++c, ++kq) {
+                        const int st = kq % kFlashKStages;
+                        if (kq >= kFlashKStages &&
+                            !fwait(bar(kKEmpty + st), ((kq / kFlashKStages) - 1) & 1, abort, args.timeout_ns)) {
+                            go = false;
+                            break;
+                        }
+                        const uint32_t dst = base + lay.kring + st * 32768u;
+                        const int key0 = ((j + t) % nb) * 128;
+                        mbar_arrive_expect_tx(bar(kKFull + st), 32768u);
+                        tma_load_2d(dst, &map_k, c * 128, key0, bar(kKFull + st));
+                        tma_load_2d(dst + 16384u, &map_k, c * 128 + 64, key0, bar(kKFull + st));
+                        counters[1] = kq + 1;   // k chunks issued
+                    }
+                }
+            }
+        } else if (!skip && (warp == 1 || warp == 10 || warp >= 12)) {
+            // ---- MMA: S = q k^T per block into alternate buffers; warp 1 issues
+            // the even blocks, warp 10 the odd ones.  Warp 12 (13) does the
+            // waiting for warp 1 (10) and hands each go-ahead over at named
+            // barrier 3 (4), so that the issuing thread never polls ----
+            constexpr uint32_t idesc = umma_idesc_bf16_f32(128, 128);
+            const bool waiter = warp >= 12;
+            const int mine = (warp == 1 || warp == 12) ? 0 : 1;
+            const uint32_t hb = 3u + static_cast<uint32_t>(mine);   // hand-offs that carry a failure
+            const uint32_t hs = 5u + static_cast<uint32_t>(mine);   // plain hand-offs
+            const int cpb = D / 128;   // chunks per block
+            int g = 0, tq = 0;
+            bool go = true, bad = false;   // bad: a wait of the waiter failed (sticky)
+            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
+                if (waiter && lane == 0) bad = bad || !fwait(bar(kQFull), tq & 1, abort, args.timeout_ns);
+                __syncwarp();
+                if (bar_any(hb, 64, bad)) break;
+                for (int j = 0; go && j < nb; ++j, ++g) {
+                    if ((g & 1) != mine) continue;
+                    const int buf = g & 1;
+                    const uint32_t d = tmem + static_cast<uint32_t>(buf * 128);
+                    for (int c = 0; c < cpb; ++c) {
+                        const int kq = g * cpb + c;
+                        const int st = kq % kFlashKStages;
+                        if (waiter && lane == 0) {
+                            if (c == 0 && g >= 2)
+                                bad = bad || !fwait(bar(kSEmpty + buf), ((g >> 1) - 1) & 1, abort, args.timeout_ns);
+                            bad = bad || !fwait(bar(kKFull + st), (kq / kFlashKStages) & 1, abort, args.timeout_ns);
+                        }
+                        __syncwarp();
+                        // a block's first chunk carries any failure so far; within the
+                        // block a plain barrier, which costs the issuer less (a failure
+                        // there lets the issuer run on stale operands until the next
+                        // block: wrong scores, never a wrong address, and the status
+                        // word reports the call as failed)
+                        if (c == 0) {
+                            if (bar_any(hb, 64, bad)) {
+                                go = false;
+                                break;
+                            }
+                        } else {
+                            named_sync(hs, 64);
+                        }
+                        if (!waiter && lane == 0) {
+                            tc_fence_after_sync();
+                            const uint32_t qa = tmem + 256u + static_cast<uint32_t>(c * 64);
+                            const uint32_t ka = base + lay.kring + st * 32768u;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                umma_f16_ta(d, qa + kk * 8, sw128_kmajor_desc(ka + (kk >> 2) * 16384u + (kk & 3) * 32),
+                                            idesc, (c > 0 || kk > 0) ? 1u : 0u);
+                            umma_commit(bar(kKEmpty + st));
+                        }
+                        __syncwarp();
+                    }
+                    if (go && !waiter && lane == 0) umma_commit(bar(kSFull + buf));
+                }
+                if (go && !waiter && lane == 0) umma_commit(bar(kQFree));
+            }
+            if (!waiter && lane == 0) umma_commit(bar(kSDrain));
+        } else if (!skip && warp >= 2 && warp < 6) {
+            // ---- softmax: one query row per thread ----
+            const int quad = warp & 3;
+            const int row = quad * 32 + lane;
+            const bool shipper = threadIdx.x == 64;   // issues the bulk copies to the output CTA
+            const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+            const uint32_t remote = mapa_shared(base, 1) - base;   // add to an offset for CTA 1's address
+            const uint32_t prow = base + lay.pstage + static_cast<uint32_t>(row) * 128u;
+            const uint32_t sw = static_cast<uint32_t>(row & 7);
+            float *astage = reinterpret_cast<float *>(gbase + lay.astage);
+            unsigned int *fstage = reinterpret_cast<unsigned int *>(gbase + lay.fstage);
+            float *lstage = reinterpret_cast<float *>(gbase + lay.lstage);
+            int g = 0, tq = 0;
+            bool go = true, pending = false;
+            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
+                float m = -INFINITY, l = 0.f;
+                {
+                    // the tile's q row of this thread into tensor memory (columns
+                    // 256 + d/2), once the previous tile's MMAs are done with it
+                    const bool ok = tq == 0 || fwait(bar(kQFree), (tq - 1) & 1, abort, args.timeout_ns);
+                    if (bar_any(1, 128, !ok || *abort)) break;
+                    tc_fence_after_sync();
+                    const uint4 *src = reinterpret_cast<const uint4 *>(args.q + (static_cast<int64_t>(t) * 128 + row) * D);
+#pragma unroll 1
+                    for (int c = 0; c < D / 64; ++c) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint4 u = __ldg(src + c * 8 + i);
+                            v[4 * i] = u.x;
+                            v[4 * i + 1] = u.y;
+                            v[4 * i + 2] = u.z;
+                            v[4 * i + 3] = u.w;
+                        }
+                        tmem_st_32x32b_x32(tmem + lane_base + 256u + static_cast<uint32_t>(c * 32), v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kQFull));
+                }
+                for (int j = 0; j < nb; ++j, ++g) {
+                    const int buf = g & 1;
+                    const bool ok = fwait(bar(kSFull + buf), (g >> 1) & 1, abort, args.timeout_ns);
+                    tc_fence_after_sync();
+                    // the staging buffer is free once the previous copy has read it
+                    if (shipper && pending) {
+                        bulk_wait_read_all();
+                        pending = false;
+                    }
+                    // one decision for all four warps, so that none is left at a barrier
+                    if (bar_any(1, 128, !ok || *abort)) {
+                        go = false;
+                        break;
+                    }
+                    const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(buf * 128);
+                    // one pass with the running maximum m, redone with the block's
+                    // maximum when that exceeds m by more than the threshold (a
+                    // decision per warp: tensor-memory loads are warp-collective)
+                    float m_new = m, lb = 0.f;
+                    bool resc = false;
+#pragma unroll 1
+                    for (int pass = 0; pass < 2; ++pass) {
+                        float mx = -INFINITY;
+                        lb = 0.f;
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t v[32];
+                            tmem_ld_32x32b_x32(taddr + c * 32, v);
+                            tmem_wait_ld();
+                            uint32_t w[16];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const float s0 = __uint_as_float(v[2 * k]), s1 = __uint_as_float(v[2 * k + 1]);
+                                mx = fmaxf(mx, fmaxf(s0, s1));
+                                const float p0 = ex2_approx(fmaf(s0, args.scale_log2, -m_new));
+                                const float p1 = ex2_approx(fmaf(s1, args.scale_log2, -m_new));
+                                w[k] = pack_bf16(p0, p1);
+                                lb += __uint_as_float(w[k] << 16) + __uint_as_float(w[k] & 0xffff0000u);
+                            }
+                            // keys 32c .. 32c + 31: subtile c / 2, 16-byte chunks 4 (c % 2) .. + 3
+                            const uint32_t sub = prow + static_cast<uint32_t>(c >> 1) * 16384u;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q);
+                                sts128(sub + ((chunk ^ sw) << 4), make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+                            }
+                        }
+                        if (pass == 0) {
+                            mx *= args.scale_log2;
+                            resc = mx > m + kFlashRescaleLog2;
+                            if (resc) m_new = mx;
+                            if (!__any_sync(0xffffffffu, resc)) break;
+                        }
+                    }
+                    const float alpha = resc ? ex2_approx(m - m_new) : 1.0f;
+                    l = l * alpha + lb;
+                    m = m_new;
+                    // the scores are read: the MMA may overwrite the buffer
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kSEmpty + buf));
+                    astage[row] = alpha;
+                    const unsigned any = __any_sync(0xffffffffu, resc) ? 1u : 0u;
+                    if (lane == 0) fstage[quad] = any;
+                    fence_proxy_async_smem();   // the staged block, visible to the bulk copy
+                    named_sync(2, 128);
+                    if (shipper) {
+                        // once the output CTA's MMAs have consumed the buffer two blocks back
+                        if (g < 2 || fwait(bar(kPEmpty + buf), ((g >> 1) - 1) & 1, abort, args.timeout_ns)) {
+                            // (the output CTA armed its barrier for these bytes)
+                            const uint32_t full = base + remote + lay.bars + 8u * (kPFull + buf);
+                            bulk_copy_to_peer(base + remote + lay.p + static_cast<uint32_t>(buf) * 32768u,
+                                              base + lay.pstage, 32768u, full);
+                            bulk_copy_to_peer(base + remote + lay.alpha + static_cast<uint32_t>(buf) * 512u,
+                                              base + lay.astage, 512u, full);
+                            bulk_copy_to_peer(base + remote + lay.flags + static_cast<uint32_t>(buf) * 16u,
+                                              base + lay.fstage, 16u, full);
+                            bulk_commit();
+                            pending = true;
+                        }
+                    }
+                }
+                if (!go) break;
+                // the tile's row sums
+                lstage[row] = l;
+                fence_proxy_async_smem();
+                named_sync(2, 128);
+                if (shipper) {
+                    const uint32_t full = base + remote + lay.bars + 8u * (kLFull + (tq & 1));
+                    bulk_copy_to_peer(base + remote + lay.lsum + static_cast<uint32_t>(tq & 1) * 512u,
+                                      base + lay.lstage, 512u, full);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                    pending = false;
+                }
+            }
+            // every copy has landed in the output CTA before this CTA can leave
+            if (shipper) bulk_wait_all();
+        }
+    } else {
+        if (!skip && warp == 0 && lane == 0) {
+            // ---- producer: V'^T, stages of 64 keys x one half of D ----
+            int vq = 0;
+            bool go = true;
+            const uint32_t stage_bytes = static_cast<uint32_t>(half) * 128u;
+            for (int t = cl; go && t < args.tiles; t += ncl)
+                for (int j = 0; go && j < nb; ++j)
+                    for (int kh = 0; kh < 4; ++kh, ++vq) {   // (64-key chunk, half) pairs
+                        const int st = vq % kFlashVStages;
+                        if (vq >= kFlashVStages &&
+                            !fwait(bar(kVEmpty + st), ((vq / kFlashVStages) - 1) & 1, abort, args.timeout_ns)) {
+                            go = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(kVFull + st), stage_bytes);
+                        tma_load_2d(base + lay.vring + static_cast<uint32_t>(st) * stage_bytes, &map_v,
+                                    ((j + t) % nb) * 128 + (kh >> 1) * 64, (kh & 1) * half, bar(kVFull + st));
+                        counters[4] = vq + 1;   // V stages issued
+                    }
+        } else if (!skip && (warp == 1 || warp == 10 || warp >= 12)) {
+            // ---- MMA: O += P V' per block, one half of D per issuer (warp 1
+            // the first, warp 10 the second).  Warp 12 (13) does the waiting
+            // for warp 1 (10), including the rescale handshake with the
+            // epilogue, and hands each go-ahead over at named barrier 3 (4) ----
+            const bool waiter = warp >= 12;
+            const int h = (warp == 1 || warp == 12) ? 0 : 1;
+            const uint32_t hb = 3u + static_cast<uint32_t>(h);   // hand-offs that carry a failure
+            const uint32_t hs = 5u + static_cast<uint32_t>(h);   // plain hand-offs
+            const bool lead = h == 0;   // its waiter posts the rescale requests and the tile's end
+            const uint32_t idesc = umma_idesc_bf16_f32(128, half);
+            volatile int *mailbox = reinterpret_cast<volatile int *>(gbase + lay.mailbox);
+            volatile int *flags = reinterpret_cast<volatile int *>(gbase + lay.flags);
+            int g = 0, tq = 0, ro = 0;
+            bool go = true, bad = false;   // bad: a wait of the waiter failed (sticky)
+            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
+                for (int j = 0; j < nb; ++j, ++g) {
+                    const int buf = g & 1;
+                    for (int kc = 0; kc < 2; ++kc) {   // the two 64-key chunks of this half
+                        const int vq = g * 4 + kc * 2 + h;
+                        const int st = vq % kFlashVStages;
+                        if (waiter && lane == 0) {
+                            if (kc == 0) {
+                                bad = bad || !wait_cluster(bar(kPFull + buf), (g >> 1) & 1, abort, args.timeout_ns);
+                                if (!bad && j == 0) {
+                                    // the previous tile's output has been written out
+                                    bad = tq > 0 && !fwait(bar(kOFree), (tq - 1) & 1, abort, args.timeout_ns);
+                                } else if (!bad && (flags[buf * 4] | flags[buf * 4 + 1] | flags[buf * 4 + 2] |
+                                                    flags[buf * 4 + 3])) {
+                                    // O (both halves) complete up to the previous block, then
+                                    // its rows rescaled by the epilogue
+                                    bad = !fwait(bar(kPDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort, args.timeout_ns);
+                                    if (!bad && lead) {
+                                        *mailbox = buf;
+                                        mbar_arrive(bar(kRescaleReq));
+                                    }
+                                    bad = bad || !fwait(bar(kORescaled), ro & 1, abort, args.timeout_ns);
+                                    ++ro;
+                                }
+                            }
+                            bad = bad || !fwait(bar(kVFull + st), (vq / kFlashVStages) & 1, abort, args.timeout_ns);
+                        }
+                        __syncwarp();
+                        // as on the score side: the block's first chunk carries failures
+                        if (kc == 0) {
+                            if (bar_any(hb, 64, bad)) {
+                                go = false;
+                                break;
+                            }
+                        } else {
+                            named_sync(hs, 64);
+                        }
+                        if (!waiter && lane == 0) {
+                            tc_fence_after_sync();
+                            const uint32_t pa = base + lay.p + static_cast<uint32_t>(buf) * 32768u + kc * 16384u;
+                            const uint32_t va = base + lay.vring + static_cast<uint32_t>(st * half) * 128u;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_f16(tmem + static_cast<uint32_t>(h * half), sw128_kmajor_desc(pa + kk * 32),
+                                         sw128_kmajor_desc(va + kk * 32), idesc, (j > 0 || kc > 0 || kk > 0) ? 1u : 0u);
+                            umma_commit(bar(kVEmpty + st));
+                        }
+                        __syncwarp();
+                    }
+                    if (!go) break;
+                    if (!waiter && lane == 0) umma_commit(bar(kPDone + buf));
+                }
+                if (!go) break;
+                if (!waiter && lane == 0) umma_commit(bar(kOFull));
+                if (waiter && lead && lane == 0 && !bad) {
+                    *mailbox = kFlashEnd;
+                    mbar_arrive(bar(kRescaleReq));
+                }
+            }
+            if (!waiter && lane == 0) umma_commit(bar(kODrain));
+        } else if (!skip && warp == 11 && lane == 0) {
+            // ---- forwarder: a weights buffer goes back to the score CTA once its MMAs are done ----
+            const uint32_t peer = mapa_shared(base, 0) - base;
+            int g = 0;
+            bool go = true;
+            for (int t = cl; go && t < args.tiles; t += ncl)
+                for (int j = 0; j < nb; ++j, ++g) {
+                    if (!fwait(bar(kPDone + (g & 1)), (g >> 1) & 1, abort, args.timeout_ns)) {
+                        go = false;
+                        break;
+                    }
+                    // the buffer's next use expects its bytes; then it goes back
+                    mbar_arrive_expect_tx(bar(kPFull + (g & 1)), kFlashPBytes);
+                    mbar_arrive_cluster(base + peer + lay.bars + 8u * (kPEmpty + (g & 1)));
+                }
+        } else if (!skip && warp >= 2 && warp < 10) {
+            // ---- epilogue warps: rescale O on request; out = O / l + residual at the tile's end ----
+            const int quad = warp & 3, h = (warp - 2) >> 2;
+            const int row = quad * 32 + lane;
+            const uint32_t taddr0 = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(h * half);
+            volatile int *mailbox = reinterpret_cast<volatile int *>(gbase + lay.mailbox);
+            const float *alpha = reinterpret_cast<const float *>(gbase + lay.alpha);
+            const float *lsum = reinterpret_cast<const float *>(gbase + lay.lsum);
+            int rr = 0, tq = 0;
+            bool go = true;
+            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
+                for (;;) {
+                    const bool ok = fwait(bar(kRescaleReq), rr & 1, abort, args.timeout_ns);
+                    ++rr;
+                    if (!__all_sync(0xffffffffu, ok && !*abort)) {
+                        go = false;
+                        break;
+                    }
+                    const int mb = *mailbox;
+                    if (mb == kFlashEnd) break;
+                    tc_fence_after_sync();
+                    const float a = alpha[mb * 128 + row];
+#pragma unroll 1
+                    for (int c = 0; c < half; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(taddr0 + c, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * a);
+                        tmem_st_32x32b_x32(taddr0 + c, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kORescaled));
+                }
+                if (!go) break;
+                bool ok = fwait(bar(kOFull), tq & 1, abort, args.timeout_ns);
+                ok = ok && wait_cluster(bar(kLFull + (tq & 1)), (tq >> 1) & 1, abort, args.timeout_ns);
+                // the buffer's next use (at the end of the tile two on, long after
+                // this tile's sums are read) expects its bytes
+                if (ok && warp == 2 && lane == 0) mbar_arrive_expect_tx(bar(kLFull + (tq & 1)), 512u);
+                tc_fence_after_sync();
+                if (!__all_sync(0xffffffffu, ok && !*abort)) break;
+                const float inv = 1.0f / lsum[(tq & 1) * 128 + row];
+                const int64_t orow = static_cast<int64_t>(t) * 128 + row;
+                __nv_bfloat16 *dst = args.out + orow * D + h * half;
+                const __nv_bfloat16 *res = args.residual ? args.residual + orow * D + h * half : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < half; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr0 + c, v);
+                    tmem_wait_ld();
+                    float f[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(v[k]) * inv;
+                    if (res) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 rr4 = *reinterpret_cast<const uint4 *>(res + c + 8 * q);
+                            const uint32_t w[4] = {rr4.x, rr4.y, rr4.z, rr4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                f[8 * q + 2 * e] += __uint_as_float(w[e] << 16);
+                                f[8 * q + 2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4 *>(dst + c + 8 * q) =
+                            make_uint4(pack_bf16(f[8 * q], f[8 * q + 1]), pack_bf16(f[8 * q + 2], f[8 * q + 3]),
+                                       pack_bf16(f[8 * q + 4], f[8 * q + 5]), pack_bf16(f[8 * q + 6], f[8 * q + 7]));
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kOFree));
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort && !skip && threadIdx.x == 0) {
+        // let every copy and MMA this CTA started land before it leaves
+        if (scorer) {
+            // the last loads of every stage (earlier phases of a stage are complete)
+            for (int q = counters[1] > kFlashKStages ? counters[1] - kFlashKStages : 0; q < counters[1]; ++q)
+                tc::drain(bar(kKFull + q % kFlashKStages), (q / kFlashKStages) & 1, args.timeout_ns);
+            tc::drain(bar(kSDrain), 0, args.timeout_ns);
+        } else {
+            for (int q = counters[4] > kFlashVStages ? counters[4] - kFlashVStages : 0; q < counters[4]; ++q)
+                tc::drain(bar(kVFull + q % kFlashVStages), (q / kFlashVStages) & 1, args.timeout_ns);
+            tc::drain(bar(kODrain), 0, args.timeout_ns);
+        }
+    }
+    __syncthreads();
+    __syncwarp();
+    cluster_sync_all();   // neither CTA leaves while the other may still write into it
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 namespace {
@@ -769,13 +1515,68 @@ AttnWorkspace attn_layout(int64_t S, int64_t D)
 
 size_t attn_workspace_bytes(int64_t S, int64_t D) { return attn_layout(S, D).total; }
 
+namespace {
+
+// 0 = launched; 2 = tensor-map encoding failed; 3 = the launch failed.
+int run_flash(const void *q, const void *k, const void *vt, const void *residual, void *out, int S, int D,
+              int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err)
+{
+    tc::EncodeTiledFn enc = tc::encode_fn();
+    if (!enc) return 2;
+    CUtensorMap mq, mk, mv;
+    if (!encode_kmajor(enc, &mq, q, S, D, 128) || !encode_kmajor(enc, &mk, k, S, D, 128) ||
+        !encode_kmajor(enc, &mv, vt, D, S, D / 2))
+        return 2;
+    FlashArgs a;
+    a.S = S;
+    a.D = D;
+    a.tiles = S / 128;
+    a.nblocks = S / 128;
+    a.scale_log2 = kLog2e / sqrtf(static_cast<float>(D));
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.residual = static_cast<const __nv_bfloat16 *>(residual);
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.timeout_ns = timeout_ns;
+    const uint32_t smem = flash_layout(D).total + 1024u;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(flash_layout(512).total + 1024u));
+    });
+    if (attr != cudaSuccess) {
+        *err = attr;
+        return 3;
+    }
+    int clusters = tc::pair_clusters(attn_flash_kernel, kFlashThreads, smem, sm_count);
+    if (clusters > a.tiles) clusters = a.tiles;
+    if (clusters < 1) clusters = 1;
+    attn_flash_kernel<<<2 * clusters, kFlashThreads, smem, s>>>(mq, mk, mv, a);
+    *err = cudaGetLastError();
+    return *err == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace
+
 int launch_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
-                       const void *residual, void *out, int S, int D, void *workspace, int sm_count,
+                       const void *residual, void *out, int S, int D, void *workspace, bool one_pass, int sm_count,
                        uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches)
 {
     const AttnWorkspace lay = attn_layout(S, D);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *vt = ws + lay.vt;
+    if (one_pass) {
+        *launches = 0;
+        // V'^T = W' xn^T + b', then the one-pass softmax and weighted sum
+        int r = run_gemm(wf, xn, vt, D, S, D, 1.0f, bf, nullptr, nullptr, false, kGemmPlain, nullptr, nullptr,
+                         sm_count, timeout_ns, s, err);
+        if (r) return r;
+        ++*launches;
+        r = run_flash(q, k, vt, residual, out, S, D, sm_count, timeout_ns, s, err);
+        if (r) return r;
+        ++*launches;
+        return 0;
+    }
     float2 *stats = reinterpret_cast<float2 *>(ws + lay.stats);
     float2 *row_ml = reinterpret_cast<float2 *>(ws + lay.row_ml);
     void *p = ws + lay.p;

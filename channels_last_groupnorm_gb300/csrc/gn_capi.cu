@@ -721,6 +721,6 @@ int gn_residual_gate_add(const void *residual, const void *update, const void *g
     return GN_OK;
 }
 
-int gn_abi_version(void) { return 6; }
+int gn_abi_version(void) { return 7; }
 
 }  // extern "C"

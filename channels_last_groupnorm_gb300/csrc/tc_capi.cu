@@ -147,9 +147,22 @@ int gn_attn_folded(const void *q, const void *k, const void *xn, const void *wf,
                    const void *residual, void *out, int64_t S, int64_t D, void *workspace, size_t workspace_bytes,
                    void *stream)
 {
+    return gn_attn_folded_ex(q, k, xn, wf, bf, residual, out, S, D, workspace, workspace_bytes, GN_ATTN_AUTO,
+                             stream);
+}
+
+int gn_attn_folded_ex(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
+                      const void *residual, void *out, int64_t S, int64_t D, void *workspace, size_t workspace_bytes,
+                      int schedule, void *stream)
+{
     if (!q || !k || !xn || !wf || !bf || !out || !workspace) return GN_ERR_NULL;
     if (!attn_tokens_ok(S)) return GN_ERR_SHAPE;
     if (!attn_width_ok(D)) return GN_ERR_CHANNELS;
+    if (schedule != GN_ATTN_AUTO && schedule != GN_ATTN_ONE_PASS && schedule != GN_ATTN_STORED_WEIGHTS)
+        return GN_ERR_VARIANT;
+    if (schedule == GN_ATTN_ONE_PASS && !gn::attn_one_pass_ok(D)) return GN_ERR_VARIANT;
+    const bool one_pass = schedule == GN_ATTN_ONE_PASS ||
+                          (schedule == GN_ATTN_AUTO && gn::attn_one_pass_preferred(S, D));
     const auto addr = [](const void *p) { return reinterpret_cast<uintptr_t>(p); };
     if (addr(q) % 16 || addr(k) % 16 || addr(xn) % 16 || addr(wf) % 16 || addr(bf) % 16 || addr(out) % 16 ||
         addr(workspace) % 256 || (residual && addr(residual) % 16))
@@ -175,8 +188,8 @@ int gn_attn_folded(const void *q, const void *k, const void *xn, const void *wf,
     cudaError_t e = cudaSuccess;
     int launches = 0;
     const int r = gn::launch_attn_folded(q, k, xn, wf, bf, residual, out, static_cast<int>(S), static_cast<int>(D),
-                                         workspace, d.sm_count, wait_timeout_ns(), static_cast<cudaStream_t>(stream),
-                                         &e, &launches);
+                                         workspace, one_pass, d.sm_count, wait_timeout_ns(),
+                                         static_cast<cudaStream_t>(stream), &e, &launches);
     count_launches(static_cast<uint64_t>(launches));
     if (r != 0) {
         cudaGetLastError();

@@ -34,10 +34,17 @@ constexpr int kAttnMaxS = 32768;   // the longest sequence gn_attn_folded takes
 cudaError_t launch_attn_fold(const void *wv, const void *bv, const void *wo, const void *bo, void *wf, float *bf,
                              int D, int sm_count, cudaStream_t s);
 size_t attn_workspace_bytes(int64_t S, int64_t D);
+// The one-pass schedule (scores on chip) handles widths up to 512.
+inline bool attn_one_pass_ok(int64_t D) { return D <= 512; }
+// The automatic choice: the one-pass schedule once there are 64 query tiles
+// of 128 rows (S >= 8192); below that its CTA pairs leave most SMs idle and
+// the stored-weights schedule is faster (GB300: 69 against 90 us at S = 4096,
+// 170 against 151 us at S = 8192, D = 512).
+inline bool attn_one_pass_preferred(int64_t S, int64_t D) { return attn_one_pass_ok(D) && S >= 8192; }
 // 0 = launched (*launches kernels); 2 = tensor-map encoding failed; 3 = a
-// launch failed (*err holds the CUDA error).
+// launch failed (*err holds the CUDA error).  one_pass selects the schedule.
 int launch_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
-                       const void *residual, void *out, int S, int D, void *workspace, int sm_count,
+                       const void *residual, void *out, int S, int D, void *workspace, bool one_pass, int sm_count,
                        uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches);
 cudaError_t read_attn_status(unsigned int *status);
 cudaError_t clear_attn_status();

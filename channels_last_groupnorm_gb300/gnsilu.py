@@ -49,6 +49,11 @@ VARIANT_TWO_PASS = 1
 VARIANT_FUSED = 2
 VARIANT_CLUSTER = 3
 
+# schedules of gn_attn_folded_ex (GN_ATTN_* in gnsilu.h)
+ATTN_AUTO = 0
+ATTN_ONE_PASS = 1
+ATTN_STORED_WEIGHTS = 2
+
 # statuses that mean "this input is not supported" (the caller falls back)
 UNSUPPORTED = {GN_ERR_SHAPE, GN_ERR_CHANNELS, GN_ERR_ALIGN, GN_ERR_EPS, GN_ERR_ALIAS, GN_ERR_FORMAT}
 
@@ -78,6 +83,8 @@ EXPORTS = {
     "gn_attn_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 2),
     "gn_attn_folded": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int64] * 2
                        + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gn_attn_folded_ex": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int64] * 2
+                          + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
     "gn_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                 ctypes.c_int, ctypes.c_void_p]),
     "gn_silu_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4),
@@ -506,6 +513,12 @@ def raw_gn_attn_folded(q, k, xn, wf, bf, residual, out, S, D, workspace, workspa
                                 stream or None)
 
 
+def raw_gn_attn_folded_ex(q, k, xn, wf, bf, residual, out, S, D, workspace, workspace_bytes, schedule,
+                          stream=0) -> int:
+    return lib().gn_attn_folded_ex(q, k, xn, wf, bf, residual or None, out, S, D, workspace, workspace_bytes,
+                                   schedule, stream or None)
+
+
 def gn_attn_workspace_bytes(S: int, D: int) -> int:
     return int(lib().gn_attn_workspace_bytes(S, D))
 
@@ -533,7 +546,8 @@ def attn_fold(wv, bv, wo, bo, stream=None):
     return (wf, bf) if _finish(rc, "gn_attn_fold") else None
 
 
-def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, stream=None):
+def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, stream=None,
+                     schedule=ATTN_AUTO):
     """``softmax(q k^T / sqrt(D)) (xn W'^T + b') + residual`` for bf16 CUDA
     tensors q, k, xn (and residual) of shape [S, D] and the folded weight
     from ``attn_fold``; equal to the unfolded single-head attention block
@@ -541,7 +555,9 @@ def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, 
     out [S, D] bf16, or None when not supported (S not a multiple of 128 in
     [128, 32768], D not a multiple of 128 in [128, 1024], layouts, dtypes,
     a ``workspace`` that is not a contiguous 1-D uint8 tensor on q's
-    device; a smaller one is replaced by a fresh one)."""
+    device -- a smaller one is replaced by a fresh one --, ATTN_ONE_PASS
+    with D > 512).  ``schedule``: ATTN_AUTO, ATTN_ONE_PASS (scores kept on
+    chip) or ATTN_STORED_WEIGHTS (softmax weights through the workspace)."""
     lib()
     torch = _torch()
     ts = (q, k, xn)
@@ -561,6 +577,8 @@ def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, 
         return None
     if _grad_blocked(q, k, xn, wf, bf, residual):
         return None
+    if schedule not in (ATTN_AUTO, ATTN_ONE_PASS, ATTN_STORED_WEIGHTS) or (schedule == ATTN_ONE_PASS and D > 512):
+        return None
     need = gn_attn_workspace_bytes(S, D)
     if need == 0:
         warnings.warn("attention_folded: unsupported S or D", stacklevel=2)
@@ -575,8 +593,8 @@ def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, 
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
-        rc = raw_gn_attn_folded(q.data_ptr(), k.data_ptr(), xn.data_ptr(), wf.data_ptr(), bf.data_ptr(),
-                                0 if residual is None else residual.data_ptr(), out.data_ptr(), S, D,
-                                workspace.data_ptr(), workspace.numel(),
-                                _stream_handle(q.device, stream))
+        rc = raw_gn_attn_folded_ex(q.data_ptr(), k.data_ptr(), xn.data_ptr(), wf.data_ptr(), bf.data_ptr(),
+                                   0 if residual is None else residual.data_ptr(), out.data_ptr(), S, D,
+                                   workspace.data_ptr(), workspace.numel(), schedule,
+                                   _stream_handle(q.device, stream))
     return out if _finish(rc, "gn_attn_folded") else None

@@ -377,10 +377,24 @@ int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf1
  * (exact because every softmax row sums to 1).  gn_attn_fold() forms W'
  * (fp32 sums rounded once to bf16) and b' (fp32) once per weight;
  * gn_attn_folded() evaluates the second form on the tensor cores (fp32
- * accumulation): the folded value rows, then the fp32 scores twice -- once
- * reduced to each row's softmax maximum and sum, once written as softmax
- * weights rounded to bf16 -- and the weighted sum.
+ * accumulation), first the folded value rows, then the softmax and the
+ * weighted sum by one of two schedules:
+ *   GN_ATTN_ONE_PASS: one pass over the keys per tile of 128 query rows,
+ *     on pairs of CTAs (D <= 512): the scores stay on chip (tensor memory),
+ *     the weights go from one CTA of the pair to the other through
+ *     distributed shared memory; a running row maximum rescales the output
+ *     when it moves.
+ *   GN_ATTN_STORED_WEIGHTS: the fp32 scores twice -- once reduced to each
+ *     row's softmax maximum and sum, once written to the workspace as
+ *     softmax weights rounded to bf16 -- then the weighted sum as a GEMM.
+ * Both round the weights to bf16 before the weighted sum.  GN_ATTN_AUTO
+ * takes the one-pass schedule when D <= 512 and there are at least 64 query
+ * tiles (S >= 8192): with fewer tiles it leaves most SMs idle and the
+ * stored-weights schedule is faster.
  */
+
+/* Schedules of gn_attn_folded_ex(). */
+enum { GN_ATTN_AUTO = 0, GN_ATTN_ONE_PASS = 1, GN_ATTN_STORED_WEIGHTS = 2 };
 
 /* Fold the value projection (wv [D][D], bv [D]) and the output projection
  * (wo [D][D], bo [D]) -- DEVICE bf16, PyTorch Linear layout [out][in],
@@ -392,11 +406,11 @@ int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf1
 int gn_attn_fold(const void *wv_bf16, const void *bv_bf16, const void *wo_bf16, const void *bo_bf16,
                  void *wf_bf16, float *bf, int64_t D, void *stream);
 
-/* Workspace bytes gn_attn_folded() needs for S tokens of width D: the
- * folded value rows (2 D S bytes), per-row-segment softmax records
- * (16 S^2 / 128 bytes), the rows' softmax statistics (8 S) and the bf16
- * softmax weights (2 S^2), each rounded up to 256 bytes; 0 if S or D is out
- * of range. */
+/* Workspace bytes gn_attn_folded() needs for S tokens of width D, whatever
+ * the schedule: the folded value rows (2 D S bytes), per-row-segment softmax
+ * records (16 S^2 / 128 bytes), the rows' softmax statistics (8 S) and the
+ * bf16 softmax weights (2 S^2), each rounded up to 256 bytes (the one-pass
+ * schedule uses only the value rows); 0 if S or D is out of range. */
 size_t gn_attn_workspace_bytes(int64_t S, int64_t D);
 
 /* The folded attention.
@@ -417,11 +431,19 @@ int gn_attn_folded(const void *q_bf16, const void *k_bf16, const void *xn_bf16, 
                    const void *residual_bf16, void *out_bf16, int64_t S, int64_t D, void *workspace,
                    size_t workspace_bytes, void *stream);
 
+/* gn_attn_folded() with the schedule named (GN_ATTN_*).  Errors as for
+ * gn_attn_folded(), and GN_ERR_VARIANT for an unknown schedule or
+ * GN_ATTN_ONE_PASS with D > 512. */
+int gn_attn_folded_ex(const void *q_bf16, const void *k_bf16, const void *xn_bf16, const void *wf_bf16,
+                      const float *bf, const void *residual_bf16, void *out_bf16, int64_t S, int64_t D,
+                      void *workspace, size_t workspace_bytes, int schedule, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gn_status_string(int status);
 
-/* ABI version of this header: 6 (5 lacked gn_release_workspaces and
- * gn_library_workspaces, and its entry points did not return GN_ERR_KERNEL;
+/* ABI version of this header: 7 (6 lacked gn_attn_folded_ex; 5 also lacked
+ * gn_release_workspaces and gn_library_workspaces, and its entry points did
+ * not return GN_ERR_KERNEL;
  * 4 also lacked the gn_attn_* calls; 3 also the gn_upconv_* calls; 2 also
  * gn_residual_gate_add; 1 also gn_silu_rows_any and gn_silu_ndhwc). */
 int gn_abi_version(void);

@@ -1,6 +1,7 @@
 """Single-head attention with the output projection folded into V on the
-GPU (gn_attn_fold + gn_attn_folded: three tcgen05 GEMMs and a row softmax)
-against the fp64 oracle of the UNFOLDED block (value projection, softmax
+GPU (gn_attn_fold + gn_attn_folded, both schedules: the one-pass CTA-pair
+kernel with the scores kept on chip, and the stored-weights GEMMs) against
+the fp64 oracle of the UNFOLDED block (value projection, softmax
 attention, output projection, residual; sglang PR #33451, "FLUX.2 VAE
 decoder fast path behind quality=high", section "Modifications", item 2,
 attention bullet).
@@ -45,11 +46,16 @@ def dev(bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
 
-def run(c, residual_in_place=False):
+ONE_PASS, STORED = gs.ATTN_ONE_PASS, gs.ATTN_STORED_WEIGHTS
+SCHEDULES = pytest.mark.parametrize("schedule", [ONE_PASS, STORED], ids=["one_pass", "stored_weights"])
+
+
+def run(c, residual_in_place=False, schedule=gs.ATTN_AUTO):
     wf, bf = gs.attn_fold(dev(c["wv"]), dev(c["bv"]), dev(c["wo"]), dev(c["bo"]))
     res = dev(c["residual"])
     out = res if residual_in_place else None
-    y = gs.attention_folded(dev(c["q"]), dev(c["k"]), dev(c["xn"]), wf, bf, residual=res, out=out)
+    y = gs.attention_folded(dev(c["q"]), dev(c["k"]), dev(c["xn"]), wf, bf, residual=res, out=out,
+                            schedule=schedule)
     assert y is not None, "the CUDA path rejected a supported input"
     torch.cuda.synchronize()
     assert gs.gn_device_status(False) == 0
@@ -70,22 +76,48 @@ def oracle_args(c):
     return (c["q"], c["k"], c["xn"], c["wv"], c["bv"], c["wo"], c["bo"], c["residual"])
 
 
+@SCHEDULES
 @pytest.mark.parametrize("S,D,residual", [(256, 512, True), (256, 512, False), (384, 128, True),
                                           (128, 256, True), (640, 384, False),
                                           (1024, 512, True),    # weighted sum on CTA pairs (K = S >= 1024)
                                           (256, 1024, False)])  # the widest D the entry takes
-def test_matches_oracle(S, D, residual):
+def test_matches_oracle(S, D, residual, schedule):
     c = wl.make_attn_case(S, D, S + D, residual)
-    y = run(c).float().cpu().numpy().astype(np.float64)
+    if schedule == ONE_PASS and D > 512:
+        assert run_none(c, schedule), "the one-pass schedule takes D <= 512 only"
+        return
+    y = run(c, schedule=schedule).float().cpu().numpy().astype(np.float64)
     ref, mag = oracle.attn().forward(*oracle_args(c), with_mag=True)
     check(y, ref, mag, f"S={S} D={D} residual={residual}")
 
 
-def test_in_place_on_the_residual():
+def run_none(c, schedule):
+    wf, bf = gs.attn_fold(dev(c["wv"]), dev(c["bv"]), dev(c["wo"]), dev(c["bo"]))
+    return gs.attention_folded(dev(c["q"]), dev(c["k"]), dev(c["xn"]), wf, bf, schedule=schedule) is None
+
+
+@SCHEDULES
+def test_in_place_on_the_residual(schedule):
     c = wl.make_attn_case(256, 512, 3)
     ref, mag = oracle.attn().forward(*oracle_args(c), with_mag=True)
-    y = run(c, residual_in_place=True).float().cpu().numpy().astype(np.float64)
+    y = run(c, residual_in_place=True, schedule=schedule).float().cpu().numpy().astype(np.float64)
     check(y, ref, mag, "in place")
+
+
+@pytest.mark.parametrize("S,one_pass", [(4096, False), (8192, True), (16384, True)])
+def test_auto_schedule(S, one_pass):
+    """ATTN_AUTO takes the one-pass kernel from 64 query tiles on (two
+    launches: the value rows, then the pair kernel) and the stored-weights
+    GEMMs below (five launches)."""
+    D = 512
+    q = torch.zeros(S, D, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(D, D, dtype=torch.bfloat16, device="cuda")
+    wf, bf = gs.attn_fold(w, q[0], w.clone(), q[1])
+    torch.cuda.synchronize()
+    before = gs.gn_kernel_launch_count()
+    assert gs.attention_folded(q, q, q, wf, bf) is not None
+    torch.cuda.synchronize()
+    assert gs.gn_kernel_launch_count() - before == (2 if one_pass else 5)
 
 
 def test_fold_matches_the_weight_product():
@@ -106,13 +138,14 @@ def test_fold_matches_the_weight_product():
     assert np.all(np.abs(bg - b_want) <= 2.0 ** -14 * b_abs)
 
 
+@SCHEDULES
 @pytest.mark.parametrize("name,rows", [("attn_s4096_d512", 48), ("attn_s16384_d512", 24)])
-def test_decoder_shapes_sampled(name, rows):
+def test_decoder_shapes_sampled(name, rows, schedule):
     """The FLUX.2 mid-block shapes in full, sampled query rows (first, last,
     tile edges, random) against the oracle row by row."""
     w = wl.ATTN_BY_NAME[name]
     c = wl.make_attn_inputs(w)
-    y = run(c)
+    y = run(c, schedule=schedule)
     idx = np.unique(np.concatenate([[0, 1, 127, 128, w.S - 1],
                                     np.random.default_rng(7).integers(0, w.S, rows)]))
     got = y[torch.from_numpy(idx).cuda()].float().cpu().numpy().astype(np.float64)
@@ -120,10 +153,11 @@ def test_decoder_shapes_sampled(name, rows):
     check(got, ref, mag, name)
 
 
-def test_deterministic():
+@SCHEDULES
+def test_deterministic(schedule):
     c = wl.make_attn_case(512, 512, 5)
-    a = run(c).cpu()
-    b = run(c).cpu()
+    a = run(c, schedule=schedule).cpu()
+    b = run(c, schedule=schedule).cpu()
     assert torch.equal(a, b)
 
 

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert gs.gn_abi_version() == 6
+    assert gs.gn_abi_version() == 7
     for code in range(13):
         s = gs.status_string(code)
         assert s.startswith("GN_"), (code, s)
@@ -419,8 +419,36 @@ def test_attn_fold_rejects(kw, code):
     assert gs.raw_gn_attn_fold(a["wv"], a["bv"], a["wo"], a["bo"], a["wf"], a["bf"], a["D"]) == code
 
 
+def attn_ex(schedule, **kw):
+    a = dict(q=AQ, k=AK, xn=AX, wf=AW, bf=AB, residual=AR, out=AO, S=256, D=512, ws=AWS,
+             ws_bytes=gs.gn_attn_workspace_bytes(256, 512))
+    a.update(kw)
+    return gs.raw_gn_attn_folded_ex(a["q"], a["k"], a["xn"], a["wf"], a["bf"], a["residual"], a["out"], a["S"],
+                                    a["D"], a["ws"], a["ws_bytes"], schedule)
+
+
+@pytest.mark.parametrize("schedule,kw,code", [
+    (3, {}, gs.GN_ERR_VARIANT),
+    (-1, {}, gs.GN_ERR_VARIANT),
+    (gs.ATTN_ONE_PASS, dict(D=1024, ws_bytes=gs.gn_attn_workspace_bytes(256, 1024)), gs.GN_ERR_VARIANT),
+    (gs.ATTN_ONE_PASS, dict(q=0), gs.GN_ERR_NULL),
+    (gs.ATTN_STORED_WEIGHTS, dict(S=100), gs.GN_ERR_SHAPE),
+    (gs.ATTN_ONE_PASS, dict(ws_bytes=1024), gs.GN_ERR_WORKSPACE),
+])
+def test_attn_ex_rejects(schedule, kw, code):
+    assert attn_ex(schedule, **kw) == code
+
+
+def test_attention_binding_refuses_a_bad_schedule():
+    t = torch.zeros(256, 512, dtype=torch.bfloat16)
+    w = torch.zeros(512, 512, dtype=torch.bfloat16)
+    assert gs.attention_folded(t, t, t, w, torch.zeros(512), schedule=7) is None
+
+
 @no_gpu
 def test_attn_valid_arguments_without_a_device():
+    for schedule in (gs.ATTN_AUTO, gs.ATTN_ONE_PASS, gs.ATTN_STORED_WEIGHTS):
+        assert attn_ex(schedule) == gs.GN_ERR_DEVICE
     assert attn() == gs.GN_ERR_DEVICE
     assert attn(residual=0) == gs.GN_ERR_DEVICE
     assert attn(residual=AO) == gs.GN_ERR_DEVICE        # in place on the residual
