@@ -923,7 +923,7 @@ def run_attn(args, w, device, rank, world):
         "roofline": {"bound": "tensor", "achieved": r["tflops_per_call_events"], "peak": peak,
                      "unit": "TFLOP/s", "frac": round(r["tflops_per_call_events"] / peak, 4),
                      "peak_kind": peak_kind, "peak_sustained": sustained,
-                     "traffic": recorded_traffic(w.name, "attn", ATTN_SOURCES),
+                     "traffic": recorded_traffic(w.name, "attn_" + r["schedule"], ATTN_SOURCES),
                      "kernel": ("whole call: the value-row gemm_kernel + attn_flash_kernel" if r["schedule"] == "one_pass"
                                 else "whole call: 4 gemm_kernel launches + softmax_stats_kernel")
                                + " (shares in the committed ncu launch list); traffic = DRAM bytes of the "
