@@ -806,7 +806,8 @@ def measure_attn(w, steps, device, stream, peak, torch_context=True, schedule=No
     are folded once (gn_attn_fold, untimed: per model), then a CUDA graph of
     `steps` calls is replayed.  ``schedule`` (default: the library's
     automatic choice) is reported with the kernels one call launches: the
-    one-pass schedule keeps the scores on chip (2 launches), the
+    one-pass schedule keeps the scores on chip (2 launches, 3 when tiles are
+    split between CTA pairs), the
     stored-weights one writes and reads the 2 S^2 bytes of softmax weights
     (5 launches; more than L2 at S = 16384).  TFLOP/s counts the folded
     evaluation: 2 S D^2 (value rows) + 4 S^2 D (scores, weighted sum)."""
@@ -852,7 +853,7 @@ def measure_attn(w, steps, device, stream, peak, torch_context=True, schedule=No
     r = {"workload": w.name, "us_per_call": round(us, 2), "tflops": round(w.flops / (us * 1e-6) / 1e12, 1),
          "frac": round(w.flops / (us * 1e-6) / 1e12 / peak, 3), "launch_us_mean": round(launch_us, 2),
          "tflops_per_call_events": round(w.flops / (launch_us * 1e-6) / 1e12, 1),
-         "kernels_per_call": kernels, "schedule": "one_pass" if kernels == 2 else "stored_weights",
+         "kernels_per_call": kernels, "schedule": "stored_weights" if kernels == 5 else "one_pass",
          "workspace_bytes": need, "launch": "cuda-graph"}
     if torch_context:
         # context only: the stock block (value projection, SDPA, output projection, residual) in PyTorch

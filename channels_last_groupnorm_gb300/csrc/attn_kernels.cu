@@ -590,8 +590,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 // The softmax and the weighted sum in one pass over the keys, on CTA pairs,
 // for widths D <= 512 (see the file comment):
 //   out = softmax(q k^T / sqrt(D)) V' + residual,  given V'^T [D][S].
-// A cluster of two CTAs owns one tile of 128 query rows at a time
-// (persistent over the tiles).
+// The work is split into (tile of 128 query rows, block of 128 keys) units,
+// and each cluster of two CTAs takes an equal run of consecutive units: whole
+// tiles, and at either end possibly a piece of a tile that another cluster
+// finishes (or starts).  A whole tile is written out by its cluster; a piece
+// leaves its unnormalised output with the rows' running maxima and sums in
+// the workspace, and attn_combine_kernel merges the pieces afterwards.
 //  * CTA 0, the score CTA, keeps the tile's q rows in tensor memory (the
 //    A operand of its MMAs; its softmax warps load them, one row per
 //    thread), streams k in blocks of 128 keys (128-dimension chunks through
@@ -621,7 +625,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 //  * Tile t visits the key blocks starting at block t (the softmax does not
 //    depend on the order): clusters working at the same time then read
 //    different key and value rows, instead of all asking L2 for the same
-//    lines at once.
+//    lines at once.  A tile's pieces cover disjoint runs of that order.
 // Every wait is bounded; a timeout records the sticky status and both CTAs
 // still meet at the final cluster barrier before either leaves.
 // ---------------------------------------------------------------------------
@@ -650,17 +654,45 @@ enum FlashBar {
     // output CTA
     kPFull = kSDrain + 1, kVFull = kPFull + 2, kVEmpty = kVFull + kFlashVStages, kPDone = kVEmpty + kFlashVStages,
     kRescaleReq = kPDone + 2, kORescaled = kRescaleReq + 1, kOFull = kORescaled + 1, kOFree = kOFull + 1,
-    kLFull = kOFree + 1, kODrain = kLFull + 2, kFlashBars = kODrain + 1
+    kLFull = kOFree + 1, kODrain = kLFull + 2,
+    // score CTA: a row-sum buffer of the output CTA is free again (its 8 epilogue warps)
+    kLEmpty = kODrain + 1, kFlashBars = kLEmpty + 2
 };
 
 struct FlashArgs {
     int S, D, tiles, nblocks;
+    // The work is tiles x nblocks (tile, key block) units; cluster c takes
+    // the units [flash_unit_begin(c), flash_unit_begin(c + 1)): with split
+    // set, an equal share whose ends may fall inside a tile (that tile's
+    // parts are merged by attn_combine_kernel), else whole tiles.
+    int units, clusters, split;
     float scale_log2;                  // log2(e) / sqrt(D)
     const __nv_bfloat16 *q;            // [S][D]
     const __nv_bfloat16 *residual;     // [S][D] or null
     __nv_bfloat16 *out;                // [S][D]
+    // split: two slots per cluster (its first and its last piece of a tile),
+    // each [D][128] fp32 unnormalised output, then 128 row maxima m and 128
+    // row sums l
+    float *partial;
     uint64_t timeout_ns;
 };
+
+__host__ __device__ inline int flash_unit_begin(const FlashArgs &a, int c)
+{
+    if (a.split) return static_cast<int>(static_cast<long long>(c) * a.units / a.clusters);
+    return static_cast<int>(static_cast<long long>(c) * a.tiles / a.clusters) * a.nblocks;
+}
+
+// The cluster whose units contain unit u.
+__device__ inline int flash_unit_cluster(const FlashArgs &a, int u)
+{
+    int c = static_cast<int>(static_cast<long long>(u) * a.clusters / a.units);
+    while (c + 1 < a.clusters && flash_unit_begin(a, c + 1) <= u) ++c;
+    while (c > 0 && flash_unit_begin(a, c) > u) --c;
+    return c;
+}
+
+__host__ __device__ inline size_t flash_slot_floats(int D) { return static_cast<size_t>(D) * 128 + 256; }
 
 // Shared-memory layout.  The score CTA uses q / kring, the output CTA
 // p / vring / alpha / flags / lsum / mailbox; the barriers and the small
@@ -680,14 +712,14 @@ __host__ __device__ inline FlashLayout flash_layout(int D)
     l.pstage = l.kring + kFlashKStages * 32768u;         // one block's weights, as the output CTA lays them out
     l.astage = l.pstage + 32768u;                        // 128 rescale factors
     l.fstage = l.astage + 512u;                          // 4 flags
-    l.lstage = l.fstage + 16u;                           // 128 row sums
-    const uint32_t score_end = l.lstage + 512u;
+    l.lstage = l.fstage + 16u;                           // 128 row sums, then 128 row maxima
+    const uint32_t score_end = l.lstage + 1024u;
     l.p = 0;                                             // two buffers of two [128][64] subtiles
     l.vring = 2u * 32768u;
     l.alpha = l.vring + kFlashVStages * static_cast<uint32_t>(D) * 64u;
     l.flags = l.alpha + 2u * 128u * 4u;
     l.lsum = l.flags + 2u * 4u * 4u;
-    l.mailbox = l.lsum + 2u * 128u * 4u;
+    l.mailbox = l.lsum + 2u * 256u * 4u;
     const uint32_t out_end = l.mailbox + 16u;
     l.bars = (score_end > out_end ? score_end : out_end);
     l.bars = (l.bars + 15u) & ~15u;
@@ -832,8 +864,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = static_cast<int>(cluster_ctarank());
     const bool scorer = rank == 0;
-    const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int cl = blockIdx.x >> 1;   // this cluster's share of the work units
     const int D = args.D, half = D / 2, nb = args.nblocks;
+    const int ub = flash_unit_begin(args, cl), ue = flash_unit_begin(args, cl + 1);
     // score CTA: two score buffers (columns 0-255) and the q rows (from 256);
     // output CTA: the output, D columns
     const uint32_t tmem_cols = scorer ? 512u : (D <= 128 ? 128u : (D <= 256 ? 256u : 512u));
@@ -852,6 +885,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                 mbar_init(bar(kPEmpty + i), 1);      // the output CTA's forwarder
             }
             mbar_init(bar(kSDrain), 2);
+            for (int i = 0; i < 2; ++i) mbar_init(bar(kLEmpty + i), 8);
         } else {
             for (int i = 0; i < 2; ++i) {
                 mbar_init(bar(kPFull + i), 1);       // armed here (plus the bytes the score CTA copies)
@@ -870,7 +904,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             // the first uses of the weights and row-sum buffers expect their bytes
             for (int i = 0; i < 2; ++i) {
                 mbar_arrive_expect_tx(bar(kPFull + i), kFlashPBytes);
-                mbar_arrive_expect_tx(bar(kLFull + i), 512u);
+                mbar_arrive_expect_tx(bar(kLFull + i), 1024u);
             }
         }
         *abort = (*reinterpret_cast<volatile unsigned int *>(&g_at_status) != 0u) ? 1 : 0;
@@ -899,8 +933,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             // ---- producer: k in 128-dimension chunks (two boxes each) ----
             int kq = 0;
             bool go = true;
-            for (int t = cl; go && t < args.tiles; t += ncl) {
-                for (int j = 0; go && j < nb; ++j) {
+            for (int u = ub, nu = 0; go && u < ue; u = nu) {
+                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                nu = u + (j1 - j0);
+                for (int j = j0; go && j < j1; ++j) {
                     for (int c = 0; c < D / 128; ++c, ++kq) {
                         const int st = kq % kFlashKStages;
                         if (kq >= kFlashKStages &&
@@ -930,11 +966,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             const int cpb = D / 128;   // chunks per block
             int g = 0, tq = 0;
             bool go = true, bad = false;   // bad: a wait of the waiter failed (sticky)
-            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
+            for (int u = ub, nu = 0; go && u < ue; u = nu, ++tq) {
+                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                nu = u + (j1 - j0);
                 if (waiter && lane == 0) bad = bad || !fwait(bar(kQFull), tq & 1, abort, args.timeout_ns);
                 __syncwarp();
                 if (bar_any(hb, 64, bad)) break;
-                for (int j = 0; go && j < nb; ++j, ++g) {
+                for (int j = j0; go && j < j1; ++j, ++g) {
                     if ((g & 1) != mine) continue;
                     const int buf = g & 1;
                     const uint32_t d = tmem + static_cast<uint32_t>(buf * 128);
@@ -991,7 +1029,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             float *lstage = reinterpret_cast<float *>(gbase + lay.lstage);
             int g = 0, tq = 0;
             bool go = true, pending = false;
-            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
+            for (int u = ub, nu = 0; go && u < ue; u = nu, ++tq) {
+                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                nu = u + (j1 - j0);
                 float m = -INFINITY, l = 0.f;
                 {
                     // the tile's q row of this thread into tensor memory (columns
@@ -1018,7 +1058,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(kQFull));
                 }
-                for (int j = 0; j < nb; ++j, ++g) {
+                for (int j = j0; j < j1; ++j, ++g) {
                     const int buf = g & 1;
                     const bool ok = fwait(bar(kSFull + buf), (g >> 1) & 1, abort, args.timeout_ns);
                     tc_fence_after_sync();
@@ -1101,14 +1141,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                     }
                 }
                 if (!go) break;
-                // the tile's row sums
+                // the piece's row sums and maxima, once the output CTA has read the
+                // ones that went into the same buffer two pieces back (a failed wait
+                // sets the abort flag, which every softmax warp sees at the next block)
                 lstage[row] = l;
+                lstage[128 + row] = m;
                 fence_proxy_async_smem();
                 named_sync(2, 128);
-                if (shipper) {
+                if (shipper &&
+                    (tq < 2 || fwait(bar(kLEmpty + (tq & 1)), ((tq >> 1) - 1) & 1, abort, args.timeout_ns))) {
                     const uint32_t full = base + remote + lay.bars + 8u * (kLFull + (tq & 1));
-                    bulk_copy_to_peer(base + remote + lay.lsum + static_cast<uint32_t>(tq & 1) * 512u,
-                                      base + lay.lstage, 512u, full);
+                    bulk_copy_to_peer(base + remote + lay.lsum + static_cast<uint32_t>(tq & 1) * 1024u,
+                                      base + lay.lstage, 1024u, full);
                     bulk_commit();
                     bulk_wait_read_all();
                     pending = false;
@@ -1123,8 +1167,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             int vq = 0;
             bool go = true;
             const uint32_t stage_bytes = static_cast<uint32_t>(half) * 128u;
-            for (int t = cl; go && t < args.tiles; t += ncl)
-                for (int j = 0; go && j < nb; ++j)
+            for (int u = ub, nu = 0; go && u < ue; u = nu) {
+                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                nu = u + (j1 - j0);
+                for (int j = j0; go && j < j1; ++j)
                     for (int kh = 0; kh < 4; ++kh, ++vq) {   // (64-key chunk, half) pairs
                         const int st = vq % kFlashVStages;
                         if (vq >= kFlashVStages &&
@@ -1137,6 +1183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                                     ((j + t) % nb) * 128 + (kh >> 1) * 64, (kh & 1) * half, bar(kVFull + st));
                         counters[4] = vq + 1;   // V stages issued
                     }
+            }
         } else if (!skip && (warp == 1 || warp == 10 || warp >= 12)) {
             // ---- MMA: O += P V' per block, one half of D per issuer (warp 1
             // the first, warp 10 the second).  Warp 12 (13) does the waiting
@@ -1152,8 +1199,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             volatile int *flags = reinterpret_cast<volatile int *>(gbase + lay.flags);
             int g = 0, tq = 0, ro = 0;
             bool go = true, bad = false;   // bad: a wait of the waiter failed (sticky)
-            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
-                for (int j = 0; j < nb; ++j, ++g) {
+            for (int u = ub, nu = 0; go && u < ue; u = nu, ++tq) {
+                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                nu = u + (j1 - j0);
+                for (int j = j0; j < j1; ++j, ++g) {
                     const int buf = g & 1;
                     for (int kc = 0; kc < 2; ++kc) {   // the two 64-key chunks of this half
                         const int vq = g * 4 + kc * 2 + h;
@@ -1161,7 +1210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                         if (waiter && lane == 0) {
                             if (kc == 0) {
                                 bad = bad || !wait_cluster(bar(kPFull + buf), (g >> 1) & 1, abort, args.timeout_ns);
-                                if (!bad && j == 0) {
+                                if (!bad && j == j0) {
                                     // the previous tile's output has been written out
                                     bad = tq > 0 && !fwait(bar(kOFree), (tq - 1) & 1, abort, args.timeout_ns);
                                 } else if (!bad && (flags[buf * 4] | flags[buf * 4 + 1] | flags[buf * 4 + 2] |
@@ -1196,7 +1245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
                                 umma_f16(tmem + static_cast<uint32_t>(h * half), sw128_kmajor_desc(pa + kk * 32),
-                                         sw128_kmajor_desc(va + kk * 32), idesc, (j > 0 || kc > 0 || kk > 0) ? 1u : 0u);
+                                         sw128_kmajor_desc(va + kk * 32), idesc, (j > j0 || kc > 0 || kk > 0) ? 1u : 0u);
                             umma_commit(bar(kVEmpty + st));
                         }
                         __syncwarp();
@@ -1217,27 +1266,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             const uint32_t peer = mapa_shared(base, 0) - base;
             int g = 0;
             bool go = true;
-            for (int t = cl; go && t < args.tiles; t += ncl)
-                for (int j = 0; j < nb; ++j, ++g) {
-                    if (!fwait(bar(kPDone + (g & 1)), (g >> 1) & 1, abort, args.timeout_ns)) {
-                        go = false;
-                        break;
-                    }
-                    // the buffer's next use expects its bytes; then it goes back
-                    mbar_arrive_expect_tx(bar(kPFull + (g & 1)), kFlashPBytes);
-                    mbar_arrive_cluster(base + peer + lay.bars + 8u * (kPEmpty + (g & 1)));
+            for (int u = ub; go && u < ue; ++u, ++g) {   // one key block per unit
+                if (!fwait(bar(kPDone + (g & 1)), (g >> 1) & 1, abort, args.timeout_ns)) {
+                    go = false;
+                    break;
                 }
+                // the buffer's next use expects its bytes; then it goes back
+                mbar_arrive_expect_tx(bar(kPFull + (g & 1)), kFlashPBytes);
+                mbar_arrive_cluster(base + peer + lay.bars + 8u * (kPEmpty + (g & 1)));
+            }
         } else if (!skip && warp >= 2 && warp < 10) {
             // ---- epilogue warps: rescale O on request; out = O / l + residual at the tile's end ----
             const int quad = warp & 3, h = (warp - 2) >> 2;
             const int row = quad * 32 + lane;
             const uint32_t taddr0 = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(h * half);
+            const uint32_t peer0 = mapa_shared(base, 0) - base;   // add to an offset for CTA 0's address
             volatile int *mailbox = reinterpret_cast<volatile int *>(gbase + lay.mailbox);
             const float *alpha = reinterpret_cast<const float *>(gbase + lay.alpha);
             const float *lsum = reinterpret_cast<const float *>(gbase + lay.lsum);
             int rr = 0, tq = 0;
             bool go = true;
-            for (int t = cl; go && t < args.tiles; t += ncl, ++tq) {
+            for (int u = ub, nu = 0; go && u < ue; u = nu, ++tq) {
+                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                nu = u + (j1 - j0);
                 for (;;) {
                     const bool ok = fwait(bar(kRescaleReq), rr & 1, abort, args.timeout_ns);
                     ++rr;
@@ -1268,38 +1319,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                 ok = ok && wait_cluster(bar(kLFull + (tq & 1)), (tq >> 1) & 1, abort, args.timeout_ns);
                 // the buffer's next use (at the end of the tile two on, long after
                 // this tile's sums are read) expects its bytes
-                if (ok && warp == 2 && lane == 0) mbar_arrive_expect_tx(bar(kLFull + (tq & 1)), 512u);
+                if (ok && warp == 2 && lane == 0) mbar_arrive_expect_tx(bar(kLFull + (tq & 1)), 1024u);
                 tc_fence_after_sync();
                 if (!__all_sync(0xffffffffu, ok && !*abort)) break;
-                const float inv = 1.0f / lsum[(tq & 1) * 128 + row];
-                const int64_t orow = static_cast<int64_t>(t) * 128 + row;
-                __nv_bfloat16 *dst = args.out + orow * D + h * half;
-                const __nv_bfloat16 *res = args.residual ? args.residual + orow * D + h * half : nullptr;
+                const float lrow = lsum[(tq & 1) * 256 + row], mrow = lsum[(tq & 1) * 256 + 128 + row];
+                __syncwarp();
+                // the score CTA may ship the next sums into this buffer
+                if (lane == 0) mbar_arrive_cluster(base + peer0 + lay.bars + 8u * (kLEmpty + (tq & 1)));
+                if (j0 == 0 && j1 == nb) {
+                    // the whole tile: out = O / l + residual
+                    const float inv = 1.0f / lrow;
+                    const int64_t orow = static_cast<int64_t>(t) * 128 + row;
+                    __nv_bfloat16 *dst = args.out + orow * D + h * half;
+                    const __nv_bfloat16 *res = args.residual ? args.residual + orow * D + h * half : nullptr;
 #pragma unroll 1
-                for (int c = 0; c < half; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr0 + c, v);
-                    tmem_wait_ld();
-                    float f[32];
+                    for (int c = 0; c < half; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(taddr0 + c, v);
+                        tmem_wait_ld();
+                        float f[32];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(v[k]) * inv;
-                    if (res) {
+                        for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(v[k]) * inv;
+                        if (res) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 rr4 = *reinterpret_cast<const uint4 *>(res + c + 8 * q);
-                            const uint32_t w[4] = {rr4.x, rr4.y, rr4.z, rr4.w};
+                            for (int q = 0; q < 4; ++q) {
+                                const uint4 rr4 = *reinterpret_cast<const uint4 *>(res + c + 8 * q);
+                                const uint32_t w[4] = {rr4.x, rr4.y, rr4.z, rr4.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                f[8 * q + 2 * e] += __uint_as_float(w[e] << 16);
-                                f[8 * q + 2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+                                for (int e = 0; e < 4; ++e) {
+                                    f[8 * q + 2 * e] += __uint_as_float(w[e] << 16);
+                                    f[8 * q + 2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+                                }
                             }
                         }
-                    }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4 *>(dst + c + 8 * q) =
-                            make_uint4(pack_bf16(f[8 * q], f[8 * q + 1]), pack_bf16(f[8 * q + 2], f[8 * q + 3]),
-                                       pack_bf16(f[8 * q + 4], f[8 * q + 5]), pack_bf16(f[8 * q + 6], f[8 * q + 7]));
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(dst + c + 8 * q) = make_uint4(
+                                pack_bf16(f[8 * q], f[8 * q + 1]), pack_bf16(f[8 * q + 2], f[8 * q + 3]),
+                                pack_bf16(f[8 * q + 4], f[8 * q + 5]), pack_bf16(f[8 * q + 6], f[8 * q + 7]));
+                    }
+                } else {
+                    // a piece of the tile: the unnormalised O ([D][128], so that a
+                    // warp's stores of one column are contiguous) with the row's m
+                    // and l, for attn_combine_kernel
+                    float *slot = args.partial + static_cast<size_t>(2 * cl + (u == ub ? 0 : 1)) * flash_slot_floats(D);
+#pragma unroll 1
+                    for (int c = 0; c < half; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(taddr0 + c, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            slot[static_cast<size_t>(h * half + c + k) * 128 + row] = __uint_as_float(v[k]);
+                    }
+                    if (h == 0) {
+                        slot[static_cast<size_t>(D) * 128 + row] = mrow;
+                        slot[static_cast<size_t>(D) * 128 + 128 + row] = lrow;
+                    }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -1329,6 +1405,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// Merges the pieces of each tile that more than one cluster worked on: with
+// M the largest of the pieces' row maxima m_i and w_i = 2^(m_i - M),
+//   out = (sum_i w_i O_i) / (sum_i w_i l_i) + residual.
+// Grid (tiles, D / kCombineCols), 128 threads: one row each, kCombineCols
+// columns per thread (many small CTAs, so that enough loads are in flight).
+constexpr int kCombineCols = 16;
+
+__global__ void __launch_bounds__(128) attn_combine_kernel(const FlashArgs a)
+{
+    const int t = blockIdx.x, nb = a.nblocks, D = a.D;
+    const int c_lo = flash_unit_cluster(a, t * nb), c_hi = flash_unit_cluster(a, t * nb + nb - 1);
+    if (c_lo == c_hi) return;   // one cluster did the whole tile and wrote it out
+    const int row = threadIdx.x, col0 = blockIdx.y * kCombineCols;
+    const size_t sf = flash_slot_floats(D), ml = static_cast<size_t>(D) * 128;
+    // a cluster's piece of tile t is its first one if its units begin in tile t, else its last
+    const auto slot_of = [&](int c) {
+        return a.partial + static_cast<size_t>(2 * c + (flash_unit_begin(a, c) / nb == t ? 0 : 1)) * sf;
+    };
+    float M = -INFINITY;
+    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, slot_of(c)[ml + row]);
+    float acc[kCombineCols];
+#pragma unroll
+    for (int k = 0; k < kCombineCols; ++k) acc[k] = 0.f;
+    float L = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const float *sl = slot_of(c);
+        const float w = exp2f(sl[ml + row] - M);
+        L += w * sl[ml + 128 + row];
+#pragma unroll
+        for (int k = 0; k < kCombineCols; ++k) acc[k] += w * sl[static_cast<size_t>(col0 + k) * 128 + row];
+    }
+    const float inv = 1.0f / L;
+    const int64_t orow = static_cast<int64_t>(t) * 128 + row;
+    __nv_bfloat16 *dst = a.out + orow * D + col0;
+    const __nv_bfloat16 *res = a.residual ? a.residual + orow * D + col0 : nullptr;
+#pragma unroll
+    for (int q = 0; q < kCombineCols / 8; ++q) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = acc[8 * q + e] * inv;
+        if (res) {
+            const uint4 r4 = *reinterpret_cast<const uint4 *>(res + 8 * q);
+            const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] += __uint_as_float(w[e] << 16);
+                f[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+            }
+        }
+        *reinterpret_cast<uint4 *>(dst + 8 * q) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                                            pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
     }
 }
 
@@ -1517,9 +1647,12 @@ size_t attn_workspace_bytes(int64_t S, int64_t D) { return attn_layout(S, D).tot
 
 namespace {
 
-// 0 = launched; 2 = tensor-map encoding failed; 3 = the launch failed.
+// 0 = launched (*launches kernels); 2 = tensor-map encoding failed; 3 = a
+// launch failed.  partial / partial_bytes: workspace the pieces of split
+// tiles may use.
 int run_flash(const void *q, const void *k, const void *vt, const void *residual, void *out, int S, int D,
-              int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err)
+              void *partial, size_t partial_bytes, int sm_count, uint64_t timeout_ns, cudaStream_t s,
+              cudaError_t *err, int *launches)
 {
     tc::EncodeTiledFn enc = tc::encode_fn();
     if (!enc) return 2;
@@ -1532,10 +1665,12 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
     a.D = D;
     a.tiles = S / 128;
     a.nblocks = S / 128;
+    a.units = a.tiles * a.nblocks;
     a.scale_log2 = kLog2e / sqrtf(static_cast<float>(D));
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.residual = static_cast<const __nv_bfloat16 *>(residual);
     a.out = static_cast<__nv_bfloat16 *>(out);
+    a.partial = static_cast<float *>(partial);
     a.timeout_ns = timeout_ns;
     const uint32_t smem = flash_layout(D).total + 1024u;
     static std::once_flag once;
@@ -1548,19 +1683,38 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
         *err = attr;
         return 3;
     }
-    int clusters = tc::pair_clusters(attn_flash_kernel, kFlashThreads, smem, sm_count);
-    if (clusters > a.tiles) clusters = a.tiles;
+    // Every resident CTA pair takes an equal share of the (tile, key block)
+    // units, which may end inside a tile (its pieces are merged afterwards),
+    // when the workspace holds two pieces per cluster and whole tiles would
+    // not divide evenly; otherwise whole tiles.
+    const int cap = tc::pair_clusters(attn_flash_kernel, kFlashThreads, smem, sm_count);
+    int clusters = cap < a.units ? cap : a.units;
     if (clusters < 1) clusters = 1;
+    const size_t slot_bytes = flash_slot_floats(D) * sizeof(float);
+    const size_t fit = partial_bytes / (2 * slot_bytes);   // clusters whose pieces fit
+    if (static_cast<size_t>(clusters) > fit && fit > static_cast<size_t>(a.tiles)) clusters = static_cast<int>(fit);
+    a.split = (a.tiles % clusters != 0) && static_cast<size_t>(clusters) <= fit;
+    if (!a.split && clusters > a.tiles) clusters = a.tiles;
+    a.clusters = clusters;
     attn_flash_kernel<<<2 * clusters, kFlashThreads, smem, s>>>(mq, mk, mv, a);
     *err = cudaGetLastError();
-    return *err == cudaSuccess ? 0 : 3;
+    if (*err != cudaSuccess) return 3;
+    ++*launches;
+    if (a.split) {
+        attn_combine_kernel<<<dim3(a.tiles, D / kCombineCols), 128, 0, s>>>(a);
+        *err = cudaGetLastError();
+        if (*err != cudaSuccess) return 3;
+        ++*launches;
+    }
+    return 0;
 }
 
 }  // namespace
 
 int launch_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
-                       const void *residual, void *out, int S, int D, void *workspace, bool one_pass, int sm_count,
-                       uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches)
+                       const void *residual, void *out, int S, int D, void *workspace, size_t workspace_bytes,
+                       bool one_pass, int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err,
+                       int *launches)
 {
     const AttnWorkspace lay = attn_layout(S, D);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -1572,10 +1726,8 @@ int launch_attn_folded(const void *q, const void *k, const void *xn, const void 
                          sm_count, timeout_ns, s, err);
         if (r) return r;
         ++*launches;
-        r = run_flash(q, k, vt, residual, out, S, D, sm_count, timeout_ns, s, err);
-        if (r) return r;
-        ++*launches;
-        return 0;
+        return run_flash(q, k, vt, residual, out, S, D, ws + lay.stats, workspace_bytes - lay.stats, sm_count,
+                         timeout_ns, s, err, launches);
     }
     float2 *stats = reinterpret_cast<float2 *>(ws + lay.stats);
     float2 *row_ml = reinterpret_cast<float2 *>(ws + lay.row_ml);

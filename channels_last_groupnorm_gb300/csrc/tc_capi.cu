@@ -174,11 +174,14 @@ int gn_attn_folded_ex(const void *q, const void *k, const void *xn, const void *
         const void *p;
         size_t n;
     } ins[] = {{q, act}, {k, act}, {xn, act}, {wf, static_cast<size_t>(2 * D * D)}, {bf, static_cast<size_t>(4 * D)}};
+    // the whole workspace the caller hands over may be used (the one-pass
+    // schedule keeps the pieces of split tiles beyond the minimum)
+    const size_t wsb = workspace_bytes;
     for (const auto &in : ins)
-        if (ranges_overlap(out, act, in.p, in.n) || ranges_overlap(workspace, need, in.p, in.n)) return GN_ERR_ALIAS;
-    if (ranges_overlap(out, act, workspace, need)) return GN_ERR_ALIAS;
+        if (ranges_overlap(out, act, in.p, in.n) || ranges_overlap(workspace, wsb, in.p, in.n)) return GN_ERR_ALIAS;
+    if (ranges_overlap(out, act, workspace, wsb)) return GN_ERR_ALIAS;
     if (residual && residual != out &&
-        (ranges_overlap(out, act, residual, act) || ranges_overlap(workspace, need, residual, act)))
+        (ranges_overlap(out, act, residual, act) || ranges_overlap(workspace, wsb, residual, act)))
         return GN_ERR_ALIAS;
     int dev = -1;
     DeviceInfo d;
@@ -188,7 +191,7 @@ int gn_attn_folded_ex(const void *q, const void *k, const void *xn, const void *
     cudaError_t e = cudaSuccess;
     int launches = 0;
     const int r = gn::launch_attn_folded(q, k, xn, wf, bf, residual, out, static_cast<int>(S), static_cast<int>(D),
-                                         workspace, one_pass, d.sm_count, wait_timeout_ns(),
+                                         workspace, workspace_bytes, one_pass, d.sm_count, wait_timeout_ns(),
                                          static_cast<cudaStream_t>(stream), &e, &launches);
     count_launches(static_cast<uint64_t>(launches));
     if (r != 0) {

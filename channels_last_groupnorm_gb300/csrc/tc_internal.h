@@ -42,10 +42,13 @@ inline bool attn_one_pass_ok(int64_t D) { return D <= 512; }
 // 170 against 151 us at S = 8192, D = 512).
 inline bool attn_one_pass_preferred(int64_t S, int64_t D) { return attn_one_pass_ok(D) && S >= 8192; }
 // 0 = launched (*launches kernels); 2 = tensor-map encoding failed; 3 = a
-// launch failed (*err holds the CUDA error).  one_pass selects the schedule.
+// launch failed (*err holds the CUDA error).  one_pass selects the schedule;
+// it may use workspace beyond gn_attn_workspace_bytes() (workspace_bytes) for
+// the pieces of tiles it splits between CTA pairs.
 int launch_attn_folded(const void *q, const void *k, const void *xn, const void *wf, const float *bf,
-                       const void *residual, void *out, int S, int D, void *workspace, bool one_pass, int sm_count,
-                       uint64_t timeout_ns, cudaStream_t s, cudaError_t *err, int *launches);
+                       const void *residual, void *out, int S, int D, void *workspace, size_t workspace_bytes,
+                       bool one_pass, int sm_count, uint64_t timeout_ns, cudaStream_t s, cudaError_t *err,
+                       int *launches);
 cudaError_t read_attn_status(unsigned int *status);
 cudaError_t clear_attn_status();
 // Device address of the mapped host word that mirrors the status (current device).

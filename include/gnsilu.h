@@ -420,8 +420,11 @@ size_t gn_attn_workspace_bytes(int64_t S, int64_t D);
  *   residual  : DEVICE bf16 [S][D] added to the result, or NULL; may equal
  *               out (in place) but not overlap it otherwise.
  *   out       : DEVICE bf16 [S][D], 16-byte aligned, overlapping no input.
- *   workspace : DEVICE, >= gn_attn_workspace_bytes(S, D), 256-byte aligned,
- *               caller-owned, overlapping nothing else.
+ *   workspace : DEVICE, workspace_bytes >= gn_attn_workspace_bytes(S, D),
+ *               256-byte aligned, caller-owned, overlapping nothing else;
+ *               all workspace_bytes of it may be used (the one-pass
+ *               schedule keeps there the pieces of query tiles it splits
+ *               between CTA pairs, and splits more finely when given more).
  *   S a multiple of 128 in [128, 32768]; D as for gn_attn_fold().
  * Asynchronous on `stream`.  Errors: GN_ERR_NULL, GN_ERR_SHAPE (S),
  * GN_ERR_CHANNELS (D), GN_ERR_ALIGN, GN_ERR_ALIAS, GN_ERR_WORKSPACE,

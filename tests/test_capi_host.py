@@ -389,6 +389,7 @@ def attn(**kw):
     (dict(out=AWS + 1024), gs.GN_ERR_ALIAS),
     (dict(residual=AO + 256), gs.GN_ERR_ALIAS),
     (dict(ws=AX), gs.GN_ERR_ALIAS),
+    (dict(ws=AO - 0x100000, ws_bytes=0x200000), gs.GN_ERR_ALIAS),   # the whole declared workspace counts
 ])
 def test_attn_rejects(kw, code):
     assert attn(**kw) == code
