@@ -51,7 +51,9 @@ ATTN_METRIC = ("single-head attention, output projection folded into V, bf16 in/
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCES = ["gn_kernels.cu", "gn_cluster.cu", "gn_capi.cu", "gn_internal.h", "gn_math.cuh", "gn_ptx.cuh",
                   "capi_util.h", "rga_kernels.cu"]
-UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
+# the files that make the upsample-conv kernels and their launch plan (the
+# C-ABI checks in tc_capi.cu do not change what runs on the GPU)
+UPCONV_SOURCES = ["upconv_kernels.cu", "tc_ptx.cuh", "tc_common.cuh", "gn_ptx.cuh"]
 ATTN_SOURCES = ["attn_kernels.cu", "tc_ptx.cuh", "tc_common.cuh", "tc_internal.h", "tc_capi.cu", "gn_ptx.cuh"]
 
 

@@ -383,7 +383,10 @@ int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf1
  *     on pairs of CTAs (D <= 512): the scores stay on chip (tensor memory),
  *     the weights go from one CTA of the pair to the other through
  *     distributed shared memory; a running row maximum rescales the output
- *     when it moves.
+ *     when it moves.  The pairs share the (query tile, key block) units
+ *     equally; a tile split between pairs leaves its pieces (unnormalised
+ *     output, row maxima and sums) in the workspace, and a third kernel
+ *     merges them.
  *   GN_ATTN_STORED_WEIGHTS: the fp32 scores twice -- once reduced to each
  *     row's softmax maximum and sum, once written to the workspace as
  *     softmax weights rounded to bf16 -- then the weighted sum as a GEMM.
@@ -410,7 +413,8 @@ int gn_attn_fold(const void *wv_bf16, const void *bv_bf16, const void *wo_bf16, 
  * the schedule: the folded value rows (2 D S bytes), per-row-segment softmax
  * records (16 S^2 / 128 bytes), the rows' softmax statistics (8 S) and the
  * bf16 softmax weights (2 S^2), each rounded up to 256 bytes (the one-pass
- * schedule uses only the value rows); 0 if S or D is out of range. */
+ * schedule keeps the pieces of split tiles where the others would be);
+ * 0 if S or D is out of range. */
 size_t gn_attn_workspace_bytes(int64_t S, int64_t D);
 
 /* The folded attention.
