@@ -242,7 +242,7 @@ bool fused_launchable(const Plan &p, const DeviceInfo &d)
 bool cluster_preferred(const gn::ClusterPlan &cp)
 {
     const int64_t vectors = static_cast<int64_t>(cp.R) * (cp.SC / 8);
-    return cp.waves == 1 && (vectors <= 2048 || (vectors <= 4096 && cp.SC >= 16));
+    return cp.waves == 1 && (vectors <= 2048 || (vectors <= 8192 && cp.SC >= 16) || vectors <= 3072);
 }
 
 // The automatic choice: the cluster schedule where it is the faster one

@@ -139,6 +139,7 @@ struct ClusterPlan {
     int64_t units;     // clusters: (batch entry, slice) pairs
     int waves;         // rounds of clusters the device runs one after another
     uint32_t smem;     // dynamic shared memory per CTA
+    int tma;           // rows copied by tensor-map boxes (else 16-byte copies by every thread)
 };
 // Kernel attributes, and the co-resident clusters of each size 1..16
 // (cap[size]) at `max_smem` bytes of shared memory per CTA.
