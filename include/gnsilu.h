@@ -268,8 +268,7 @@ int gn_selftest_bounded_wait(int mode, int timeout_ms, int *done, int blocks, vo
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current, and the first call
  *     of the library on a device sets the device up (kernel attributes, the
- *     mapped status word); make that first call before any stream capture
- *     begins.
+ *     mapped status word), which takes device-wide CUDA calls.
  *   - All calls on a device share the one array, which keeps the previous
  *     call's contents; each call clears the words that must start at zero
  *     (an asynchronous memset on `stream`).  Calls whose GPU work overlaps
