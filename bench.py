@@ -166,10 +166,17 @@ class ClockSampler:
 
 
 def kernel_source_hash(sources=None) -> str:
+    """Hash of the code of the given source files, with comments and
+    blank lines removed: an edit of comments leaves recorded counters valid."""
+    import re
     h = hashlib.sha256()
     for name in (sources or KERNEL_SOURCES):
-        with open(os.path.join(ROOT, "channels_last_groupnorm_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "channels_last_groupnorm_gb300", "csrc", name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"(^|\s)//.*$", r"\1", text, flags=re.M)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

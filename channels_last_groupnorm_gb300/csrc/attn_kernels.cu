@@ -10,7 +10,13 @@
 //       = softmax(q k^T / sqrt(D)) (xn W'^T + b') + residual,
 //   W' = wo wv, b' = wo bv + bo,
 // the second form being exact because every softmax row sums to 1.  This
-// file evaluates the second form:
+// file evaluates the second form, by one of two schedules after the fold:
+//  * one pass (D <= 512): V'^T = W' xn^T + b' by gemm_kernel, then
+//    attn_flash_kernel on CTA pairs keeps each block of scores in tensor
+//    memory and accumulates softmax(...) V' without writing the scores or the
+//    weights (described at the kernel), and attn_combine_kernel merges the
+//    pieces of tiles that were split between pairs;
+//  * stored weights (any D): the kernels below.
 //   attn_fold_kernel   W' (fp32 sums over D, rounded once to bf16) and b'
 //                      (fp32), once per weight;
 //   gemm_kernel        C = alpha A B^T (+ a per-row or per-column bias, + a
@@ -26,8 +32,9 @@
 //   softmax_stats_kernel  merges each row's records into (max, 1 / sum).
 // The fp32 scores are never stored: computing them twice costs 2 S^2 D
 // tensor-core flops, far cheaper than writing and re-reading 4 S^2 bytes.
-// (A single-pass, flash-style kernel does not fit D = 512 well: an fp32
-// 128 x 512 output block alone fills the 512 tensor-memory columns of an SM.)
+// (An fp32 128 x 512 output block alone fills the 512 tensor-memory columns
+// of an SM, which is why the one-pass kernel puts the scores and the output
+// on different CTAs of a pair.)
 //
 // gemm_kernel is persistent (one CTA per SM): warp 0 issues TMA tile loads
 // (128-byte swizzle) into a STAGES-deep ring, warp 1 owns 2 BN tensor-memory
