@@ -1690,20 +1690,43 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
         *err = attr;
         return 3;
     }
-    // Every resident CTA pair takes an equal share of the (tile, key block)
-    // units, which may end inside a tile (its pieces are merged afterwards),
-    // when the workspace holds two pieces per cluster and whole tiles would
-    // not divide evenly; otherwise whole tiles.
+    // How many CTA pairs, and whether they share the (tile, key block) units
+    // equally (runs may end inside a tile: its pieces are merged afterwards,
+    // which needs two workspace slots per pair) or take whole tiles: the
+    // cheapest by an estimate calibrated on a GB300 at D = 512 -- ~2 us per
+    // key block on the busiest pair, ~9 us per piece of a tile a pair
+    // starts (pipeline fill and drain), ~5 us for the merge.  (Measured at
+    // S = 4096: 64 pairs with half a tile each 63 us, 67 pairs with runs
+    // that cross a tile boundary 73 us, 32 pairs with a tile each 91 us.)
     const int cap = tc::pair_clusters(attn_flash_kernel, kFlashThreads, smem, sm_count);
-    int clusters = cap < a.units ? cap : a.units;
-    if (clusters < 1) clusters = 1;
     const size_t slot_bytes = flash_slot_floats(D) * sizeof(float);
-    const size_t fit = partial_bytes / (2 * slot_bytes);   // clusters whose pieces fit
-    if (static_cast<size_t>(clusters) > fit && fit > static_cast<size_t>(a.tiles)) clusters = static_cast<int>(fit);
-    a.split = (a.tiles % clusters != 0) && static_cast<size_t>(clusters) <= fit;
-    if (!a.split && clusters > a.tiles) clusters = a.tiles;
-    a.clusters = clusters;
-    attn_flash_kernel<<<2 * clusters, kFlashThreads, smem, s>>>(mq, mk, mv, a);
+    const size_t fit = partial_bytes / (2 * slot_bytes);   // pairs whose pieces fit
+    int best_c = 1, best_split = 0;
+    double best_cost = 0.0;
+    for (int c = 1; c <= cap && c <= a.units; ++c) {
+        FlashArgs t = a;
+        t.clusters = c;
+        t.split = (a.tiles % c != 0) ? 1 : 0;
+        if (t.split && static_cast<size_t>(c) > fit) continue;   // no room for the pieces
+        if (!t.split && c > a.tiles) continue;
+        int max_blocks = 0, max_pieces = 0;
+        for (int k = 0; k < c; ++k) {
+            const int ub = flash_unit_begin(t, k), ue = flash_unit_begin(t, k + 1);
+            if (ue <= ub) continue;
+            max_blocks = max_blocks > ue - ub ? max_blocks : ue - ub;
+            const int pieces = (ue - 1) / a.nblocks - ub / a.nblocks + 1;
+            max_pieces = max_pieces > pieces ? max_pieces : pieces;
+        }
+        const double cost = 2.0 * max_blocks + 9.0 * max_pieces + (t.split ? 5.0 : 0.0);
+        if (c == 1 || cost < best_cost) {
+            best_cost = cost;
+            best_c = c;
+            best_split = t.split;
+        }
+    }
+    a.clusters = best_c;
+    a.split = best_split;
+    attn_flash_kernel<<<2 * a.clusters, kFlashThreads, smem, s>>>(mq, mk, mv, a);
     *err = cudaGetLastError();
     if (*err != cudaSuccess) return 3;
     ++*launches;

@@ -36,11 +36,12 @@ cudaError_t launch_attn_fold(const void *wv, const void *bv, const void *wo, con
 size_t attn_workspace_bytes(int64_t S, int64_t D);
 // The one-pass schedule (scores on chip) handles widths up to 512.
 inline bool attn_one_pass_ok(int64_t D) { return D <= 512; }
-// The automatic choice: the one-pass schedule once there are 64 query tiles
-// of 128 rows (S >= 8192); below that its CTA pairs leave most SMs idle and
-// the stored-weights schedule is faster (GB300: 69 against 90 us at S = 4096,
-// 170 against 151 us at S = 8192, D = 512).
-inline bool attn_one_pass_preferred(int64_t S, int64_t D) { return attn_one_pass_ok(D) && S >= 8192; }
+// The automatic choice: the one-pass schedule once there are 32 query tiles
+// of 128 rows (S >= 4096); below that its CTA pairs leave most SMs idle (the
+// minimum workspace holds too few pieces to split tiles finely) and the
+// stored-weights schedule is faster (GB300, D = 512: 38 against 60 us at
+// S = 2048, 69 against 64 us at S = 4096, 170 against 157 us at S = 8192).
+inline bool attn_one_pass_preferred(int64_t S, int64_t D) { return attn_one_pass_ok(D) && S >= 4096; }
 // 0 = launched (*launches kernels); 2 = tensor-map encoding failed; 3 = a
 // launch failed (*err holds the CUDA error).  one_pass selects the schedule;
 // it may use workspace beyond gn_attn_workspace_bytes() (workspace_bytes) for

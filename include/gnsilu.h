@@ -390,8 +390,8 @@ int gn_upconv_nhwc(const void *x_bf16, const void *wf_bf16, const void *bias_bf1
  *     row's softmax maximum and sum, once written to the workspace as
  *     softmax weights rounded to bf16 -- then the weighted sum as a GEMM.
  * Both round the weights to bf16 before the weighted sum.  GN_ATTN_AUTO
- * takes the one-pass schedule when D <= 512 and there are at least 64 query
- * tiles (S >= 8192): with fewer tiles it leaves most SMs idle and the
+ * takes the one-pass schedule when D <= 512 and there are at least 32 query
+ * tiles (S >= 4096): with fewer tiles it leaves most SMs idle and the
  * stored-weights schedule is faster.
  */
 

@@ -104,9 +104,9 @@ def test_in_place_on_the_residual(schedule):
     check(y, ref, mag, "in place")
 
 
-@pytest.mark.parametrize("S,one_pass", [(4096, False), (8192, True), (16384, True)])
+@pytest.mark.parametrize("S,one_pass", [(2048, False), (4096, True), (16384, True)])
 def test_auto_schedule(S, one_pass):
-    """ATTN_AUTO takes the one-pass kernel from 64 query tiles on and the
+    """ATTN_AUTO takes the one-pass kernel from 32 query tiles on and the
     stored-weights GEMMs below (five launches)."""
     D = 512
     q = torch.zeros(S, D, dtype=torch.bfloat16, device="cuda")
@@ -121,12 +121,13 @@ def test_auto_schedule(S, one_pass):
     assert gs.gn_kernel_launch_count() - before in ((2, 3) if one_pass else (5,))
 
 
-@pytest.mark.parametrize("S,D,residual", [(640, 512, True), (1024, 512, False), (512, 256, True), (384, 384, True)])
+@pytest.mark.parametrize("S,D,residual", [(640, 512, True), (1024, 512, False), (512, 256, True), (768, 384, True)])
 def test_one_pass_split_tiles_match_oracle(S, D, residual):
-    """With a workspace larger than the minimum the one-pass schedule gives
-    every CTA pair an equal share of (tile, key block) units, so most tiles
-    are split into pieces (down to one key block each) that a third kernel
-    merges by their row maxima and sums."""
+    """With a workspace larger than the minimum the one-pass schedule can
+    give CTA pairs equal shares of (tile, key block) units; at these shapes
+    its estimate prefers that, so the tiles are split into pieces (down to
+    one key block each) that a third kernel merges by their row maxima and
+    sums."""
     c = wl.make_attn_case(S, D, 3 * S + D, residual)
     wf, bf = gs.attn_fold(dev(c["wv"]), dev(c["bv"]), dev(c["wo"]), dev(c["bo"]))
     need = gs.gn_attn_workspace_bytes(S, D)
