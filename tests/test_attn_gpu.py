@@ -176,6 +176,21 @@ def test_decoder_shapes_sampled(name, rows, schedule):
     check(got, ref, mag, name)
 
 
+def test_longest_sequence_one_pass_sampled():
+    """S = 32768, the longest the entry takes, on the one-pass schedule: every
+    CTA pair takes ~6.7 tiles' worth of units, so its run crosses several
+    tile boundaries (pieces at both ends); sampled rows, including the
+    first and last rows of tiles, against the oracle."""
+    S, D = 32768, 512
+    c = wl.make_attn_case(S, D, 5, True)
+    y = run(c, schedule=ONE_PASS)
+    idx = np.unique(np.concatenate([[0, 127, 128, 255, S - 129, S - 128, S - 1],
+                                    np.random.default_rng(11).integers(0, S, 12)]))
+    got = y[torch.from_numpy(idx).cuda()].float().cpu().numpy().astype(np.float64)
+    ref, mag = oracle.attn().rows(*oracle_args(c), idx, with_mag=True)
+    check(got, ref, mag, "S=32768 one pass")
+
+
 @SCHEDULES
 def test_deterministic(schedule):
     c = wl.make_attn_case(512, 512, 5)
