@@ -121,8 +121,10 @@ def test_auto_schedule(S, one_pass):
     assert gs.gn_kernel_launch_count() - before in ((2, 3) if one_pass else (5,))
 
 
-@pytest.mark.parametrize("S,D,residual", [(640, 512, True), (1024, 512, False), (512, 256, True), (768, 384, True)])
-def test_one_pass_split_tiles_match_oracle(S, D, residual):
+@pytest.mark.parametrize("S,D,residual,in_place", [(640, 512, True, False), (1024, 512, False, False),
+                                                   (512, 256, True, False), (768, 384, True, False),
+                                                   (640, 512, True, True)])
+def test_one_pass_split_tiles_match_oracle(S, D, residual, in_place):
     """With a workspace larger than the minimum the one-pass schedule can
     give CTA pairs equal shares of (tile, key block) units; at these shapes
     its estimate prefers that, so the tiles are split into pieces (down to
@@ -134,8 +136,9 @@ def test_one_pass_split_tiles_match_oracle(S, D, residual):
     ws = torch.zeros(need + 2 * 152 * (D * 128 + 256) * 4, dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
     before = gs.gn_kernel_launch_count()
-    y = gs.attention_folded(dev(c["q"]), dev(c["k"]), dev(c["xn"]), wf, bf, residual=dev(c["residual"]),
-                            workspace=ws, schedule=ONE_PASS)
+    res = dev(c["residual"])
+    y = gs.attention_folded(dev(c["q"]), dev(c["k"]), dev(c["xn"]), wf, bf, residual=res,
+                            out=res if in_place else None, workspace=ws, schedule=ONE_PASS)
     torch.cuda.synchronize()
     assert y is not None and gs.gn_device_status(False) == 0
     assert gs.gn_kernel_launch_count() - before == 3, "expected the pieces to be merged"
