@@ -557,7 +557,9 @@ def attention_folded(q, k, xn, wf, bf, residual=None, out=None, workspace=None, 
     a ``workspace`` that is not a contiguous 1-D uint8 tensor on q's
     device -- a smaller one is replaced by a fresh one --, ATTN_ONE_PASS
     with D > 512).  ``schedule``: ATTN_AUTO, ATTN_ONE_PASS (scores kept on
-    chip) or ATTN_STORED_WEIGHTS (softmax weights through the workspace)."""
+    chip) or ATTN_STORED_WEIGHTS (softmax weights through the workspace).
+    All of a given ``workspace`` may be used: the one-pass schedule keeps
+    there the pieces of query tiles it splits between CTA pairs."""
     lib()
     torch = _torch()
     ts = (q, k, xn)
