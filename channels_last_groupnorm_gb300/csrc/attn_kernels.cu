@@ -49,7 +49,10 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <utility>
 
 #include "tc_internal.h"
 #include "gn_ptx.cuh"
@@ -1654,6 +1657,74 @@ size_t attn_workspace_bytes(int64_t S, int64_t D) { return attn_layout(S, D).tot
 
 namespace {
 
+// Co-resident CTA pairs of the one-pass kernel at this shared-memory size
+// (the occupancy query, once per size and device SM count).
+int flash_pair_capacity(uint32_t smem, int sm_count)
+{
+    static std::mutex mu;
+    static std::map<std::pair<uint32_t, int>, int> known;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(smem, sm_count);
+    const auto it = known.find(key);
+    if (it != known.end()) return it->second;
+    const int cap = tc::pair_clusters(attn_flash_kernel, kFlashThreads, smem, sm_count);
+    known[key] = cap;
+    return cap;
+}
+
+// How many CTA pairs, and whether they share the (tile, key block) units
+// equally (runs may end inside a tile: its pieces are merged afterwards,
+// which needs two workspace slots per pair -- at most `fit` pairs) or take
+// whole tiles: the cheapest by an estimate calibrated on a GB300 at D = 512,
+// ~2 us per key block on the busiest pair, ~9 us per piece of a tile a pair
+// starts (pipeline fill and drain), ~5 us for the merge.  (Measured at
+// S = 4096: 64 pairs with half a tile each 63 us, 67 pairs with runs that
+// cross a tile boundary 73 us, 32 pairs with a tile each 91 us.)  The
+// result is remembered per shape.
+void choose_flash_pairs(int tiles, int nblocks, int cap, size_t fit, int *pairs, int *split)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, size_t>, std::pair<int, int>> known;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(tiles, nblocks, cap, fit);
+    const auto it = known.find(key);
+    if (it != known.end()) {
+        *pairs = it->second.first;
+        *split = it->second.second;
+        return;
+    }
+    FlashArgs t{};
+    t.tiles = tiles;
+    t.nblocks = nblocks;
+    t.units = tiles * nblocks;
+    int best_c = 1, best_split = 0;
+    double best_cost = 0.0;
+    for (int c = 1; c <= cap && c <= t.units; ++c) {
+        t.clusters = c;
+        t.split = (tiles % c != 0) ? 1 : 0;
+        if (t.split && static_cast<size_t>(c) > fit) continue;   // no room for the pieces
+        if (!t.split && c > tiles) continue;
+        int max_blocks = 0, max_pieces = 0;
+        for (int k = 0; k < c; ++k) {
+            const int ub = flash_unit_begin(t, k), ue = flash_unit_begin(t, k + 1);
+            if (ue <= ub) continue;
+            max_blocks = max_blocks > ue - ub ? max_blocks : ue - ub;
+            const int pieces = (ue - 1) / nblocks - ub / nblocks + 1;
+            max_pieces = max_pieces > pieces ? max_pieces : pieces;
+        }
+        const double cost = 2.0 * max_blocks + 9.0 * max_pieces + (t.split ? 5.0 : 0.0);
+        if (c == 1 || cost < best_cost) {
+            best_cost = cost;
+            best_c = c;
+            best_split = t.split;
+        }
+    }
+    if (known.size() >= 256) known.clear();   // callers with ever new workspace sizes
+    known[key] = std::make_pair(best_c, best_split);
+    *pairs = best_c;
+    *split = best_split;
+}
+
 // 0 = launched (*launches kernels); 2 = tensor-map encoding failed; 3 = a
 // launch failed.  partial / partial_bytes: workspace the pieces of split
 // tiles may use.
@@ -1690,40 +1761,12 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
         *err = attr;
         return 3;
     }
-    // How many CTA pairs, and whether they share the (tile, key block) units
-    // equally (runs may end inside a tile: its pieces are merged afterwards,
-    // which needs two workspace slots per pair) or take whole tiles: the
-    // cheapest by an estimate calibrated on a GB300 at D = 512 -- ~2 us per
-    // key block on the busiest pair, ~9 us per piece of a tile a pair
-    // starts (pipeline fill and drain), ~5 us for the merge.  (Measured at
-    // S = 4096: 64 pairs with half a tile each 63 us, 67 pairs with runs
-    // that cross a tile boundary 73 us, 32 pairs with a tile each 91 us.)
-    const int cap = tc::pair_clusters(attn_flash_kernel, kFlashThreads, smem, sm_count);
+    // the number of CTA pairs and the split (choose_flash_pairs)
+    const int cap = flash_pair_capacity(smem, sm_count);
     const size_t slot_bytes = flash_slot_floats(D) * sizeof(float);
     const size_t fit = partial_bytes / (2 * slot_bytes);   // pairs whose pieces fit
     int best_c = 1, best_split = 0;
-    double best_cost = 0.0;
-    for (int c = 1; c <= cap && c <= a.units; ++c) {
-        FlashArgs t = a;
-        t.clusters = c;
-        t.split = (a.tiles % c != 0) ? 1 : 0;
-        if (t.split && static_cast<size_t>(c) > fit) continue;   // no room for the pieces
-        if (!t.split && c > a.tiles) continue;
-        int max_blocks = 0, max_pieces = 0;
-        for (int k = 0; k < c; ++k) {
-            const int ub = flash_unit_begin(t, k), ue = flash_unit_begin(t, k + 1);
-            if (ue <= ub) continue;
-            max_blocks = max_blocks > ue - ub ? max_blocks : ue - ub;
-            const int pieces = (ue - 1) / a.nblocks - ub / a.nblocks + 1;
-            max_pieces = max_pieces > pieces ? max_pieces : pieces;
-        }
-        const double cost = 2.0 * max_blocks + 9.0 * max_pieces + (t.split ? 5.0 : 0.0);
-        if (c == 1 || cost < best_cost) {
-            best_cost = cost;
-            best_c = c;
-            best_split = t.split;
-        }
-    }
+    choose_flash_pairs(a.tiles, a.nblocks, cap, fit, &best_c, &best_split);
     a.clusters = best_c;
     a.split = best_split;
     attn_flash_kernel<<<2 * a.clusters, kFlashThreads, smem, s>>>(mq, mk, mv, a);
