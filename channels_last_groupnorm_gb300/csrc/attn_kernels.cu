@@ -687,19 +687,15 @@ struct FlashArgs {
     uint64_t timeout_ns;
 };
 
+// 32-bit arithmetic: S <= kAttnMaxS gives at most 256 tiles and 65536 units,
+// and c <= clusters <= the SM count, so c * units stays far below 2^32.
+static_assert(static_cast<unsigned long long>(kAttnMaxS / 128) * (kAttnMaxS / 128) * 1024ull < (1ull << 32),
+              "unit boundaries need 32 bits");
 __host__ __device__ inline int flash_unit_begin(const FlashArgs &a, int c)
 {
-    if (a.split) return static_cast<int>(static_cast<long long>(c) * a.units / a.clusters);
-    return static_cast<int>(static_cast<long long>(c) * a.tiles / a.clusters) * a.nblocks;
-}
-
-// The cluster whose units contain unit u.
-__device__ inline int flash_unit_cluster(const FlashArgs &a, int u)
-{
-    int c = static_cast<int>(static_cast<long long>(u) * a.clusters / a.units);
-    while (c + 1 < a.clusters && flash_unit_begin(a, c + 1) <= u) ++c;
-    while (c > 0 && flash_unit_begin(a, c) > u) --c;
-    return c;
+    const uint32_t uc = static_cast<uint32_t>(c), cl = static_cast<uint32_t>(a.clusters);
+    if (a.split) return static_cast<int>(uc * static_cast<uint32_t>(a.units) / cl);
+    return static_cast<int>(uc * static_cast<uint32_t>(a.tiles) / cl) * a.nblocks;
 }
 
 __host__ __device__ inline size_t flash_slot_floats(int D) { return static_cast<size_t>(D) * 128 + 256; }
@@ -1421,46 +1417,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
 // Merges the pieces of each tile that more than one cluster worked on: with
 // M the largest of the pieces' row maxima m_i and w_i = 2^(m_i - M),
 //   out = (sum_i w_i O_i) / (sum_i w_i l_i) + residual.
-// Grid (tiles, D / kCombineCols), 128 threads: one row each, kCombineCols
-// columns per thread (many small CTAs, so that enough loads are in flight).
+// Grid (split tiles, D / kCombineCols), 128 threads, one row per thread and
+// kCombineCols columns.  The residual and every piece's row maximum, row sum
+// and outputs are loaded before any of them is used, so the merge waits for
+// one round of loads (pieces past kCombineHeld, which the usual splits do
+// not make, are folded in afterwards one at a time); the register bound
+// keeps eight CTAs on an SM, so that the usual grids run in one or two rounds.
 constexpr int kCombineCols = 16;
+constexpr int kCombineHeld = 2;
+constexpr int kCombineMaxTiles = kAttnMaxS / 128;
 
-__global__ void __launch_bounds__(128) attn_combine_kernel(const FlashArgs a)
+// The split tiles of a launch, each by the cluster that holds its first unit.
+struct CombineTiles {
+    int n;
+    uint16_t c_lo[kCombineMaxTiles];
+};
+
+__global__ void __launch_bounds__(128, 8) attn_combine_kernel(const FlashArgs a, const __grid_constant__ CombineTiles ct)
 {
-    const int t = blockIdx.x, nb = a.nblocks, D = a.D;
-    const int c_lo = flash_unit_cluster(a, t * nb), c_hi = flash_unit_cluster(a, t * nb + nb - 1);
-    if (c_lo == c_hi) return;   // one cluster did the whole tile and wrote it out
+    const int nb = a.nblocks, D = a.D;
+    const int c_lo = ct.c_lo[blockIdx.x];
+    const int t = flash_unit_begin(a, c_lo + 1) / nb;   // the tile's first inner boundary follows cluster c_lo
+    int c_hi = c_lo + 1;                                // the cluster holding the tile's last unit
+    while (c_hi + 1 < a.clusters && flash_unit_begin(a, c_hi + 1) < (t + 1) * nb) ++c_hi;
+    const int np = c_hi - c_lo + 1;
     const int row = threadIdx.x, col0 = blockIdx.y * kCombineCols;
     const size_t sf = flash_slot_floats(D), ml = static_cast<size_t>(D) * 128;
     // a cluster's piece of tile t is its first one if its units begin in tile t, else its last
     const auto slot_of = [&](int c) {
         return a.partial + static_cast<size_t>(2 * c + (flash_unit_begin(a, c) / nb == t ? 0 : 1)) * sf;
     };
-    float M = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, slot_of(c)[ml + row]);
+    const int64_t orow = static_cast<int64_t>(t) * 128 + row;
+    uint4 r4[kCombineCols / 8];
+#pragma unroll
+    for (int q = 0; q < kCombineCols / 8; ++q) r4[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (a.residual) {
+        const uint4 *res = reinterpret_cast<const uint4 *>(a.residual + orow * D + col0);
+#pragma unroll
+        for (int q = 0; q < kCombineCols / 8; ++q) r4[q] = res[q];
+    }
+    float m[kCombineHeld], l[kCombineHeld], o[kCombineHeld][kCombineCols];
+#pragma unroll
+    for (int i = 0; i < kCombineHeld; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCombineCols; ++k) o[i][k] = 0.f;
+        if (i < np) {
+            const float *sl = slot_of(c_lo + i);
+            m[i] = sl[ml + row];
+            l[i] = sl[ml + 128 + row];
+#pragma unroll
+            for (int k = 0; k < kCombineCols; ++k) o[i][k] = sl[static_cast<size_t>(col0 + k) * 128 + row];
+        }
+    }
+    float M = m[0];
+#pragma unroll
+    for (int i = 1; i < kCombineHeld; ++i) M = fmaxf(M, m[i]);
+    for (int i = kCombineHeld; i < np; ++i) M = fmaxf(M, slot_of(c_lo + i)[ml + row]);
     float acc[kCombineCols];
 #pragma unroll
     for (int k = 0; k < kCombineCols; ++k) acc[k] = 0.f;
     float L = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-        const float *sl = slot_of(c);
+#pragma unroll
+    for (int i = 0; i < kCombineHeld; ++i) {
+        const float w = exp2f(m[i] - M);   // 0 for the pieces past np (m = -inf)
+        L += w * l[i];
+#pragma unroll
+        for (int k = 0; k < kCombineCols; ++k) acc[k] += w * o[i][k];
+    }
+    for (int i = kCombineHeld; i < np; ++i) {
+        const float *sl = slot_of(c_lo + i);
         const float w = exp2f(sl[ml + row] - M);
         L += w * sl[ml + 128 + row];
 #pragma unroll
         for (int k = 0; k < kCombineCols; ++k) acc[k] += w * sl[static_cast<size_t>(col0 + k) * 128 + row];
     }
     const float inv = 1.0f / L;
-    const int64_t orow = static_cast<int64_t>(t) * 128 + row;
     __nv_bfloat16 *dst = a.out + orow * D + col0;
-    const __nv_bfloat16 *res = a.residual ? a.residual + orow * D + col0 : nullptr;
 #pragma unroll
     for (int q = 0; q < kCombineCols / 8; ++q) {
         float f[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] = acc[8 * q + e] * inv;
-        if (res) {
-            const uint4 r4 = *reinterpret_cast<const uint4 *>(res + 8 * q);
-            const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+        if (a.residual) {
+            const uint32_t w[4] = {r4[q].x, r4[q].y, r4[q].z, r4[q].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 f[2 * e] += __uint_as_float(w[e] << 16);
@@ -1725,6 +1766,24 @@ void choose_flash_pairs(int tiles, int nblocks, int cap, size_t fit, int *pairs,
     *split = best_split;
 }
 
+// The tiles that the clusters' runs of units split: a boundary between two
+// runs that falls inside a tile splits it, and the first such boundary of
+// the tile names it (by the cluster before it, which holds the tile's first
+// unit).
+CombineTiles split_tiles(const FlashArgs &a)
+{
+    CombineTiles ct;
+    ct.n = 0;
+    int last = -1;
+    for (int c = 1; c < a.clusters; ++c) {
+        const int b = flash_unit_begin(a, c);
+        if (b % a.nblocks == 0 || b / a.nblocks == last) continue;
+        last = b / a.nblocks;
+        ct.c_lo[ct.n++] = static_cast<uint16_t>(c - 1);
+    }
+    return ct;
+}
+
 // 0 = launched (*launches kernels); 2 = tensor-map encoding failed; 3 = a
 // launch failed.  partial / partial_bytes: workspace the pieces of split
 // tiles may use.
@@ -1773,8 +1832,9 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
     *err = cudaGetLastError();
     if (*err != cudaSuccess) return 3;
     ++*launches;
-    if (a.split) {
-        attn_combine_kernel<<<dim3(a.tiles, D / kCombineCols), 128, 0, s>>>(a);
+    const CombineTiles ct = split_tiles(a);
+    if (a.split && ct.n > 0) {
+        attn_combine_kernel<<<dim3(ct.n, D / kCombineCols), 128, 0, s>>>(a, ct);
         *err = cudaGetLastError();
         if (*err != cudaSuccess) return 3;
         ++*launches;
