@@ -235,10 +235,11 @@ bool fused_launchable(const Plan &p, const DeviceInfo &d)
 // its slice rows (16-64 bytes each, one request per row segment) costs less
 // than the fused schedule's grid barrier and global merge.  Measured on a
 // GB300 (graph of calls, inputs larger than L2): up to 2048 vectors per CTA
-// the cluster schedule takes 6.8-8.5 us against 10.6-11.6 us; at 4096 it
-// still wins with 32-byte or wider row segments (10.1-10.9 us against
-// 11.8-12.2) but not with 16-byte ones (14.3 against 12.1); at 8192 (C = 512,
-// 128 x 128) it loses (16.3 against 15.1).
+// the cluster schedule takes 6.8-8.5 us against 10.6-11.6 us; up to 8192
+// vectors with 32-byte or wider row segments (rows copied by tensor-map
+// boxes beyond 2048) it still wins (16 MiB, C = 512: 13.9 against 15.1 us;
+// 8 MiB, C = 256: 11.0 against 12.0), with 16-byte ones only up to about
+// 3072; at 10924 vectors (16 MiB, C = 128) it loses (15.7 against 15.1).
 bool cluster_preferred(const gn::ClusterPlan &cp)
 {
     const int64_t vectors = static_cast<int64_t>(cp.R) * (cp.SC / 8);
