@@ -853,6 +853,65 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Rows 32 quarter .. 32 quarter + 31 of query tile t, 64-dimension chunks
+// [c0, c1), into tensor memory (columns 256 + d/2 of the calling warp's lane
+// quarter).  The loads are coalesced (eight lanes read one row's 128 bytes
+// of a chunk; a lane reading its own row would make every 16-byte load a
+// separate request) and go through 8 KB of staging shared memory, 16-byte
+// pieces XOR-swizzled by the row so that neither the writes nor the
+// row-wise reads meet in a bank; each lane then takes its own row.  Two
+// chunks' loads are in flight at a time.
+__device__ __forceinline__ void flash_load_q(const FlashArgs &args, uint32_t tmem, uint32_t lane_base, int t,
+                                             int quarter, int lane, uint32_t stage, int c0, int c1)
+{
+    const int D = args.D, piece = lane & 7;
+    const __nv_bfloat16 *src =
+        args.q + (static_cast<int64_t>(t) * 128 + quarter * 32 + (lane >> 3)) * D + piece * 8;
+#pragma unroll 1
+    for (int c = c0; c < c1; c += 2) {
+        const int nh = c + 1 < c1 ? 2 : 1;
+        uint4 g[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                g[h][i] = h < nh ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(4 * i) * D + (c + h) * 64))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h < nh) {
+                const uint32_t st = stage + static_cast<uint32_t>(h) * 4096u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t r = static_cast<uint32_t>(4 * i + (lane >> 3));
+                    sts128(st + r * 128u + ((static_cast<uint32_t>(piece) ^ (r & 7u)) << 4), g[h][i]);
+                }
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h < nh) {
+                const uint32_t st = stage + static_cast<uint32_t>(h) * 4096u;
+                uint32_t v[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 x = lds128(st + static_cast<uint32_t>(lane) * 128u +
+                                           ((static_cast<uint32_t>(k) ^ (static_cast<uint32_t>(lane) & 7u)) << 4));
+                    v[4 * k] = x.x;
+                    v[4 * k + 1] = x.y;
+                    v[4 * k + 2] = x.z;
+                    v[4 * k + 3] = x.w;
+                }
+                tmem_st_32x32b_x32(tmem + lane_base + 256u + static_cast<uint32_t>((c + h) * 32), v);
+            }
+        }
+        __syncwarp();
+    }
+    tmem_wait_st();
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
     attn_flash_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const FlashArgs args)
@@ -1040,26 +1099,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                 nu = u + (j1 - j0);
                 float m = -INFINITY, l = 0.f;
                 {
-                    // the tile's q row of this thread into tensor memory (columns
-                    // 256 + d/2), once the previous tile's MMAs are done with it
+                    // the tile's q rows of this warp into tensor memory (columns
+                    // 256 + d/2), once the previous tile's MMAs are done with them
                     const bool ok = tq == 0 || fwait(bar(kQFree), (tq - 1) & 1, abort, args.timeout_ns);
                     if (bar_any(1, 128, !ok || *abort)) break;
                     tc_fence_after_sync();
-                    const uint4 *src = reinterpret_cast<const uint4 *>(args.q + (static_cast<int64_t>(t) * 128 + row) * D);
-#pragma unroll 1
-                    for (int c = 0; c < D / 64; ++c) {
-                        uint32_t v[32];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const uint4 u = __ldg(src + c * 8 + i);
-                            v[4 * i] = u.x;
-                            v[4 * i + 1] = u.y;
-                            v[4 * i + 2] = u.z;
-                            v[4 * i + 3] = u.w;
-                        }
-                        tmem_st_32x32b_x32(tmem + lane_base + 256u + static_cast<uint32_t>(c * 32), v);
-                    }
-                    tmem_wait_st();
+                    // (through the weights staging buffer: it holds no weights
+                    // now, the previous piece ended with every copy out of it read)
+                    flash_load_q(args, tmem, lane_base, t, quad, lane,
+                                 base + lay.pstage + static_cast<uint32_t>(quad) * 8192u, 0, D / 64);
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(kQFull));
