@@ -81,6 +81,14 @@ uint32_t l2_hints()
     return h;
 }
 
+// GN_DYNAMIC_PASS2=0 keeps the fused kernel's pass 2 on its static piece
+// assignment everywhere (for comparisons).
+bool dynamic_pass2_enabled()
+{
+    static const bool on = env_u64("GN_DYNAMIC_PASS2", 1) != 0;
+    return on;
+}
+
 
 // Channel counts an entry point serves: the power-of-two entries take the
 // page's contract (C a power of two in [8, 2048]); the general entries take
@@ -201,6 +209,14 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     int64_t ring = (budget - static_cast<int64_t>(gn::aux_smem_bytes(g, kind_smem))) / pb;
     if (ring > gn::kMaxRing) ring = gn::kMaxRing;
     g.ring = static_cast<int32_t>(ring);
+    // the fused kernel deals out pass 2 at run time for one batch entry
+    // with one item per CTA and at least three ring-fulls of pieces per CTA
+    // (the shapes where its SMs' unequal streaming rates show)
+    g.dyn_top = g.base_pieces - g.ring;
+    g.dyn_p2 = (kind == GN_VARIANT_FUSED && N == 1 && g.items == p.grid && g.base_pieces >= 3 * ring &&
+                dynamic_pass2_enabled())
+                   ? 1
+                   : 0;
     // workspace
     size_t off = 256;   // barrier words
     p.off_partial = off;

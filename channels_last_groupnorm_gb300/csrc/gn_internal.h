@@ -47,6 +47,12 @@ struct Geom {
     int32_t stat_log2, stat_passes;   // log2(stat_lanes); passes over the groups
     float rows_lo, rows_hi, rows_short;   // item rows (base_pieces, base_pieces + 1 pieces) and the
                                           // short last piece's missing rows, as floats
+    // fused kernel, one batch entry and one item per CTA: pass 2 deals the
+    // pieces not resident in a ring out at run time (gn_kernels.cu,
+    // produce_pass2_dyn); dyn_top is the highest row of the item sequences
+    // that holds such a piece (base_pieces - ring; negative: none)
+    int32_t dyn_p2;
+    int64_t dyn_top;
 };
 
 struct Args {
@@ -62,7 +68,8 @@ struct Args {
     float2 *gstat;                // [N][G]    group (mean, rstd)   (fused)
     float2 *st;                   // [N][C]    (scale, shift)       (two-pass)
     float *mean, *rstd;           // [N][G]
-    unsigned int *sync;           // barrier words (fused)
+    unsigned int *sync;           // fused: [0] grid-barrier arrivals, [1] re-arm count, [2] pass-2
+                                  // piece counter, [3] exits (the last CTA zeroes [2] and [3])
     uint64_t timeout_ns;          // bound on every wait
 };
 
@@ -70,7 +77,7 @@ struct Args {
 // mean / rstd of the fused kernel) shares the pass-1 scratch; `chs` (the
 // per-channel (mean, M2) of one work item) shares `st` in the fused kernel.
 struct Layout {
-    uint32_t ring, scratch, kvec, chs, st, gb, gstat, bars, flags, total;
+    uint32_t ring, scratch, kvec, chs, st, gb, gstat, bars, flags, tags, total;
 };
 
 enum Kind { kPass1 = 1, kPass2 = 2, kFused = 3 };
@@ -100,6 +107,8 @@ __host__ __device__ inline Layout make_layout(const Geom &g, int kind)
     off = s.bars + 16u * g.ring;
     s.flags = off;
     off += 16;
+    s.tags = off;   // fused kernel: the piece each ring slot holds in a dynamic pass 2
+    if (kind == kFused) off += 4u * kMaxRing;
     s.total = off;
     return s;
 }

@@ -364,6 +364,79 @@ __device__ void drain_loads(const Smem &sm, const ProducerState &ps, int ring)
 }
 
 // ---------------------------------------------------------------------------
+// dynamic pass 2 (fused kernel, one batch entry, one item per CTA).  A CTA
+// first applies the pieces still in its ring; the others are dealt out at
+// run time: the producers take batches of kDynBatch entries from a
+// grid-wide counter over (row i of the item sequences from dyn_top down,
+// item s from the last down) -- the reverse of the order pass 1 read them
+// in, so the first ones are still in L2 -- skipping resident pieces.  SMs
+// that stream faster apply more pieces (the per-SM rates on a GB300 differ
+// by up to 1.5x between SMs, the same SMs slow from call to call).  The
+// producer hands each piece's index to the consumers in a word per ring
+// slot; -1 ends the pass.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kDynBatch = 4;
+
+// Piece of counter entry q: -1 past the last one, -2 for an entry with no
+// piece to load (item s has no row i, or the piece is resident in its
+// owner's ring: the last min(pieces, ring) of the item).
+__device__ __forceinline__ int64_t dyn_piece(const Geom &g, uint32_t q)
+{
+    const uint32_t S = static_cast<uint32_t>(g.S);
+    const int64_t i = g.dyn_top - static_cast<int64_t>(q / S);
+    if (i < 0) return -1;
+    const int32_t s = g.S - 1 - static_cast<int32_t>(q % S);
+    const int64_t np = item_pieces(g, s);
+    if (i >= np - min(np, static_cast<int64_t>(g.ring))) return -2;
+    return s + i * g.S;
+}
+
+// The ring position j of pass 2 uses slot (T - 1 - j) mod ring: positions
+// 0 .. resident - 1 are the CTA's last pass-1 pieces, still in place.
+__device__ __forceinline__ int dyn_slot(int64_t T, int64_t j, int ring)
+{
+    const int64_t r = (T - 1 - j) % ring;
+    return static_cast<int>(r < 0 ? r + ring : r);
+}
+
+__device__ void produce_pass2_dyn(const Args &a, const Smem &sm, int64_t T, int64_t resident,
+                                  ProducerState &ps, const Ctl &ctl)
+{
+    const Geom &g = a.g;
+    const bool hint = (a.l2_hints & 1u) != 0;
+    const uint64_t pol = hint ? policy_evict_first() : 0;
+    volatile int32_t *tags = reinterpret_cast<volatile int32_t *>(sm.base + sm.lay.tags);
+    uint32_t q = 0, q_end = 0;   // the batch of counter entries in hand
+    for (int64_t j = resident;; ++j) {
+        int64_t k;
+        do {
+            if (q == q_end) {
+                q = atomicAdd(a.sync + 2, kDynBatch);
+                q_end = q + kDynBatch;
+            }
+            k = dyn_piece(g, q++);
+        } while (k == -2);
+        const int slot = dyn_slot(T, j, g.ring);
+        if (j >= g.ring) {
+            // the slot holds position j - ring of this pass
+            if (!wait_phase(sm.empty(slot), (ps.empty_par >> slot) & 1u, ctl)) return;
+            ps.empty_par ^= 1u << slot;
+        }
+        if (k < 0) {
+            tags[slot] = -1;
+            mbar_arrive(sm.full(slot));   // a phase without bytes: the end of the pass
+            ps.issued_par ^= 1u << slot;
+            return;
+        }
+        tags[slot] = static_cast<int32_t>(k);
+        Cursor c;
+        c.n = 0;
+        c.k = k;
+        issue_load(a, sm, c, slot, ps, pol, hint);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // consumers: pass 1
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v)
@@ -1070,6 +1143,68 @@ __device__ void consume_pass2(const Args &a, const Smem &sm, int64_t T, int64_t 
     full_par = rp.full_par;
 }
 
+template <bool SILU, bool POW2>
+__device__ void consume_pass2_dyn(const Args &a, const Smem &sm, int64_t T, int64_t resident, uint32_t &full_par,
+                                  const Ctl &ctl)
+{
+    const Geom &g = a.g;
+    const int tid = threadIdx.x;
+    const int32_t s = static_cast<int32_t>(blockIdx.x);   // this CTA's item
+    if (g.G * g.S <= kOneBarrierRecords)
+        fused_local_stats(a, sm, 0, s == 0);
+    else
+        fused_scale_shift(a, sm, 0);
+    const int vslot = vec_slot<POW2>(g, tid);
+    const int A = carriers<POW2>(g);
+    const bool carrier = POW2 || tid < A;
+    const int full_nvec = g.rows_per_piece * g.V;
+    const int tail_nvec = g.tail_rows * g.V;
+    const int kind_full = vec_kind(full_nvec, A);
+    f2_t Sc[4], Tt[4];
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(sm.base + sm.lay.st) + 4 * vslot;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 v = src[j];
+            Sc[j] = pk(v.x, v.z);
+            Tt[j] = pk(v.y, v.w);
+        }
+    }
+    const volatile int32_t *tags = reinterpret_cast<const volatile int32_t *>(sm.base + sm.lay.tags);
+    const int64_t np = item_pieces(g, s);
+    bool ok = !*ctl.abort;
+    for (int64_t j = 0;; ++j) {
+        const int slot = dyn_slot(T, j, g.ring);
+        int64_t k;
+        if (j < resident) {
+            k = s + (np - 1 - j) * g.S;   // still in the ring from pass 1
+        } else {
+            if (ok) ok = wait_phase(sm.full(slot), (full_par >> slot) & 1u, ctl);
+            full_par ^= 1u << slot;
+            if (!ok) break;
+            k = tags[slot];
+            if (k < 0) break;
+        }
+        const uint32_t base = sm.slot_addr(slot, g.piece_bytes);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.y + piece_elem_offset(g, 0, k)) + tid;
+        if (ok && carrier) {
+            if (k == g.pieces_per_n - 1) {
+                p2_piece<SILU, 0>(base, dst, tid, A, tail_nvec, Sc, Tt);
+            } else {
+                switch (kind_full) {
+                case 8: p2_piece<SILU, 8>(base, dst, tid, A, full_nvec, Sc, Tt); break;
+                case 4: p2_piece<SILU, 4>(base, dst, tid, A, full_nvec, Sc, Tt); break;
+                case 2: p2_piece<SILU, 2>(base, dst, tid, A, full_nvec, Sc, Tt); break;
+                case 1: p2_piece<SILU, 1>(base, dst, tid, A, full_nvec, Sc, Tt); break;
+                default: p2_piece<SILU, 0>(base, dst, tid, A, full_nvec, Sc, Tt); break;
+                }
+            }
+        }
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(sm.empty(slot));   // the slot may be refilled now
+    }
+}
+
 // ---------------------------------------------------------------------------
 // kernel prologue: shared memory carve-up, mbarrier init, status check
 // ---------------------------------------------------------------------------
@@ -1223,10 +1358,25 @@ __global__ void __launch_bounds__(kThreads, 1) gn_fused_kernel(const __grid_cons
 
     // group statistics / scale and shift (per CTA, in consume_pass2), pass 2
     if (producer) {
-        produce_pass2(a, sm, T, resident, ps, ctl);
+        if (g.dyn_p2)
+            produce_pass2_dyn(a, sm, T, resident, ps, ctl);
+        else
+            produce_pass2(a, sm, T, resident, ps, ctl);
         if (*ctl.abort) drain_loads(sm, ps, g.ring);
     } else if (threadIdx.x < kConsumers) {
-        consume_pass2<SILU, true, POW2>(a, sm, T, resident, full_par, ctl, start);
+        if (g.dyn_p2)
+            consume_pass2_dyn<SILU, POW2>(a, sm, T, resident, full_par, ctl);
+        else
+            consume_pass2<SILU, true, POW2>(a, sm, T, resident, full_par, ctl, start);
+    }
+    if (g.dyn_p2) {
+        // every piece this CTA took is done; the last CTA out zeroes the
+        // counter for the next call
+        __syncthreads();
+        if (threadIdx.x == 0 && atomicAdd(a.sync + 3, 1u) == gridDim.x - 1) {
+            atomicExch(a.sync + 2, 0u);
+            atomicExch(a.sync + 3, 0u);
+        }
     }
 }
 
