@@ -209,6 +209,43 @@ def test_ring_reuse_is_race_free(N, L, C, variant):
                "ring reuse sampled")
 
 
+_STATIC_PASS2_CHILD = """
+import sys
+import numpy as np
+import torch
+from channels_last_groupnorm_gb300 import gnsilu as gs
+from channels_last_groupnorm_gb300 import workloads as wl
+from tests import gpu_util as gu
+N, L, C = (int(v) for v in sys.argv[1:4])
+case = wl.make_case(N, L, C, seed=L + C, mean=1.0, std=2.0)
+x, gamma, beta = gu.device_inputs(case)
+y, mean, rstd = gu.run_rows_ex(x, gamma, beta, 32, 1e-6, True, gs.VARIANT_FUSED)
+np.save(sys.argv[4], y.view(torch.int16).cpu().numpy())
+np.save(sys.argv[5], torch.stack([mean, rstd]).cpu().numpy())
+"""
+
+
+@pytest.mark.parametrize("N,L,C", [(1, 131072, 512), (1, 262144, 256)])
+def test_dynamic_pass2_matches_the_static_assignment_bitwise(N, L, C, tmp_path):
+    """For large single-entry tensors the fused kernel deals the pieces of
+    pass 2 out at run time.  Which CTA applies a piece must not change a bit
+    of the output: compare with the static assignment (GN_DYNAMIC_PASS2=0,
+    read once per process, so in a child process)."""
+    import os
+    import subprocess
+    import sys
+    case = wl.make_case(N, L, C, seed=L + C, mean=1.0, std=2.0)
+    x, gamma, beta = gu.device_inputs(case)
+    y, mean, rstd = gu.run_rows_ex(x, gamma, beta, 32, 1e-6, True, gs.VARIANT_FUSED)
+    env = dict(os.environ, GN_DYNAMIC_PASS2="0")
+    yf, sf = tmp_path / "y.npy", tmp_path / "s.npy"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([sys.executable, "-c", _STATIC_PASS2_CHILD, str(N), str(L), str(C), str(yf), str(sf)],
+                   env=env, cwd=root, check=True, timeout=600)
+    assert np.array_equal(np.load(yf), y.view(torch.int16).cpu().numpy()), "outputs differ from the static assignment"
+    assert np.array_equal(np.load(sf), torch.stack([mean, rstd]).cpu().numpy())
+
+
 # ---------------------------------------------------------------------------
 # the cluster schedule: where the automatic choice takes it, and where not
 # ---------------------------------------------------------------------------
