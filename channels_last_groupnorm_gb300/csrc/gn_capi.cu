@@ -210,10 +210,12 @@ Plan make_plan(int64_t N, int64_t L, int64_t C, int64_t G, int kind, const Devic
     if (ring > gn::kMaxRing) ring = gn::kMaxRing;
     g.ring = static_cast<int32_t>(ring);
     // the fused kernel deals out pass 2 at run time for one batch entry
-    // with one item per CTA and at least three ring-fulls of pieces per CTA
-    // (the shapes where its SMs' unequal streaming rates show)
+    // with one item per CTA and at least eight ring-fulls of pieces per CTA
+    // (measured: 512 MiB 254 -> 243 us, 256 MiB 127.0 -> 125.8 us, but 96-128
+    // MiB 49.8 -> 52.7 and 65.7 -> 68.9 us, where the unequal streaming
+    // rates of the SMs matter less than taking pieces from the counter)
     g.dyn_top = g.base_pieces - g.ring;
-    g.dyn_p2 = (kind == GN_VARIANT_FUSED && N == 1 && g.items == p.grid && g.base_pieces >= 3 * ring &&
+    g.dyn_p2 = (kind == GN_VARIANT_FUSED && N == 1 && g.items == p.grid && g.base_pieces >= 8 * ring &&
                 dynamic_pass2_enabled())
                    ? 1
                    : 0;
