@@ -107,6 +107,22 @@ def test_large_workloads_sampled(index, variant):
         del y
 
 
+@pytest.mark.parametrize("N,L,C,G", [(1, 262144, 512, 64), (1, 1048576, 256, 128)])
+def test_dealt_out_pass2_with_the_grid_wide_finalize(N, L, C, G):
+    """Large single-entry tensors with many groups: the fused kernel merges
+    the records with its grid-wide finalize (a second barrier) and deals
+    pass 2 out at run time; sampled outputs and every statistic against the
+    oracle."""
+    case = wl.make_case(N, L, C, seed=L + G, mean=0.5, std=1.5)
+    x, gamma, beta = gu.device_inputs(case)
+    y, mean, rstd = gu.run_rows_ex(x, gamma, beta, G, 1e-6, True, gs.VARIANT_FUSED)
+    m_ref, _, r_ref = oracle.stats(case["x_bits"], G, 1e-6)
+    gu.check_stats(mean.cpu().numpy(), rstd.cpu().numpy(), m_ref, r_ref, f"G={G}")
+    idx = np.random.default_rng(G).integers(0, N * L * C, 1 << 20)
+    y_ref = oracle.apply_at(case["x_bits"], case["gamma"], case["beta"], G, m_ref, r_ref, True, idx)
+    gu.check_y(gu.bf16_to_f64(y.reshape(-1)[torch.from_numpy(idx).cuda()]), y_ref, f"G={G} sampled")
+
+
 # ---------------------------------------------------------------------------
 # edge cases: every C, ragged and tiny L, several batch entries, G extremes
 # ---------------------------------------------------------------------------
