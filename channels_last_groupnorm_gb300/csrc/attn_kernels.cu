@@ -1032,7 +1032,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             int g = 0, tq = 0;
             bool go = true, bad = false;   // bad: a wait of the waiter failed (sticky)
             for (int u = ub, nu = 0; go && u < ue; u = nu, ++tq) {
-                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                const int j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile u / nb
                 nu = u + (j1 - j0);
                 if (waiter && lane == 0) bad = bad || !fwait(bar(kQFull), tq & 1, abort, args.timeout_ns);
                 __syncwarp();
@@ -1254,7 +1254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             int g = 0, tq = 0, ro = 0;
             bool go = true, bad = false;   // bad: a wait of the waiter failed (sticky)
             for (int u = ub, nu = 0; go && u < ue; u = nu, ++tq) {
-                const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
+                const int j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile u / nb
                 nu = u + (j1 - j0);
                 for (int j = j0; j < j1; ++j, ++g) {
                     const int buf = g & 1;
