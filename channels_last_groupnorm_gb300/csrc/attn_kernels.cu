@@ -859,8 +859,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 // of a chunk; a lane reading its own row would make every 16-byte load a
 // separate request) and go through 8 KB of staging shared memory, 16-byte
 // pieces XOR-swizzled by the row so that neither the writes nor the
-// row-wise reads meet in a bank; each lane then takes its own row.  Two
-// chunks' loads are in flight at a time.
+// row-wise reads meet in a bank; each lane then takes its own row.  NF
+// chunks' loads are in flight at a time, staged in NF x 4 KB.
+template <int NF>
 __device__ __forceinline__ void flash_load_q(const FlashArgs &args, uint32_t tmem, uint32_t lane_base, int t,
                                              int quarter, int lane, uint32_t stage, int c0, int c1)
 {
@@ -868,18 +869,18 @@ __device__ __forceinline__ void flash_load_q(const FlashArgs &args, uint32_t tme
     const __nv_bfloat16 *src =
         args.q + (static_cast<int64_t>(t) * 128 + quarter * 32 + (lane >> 3)) * D + piece * 8;
 #pragma unroll 1
-    for (int c = c0; c < c1; c += 2) {
-        const int nh = c + 1 < c1 ? 2 : 1;
-        uint4 g[2][8];
+    for (int c = c0; c < c1; c += NF) {
+        const int nh = c1 - c < NF ? c1 - c : NF;
+        uint4 g[NF][8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NF; ++h) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 g[h][i] = h < nh ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(4 * i) * D + (c + h) * 64))
                                  : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NF; ++h) {
             if (h < nh) {
                 const uint32_t st = stage + static_cast<uint32_t>(h) * 4096u;
 #pragma unroll
@@ -891,7 +892,7 @@ __device__ __forceinline__ void flash_load_q(const FlashArgs &args, uint32_t tme
         }
         __syncwarp();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NF; ++h) {
             if (h < nh) {
                 const uint32_t st = stage + static_cast<uint32_t>(h) * 4096u;
                 uint32_t v[32];
@@ -938,7 +939,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
 
     if (threadIdx.x == 0) {
         if (scorer) {
-            mbar_init(bar(kQFull), 4);               // the four softmax warps, once q is in tensor memory
+            mbar_init(bar(kQFull), 8);               // the eight softmax warps, once q is in tensor memory
             mbar_init(bar(kQFree), 2);               // both issuers, after a tile's MMAs
             for (int i = 0; i < kFlashKStages; ++i) {
                 mbar_init(bar(kKFull + i), 1);
@@ -946,7 +947,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             }
             for (int i = 0; i < 2; ++i) {
                 mbar_init(bar(kSFull + i), 1);
-                mbar_init(bar(kSEmpty + i), 4);      // the four softmax warps
+                mbar_init(bar(kSEmpty + i), 8);      // the eight softmax warps
                 mbar_init(bar(kPEmpty + i), 1);      // the output CTA's forwarder
             }
             mbar_init(bar(kSDrain), 2);
@@ -1080,34 +1081,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                 if (go && !waiter && lane == 0) umma_commit(bar(kQFree));
             }
             if (!waiter && lane == 0) umma_commit(bar(kSDrain));
-        } else if (!skip && warp >= 2 && warp < 6) {
-            // ---- softmax: one query row per thread ----
-            const int quad = warp & 3;
+        } else if (!skip && warp >= 2 && warp < 10) {
+            // ---- softmax: two warps per quarter of the query rows (warps w and
+            // w + 4 share a lane quarter of tensor memory), each with 64 of a
+            // block's 128 key columns, one row per thread.  The two halves of a
+            // row exchange their maxima at a barrier of the pair, so that both
+            // take the same rescale decision and weigh against the same m ----
+            const int quad = warp & 3, hc = (warp - 2) >> 2;
             const int row = quad * 32 + lane;
             const bool shipper = threadIdx.x == 64;   // issues the bulk copies to the output CTA
             const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
             const uint32_t remote = mapa_shared(base, 1) - base;   // add to an offset for CTA 1's address
-            const uint32_t prow = base + lay.pstage + static_cast<uint32_t>(row) * 128u;
+            // keys 64 hc .. 64 hc + 63 of the block: weights subtile hc
+            const uint32_t prow = base + lay.pstage + static_cast<uint32_t>(hc) * 16384u + static_cast<uint32_t>(row) * 128u;
             const uint32_t sw = static_cast<uint32_t>(row & 7);
+            const uint32_t pair = 7u + static_cast<uint32_t>(quad);   // named barrier of the two warps of a quarter
             float *astage = reinterpret_cast<float *>(gbase + lay.astage);
             unsigned int *fstage = reinterpret_cast<unsigned int *>(gbase + lay.fstage);
             float *lstage = reinterpret_cast<float *>(gbase + lay.lstage);
+            // the half-row maxima go through the row-sum staging area, which
+            // holds nothing from the copy of a piece's sums to the next piece's end
+            float *xstage = lstage;
             int g = 0, tq = 0;
             bool go = true, pending = false;
             for (int u = ub, nu = 0; go && u < ue; u = nu, ++tq) {
                 const int t = u / nb, j0 = u % nb, j1 = min(nb, j0 + (ue - u));   // a piece of tile t
                 nu = u + (j1 - j0);
-                float m = -INFINITY, l = 0.f;
+                float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
                 {
-                    // the tile's q rows of this warp into tensor memory (columns
-                    // 256 + d/2), once the previous tile's MMAs are done with them
+                    // the tile's q rows into tensor memory (columns 256 + d/2; each
+                    // warp one half of the dimensions of its quarter's rows), once
+                    // the previous tile's MMAs are done with them
                     const bool ok = tq == 0 || fwait(bar(kQFree), (tq - 1) & 1, abort, args.timeout_ns);
-                    if (bar_any(1, 128, !ok || *abort)) break;
+                    if (bar_any(1, 256, !ok || *abort)) break;
                     tc_fence_after_sync();
                     // (through the weights staging buffer: it holds no weights
                     // now, the previous piece ended with every copy out of it read)
-                    flash_load_q(args, tmem, lane_base, t, quad, lane,
-                                 base + lay.pstage + static_cast<uint32_t>(quad) * 8192u, 0, D / 64);
+                    flash_load_q<1>(args, tmem, lane_base, t, quad, lane,
+                                    base + lay.pstage + static_cast<uint32_t>(quad) * 8192u + static_cast<uint32_t>(hc) * 4096u,
+                                    hc * (D / 128), (hc + 1) * (D / 128));
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(kQFull));
@@ -1121,45 +1133,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                         bulk_wait_read_all();
                         pending = false;
                     }
-                    // one decision for all four warps, so that none is left at a barrier
-                    if (bar_any(1, 128, !ok || *abort)) {
+                    // one decision for all eight warps, so that none is left at a barrier
+                    if (bar_any(1, 256, !ok || *abort)) {
                         go = false;
                         break;
                     }
-                    const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(buf * 128);
+                    const uint32_t taddr = tmem + lane_base + static_cast<uint32_t>(buf * 128 + hc * 64);
                     // one pass with the running maximum m, redone with the block's
                     // maximum when that exceeds m by more than the threshold (a
-                    // decision per warp: tensor-memory loads are warp-collective)
+                    // decision per warp pair: tensor-memory loads are warp-collective,
+                    // and both halves of a row decide alike)
                     float m_new = m, lb = 0.f;
                     bool resc = false;
 #pragma unroll 1
                     for (int pass = 0; pass < 2; ++pass) {
                         float mx = -INFINITY;
                         lb = 0.f;
-#pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t v[32];
-                            tmem_ld_32x32b_x32(taddr + c * 32, v);
-                            tmem_wait_ld();
+                        uint32_t v0[32], v1[32];
+                        tmem_ld_32x32b_x32(taddr, v0);
+                        tmem_ld_32x32b_x32(taddr + 32u, v1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
                             uint32_t w[16];
 #pragma unroll
                             for (int k = 0; k < 16; ++k) {
-                                const float s0 = __uint_as_float(v[2 * k]), s1 = __uint_as_float(v[2 * k + 1]);
+                                const uint32_t x0 = c ? v1[2 * k] : v0[2 * k], x1 = c ? v1[2 * k + 1] : v0[2 * k + 1];
+                                const float s0 = __uint_as_float(x0), s1 = __uint_as_float(x1);
                                 mx = fmaxf(mx, fmaxf(s0, s1));
                                 const float p0 = ex2_approx(fmaf(s0, args.scale_log2, -m_new));
                                 const float p1 = ex2_approx(fmaf(s1, args.scale_log2, -m_new));
                                 w[k] = pack_bf16(p0, p1);
                                 lb += __uint_as_float(w[k] << 16) + __uint_as_float(w[k] & 0xffff0000u);
                             }
-                            // keys 32c .. 32c + 31: subtile c / 2, 16-byte chunks 4 (c % 2) .. + 3
-                            const uint32_t sub = prow + static_cast<uint32_t>(c >> 1) * 16384u;
+                            // keys 64 hc + 32c .. + 31: 16-byte chunks 4c .. 4c + 3 of the subtile row
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
-                                const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q);
-                                sts128(sub + ((chunk ^ sw) << 4), make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+                                const uint32_t chunk = static_cast<uint32_t>(c * 4 + q);
+                                sts128(prow + ((chunk ^ sw) << 4), make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
                             }
                         }
                         if (pass == 0) {
+                            xstage[hc * 128 + row] = mx;
+                            named_sync(pair, 64);
+                            mx = fmaxf(mx, xstage[(hc ^ 1) * 128 + row]);
                             mx *= args.scale_log2;
                             resc = mx > m + kFlashRescaleLog2;
                             if (resc) m_new = mx;
@@ -1173,11 +1190,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(kSEmpty + buf));
-                    astage[row] = alpha;
                     const unsigned any = __any_sync(0xffffffffu, resc) ? 1u : 0u;
-                    if (lane == 0) fstage[quad] = any;
+                    if (hc == 0) {
+                        astage[row] = alpha;
+                        if (lane == 0) fstage[quad] = any;
+                    }
                     fence_proxy_async_smem();   // the staged block, visible to the bulk copy
-                    named_sync(2, 128);
+                    named_sync(2, 256);
                     if (shipper) {
                         // once the output CTA's MMAs have consumed the buffer two blocks back
                         if (g < 2 || fwait(bar(kPEmpty + buf), ((g >> 1) - 1) & 1, abort, args.timeout_ns)) {
@@ -1195,13 +1214,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
                     }
                 }
                 if (!go) break;
-                // the piece's row sums and maxima, once the output CTA has read the
-                // ones that went into the same buffer two pieces back (a failed wait
-                // sets the abort flag, which every softmax warp sees at the next block)
-                lstage[row] = l;
-                lstage[128 + row] = m;
+                // the piece's row sums (the two halves added) and maxima, once the
+                // output CTA has read the ones that went into the same buffer two
+                // pieces back (a failed wait sets the abort flag, which every
+                // softmax warp sees at the next block)
+                if (hc == 1) lstage[row] = l;
+                named_sync(2, 256);
+                if (hc == 0) {
+                    lstage[row] = l + lstage[row];
+                    lstage[128 + row] = m;
+                }
                 fence_proxy_async_smem();
-                named_sync(2, 128);
+                named_sync(2, 256);
                 if (shipper &&
                     (tq < 2 || fwait(bar(kLEmpty + (tq & 1)), ((tq >> 1) - 1) & 1, abort, args.timeout_ns))) {
                     const uint32_t full = base + remote + lay.bars + 8u * (kLFull + (tq & 1));
