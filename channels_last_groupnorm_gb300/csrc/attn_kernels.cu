@@ -302,6 +302,17 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs &args, uint32_t tba
 // C = alpha A B^T (+ bias, + residual): persistent, one CTA per SM; tile t:
 // the N tile varies fastest.
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream has
+// finished, once every CTA of that kernel has signalled (or exited); it must
+// wait before it reads what that kernel writes.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -322,6 +333,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // a kernel launched after this one with programmatic serialization may
+    // start on the SMs this grid leaves free (it waits before reading the
+    // output); for any other successor this has no effect
+    if (threadIdx.x == 0) griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
@@ -1242,6 +1257,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
     } else {
         if (!skip && warp == 0 && lane == 0) {
             // ---- producer: V'^T, stages of 64 keys x one half of D ----
+            // (V'^T is the output of the kernel launched before this one,
+            // which may still be running: this CTA's only read of it)
+            griddep_wait();
             int vq = 0;
             bool go = true;
             const uint32_t stage_bytes = static_cast<uint32_t>(half) * 128u;
@@ -1507,6 +1525,7 @@ struct CombineTiles {
 
 __global__ void __launch_bounds__(128, 8) attn_combine_kernel(const FlashArgs a, const __grid_constant__ CombineTiles ct)
 {
+    griddep_wait();   // the pieces come from the pair kernel launched before this one
     const int nb = a.nblocks, D = a.D;
     const int c_lo = ct.c_lo[blockIdx.x];
     const int t = flash_unit_begin(a, c_lo + 1) / nb;   // the tile's first inner boundary follows cluster c_lo
@@ -1900,15 +1919,36 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
     choose_flash_pairs(a.tiles, a.nblocks, cap, fit, &best_c, &best_split);
     a.clusters = best_c;
     a.split = best_split;
-    attn_flash_kernel<<<2 * a.clusters, kFlashThreads, smem, s>>>(mq, mk, mv, a);
-    *err = cudaGetLastError();
-    if (*err != cudaSuccess) return 3;
+    // both launches with programmatic serialization: the pair kernel starts
+    // (barriers, tensor memory, q rows, key blocks, scores) while the
+    // value-row GEMM ahead of it finishes, and waits only before loading its
+    // output; the merge waits at entry
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * a.clusters);
+    cfg.blockDim = dim3(kFlashThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    *err = cudaLaunchKernelEx(&cfg, attn_flash_kernel, mq, mk, mv, a);
+    if (*err != cudaSuccess) {
+        cudaGetLastError();
+        return 3;
+    }
     ++*launches;
     const CombineTiles ct = split_tiles(a);
     if (a.split && ct.n > 0) {
-        attn_combine_kernel<<<dim3(ct.n, D / kCombineCols), 128, 0, s>>>(a, ct);
-        *err = cudaGetLastError();
-        if (*err != cudaSuccess) return 3;
+        cfg.gridDim = dim3(ct.n, D / kCombineCols);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        *err = cudaLaunchKernelEx(&cfg, attn_combine_kernel, a, ct);
+        if (*err != cudaSuccess) {
+            cudaGetLastError();
+            return 3;
+        }
         ++*launches;
     }
     return 0;
