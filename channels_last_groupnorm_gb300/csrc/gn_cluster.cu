@@ -47,6 +47,18 @@
 
 namespace gn {
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream has
+// finished, once every CTA of that kernel has signalled (or exited); it
+// touches no global memory before griddep_wait returns.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
 namespace {
 
 constexpr int kClThreads = 512;
@@ -147,6 +159,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int issued = (rows + a.BR - 1) / a.BR;      // boxes it copies
     const uint32_t bars = base + lay.bars;
     volatile int *abort = reinterpret_cast<volatile int *>(sm + lay.flag);
+    // shared memory only until the kernel ahead in the stream has finished;
+    // a kernel launched after this one may start as soon as every CTA of
+    // this one is running (it waits the same way)
+    if (tid == 0) {
+        griddep_launch_dependents();
+        *abort = 0;
+        for (int b = 0; b < issued; ++b) mbar_init(bars + 8u * b, a.tma ? 1 : kClThreads);
+        mbar_init_fence();
+    }
+    griddep_wait();
     // Loads whose values are needed only later go out first, so that their
     // latency hides behind the copies: the sticky status (checked before
     // anything is written) and gamma / beta of the slice.
@@ -155,11 +177,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (tid < a.SC) {
         gam = __ldg(a.gamma + s * a.SC + tid);
         bet = __ldg(a.beta + s * a.SC + tid);
-    }
-    if (tid == 0) {
-        *abort = 0;
-        for (int b = 0; b < issued; ++b) mbar_init(bars + 8u * b, a.tma ? 1 : kClThreads);
-        mbar_init_fence();
     }
     __syncthreads();
     const int VS = a.VS;
@@ -573,13 +590,15 @@ cudaError_t launch_cluster(const ClusterPlan &p, const uint16_t *x, uint16_t *y,
     cfg.blockDim = dim3(kClThreads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = p.CL;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void *params[] = {&a};
     return cudaLaunchKernelExC(&cfg, cluster_fn(silu), params);
 }

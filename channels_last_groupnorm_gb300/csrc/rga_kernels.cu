@@ -49,6 +49,14 @@ __device__ __forceinline__ uint4 rga_vec(const uint4 &r, const uint4 &u, const u
                       rga_pair<BF16>(r.w, u.w, g.w));
 }
 
+// Programmatic dependent launch (see launch_residual_gate).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // streaming load (cache-streaming: evict-first; every element is read once)
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
 
@@ -60,6 +68,8 @@ __global__ void __launch_bounds__(kRgaThreads) rga_kernel(const uint4 *__restric
                                                            const uint4 *__restrict__ gate, uint4 *out,
                                                            int64_t nvec, int V)
 {
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();   // residual, update and gate may come from the kernel ahead in the stream
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int step = static_cast<int>(stride % V);
     int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -100,11 +110,21 @@ cudaError_t launch_residual_gate(const void *residual, const void *update, const
     const auto *u = static_cast<const uint4 *>(update);
     const auto *g = static_cast<const uint4 *>(gate);
     auto *y = static_cast<uint4 *>(out);
-    if (bf16)
-        rga_kernel<true><<<blocks, kRgaThreads, 0, s>>>(r, u, g, y, nvec, V);
-    else
-        rga_kernel<false><<<blocks, kRgaThreads, 0, s>>>(r, u, g, y, nvec, V);
-    return cudaGetLastError();
+    // launched with programmatic stream serialization: the blocks may start
+    // while the kernel ahead in the stream finishes, and wait for it before
+    // their first access to global memory; a kernel launched after this one
+    // the same way may start once every block of this one is running
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kRgaThreads);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return bf16 ? cudaLaunchKernelEx(&cfg, rga_kernel<true>, r, u, g, y, nvec, V)
+                : cudaLaunchKernelEx(&cfg, rga_kernel<false>, r, u, g, y, nvec, V);
 }
 
 }  // namespace gn
