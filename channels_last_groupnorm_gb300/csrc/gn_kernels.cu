@@ -1219,13 +1219,21 @@ __device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl 
     sm.ring_s = smem_addr(g_smem);
     sm.bars_s = sm.ring_s + sm.lay.bars;
     volatile int *flags = reinterpret_cast<volatile int *>(g_smem + sm.lay.flags);
+    // With programmatic stream serialization (the fused launch) the kernel
+    // ahead in the stream may still be running: shared memory only until
+    // griddepcontrol.wait returns (for other launches it returns at once).
+    // A kernel launched after this one the same way may start once every
+    // CTA of this one is running.
     if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         for (int s = threadIdx.x; s < a.g.ring; s += 32) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), kConsumerWarps);
         }
         mbar_init_fence();
-    } else if (threadIdx.x == 32) {
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 32) {
         const unsigned int st = *reinterpret_cast<volatile unsigned int *>(&g_status);
         flags[0] = (st != 0u) ? 1 : 0;
     }
@@ -1505,8 +1513,21 @@ cudaError_t launch_fused(const Args &a, int grid, bool silu, cudaStream_t s)
 {
     Args copy = a;
     void *params[] = {&copy};
-    return cudaLaunchCooperativeKernel(fused_fn(silu, pow2_slots(a.g)), dim3(grid), dim3(kThreads), params,
-                                       smem_for(a, kFused), s);
+    // cooperative (the grid barrier), and with programmatic serialization:
+    // the CTAs may start while the kernel ahead in the stream finishes
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_for(a, kFused);
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelExC(&cfg, fused_fn(silu, pow2_slots(a.g)), params);
 }
 
 cudaError_t launch_selftest_wait(int mode, uint64_t timeout_ns, int *done, int blocks, cudaStream_t s)
