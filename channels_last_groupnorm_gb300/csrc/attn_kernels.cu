@@ -302,17 +302,6 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs &args, uint32_t tba
 // C = alpha A B^T (+ bias, + residual): persistent, one CTA per SM; tile t:
 // the N tile varies fastest.
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialization may start before the kernel ahead of it in the stream has
-// finished, once every CTA of that kernel has signalled (or exited); it must
-// wait before it reads what that kernel writes.
-__device__ __forceinline__ void griddep_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -333,10 +322,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     volatile int *consumed_sh = reinterpret_cast<volatile int *>(gbase + L::kConsumed);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // a kernel launched after this one with programmatic serialization may
-    // start on the SMs this grid leaves free (it waits before reading the
-    // output); for any other successor this has no effect
-    if (threadIdx.x == 0) griddep_launch_dependents();
+    // launched with programmatic serialization (tc::launch_pdl): nothing
+    // global before the kernel ahead in the stream has finished; then a
+    // kernel launched after this one the same way may start on the SMs this
+    // grid leaves free
+    tc::griddep_wait();
+    if (threadIdx.x == 0) tc::griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
@@ -493,6 +484,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
+    // launched with programmatic serialization, as gemm_kernel
+    tc::griddep_wait();
+    if (threadIdx.x == 0) tc::griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
@@ -1259,7 +1253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFlashThreads, 1)
             // ---- producer: V'^T, stages of 64 keys x one half of D ----
             // (V'^T is the output of the kernel launched before this one,
             // which may still be running: this CTA's only read of it)
-            griddep_wait();
+            tc::griddep_wait();
             int vq = 0;
             bool go = true;
             const uint32_t stage_bytes = static_cast<uint32_t>(half) * 128u;
@@ -1525,7 +1519,7 @@ struct CombineTiles {
 
 __global__ void __launch_bounds__(128, 8) attn_combine_kernel(const FlashArgs a, const __grid_constant__ CombineTiles ct)
 {
-    griddep_wait();   // the pieces come from the pair kernel launched before this one
+    tc::griddep_wait();   // the pieces come from the pair kernel launched before this one
     const int nb = a.nblocks, D = a.D;
     const int c_lo = ct.c_lo[blockIdx.x];
     const int t = flash_unit_begin(a, c_lo + 1) / nb;   // the tile's first inner boundary follows cluster c_lo
@@ -1636,8 +1630,10 @@ cudaError_t launch_gemm_variant(const CUtensorMap &ma, const CUtensorMap &mb, co
     });
     if (attr != cudaSuccess) return attr;
     const int blocks = a.tiles < sm_count ? a.tiles : sm_count;
-    gemm_kernel<BN, STAGES><<<blocks, kGemmThreads, L::kDynamic, s>>>(ma, mb, a);
-    return cudaGetLastError();
+    const cudaError_t e = tc::launch_pdl(gemm_kernel<BN, STAGES>, dim3(blocks), dim3(kGemmThreads), L::kDynamic, s,
+                                         ma, mb, a);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
 }
 
 bool gemm_pair_enabled()
@@ -1702,8 +1698,10 @@ cudaError_t launch_gemm_pair(const CUtensorMap &ma, const CUtensorMap &mb, const
     if (attr != cudaSuccess) return attr;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const int pairs = a.tiles < max_clusters ? a.tiles : max_clusters;
-    gemm_pair_kernel<STAGES><<<2 * pairs, kGemmThreads, L::kDynamic, s>>>(ma, mb, a);
-    return cudaGetLastError();
+    const cudaError_t e = tc::launch_pdl(gemm_pair_kernel<STAGES>, dim3(2 * pairs), dim3(kGemmThreads), L::kDynamic, s,
+                                         ma, mb, a);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
 }
 
 // C[M][N] = alpha A[M][K] B[N][K]^T (+ bias_m[M], + bias_n[N], + residual),
@@ -1923,17 +1921,7 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
     // (barriers, tensor memory, q rows, key blocks, scores) while the
     // value-row GEMM ahead of it finishes, and waits only before loading its
     // output; the merge waits at entry
-    cudaLaunchAttribute pdl[1];
-    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pdl[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * a.clusters);
-    cfg.blockDim = dim3(kFlashThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cfg.attrs = pdl;
-    cfg.numAttrs = 1;
-    *err = cudaLaunchKernelEx(&cfg, attn_flash_kernel, mq, mk, mv, a);
+    *err = tc::launch_pdl(attn_flash_kernel, dim3(2 * a.clusters), dim3(kFlashThreads), smem, s, mq, mk, mv, a);
     if (*err != cudaSuccess) {
         cudaGetLastError();
         return 3;
@@ -1941,10 +1929,7 @@ int run_flash(const void *q, const void *k, const void *vt, const void *residual
     ++*launches;
     const CombineTiles ct = split_tiles(a);
     if (a.split && ct.n > 0) {
-        cfg.gridDim = dim3(ct.n, D / kCombineCols);
-        cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = 0;
-        *err = cudaLaunchKernelEx(&cfg, attn_combine_kernel, a, ct);
+        *err = tc::launch_pdl(attn_combine_kernel, dim3(ct.n, D / kCombineCols), dim3(128), 0, s, a, ct);
         if (*err != cudaSuccess) {
             cudaGetLastError();
             return 3;

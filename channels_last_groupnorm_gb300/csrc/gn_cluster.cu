@@ -160,15 +160,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const uint32_t bars = base + lay.bars;
     volatile int *abort = reinterpret_cast<volatile int *>(sm + lay.flag);
     // shared memory only until the kernel ahead in the stream has finished;
-    // a kernel launched after this one may start as soon as every CTA of
-    // this one is running (it waits the same way)
+    // then a kernel launched after this one the same way may start (it waits
+    // the same way)
     if (tid == 0) {
-        griddep_launch_dependents();
         *abort = 0;
         for (int b = 0; b < issued; ++b) mbar_init(bars + 8u * b, a.tma ? 1 : kClThreads);
         mbar_init_fence();
     }
     griddep_wait();
+    if (tid == 0) griddep_launch_dependents();
     // Loads whose values are needed only later go out first, so that their
     // latency hides behind the copies: the sticky status (checked before
     // anything is written) and gamma / beta of the slice.

@@ -1222,10 +1222,8 @@ __device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl 
     // With programmatic stream serialization (the fused launch) the kernel
     // ahead in the stream may still be running: shared memory only until
     // griddepcontrol.wait returns (for other launches it returns at once).
-    // A kernel launched after this one the same way may start once every
-    // CTA of this one is running.
+    // Then a kernel launched after this one the same way may start.
     if (threadIdx.x < 32) {
-        if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         for (int s = threadIdx.x; s < a.g.ring; s += 32) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), kConsumerWarps);
@@ -1233,6 +1231,7 @@ __device__ __forceinline__ bool prologue(const Args &a, int kind, Smem &sm, Ctl 
         mbar_init_fence();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 32) {
         const unsigned int st = *reinterpret_cast<volatile unsigned int *>(&g_status);
         flags[0] = (st != 0u) ? 1 : 0;

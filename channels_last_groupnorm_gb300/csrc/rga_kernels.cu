@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(kRgaThreads) rga_kernel(const uint4 *__restric
                                                            const uint4 *__restrict__ gate, uint4 *out,
                                                            int64_t nvec, int V)
 {
-    if (threadIdx.x == 0) griddep_launch_dependents();
     griddep_wait();   // residual, update and gate may come from the kernel ahead in the stream
+    if (threadIdx.x == 0) griddep_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int step = static_cast<int>(stride % V);
     int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -113,7 +113,7 @@ cudaError_t launch_residual_gate(const void *residual, const void *update, const
     // launched with programmatic stream serialization: the blocks may start
     // while the kernel ahead in the stream finishes, and wait for it before
     // their first access to global memory; a kernel launched after this one
-    // the same way may start once every block of this one is running
+    // the same way may start once every block of this one has waited
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;

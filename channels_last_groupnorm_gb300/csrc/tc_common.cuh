@@ -98,5 +98,39 @@ int pair_clusters(Kernel kernel, int threads, size_t smem, int sm_count)
     return n;
 }
 
+// Programmatic dependent launch.  A kernel launched by launch_pdl may start
+// while the kernel ahead of it in the stream is still running, once every
+// CTA of that kernel has called griddep_launch_dependents (or exited); it
+// must call griddep_wait before its first access to global memory, which
+// then returns once that kernel has finished and its writes are visible.
+// Every kernel here signals only after its own griddep_wait has returned, so
+// a kernel that starts early still starts after everything ahead of its
+// predecessor has finished (the one-pass attention kernel reads q and k
+// without waiting).  For a kernel launched without the attribute both are
+// no-ops.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 }  // namespace tc
 }  // namespace gn

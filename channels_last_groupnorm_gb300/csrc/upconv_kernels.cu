@@ -257,6 +257,10 @@ __global__ void __launch_bounds__(kUcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // launched with programmatic serialization (tc::launch_pdl): nothing
+    // global before the kernel ahead in the stream has finished
+    tc::griddep_wait();
+    if (threadIdx.x == 0) tc::griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
@@ -452,6 +456,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUcThreads, 1)
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
+    // launched with programmatic serialization, as upconv_kernel
+    tc::griddep_wait();
+    if (threadIdx.x == 0) tc::griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
@@ -597,8 +604,10 @@ cudaError_t launch_variant(const CUtensorMap &mx, const CUtensorMap &mw, const U
                                     static_cast<int>(L::kDynamic));
     });
     if (attr != cudaSuccess) return attr;
-    upconv_kernel<BN, STAGES><<<blocks, kUcThreads, L::kDynamic, s>>>(mx, mw, a);
-    return cudaGetLastError();
+    const cudaError_t e = tc::launch_pdl(upconv_kernel<BN, STAGES>, dim3(blocks), dim3(kUcThreads), L::kDynamic, s,
+                                         mx, mw, a);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
 }
 
 template <int STAGES>
@@ -618,8 +627,10 @@ cudaError_t launch_pair(const CUtensorMap &mx, const CUtensorMap &mw, const UcAr
     if (attr != cudaSuccess) return attr;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const int pairs = a.tiles < max_clusters ? a.tiles : max_clusters;
-    upconv_pair_kernel<STAGES><<<2 * pairs, kUcThreads, L::kDynamic, s>>>(mx, mw, a);
-    return cudaGetLastError();
+    const cudaError_t e = tc::launch_pdl(upconv_pair_kernel<STAGES>, dim3(2 * pairs), dim3(kUcThreads), L::kDynamic, s,
+                                         mx, mw, a);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
 }
 
 bool pair_kernel_enabled()

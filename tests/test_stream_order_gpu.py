@@ -122,3 +122,44 @@ def test_residual_gate_and_cluster_calls_read_each_others_output(rep):
     ok = rp.same(rp.bits(r.cpu().reshape(-1, C)), want, "bf16")
     assert ok.all(), f"residual-gate after GroupNorm, rep {rep}: {int((~ok).sum())} outputs differ"
     check_gn(y, r, gamma, beta, f"GroupNorm after residual-gate, rep {rep}")
+
+
+def attn_check(got, ref, mag, what):
+    # the bound of the attention parity tests
+    err = np.abs(got - ref)
+    bound = 2.0 ** -6 * mag + 2.0 ** -7 * np.abs(ref)
+    assert not (err > bound).any(), f"{what}: {int((err > bound).sum())} of {err.size} outside the bound"
+
+
+@pytest.mark.parametrize("schedule", [gs.ATTN_ONE_PASS, gs.ATTN_STORED_WEIGHTS], ids=["one_pass", "stored_weights"])
+def test_attention_reads_q_and_k_written_just_before(schedule):
+    """q from a GroupNorm call and k from a residual-gate call, each into a
+    NaN-filled buffer right before the attention call: the one-pass kernel's
+    score side reads q and k without waiting itself, so this also checks that
+    it cannot start before everything ahead of the value-row GEMM is done."""
+    from channels_last_groupnorm_gb300 import workloads as wl
+
+    S, D = 1024, 512
+    c = wl.make_attn_case(S, D, 77, True)
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).cuda().view(torch.bfloat16)
+    wf, bf = gs.attn_fold(dev(c["wv"]), dev(c["bv"]), dev(c["wo"]), dev(c["bo"]))
+    x0 = seeded((1, S, D), 1000)
+    gamma, beta = affine(D, 1001)
+    residual2 = seeded((S, D), 1002)
+    update = seeded((S, D), 1003)
+    gate = seeded((D,), 1004, scale=0.5)
+    q = nan_like(x0)
+    k = torch.full((S, D), float("nan"), device="cuda", dtype=torch.bfloat16)
+    xn, res = dev(c["xn"]), dev(c["residual"])
+    torch.cuda.synchronize()
+    assert gs.gn_silu_rows(x0, gamma, beta, G=G, eps=EPS, out=q) is not None
+    assert gs.residual_gate_add(residual2, update, gate, out=k) is not None
+    y = gs.attention_folded(q[0], k, xn, wf, bf, residual=res, schedule=schedule)
+    assert y is not None
+    torch.cuda.synchronize()
+    assert gs.gn_device_status(False) == 0
+    qb, kb = gn_bits(q[0]), gn_bits(k)
+    assert not np.isnan(gu.bf16_to_f64(q)).any() and not np.isnan(gu.bf16_to_f64(k)).any()
+    ref, mag = oracle.attn().forward(qb, kb, c["xn"], c["wv"], c["bv"], c["wo"], c["bo"], c["residual"],
+                                     with_mag=True)
+    attn_check(y.float().cpu().numpy().astype(np.float64), ref, mag, f"attention after GroupNorm / residual-gate")
