@@ -159,6 +159,8 @@ __device__ __forceinline__ float2 merge_ml(float2 a, float2 b)
 __global__ void __launch_bounds__(256) softmax_stats_kernel(const float2 *__restrict__ parts_in, int parts,
                                                             float2 *__restrict__ row_ml, int rows)
 {
+    tc::griddep_wait();   // launched with programmatic serialization after the pass that writes the records
+    if (threadIdx.x == 0) tc::griddep_launch_dependents();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= rows) return;
     const float2 *p = parts_in + static_cast<int64_t>(warp) * parts;
@@ -1976,9 +1978,11 @@ int launch_attn_folded(const void *q, const void *k, const void *xn, const void 
     ++*launches;
     // the rows' (max, 1 / sum)
     const int parts = 2 * (S / schedule_bn(choose_gemm(S, S, D, sm_count)));   // as pass 1 runs
-    softmax_stats_kernel<<<(S + 7) / 8, 256, 0, s>>>(stats, parts, row_ml, S);
-    *err = cudaGetLastError();
-    if (*err != cudaSuccess) return 3;
+    *err = tc::launch_pdl(softmax_stats_kernel, dim3((S + 7) / 8), dim3(256), 0, s, stats, parts, row_ml, S);
+    if (*err != cudaSuccess) {
+        cudaGetLastError();
+        return 3;
+    }
     ++*launches;
     // pass 2: the scores again, written as softmax weights P (bf16)
     r = run_gemm(q, k, p, S, S, D, scale, nullptr, nullptr, nullptr, false, kGemmSoftmax, nullptr, row_ml,
